@@ -1,0 +1,158 @@
+"""CPU oracle for the decoder-layer fusions -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, the smoke check and the bench's CPU-baseline leg may import this package. It wraps the
+plain fp64 C oracle (oracle.c) through ctypes; it shares no code with the CUDA library and never imports
+it. The C source cites the pages it follows; this file only marshals numpy arrays.
+
+All functions take and return numpy arrays; bf16 tensors are uint16 bit patterns, FP8 codes uint8.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_HDR = os.path.join(_HERE, "oracle.h")
+LIB_PATH = os.path.join(_HERE, "liboracle.so")
+CFLAGS = ["-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-Wall"]
+
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so with gcc (plain C11, no FMA contraction) if it is missing or stale."""
+    stale = (not os.path.exists(LIB_PATH) or
+             os.path.getmtime(LIB_PATH) < max(os.path.getmtime(_SRC), os.path.getmtime(_HDR)))
+    if force or stale:
+        tmp = LIB_PATH + ".tmp"
+        subprocess.check_call(["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, LIB_PATH)
+    return LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        u16p = ctypes.POINTER(ctypes.c_uint16)
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        f64p = ctypes.POINTER(ctypes.c_double)
+        f32p = ctypes.POINTER(ctypes.c_float)
+        i64, f32, cint = ctypes.c_int64, ctypes.c_float, ctypes.c_int
+        lib.orc_bf16_to_double.argtypes, lib.orc_bf16_to_double.restype = [ctypes.c_uint16], ctypes.c_double
+        lib.orc_bf16_round.argtypes, lib.orc_bf16_round.restype = [ctypes.c_double], ctypes.c_uint16
+        lib.orc_e4m3_decode.argtypes, lib.orc_e4m3_decode.restype = [ctypes.c_uint8], ctypes.c_double
+        lib.orc_e4m3_encode.argtypes, lib.orc_e4m3_encode.restype = [ctypes.c_double], ctypes.c_uint8
+        lib.orc_silu.argtypes, lib.orc_silu.restype = [ctypes.c_double], ctypes.c_double
+        lib.orc_add_rmsnorm.argtypes = [u16p, u16p, u16p, i64, i64, f32, u16p, f64p, u16p]
+        lib.orc_add_rmsnorm_quant_fp8.argtypes = [u16p, u16p, u16p, i64, i64, f32, cint, f32p, u16p, u8p, f64p]
+        lib.orc_swiglu.argtypes = [u16p, i64, i64, f64p, u16p]
+        lib.orc_swiglu_quant_fp8.argtypes = [u16p, i64, i64, cint, f32p, u8p, f64p]
+        for fn in ("orc_add_rmsnorm", "orc_add_rmsnorm_quant_fp8", "orc_swiglu", "orc_swiglu_quant_fp8"):
+            getattr(lib, fn).restype = cint
+        _lib = lib
+        return lib
+
+
+def _p(a: Optional[np.ndarray], ctype):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise ValueError(f"oracle {what}: invalid argument")
+
+
+MODES = {"static": 0, "dynamic": 1}
+
+
+def bf16_to_double(b: int) -> float:
+    return _load().orc_bf16_to_double(int(b))
+
+
+def bf16_round(v: float) -> int:
+    return int(_load().orc_bf16_round(float(v)))
+
+
+def e4m3_decode(code: int) -> float:
+    return _load().orc_e4m3_decode(int(code))
+
+
+def e4m3_encode(v: float) -> int:
+    return int(_load().orc_e4m3_encode(float(v)))
+
+
+def silu(g: float) -> float:
+    return _load().orc_silu(float(g))
+
+
+def add_rmsnorm(x: np.ndarray, r: np.ndarray, w: np.ndarray, eps: float,
+                want_v: bool = True) -> Tuple[np.ndarray, np.ndarray, Optional[np.ndarray]]:
+    """Returns (residual_out bf16 bits [T,H], out bf16 bits [T,H], v exact float64 [T,H] or None)."""
+    x = np.ascontiguousarray(x, np.uint16)
+    r = np.ascontiguousarray(r, np.uint16)
+    w = np.ascontiguousarray(w, np.uint16)
+    T, H = x.shape
+    res = np.empty((T, H), np.uint16)
+    out = np.empty((T, H), np.uint16)
+    v = np.empty((T, H), np.float64) if want_v else None
+    u16, f64 = ctypes.c_uint16, ctypes.c_double
+    _check(_load().orc_add_rmsnorm(_p(x, u16), _p(r, u16), _p(w, u16), T, H, float(eps), _p(res, u16),
+                                   _p(v, f64), _p(out, u16)), "add_rmsnorm")
+    return res, out, v
+
+
+def add_rmsnorm_quant_fp8(x: np.ndarray, r: np.ndarray, w: np.ndarray, eps: float, mode: str,
+                          static_scale: float = 0.0, want_v: bool = True):
+    """Returns (residual_out [T,H] u16, q [T,H] u8, scale float32 ([1] static / [T] dynamic), v or None)."""
+    x = np.ascontiguousarray(x, np.uint16)
+    r = np.ascontiguousarray(r, np.uint16)
+    w = np.ascontiguousarray(w, np.uint16)
+    T, H = x.shape
+    res = np.empty((T, H), np.uint16)
+    q = np.empty((T, H), np.uint8)
+    scale = np.array([static_scale], np.float32) if mode == "static" else np.zeros((max(T, 1),), np.float32)
+    v = np.empty((T, H), np.float64) if want_v else None
+    u16, u8, f32, f64 = ctypes.c_uint16, ctypes.c_uint8, ctypes.c_float, ctypes.c_double
+    _check(_load().orc_add_rmsnorm_quant_fp8(_p(x, u16), _p(r, u16), _p(w, u16), T, H, float(eps),
+                                             MODES[mode], _p(scale, f32), _p(res, u16), _p(q, u8),
+                                             _p(v, f64)), "add_rmsnorm_quant_fp8")
+    return res, q, (scale if mode == "static" else scale[:T]), v
+
+
+def swiglu(gate_up: np.ndarray, want_h: bool = True) -> Tuple[np.ndarray, Optional[np.ndarray]]:
+    """Returns (out bf16 bits [T,I], h exact float64 [T,I] or None)."""
+    gu = np.ascontiguousarray(gate_up, np.uint16)
+    T, I2 = gu.shape
+    I = I2 // 2
+    out = np.empty((T, I), np.uint16)
+    h = np.empty((T, I), np.float64) if want_h else None
+    _check(_load().orc_swiglu(_p(gu, ctypes.c_uint16), T, I, _p(h, ctypes.c_double),
+                              _p(out, ctypes.c_uint16)), "swiglu")
+    return out, h
+
+
+def swiglu_quant_fp8(gate_up: np.ndarray, mode: str, static_scale: float = 0.0, want_h: bool = True):
+    """Returns (q [T,I] u8, scale float32 ([1] static / [T] dynamic), h exact float64 or None)."""
+    gu = np.ascontiguousarray(gate_up, np.uint16)
+    T, I2 = gu.shape
+    I = I2 // 2
+    q = np.empty((T, I), np.uint8)
+    scale = np.array([static_scale], np.float32) if mode == "static" else np.zeros((max(T, 1),), np.float32)
+    h = np.empty((T, I), np.float64) if want_h else None
+    _check(_load().orc_swiglu_quant_fp8(_p(gu, ctypes.c_uint16), T, I, MODES[mode],
+                                        _p(scale, ctypes.c_float), _p(q, ctypes.c_uint8),
+                                        _p(h, ctypes.c_double)), "swiglu_quant_fp8")
+    return q, (scale if mode == "static" else scale[:T]), h

@@ -1,0 +1,197 @@
+/*
+ * CPU oracle for the memory-bound decoder-layer fusions -- TEST INFRASTRUCTURE ONLY (see oracle.h).
+ *
+ * Every value is carried in double. The steps follow the source pages' order:
+ *   residual add -> mean of squares -> add epsilon -> reciprocal square root -> multiply by the
+ *   weight [P1, "Fusing operations, measured"]; silu(gate) * up over the stacked projection [P1];
+ *   quantisation of the activation to FP8 E4M3 with a per-tensor or per-token scale [P2 Part V, P5 s.3].
+ * Readings where the pages are silent:
+ *   - the norm is taken of the bf16-rounded sum, which is what the unfused model normalises;
+ *   - the product w * s * inv and silu(g) * up are not rounded before they are quantised or written;
+ *   - the quantised value is the unrounded product divided by the fp32 scale;
+ *   - magnitudes above 448 saturate to 448; an all-zero row has scale 0 and codes 0.
+ * Build: plain C11 with -ffp-contract=off so that x86 and Arm hosts give identical bits.
+ */
+#include "oracle.h"
+
+#include <math.h>
+#include <stddef.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---------------------------------------------------------------- bf16 */
+
+double orc_bf16_to_double(uint16_t b) {
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+uint16_t orc_bf16_round(double v) {
+    /* bf16 has 8 significant bits and the fp32 exponent range: the spacing of representable values
+     * in [2^(e-1), 2^e) is 2^(e-8), and never below 2^-133 (the subnormal spacing). */
+    if (isnan(v)) return (uint16_t)0x7FC0;
+    uint16_t sign = signbit(v) ? (uint16_t)0x8000 : (uint16_t)0;
+    double a = fabs(v);
+    if (a == 0.0) return sign;
+    if (isinf(a)) return (uint16_t)(sign | 0x7F80);
+    int e;
+    (void)frexp(a, &e); /* a = m * 2^e, 0.5 <= m < 1 */
+    int q = e - 8;
+    if (q < -133) q = -133;
+    double units = ldexp(a, -q);         /* exact: a scaling by a power of two */
+    double rounded = nearbyint(units);   /* default rounding mode: nearest, ties to even */
+    double res = ldexp(rounded, q);
+    const double max_bf16 = ldexp(255.0, 120); /* (2 - 2^-7) * 2^127 */
+    if (res > max_bf16) return (uint16_t)(sign | 0x7F80);
+    float f = (float)res; /* exact: res lies on the bf16 grid */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(sign | ((u >> 16) & 0x7FFFu));
+}
+
+/* ---------------------------------------------------------------- FP8 E4M3 */
+
+/* magnitude of the non-negative code c in [0, 126]: exponent field E = c >> 3, mantissa M = c & 7;
+ * E == 0 is subnormal (M / 8 * 2^-6), otherwise (1 + M / 8) * 2^(E - 7). */
+static double e4m3_magnitude(int c) {
+    int E = c >> 3, M = c & 7;
+    if (E == 0) return ldexp((double)M, -9);
+    return ldexp((double)(8 + M), E - 10);
+}
+
+double orc_e4m3_decode(uint8_t code) {
+    int c = code & 0x7F;
+    if (c == 0x7F) return NAN;
+    double m = e4m3_magnitude(c);
+    return (code & 0x80) ? -m : m;
+}
+
+uint8_t orc_e4m3_encode(double v) {
+    if (isnan(v)) return (uint8_t)0x7F;
+    uint8_t sign = signbit(v) ? (uint8_t)0x80 : (uint8_t)0;
+    double a = fabs(v);
+    int best = 126;
+    if (a < 448.0) {
+        double best_d = INFINITY;
+        for (int c = 0; c <= 126; ++c) {
+            double d = fabs(a - e4m3_magnitude(c));
+            if (d < best_d || (d == best_d && (c & 1) == 0)) {
+                best = c;
+                best_d = d;
+            }
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+/* ---------------------------------------------------------------- SiLU */
+
+double orc_silu(double g) { return g / (1.0 + exp(-g)); }
+
+/* ---------------------------------------------------------------- add + RMSNorm */
+
+/* One row: writes the residual and returns inv = 1 / sqrt(mean(s^2) + eps). */
+static double add_and_inv_rms(const uint16_t* x, const uint16_t* r, int64_t H, float eps,
+                              uint16_t* residual_out) {
+    double sum_sq = 0.0;
+    for (int64_t j = 0; j < H; ++j) {
+        uint16_t s = orc_bf16_round(orc_bf16_to_double(x[j]) + orc_bf16_to_double(r[j]));
+        residual_out[j] = s;
+        double sd = orc_bf16_to_double(s);
+        sum_sq += sd * sd;
+    }
+    double mean_sq = sum_sq / (double)H;
+    return 1.0 / sqrt(mean_sq + (double)eps);
+}
+
+static double normed(const uint16_t* residual_row, const uint16_t* w, int64_t j, double inv) {
+    return orc_bf16_to_double(w[j]) * orc_bf16_to_double(residual_row[j]) * inv;
+}
+
+int orc_add_rmsnorm(const uint16_t* x, const uint16_t* r, const uint16_t* w, int64_t T, int64_t H,
+                    float eps, uint16_t* residual_out, double* v_out, uint16_t* out) {
+    if (T < 0 || H <= 0) return -1;
+    if (T > 0 && (!x || !r || !w || !residual_out)) return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        const uint16_t* xr = x + t * H;
+        const uint16_t* rr = r + t * H;
+        uint16_t* sr = residual_out + t * H;
+        double inv = add_and_inv_rms(xr, rr, H, eps, sr);
+        for (int64_t j = 0; j < H; ++j) {
+            double v = normed(sr, w, j, inv);
+            if (v_out) v_out[t * H + j] = v;
+            if (out) out[t * H + j] = orc_bf16_round(v);
+        }
+    }
+    return 0;
+}
+
+/* quantise one row of exact values with the given fp32 scale (0 gives code 0). */
+static void quantise_row(const double* v, int64_t n, float scale, uint8_t* q) {
+    for (int64_t j = 0; j < n; ++j) q[j] = scale == 0.0f ? (uint8_t)0 : orc_e4m3_encode(v[j] / (double)scale);
+}
+
+static float dynamic_scale(const double* v, int64_t n) {
+    double amax = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+        double a = fabs(v[j]);
+        if (a > amax) amax = a;
+    }
+    return (float)(amax / 448.0);
+}
+
+int orc_add_rmsnorm_quant_fp8(const uint16_t* x, const uint16_t* r, const uint16_t* w, int64_t T,
+                              int64_t H, float eps, int mode, float* scale, uint16_t* residual_out,
+                              uint8_t* q_out, double* v_out) {
+    if (T < 0 || H <= 0 || (mode != 0 && mode != 1)) return -1;
+    if (T > 0 && (!x || !r || !w || !scale || !residual_out || !q_out)) return -1;
+    double* row = (double*)malloc((size_t)(H > 0 ? H : 1) * sizeof(double));
+    if (T > 0 && !row) return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        uint16_t* sr = residual_out + t * H;
+        double inv = add_and_inv_rms(x + t * H, r + t * H, H, eps, sr);
+        for (int64_t j = 0; j < H; ++j) row[j] = normed(sr, w, j, inv);
+        float sc = mode == 0 ? scale[0] : dynamic_scale(row, H);
+        if (mode == 1) scale[t] = sc;
+        quantise_row(row, H, sc, q_out + t * H);
+        if (v_out) memcpy(v_out + t * H, row, (size_t)H * sizeof(double));
+    }
+    free(row);
+    return 0;
+}
+
+/* ---------------------------------------------------------------- SwiGLU */
+
+int orc_swiglu(const uint16_t* gate_up, int64_t T, int64_t I, double* h_out, uint16_t* out) {
+    if (T < 0 || I <= 0) return -1;
+    if (T > 0 && !gate_up) return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        const uint16_t* g = gate_up + t * 2 * I;
+        const uint16_t* u = g + I;
+        for (int64_t j = 0; j < I; ++j) {
+            double h = orc_silu(orc_bf16_to_double(g[j])) * orc_bf16_to_double(u[j]);
+            if (h_out) h_out[t * I + j] = h;
+            if (out) out[t * I + j] = orc_bf16_round(h);
+        }
+    }
+    return 0;
+}
+
+int orc_swiglu_quant_fp8(const uint16_t* gate_up, int64_t T, int64_t I, int mode, float* scale,
+                         uint8_t* q_out, double* h_out) {
+    if (T < 0 || I <= 0 || (mode != 0 && mode != 1)) return -1;
+    if (T > 0 && (!gate_up || !scale || !q_out)) return -1;
+    double* row = (double*)malloc((size_t)(I > 0 ? I : 1) * sizeof(double));
+    if (T > 0 && !row) return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        orc_swiglu(gate_up + t * 2 * I, 1, I, row, NULL);
+        float sc = mode == 0 ? scale[0] : dynamic_scale(row, I);
+        if (mode == 1) scale[t] = sc;
+        quantise_row(row, I, sc, q_out + t * I);
+        if (h_out) memcpy(h_out + t * I, row, (size_t)I * sizeof(double));
+    }
+    free(row);
+    return 0;
+}

@@ -1,0 +1,74 @@
+/*
+ * CPU oracle for the memory-bound decoder-layer fusions -- TEST INFRASTRUCTURE ONLY.
+ *
+ * Plain, slow, fp64 C written from the definitions on the source pages. It shares no code with the
+ * CUDA library (no common header, helper, table or constant) and is used only by the tests, by the
+ * smoke check and by the bench's CPU-baseline leg. Nothing in the product path links or calls it.
+ *
+ * Sources (cited by page title and section):
+ *  [P1] "TensorRT-LLM: Compiling Inference Engines Ahead of Time", section "Fusing operations, measured":
+ *       RMSNorm is cast to float, square, mean, add epsilon, reciprocal square root, multiply, cast back,
+ *       multiply by the weight; TensorRT-LLM's RMSNorm adds the residual and normalises in one kernel;
+ *       the gated MLP is down(silu(gate(x)) * up(x)) with gate and up produced by one stacked matmul and
+ *       a swiglu kernel computing g / (1 + exp(-g)) * up per element.
+ *  [P2] "TensorRT-LLM" architecture walkthrough, "Part V continued: Deep dive: quantization co-designed
+ *       with the hardware": FP8 E4M3 for activations, with light per-tensor or per-block scaling
+ *       (format defined by Micikevicius et al., "FP8 Formats for Deep Learning").
+ *  [P5] "Introduction to torch.compile and How It Works with vLLM", section 3 (custom passes):
+ *       FusedKernel(x) = Quantize(SiLU(x)), the activation followed by FP8 quantisation in one kernel.
+ *
+ * Conventions: bf16 values are passed as their 16-bit patterns (uint16_t), row-major. Every function
+ * processes rows independently, so a caller may pass pointers offset to any row with a smaller T.
+ * Return value: 0 on success, -1 on an invalid argument (null pointer with T > 0, T < 0, width <= 0).
+ */
+#ifndef MBD_ORACLE_H
+#define MBD_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* bf16 pattern -> exact double. */
+double orc_bf16_to_double(uint16_t b);
+/* double -> nearest bf16 pattern, ties to even (8 significant bits, subnormals, overflow to inf). */
+uint16_t orc_bf16_round(double v);
+
+/* OCP E4M3FN: bias 7, 3 mantissa bits, max finite 448 (0x7E), no infinities, NaN 0x7F / 0xFF.
+ * encode: nearest code by exhaustive search over the 127 non-negative finite magnitudes, ties to the
+ * even code, magnitudes above 448 saturate to 448, the sign bit is set for negative inputs. */
+double orc_e4m3_decode(uint8_t code);
+uint8_t orc_e4m3_encode(double v);
+
+/* SiLU [P1]: g / (1 + exp(-g)). */
+double orc_silu(double g);
+
+/* Fused residual add + RMSNorm [P1]:
+ *   s = bf16(x + r)                     -> residual_out (the updated residual stream)
+ *   inv = 1 / sqrt(sum(s^2) / H + eps)
+ *   v = w * s * inv                     -> v_out (exact, fp64) and out (bf16 of v)
+ * v_out and out may be NULL. */
+int orc_add_rmsnorm(const uint16_t* x, const uint16_t* r, const uint16_t* w, int64_t T, int64_t H,
+                    float eps, uint16_t* residual_out, double* v_out, uint16_t* out);
+
+/* mode: 0 = static per-tensor scale (scale[0] is read), 1 = dynamic per-token (scale[t] is written).
+ * The scale is the dequantisation multiplier: v ~ q * scale. Dynamic: scale_t = fp32(max_j |v_j| / 448);
+ * codes are e4m3(v / scale) with the fp32 scale widened to double; a zero scale gives code 0. */
+int orc_add_rmsnorm_quant_fp8(const uint16_t* x, const uint16_t* r, const uint16_t* w, int64_t T,
+                              int64_t H, float eps, int mode, float* scale, uint16_t* residual_out,
+                              uint8_t* q_out, double* v_out);
+
+/* SwiGLU over a stacked gate_up row [P1]: h[t,j] = silu(gu[t,j]) * gu[t,I+j], computed in fp64 with no
+ * rounding of silu(g) before the product. h_out (exact) and out (bf16 of h) may be NULL. */
+int orc_swiglu(const uint16_t* gate_up, int64_t T, int64_t I, double* h_out, uint16_t* out);
+
+/* Quantize(SiLU(gate) * up) [P5], scale convention as for the norm. */
+int orc_swiglu_quant_fp8(const uint16_t* gate_up, int64_t T, int64_t I, int mode, float* scale,
+                         uint8_t* q_out, double* h_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MBD_ORACLE_H */

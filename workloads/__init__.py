@@ -1,0 +1,202 @@
+"""Seeded synthetic inputs for the decoder-layer fusions, shared by the tests, the bench and the oracle.
+
+This module holds no arithmetic of the method itself: it only draws random numbers, rounds them to the
+bf16 input type and describes the workload shapes. Both sides (the CUDA path and the CPU oracle) receive
+the same bf16 bit patterns from here.
+
+Recipe (one Philox stream per tensor, keyed by (seed, tensor id)):
+  * activations x, residual r, gate_up: float32 draws from N(0, sigma^2); optionally each element is
+    multiplied, independently with probability p, by an outlier factor k;
+  * RMSNorm weight: 1 + 0.1 * N(0, 1);
+  * every float32 draw is rounded to bf16 with round-to-nearest-even on its bit pattern.
+
+The shapes stand in for the models the source pages name (Qwen2.5-1.5B, Llama-3-8B/70B, Llama-3.1-405B):
+no dataset or trained weight is used.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import Dict, List, Optional, Tuple
+
+import numpy as np
+
+# tensor ids for the per-tensor Philox key
+_TID = {"x": 1, "residual": 2, "weight": 3, "gate_up": 4}
+
+
+def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 (nearest, ties to even) and return the 16-bit patterns as uint16."""
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    u = a.view(np.uint32).astype(np.uint64)
+    lsb = (u >> np.uint64(16)) & np.uint64(1)
+    rounded = (u + np.uint64(0x7FFF) + lsb) >> np.uint64(16)
+    out = rounded.astype(np.uint16)
+    nan = np.isnan(a)
+    if nan.any():
+        out[nan] = np.uint16(0x7FC0)
+    return out
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    """Widen bf16 bit patterns (uint16) to float32 values (exact)."""
+    return (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def _rng(seed: int, tensor: str, salt: int = 0) -> np.random.Generator:
+    return np.random.Generator(np.random.Philox(key=[int(seed), _TID[tensor] * 1000003 + int(salt)]))
+
+
+def normal_bf16(shape: Tuple[int, ...], seed: int, tensor: str, sigma: float = 1.0,
+                outlier_p: float = 0.0, outlier_k: float = 1.0, salt: int = 0) -> np.ndarray:
+    """bf16 bits of N(0, sigma^2) draws, each element independently scaled by outlier_k with prob. outlier_p."""
+    g = _rng(seed, tensor, salt)
+    v = g.standard_normal(size=shape, dtype=np.float32)
+    if sigma != 1.0:
+        v *= np.float32(sigma)
+    if outlier_p > 0.0:
+        m = g.random(size=shape, dtype=np.float32) < np.float32(outlier_p)
+        v[m] *= np.float32(outlier_k)
+    return f32_to_bf16_bits(v)
+
+
+def weight_bf16(hidden: int, seed: int, salt: int = 0) -> np.ndarray:
+    """bf16 bits of an RMSNorm weight 1 + 0.1 * N(0, 1)."""
+    g = _rng(seed, "weight", salt)
+    v = np.float32(1.0) + np.float32(0.1) * g.standard_normal(size=(hidden,), dtype=np.float32)
+    return f32_to_bf16_bits(v)
+
+
+@dataclass(frozen=True)
+class Dist:
+    sigma: float = 1.0
+    outlier_p: float = 0.0
+    outlier_k: float = 1.0
+
+
+@dataclass
+class NormInputs:
+    x: np.ndarray          # [T, H] uint16 (bf16 bits)
+    residual: np.ndarray   # [T, H] uint16
+    weight: np.ndarray     # [H] uint16
+    eps: float
+
+
+@dataclass
+class SwigluInputs:
+    gate_up: np.ndarray    # [T, 2I] uint16: gate = columns 0..I-1, up = columns I..2I-1
+
+
+def make_norm_inputs(T: int, H: int, seed: int, dist: Dist, eps: float, salt: int = 0) -> NormInputs:
+    x = normal_bf16((T, H), seed, "x", dist.sigma, dist.outlier_p, dist.outlier_k, salt)
+    r = normal_bf16((T, H), seed, "residual", dist.sigma, dist.outlier_p, dist.outlier_k, salt)
+    w = weight_bf16(H, seed, salt)
+    return NormInputs(x, r, w, float(eps))
+
+
+def make_swiglu_inputs(T: int, I: int, seed: int, dist: Dist, salt: int = 0) -> SwigluInputs:
+    return SwigluInputs(normal_bf16((T, 2 * I), seed, "gate_up", dist.sigma, dist.outlier_p,
+                                    dist.outlier_k, salt))
+
+
+# --------------------------------------------------------------------------------------------------
+# Workload descriptions. A "call" is one invocation of one entry point on one shape.
+# kind: "add_rmsnorm" | "add_rmsnorm_q8" | "swiglu" | "swiglu_q8"; mode: None | "static" | "dynamic"
+# --------------------------------------------------------------------------------------------------
+
+@dataclass(frozen=True)
+class Call:
+    kind: str
+    T: int
+    width: int                 # H for the norm, I for SwiGLU
+    dist: Dist
+    eps: float = 1e-6
+    mode: Optional[str] = None
+    static_scale: float = 0.05
+
+    @property
+    def name(self) -> str:
+        m = f"_{self.mode}" if self.mode else ""
+        w = "H" if self.kind.startswith("add") else "I"
+        return f"{self.kind}{m}_T{self.T}_{w}{self.width}"
+
+    def algorithmic_bytes(self) -> int:
+        """Minimum HBM bytes of one call: every input read once, every output written once."""
+        T, W = self.T, self.width
+        if self.kind == "add_rmsnorm":
+            return 8 * T * W + 2 * W
+        if self.kind == "add_rmsnorm_q8":
+            return 7 * T * W + 2 * W + (4 * T if self.mode == "dynamic" else 4)
+        if self.kind == "swiglu":
+            return 6 * T * W
+        if self.kind == "swiglu_q8":
+            return 5 * T * W + (4 * T if self.mode == "dynamic" else 4)
+        raise ValueError(self.kind)
+
+
+N01 = Dist()
+C3_ACT = Dist(1.0, 0.01, 50.0)
+C3_GU = Dist(float(np.sqrt(2.0)))
+C5_ACT = Dist(1.0, 0.001, 100.0)
+
+
+def _all_four(T: int, H: int, I: int, dist: Dist, eps: float) -> List[Call]:
+    return [Call("add_rmsnorm", T, H, dist, eps), Call("add_rmsnorm_q8", T, H, dist, eps, "static"),
+            Call("swiglu", T, I, dist), Call("swiglu_q8", T, I, dist, mode="dynamic")]
+
+
+@dataclass(frozen=True)
+class Workload:
+    key: str
+    description: str
+    calls: Tuple[Call, ...]
+    layers: int = 1            # back-to-back repeats with distinct buffers (decode sweep)
+
+    def algorithmic_bytes(self) -> int:
+        return self.layers * sum(c.algorithmic_bytes() for c in self.calls)
+
+    def tokens(self) -> int:
+        """Tokens pushed through the path per step: each distinct token count is one batch of rows
+        (a decode step over all layers still moves its T tokens once)."""
+        return sum(sorted({c.T for c in self.calls}))
+
+
+def qwen_t16() -> Workload:
+    return Workload("qwen2.5-1.5b_t16", "Qwen2.5-1.5B-shaped layer, 16 tokens",
+                    (Call("add_rmsnorm", 16, 1536, N01, 1e-6), Call("swiglu", 16, 8960, N01)))
+
+
+def qwen_decode_sweep(tokens: Tuple[int, ...] = (1, 2, 4, 8, 32, 64, 128, 256)) -> List[Workload]:
+    out = []
+    for T in tokens:
+        calls = (Call("add_rmsnorm", T, 1536, N01, 1e-6), Call("add_rmsnorm", T, 1536, N01, 1e-6),
+                 Call("swiglu", T, 8960, N01))
+        out.append(Workload(f"qwen2.5-1.5b_decode_T{T}", f"Qwen2.5-1.5B decode, {T} tokens, 28 layers",
+                            calls, layers=28))
+    return out
+
+
+def llama3_8b_prefill() -> Workload:
+    return Workload("llama3-8b_prefill_T8192", "Llama-3-8B-shaped prefill, 8192 tokens",
+                    (Call("add_rmsnorm", 8192, 4096, C3_ACT, 1e-5), Call("swiglu", 8192, 14336, C3_GU)))
+
+
+def llama3_70b_fp8() -> Workload:
+    return Workload("llama3-70b_fp8_T4096", "Llama-3-70B-shaped FP8 path, 4096 tokens",
+                    (Call("add_rmsnorm_q8", 4096, 8192, N01, 1e-5, "static"),
+                     Call("swiglu_q8", 4096, 28672, N01, mode="dynamic")))
+
+
+def llama31_405b_fp8_ragged() -> Workload:
+    calls = [Call("add_rmsnorm_q8", 2048, 16384, C5_ACT, 1e-5, "static"),
+             Call("swiglu_q8", 2048, 53248, C5_ACT, mode="dynamic")]
+    for T in (1, 3, 17, 1000):
+        calls += _all_four(T, 5120, 13824, C5_ACT, 1e-5)
+    return Workload("llama3.1-405b_fp8_T2048+ragged", "Llama-3.1-405B-shaped FP8 path (2048 tokens) plus "
+                    "ragged 5120/13824 shapes at 1, 3, 17, 1000 tokens", tuple(calls))
+
+
+def inputs_for(call: Call, seed: int = 0, salt: int = 0):
+    """Seeded inputs of one call (NormInputs or SwigluInputs)."""
+    if call.kind.startswith("add"):
+        return make_norm_inputs(call.T, call.width, seed, call.dist, call.eps, salt)
+    return make_swiglu_inputs(call.T, call.width, seed, call.dist, salt)
