@@ -1,0 +1,560 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused decoder-layer kernels on GB300: achieved HBM GB/s (and tokens/s) per step.
+
+A step is one pass of the whole hot path over one synthetic batch: for the default workload, the
+Llama-3.1-405B-shaped FP8 path (2048 tokens: add+RMSNorm -> E4M3 static, SwiGLU -> E4M3 dynamic) plus
+the ragged hidden 5120 / intermediate 13824 shapes at 1, 3, 17 and 1000 tokens through all four entry
+points (bf16 norm, FP8 norm, bf16 SwiGLU, FP8 SwiGLU). Every launch goes through the C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mine|reference] [--workload KEY]
+
+Prints ONE JSON line on rank 0. `value` = algorithmic bytes of all steps on all ranks / device time
+(max over ranks). The reference arm (--impl reference) times the CPU oracle on a bounded row sample.
+Diagnostics go to stderr.
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from datetime import datetime
+from typing import Dict, List, Optional
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+METRIC = "achieved HBM GB/s (% of GB300 peak) and tokens/s per fused kernel vs CPU oracle"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+DEFAULT_WORKLOAD = "llama3.1-405b_fp8_T2048+ragged"
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel, from the ncu capture
+# summarised under profiles/; valid only while the CUDA sources hash to `csrc_sha256`.
+TRAFFIC: Dict[str, Dict] = {}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def workloads_by_key() -> Dict[str, wl.Workload]:
+    ws = [wl.qwen_t16(), wl.llama3_8b_prefill(), wl.llama3_70b_fp8(), wl.llama31_405b_fp8_ragged()]
+    ws += wl.qwen_decode_sweep()
+    return {w.key: w for w in ws}
+
+
+def decode_sweep_workload() -> wl.Workload:
+    """All token counts of the Qwen2.5-1.5B decode sweep in one step (28 layers each)."""
+    calls = []
+    for w in wl.qwen_decode_sweep():
+        calls += list(w.calls)
+    return wl.Workload("qwen2.5-1.5b_decode_sweep", "Qwen2.5-1.5B decode sweep, T in 1..256, 28 layers",
+                       tuple(calls), layers=28)
+
+
+def csrc_hash() -> str:
+    d = os.path.join(ROOT, "memory_bound_decoder_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------------------------------------ CPU baseline
+
+def oracle_run_call(call: wl.Call, inp) -> None:
+    import oracle
+    oracle.build()
+    if call.kind == "add_rmsnorm":
+        oracle.add_rmsnorm(inp.x, inp.residual, inp.weight, call.eps, want_v=False)
+    elif call.kind == "add_rmsnorm_q8":
+        oracle.add_rmsnorm_quant_fp8(inp.x, inp.residual, inp.weight, call.eps, call.mode, call.static_scale,
+                                     want_v=False)
+    elif call.kind == "swiglu":
+        oracle.swiglu(inp.gate_up, want_h=False)
+    else:
+        oracle.swiglu_quant_fp8(inp.gate_up, call.mode, call.static_scale, want_h=False)
+
+
+def _split(call: wl.Call, inp, nchunks: int):
+    """Split a call's inputs into row blocks (rows are independent)."""
+    T = call.T
+    bounds = np.linspace(0, T, min(T, nchunks) + 1).astype(int)
+    out = []
+    for a, b in zip(bounds[:-1], bounds[1:]):
+        if b <= a:
+            continue
+        if call.kind.startswith("add"):
+            out.append(wl.NormInputs(inp.x[a:b], inp.residual[a:b], inp.weight, inp.eps))
+        else:
+            out.append(wl.SwigluInputs(inp.gate_up[a:b]))
+    return out
+
+
+class OracleSample:
+    """A bounded, evenly spaced row sample of every call of a workload, run by the oracle on all host cores."""
+
+    def __init__(self, work: wl.Workload, frac: float, threads: int, seed: int = 0):
+        import oracle
+        oracle.build()
+        self.work, self.threads, self.frac = work, threads, frac
+        self.items = []
+        self.bytes = 0
+        self.rows = 0
+        for ci, call in enumerate(work.calls):
+            n = max(1, int(round(call.T * frac)))
+            rows = np.unique(np.linspace(0, call.T - 1, n).round().astype(np.int64))
+            inp = wl.inputs_for(call, seed=seed, salt=ci, rows=rows)
+            sub = wl.Call(call.kind, len(rows), call.width, call.dist, call.eps, call.mode, call.static_scale)
+            self.items.append((sub, _split(sub, inp, threads)))
+            self.bytes += sub.algorithmic_bytes() * work.layers
+            self.rows += len(rows)
+        self.tokens = sum(len(np.unique(np.linspace(0, t - 1, max(1, int(round(t * frac)))).round()))
+                          for t in sorted({c.T for c in work.calls}))
+        self.pool = cf.ThreadPoolExecutor(max_workers=threads)
+
+    def run(self) -> None:
+        jobs = []
+        for _ in range(self.work.layers):
+            for call, chunks in self.items:
+                for ch in chunks:
+                    jobs.append(self.pool.submit(oracle_run_call, call, ch))
+        for j in jobs:
+            j.result()
+
+    def describe(self) -> str:
+        return (f"{self.frac:.4g} of the rows of every call, evenly spaced ({self.rows} rows, "
+                f"{self.bytes / 1e6:.1f} MB algorithmic per step), fp64 C oracle, {self.threads} threads")
+
+
+def calibrate_fraction(work: wl.Workload, threads: int, target_s: float) -> float:
+    """Row fraction whose oracle run takes about target_s on `threads` host threads: one row of every call
+    is timed on its own and scaled by that call's row count."""
+    full_s = 0.0
+    for ci, call in enumerate(work.calls):
+        rows = np.array([0], np.int64)
+        inp = wl.inputs_for(call, seed=0, salt=ci, rows=rows)
+        one = wl.Call(call.kind, 1, call.width, call.dist, call.eps, call.mode, call.static_scale)
+        t = time.perf_counter()
+        oracle_run_call(one, inp)
+        full_s += (time.perf_counter() - t) * call.T * work.layers
+    full_s /= max(1, threads)
+    return float(min(1.0, max(1e-6, target_s / max(full_s, 1e-9))))
+
+
+def cpu_baseline(work: wl.Workload, target_s: float = 1.0) -> Dict:
+    threads = os.cpu_count() or 1
+    frac = calibrate_fraction(work, threads, target_s)
+    s = OracleSample(work, frac, threads)
+    s.run()  # warm
+    t = time.perf_counter()
+    s.run()
+    dt = time.perf_counter() - t
+    return {"value": round(s.bytes / dt / 1e9, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": s.describe(), "tokens_per_s": round(s.tokens / dt, 2), "seconds": round(dt, 3)}
+
+
+# ------------------------------------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ["timestamp", "uuid", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, uuid: str):
+        self.uuid = uuid.lower().replace("gpu-", "")
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS),
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self, t0: float, t1: float) -> Optional[Dict]:
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) != len(self.FIELDS) or self.uuid not in parts[1].lower():
+                    continue
+                try:
+                    ts = datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(parts[2]), float(parts[3]), parts[4], parts[6:]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        basis = "inside the timed region"
+        if not inside:   # timed region shorter than the sampling period: nearest samples
+            inside = sorted(rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[:3]
+            basis = "nearest samples to a short timed region"
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in inside for n, v in zip(names, r[4]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside), "basis": basis}
+
+
+# ------------------------------------------------------------------------------------------------ GPU arm
+
+class DeviceCall:
+    """Device (and pinned host) buffers of one call, and the prepared C-ABI argument tuple."""
+
+    def __init__(self, torch, mbd, call: wl.Call, inp, dev, shared_residual=None):
+        self.call = call
+        self.mbd = mbd
+        T, W = call.T, call.width
+        u16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16))
+        self.h2d = []   # (device tensor, pinned host tensor): activation inputs copied in by the e2e leg
+        self.d2h = []   # (device tensor, pinned host tensor): outputs copied back by the e2e leg
+        if call.kind.startswith("add"):
+            self.x = u16(inp.x).to(dev)
+            self.res = shared_residual if shared_residual is not None else u16(inp.residual).to(dev)
+            self.w = u16(inp.weight).to(dev)
+            self.h2d += [(self.x, u16(inp.x).pin_memory()), (self.res, u16(inp.residual).pin_memory())]
+            if call.kind == "add_rmsnorm":
+                self.out = torch.empty((T, W), dtype=torch.int16, device=dev)
+                self.fn = mbd.get_lib().mbd_fused_add_rmsnorm
+                self.args = [self.out.data_ptr(), self.res.data_ptr(), self.x.data_ptr(), self.w.data_ptr(),
+                             T, W, call.eps]
+            else:
+                self.out = torch.empty((T, W), dtype=torch.uint8, device=dev)
+                self.scale = (torch.tensor([call.static_scale], dtype=torch.float32, device=dev)
+                              if call.mode == "static" else torch.zeros((T,), dtype=torch.float32, device=dev))
+                self.fn = mbd.get_lib().mbd_fused_add_rmsnorm_quant_fp8
+                self.args = [self.out.data_ptr(), self.res.data_ptr(), self.x.data_ptr(), self.w.data_ptr(),
+                             T, W, call.eps, mbd.MODES[call.mode], self.scale.data_ptr()]
+                if call.mode == "dynamic":
+                    self.d2h.append((self.scale, torch.empty_like(self.scale, device="cpu").pin_memory()))
+            self.d2h.append((self.res, torch.empty_like(self.res, device="cpu").pin_memory()))
+        else:
+            self.gu = u16(inp.gate_up).to(dev)
+            self.h2d.append((self.gu, u16(inp.gate_up).pin_memory()))
+            if call.kind == "swiglu":
+                self.out = torch.empty((T, W), dtype=torch.int16, device=dev)
+                self.fn = mbd.get_lib().mbd_swiglu
+                self.args = [self.out.data_ptr(), self.gu.data_ptr(), T, W]
+            else:
+                self.out = torch.empty((T, W), dtype=torch.uint8, device=dev)
+                self.scale = (torch.tensor([call.static_scale], dtype=torch.float32, device=dev)
+                              if call.mode == "static" else torch.zeros((T,), dtype=torch.float32, device=dev))
+                self.fn = mbd.get_lib().mbd_swiglu_quant_fp8
+                self.args = [self.out.data_ptr(), self.gu.data_ptr(), T, W, mbd.MODES[call.mode],
+                             self.scale.data_ptr()]
+                if call.mode == "dynamic":
+                    self.d2h.append((self.scale, torch.empty_like(self.scale, device="cpu").pin_memory()))
+        self.d2h.append((self.out, torch.empty_like(self.out, device="cpu").pin_memory()))
+
+    def bind(self, stream_handle: int):
+        import ctypes
+        args = list(self.args)
+        if self.call.kind in ("add_rmsnorm", "add_rmsnorm_q8"):
+            args[6] = ctypes.c_float(args[6])
+        self.bound = tuple(args) + (stream_handle,)
+
+    def launch(self):
+        rc = self.fn(*self.bound)
+        if rc != 0:
+            raise RuntimeError(f"{self.call.name}: {self.mbd.get_lib().mbd_status_string(rc).decode()}")
+
+    def bytes_in(self):
+        return sum(t.numel() * t.element_size() for t, _ in self.h2d)
+
+    def bytes_out(self):
+        return sum(t.numel() * t.element_size() for t, _ in self.d2h)
+
+
+def run_mine(args, work: wl.Workload, rank: int, world: int, local_rank: int) -> Optional[Dict]:
+    import torch
+    import memory_bound_decoder_gb300 as mbd
+    from memory_bound_decoder_gb300 import build as mbd_build
+    if rank == 0:
+        mbd_build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    mbd.get_lib()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2_bytes = int(getattr(props, "L2_cache_size", 0)) or 126 * 2 ** 20
+
+    t_gen = time.perf_counter()
+    dcalls: List[DeviceCall] = []
+    residual_by_T: Dict[int, object] = {}
+    for layer in range(work.layers):
+        for ci, call in enumerate(work.calls):
+            salt = layer * 64 + ci + 1000 * rank
+            inp = wl.inputs_for(call, seed=args.seed, salt=salt)
+            shared = None
+            if work.layers > 1 and call.kind.startswith("add"):
+                if call.T not in residual_by_T:
+                    residual_by_T[call.T] = torch.from_numpy(inp.residual.view(np.int16)).to(dev)
+                shared = residual_by_T[call.T]
+            dcalls.append(DeviceCall(torch, mbd, call, inp, dev, shared))
+    log(f"[bench] rank {rank}: inputs for {len(dcalls)} launches ready in {time.perf_counter() - t_gen:.1f}s")
+
+    stream = torch.cuda.Stream(device=dev)
+    handle = int(stream.cuda_stream)
+    for d in dcalls:
+        d.bind(handle)
+    step_bytes = work.algorithmic_bytes()
+
+    def step():
+        for d in dcalls:
+            d.launch()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize(dev)
+
+    # per-launch breakdown (untimed pass): CUDA events around every launch on the launch stream
+    nb = max(3, min(20, args.steps))
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in dcalls]
+           for _ in range(nb)]
+    with torch.cuda.stream(stream):
+        for k in range(nb):
+            for d, (a, b) in zip(dcalls, evs[k]):
+                a.record(stream)
+                d.launch()
+                b.record(stream)
+    torch.cuda.synchronize(dev)
+    per_call_ms = [statistics.median(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(nb))
+                   for i in range(len(dcalls))]
+    dom = int(np.argmax(per_call_ms))
+
+    # timed region: exactly K steps; events around the dominant launch in every step
+    clock = ClockSampler(str(getattr(props, "uuid", ""))) if rank == 0 else None
+    dom_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if clock:
+        clock.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = mbd.kernel_launches()
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for k in range(args.steps):
+            for i, d in enumerate(dcalls):
+                if i == dom:
+                    dom_ev[k][0].record(stream)
+                    d.launch()
+                    dom_ev[k][1].record(stream)
+                else:
+                    d.launch()
+        ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    launches = mbd.kernel_launches() - launches0
+    elapsed_ms = ev0.elapsed_time(ev1)
+    clocks = clock.stop(t0, t1) if clock else None
+    dom_ms = statistics.mean(a.elapsed_time(b) for a, b in dom_ev)
+
+    if world > 1:
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    # end-to-end leg through the same public entry points, host buffers, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        ke = max(1, min(args.steps, args.e2e_steps))
+        with torch.cuda.stream(stream):
+            for d in dcalls:   # one untimed round trip to warm the copy engines
+                for dt_, ht in d.h2d:
+                    dt_.copy_(ht, non_blocking=True)
+            torch.cuda.synchronize(dev)
+            if world > 1:
+                torch.distributed.barrier()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(ke):
+                for d in dcalls:
+                    for dt_, ht in d.h2d:
+                        dt_.copy_(ht, non_blocking=True)
+                    d.launch()
+                    for dt_, ht in d.d2h:
+                        ht.copy_(dt_, non_blocking=True)
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": round(step_bytes * ke * world / (e_ms / 1e3) / 1e9, 3), "unit": UNIT,
+               "h2d_bytes_per_step": sum(d.bytes_in() for d in dcalls),
+               "d2h_bytes_per_step": sum(d.bytes_out() for d in dcalls),
+               "steps": ke, "ms_per_step": round(e_ms / ke, 4),
+               "path": "pinned host inputs -> H2D copy -> C-ABI launch -> D2H copy of every output, one stream"}
+
+    if rank != 0:
+        return None
+
+    peak, peak_kind = measured_peak()
+    dcall = dcalls[dom]
+    dom_bytes = dcall.call.algorithmic_bytes()
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    kname = f"{dcall.call.kind}{'_' + dcall.call.mode if dcall.call.mode else ''}"
+    tr = TRAFFIC.get(dcall.call.name)
+    traffic = tr["bytes"] if tr and tr.get("csrc_sha256") == csrc_hash() else None
+    kernels = []
+    seen = set()
+    for i, d in enumerate(dcalls):
+        if d.call.name in seen:
+            continue
+        seen.add(d.call.name)
+        idx = [j for j, e in enumerate(dcalls) if e.call.name == d.call.name]
+        ms = statistics.mean(per_call_ms[j] for j in idx)
+        b = d.call.algorithmic_bytes()
+        kernels.append({"call": d.call.name, "us": round(ms * 1e3, 2), "GBps": round(b / (ms / 1e3) / 1e9, 1),
+                        "frac_of_measured_peak": round(b / (ms / 1e3) / 1e9 / peak, 4),
+                        "tokens_per_s": round(d.call.T / (ms / 1e3), 1), "bytes": b, "launches_per_step": len(idx)})
+    tokens = work.tokens()
+    result = {
+        "metric": METRIC, "value": round(step_bytes * args.steps * world / (elapsed_ms / 1e3) / 1e9, 3),
+        "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(elapsed_ms / args.steps, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": work.key, "description": work.description,
+                   "calls": [c.name for c in work.calls], "layers": work.layers, "seed": args.seed,
+                   "bytes_per_step": step_bytes, "tokens_per_step": tokens,
+                   "io": "bf16 inputs; bf16 or E4M3 outputs; fp32 arithmetic",
+                   "l2": f"inputs larger than L2: {step_bytes / 2 ** 20:.0f} MiB of distinct buffers per step "
+                         f"vs {l2_bytes / 2 ** 20:.0f} MiB L2, no flush",
+                   "parallelism": f"replicas x{world} (rows are independent; no collective)"},
+        "tokens_per_s": round(tokens * args.steps * world / (elapsed_ms / 1e3), 1),
+        "gpu_launches": int(launches),
+        "roofline": {"bound": "hbm", "kernel": dcall.call.name, "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes": dom_bytes, "us_per_launch": round(dom_ms * 1e3, 2),
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                     else "fallback 6.8 TB/s", "frac_of_nominal_8TBps": round(achieved / 8000.0, 4)},
+        "kernels": kernels,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    return result
+
+
+# ------------------------------------------------------------------------------------------------ main
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    help="one of: " + ", ".join(list(workloads_by_key()) + ["qwen2.5-1.5b_decode_sweep"]))
+    ap.add_argument("--calls", default="", help="comma-separated call names: run only these calls of the workload")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=1.0, help="target wall time of the oracle sample")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    work = decode_sweep_workload() if args.workload == "qwen2.5-1.5b_decode_sweep" else workloads_by_key()[args.workload]
+    if args.calls:
+        keep = set(args.calls.split(","))
+        sel = tuple(c for c in work.calls if c.name in keep)
+        if not sel:
+            ap.error(f"--calls matched nothing in {work.key}: " + ", ".join(c.name for c in work.calls))
+        work = wl.Workload(work.key + "[" + args.calls + "]", work.description + " (subset)", sel, work.layers)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        threads = os.cpu_count() or 1
+        total_steps = args.steps + args.warmup
+        per_step = max(0.02, min(2.0, 150.0 / total_steps))
+        frac = calibrate_fraction(work, threads, per_step)
+        s = OracleSample(work, frac, threads, seed=args.seed)
+        for _ in range(args.warmup):
+            s.run()
+        t = time.perf_counter()
+        for _ in range(args.steps):
+            s.run()
+        dt = time.perf_counter() - t
+        value = round(s.bytes * args.steps / dt / 1e9, 5)
+        out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+               "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+               "data": "synthetic",
+               "config": {"workload": work.key, "description": work.description,
+                          "calls": [c.name for c in work.calls], "layers": work.layers, "seed": args.seed},
+               "tokens_per_s": round(s.tokens * args.steps / dt, 2),
+               "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                "sample": s.describe()},
+               "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(out), flush=True)
+        return 0
+
+    import torch
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        res = run_mine(args, work, rank, world, local_rank)
+        if rank == 0 and res is not None:
+            if not args.no_cpu_baseline and world == 1:
+                res["cpu_baseline"] = cpu_baseline(work, args.cpu_seconds)
+            print(json.dumps(res), flush=True)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

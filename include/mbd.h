@@ -1,0 +1,144 @@
+/*
+ * mbd.h -- C ABI of the memory-bound decoder-layer fusion library (GB300, sm_103a).
+ *
+ * Four fused, HBM-bound operations of an LLM decoder layer, each one kernel launch on the caller's stream:
+ *
+ *   mbd_fused_add_rmsnorm            residual <- x + residual; out = RMSNorm(residual) * weight
+ *   mbd_fused_add_rmsnorm_quant_fp8  the same, writing FP8 E4M3 codes of the normalised row instead of bf16
+ *   mbd_swiglu                       out = silu(gate) * up over a stacked gate_up row
+ *   mbd_swiglu_quant_fp8             FP8 E4M3 codes of silu(gate) * up
+ *
+ * Definitions (cited by page title and section):
+ *   [TRT] "TensorRT-LLM: Compiling Inference Engines Ahead of Time", section "Fusing operations, measured":
+ *         RMSNorm as cast to float, square, mean, add epsilon, reciprocal square root, multiply, cast back,
+ *         multiply by the weight; TensorRT-LLM's RMSNorm "adds the residual and normalizes in one kernel";
+ *         the gated MLP runs one gate_up_proj matmul followed by a fused swiglu, g / (1 + exp(-g)) * up.
+ *   [FP8] "TensorRT-LLM" architecture walkthrough, "Part V continued: Deep dive: quantization co-designed
+ *         with the hardware": FP8 E4M3 activations with light per-tensor or per-block scaling.
+ *   [VLLM] "Introduction to torch.compile and How It Works with vLLM", section 3, custom compiler passes:
+ *         FusedKernel(x) = Quantize(SiLU(x)), the activation and its FP8 quantisation fused into one kernel;
+ *         section 4 lists AllReduce + RMSNorm + Quant (FP8) as a further fusion.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers (or managed memory visible to the device), row-major and
+ *     contiguous. bf16 tensors are passed as void* and hold IEEE bfloat16 bit patterns. The caller owns all
+ *     memory: the library allocates nothing, never synchronises, keeps no state between calls (apart from
+ *     a per-device cache of device attributes) and is safe to call from several host threads.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default stream) and runs in stream
+ *     order. Each successful call launches exactly one kernel.
+ *   - Arithmetic is fp32 in registers; every intermediate stays unrounded until the single final rounding
+ *     to bf16 or to E4M3 (round to nearest even, saturating finite overflow to +-448).
+ *   - Scale convention (both FP8 entry points): `scale` is the DEQUANTISATION multiplier, value ~ code * scale.
+ *       MBD_SCALE_STATIC_PER_TENSOR: scale points to ONE fp32 value, read on the device; it must be finite
+ *         and > 0 (0 yields all-zero codes; other values give unspecified codes).
+ *       MBD_SCALE_DYNAMIC_PER_TOKEN: scale points to n_tokens fp32 values that the kernel WRITES:
+ *         scale[t] = amax_t / 448 (fp32) where amax_t is the largest magnitude of row t before quantisation;
+ *         a row with amax_t == 0 gets scale 0 and all-zero codes.
+ *   - Argument errors are detected on the host before anything is launched; nothing is enqueued then.
+ *       MBD_ERR_INVALID_ARG : a null pointer while n_tokens > 0, n_tokens < 0, width <= 0, eps < 0 or not
+ *                             finite, an unknown mode, or overlapping buffers other than the allowed alias.
+ *       MBD_ERR_MISALIGNED  : a tensor pointer not 16-byte aligned, `scale` not 4-byte aligned, or a width
+ *                             not a multiple of 8 elements (one 16-byte vector of bf16).
+ *       MBD_ERR_UNSUPPORTED : a shape beyond the limits stated per entry point.
+ *       MBD_ERR_CUDA        : the launch itself failed; mbd_last_cuda_error() gives the cudaError_t.
+ *     n_tokens == 0 is a no-op returning MBD_OK (pointers are not inspected). Faults during execution
+ *     surface at the caller's next synchronisation, as for any kernel.
+ */
+#ifndef MBD_H
+#define MBD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t (struct CUstream_st*), declared here so that the header needs no CUDA include. */
+typedef struct CUstream_st* mbd_stream_t;
+
+typedef enum {
+    MBD_OK = 0,
+    MBD_ERR_INVALID_ARG = 1,
+    MBD_ERR_MISALIGNED = 2,
+    MBD_ERR_UNSUPPORTED = 3,
+    MBD_ERR_CUDA = 4
+} mbd_status;
+
+typedef enum {
+    MBD_SCALE_STATIC_PER_TENSOR = 0,
+    MBD_SCALE_DYNAMIC_PER_TOKEN = 1
+} mbd_scale_mode;
+
+/* Largest row width (elements) of the entry points that reduce over a row (both norms and
+ * mbd_swiglu_quant_fp8 in dynamic mode); wider rows return MBD_ERR_UNSUPPORTED. */
+#define MBD_MAX_REDUCED_WIDTH 262144
+
+/* ABI version of this header (bumped on any signature change). */
+#define MBD_ABI_VERSION 1
+int mbd_abi_version(void);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char* mbd_status_string(int status);
+
+/* cudaError_t of the most recent MBD_ERR_CUDA returned on the calling host thread (0 if none). */
+int mbd_last_cuda_error(void);
+
+/* Number of kernels this library has launched in the process so far (all threads, all devices). */
+uint64_t mbd_kernel_launches(void);
+
+/*
+ * Fused residual add + RMSNorm [TRT].
+ *   For every row t < n_tokens and column j < hidden:
+ *     s[t,j]        = bf16(x[t,j] + residual[t,j])            (fp32 add, one rounding)
+ *     residual[t,j] = s[t,j]                                  (written back in place)
+ *     inv_t         = 1 / sqrt(sum_j s[t,j]^2 / hidden + eps)
+ *     out[t,j]      = bf16(weight[j] * s[t,j] * inv_t)
+ *   out      : [n_tokens, hidden] bf16, written. May be the same pointer as x (in-place); must not
+ *              overlap residual or weight otherwise.
+ *   residual : [n_tokens, hidden] bf16, read and overwritten with s.
+ *   x        : [n_tokens, hidden] bf16, read.
+ *   weight   : [hidden] bf16, read.
+ *   eps      : >= 0, added to the mean of squares inside the square root.
+ *   Limits   : hidden <= MBD_MAX_REDUCED_WIDTH.
+ */
+mbd_status mbd_fused_add_rmsnorm(void* out, void* residual, const void* x, const void* weight,
+                                 int64_t n_tokens, int64_t hidden, float eps, mbd_stream_t stream);
+
+/*
+ * Fused residual add + RMSNorm + FP8 E4M3 quantisation [TRT], [FP8], [VLLM] (the norm-and-quantise half
+ * of AllReduce + RMSNorm + Quant, on one GPU).
+ *   s, residual and inv_t as in mbd_fused_add_rmsnorm; v[t,j] = weight[j] * s[t,j] * inv_t in fp32 (not
+ *   rounded to bf16), and out_q[t,j] = e4m3(v[t,j] / scale) with the scale of the row (see conventions).
+ *   out_q    : [n_tokens, hidden] uint8 E4M3 codes, written; must not overlap any other argument.
+ *   scale    : static -> [1] fp32 read; dynamic -> [n_tokens] fp32 written (must not overlap others).
+ *   Only the codes are written, not the bf16 normalised row.
+ *   Limits   : hidden <= MBD_MAX_REDUCED_WIDTH.
+ */
+mbd_status mbd_fused_add_rmsnorm_quant_fp8(uint8_t* out_q, void* residual, const void* x,
+                                           const void* weight, int64_t n_tokens, int64_t hidden, float eps,
+                                           mbd_scale_mode mode, float* scale, mbd_stream_t stream);
+
+/*
+ * SwiGLU over the stacked gate_up projection [TRT].
+ *   gate_up : [n_tokens, 2 * inter] bf16, read; columns 0..inter-1 are gate, inter..2*inter-1 are up.
+ *   out     : [n_tokens, inter] bf16, written: out[t,j] = bf16(silu(g) * u), silu(g) = g / (1 + exp(-g)),
+ *             computed in fp32 without rounding silu(g) first. Must not overlap gate_up.
+ */
+mbd_status mbd_swiglu(void* out, const void* gate_up, int64_t n_tokens, int64_t inter, mbd_stream_t stream);
+
+/*
+ * Quantize(SiLU(gate) * up) [VLLM], [FP8].
+ *   h[t,j] = silu(g) * u in fp32 (as mbd_swiglu, not rounded to bf16); out_q[t,j] = e4m3(h[t,j] / scale).
+ *   out_q   : [n_tokens, inter] uint8 E4M3 codes, written; must not overlap gate_up or scale.
+ *   scale   : static -> [1] fp32 read; dynamic -> [n_tokens] fp32 written.
+ *   Limits  : dynamic mode needs inter <= MBD_MAX_REDUCED_WIDTH.
+ */
+mbd_status mbd_swiglu_quant_fp8(uint8_t* out_q, const void* gate_up, int64_t n_tokens, int64_t inter,
+                                mbd_scale_mode mode, float* scale, mbd_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MBD_H */

@@ -1,0 +1,145 @@
+"""Python binding of libmbd, the GB300 library of memory-bound decoder-layer fusions.
+
+Argument marshalling only: every function here converts its arguments (torch tensors or raw integer
+device pointers) and calls the C entry point of the same name (without the `mbd_` prefix), which
+launches one CUDA kernel. Nothing is computed in Python and there is no fallback: if libmbd.so has not
+been built, the first call (or any access to `lib`) raises ImportError.
+
+    import memory_bound_decoder_gb300 as mbd
+    mbd.fused_add_rmsnorm(out, residual, x, weight, T, H, 1e-6)          # tensors on the GPU
+    mbd.swiglu_quant_fp8(q, gate_up, T, I, mbd.DYNAMIC, scales)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Any, List, Optional
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmbd.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "mbd.h")
+
+STATIC = 0   # MBD_SCALE_STATIC_PER_TENSOR
+DYNAMIC = 1  # MBD_SCALE_DYNAMIC_PER_TOKEN
+MODES = {"static": STATIC, "dynamic": DYNAMIC, STATIC: STATIC, DYNAMIC: DYNAMIC}
+
+OK, ERR_INVALID_ARG, ERR_MISALIGNED, ERR_UNSUPPORTED, ERR_CUDA = 0, 1, 2, 3, 4
+
+
+class MbdError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with memory_bound_decoder_gb300.build.build() "
+                          "(there is no non-CUDA fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i64, f32, cint = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int
+    lib.mbd_abi_version.restype = cint
+    lib.mbd_status_string.argtypes, lib.mbd_status_string.restype = [cint], ctypes.c_char_p
+    lib.mbd_last_cuda_error.restype = cint
+    lib.mbd_kernel_launches.restype = ctypes.c_uint64
+    lib.mbd_fused_add_rmsnorm.argtypes = [vp, vp, vp, vp, i64, i64, f32, vp]
+    lib.mbd_fused_add_rmsnorm_quant_fp8.argtypes = [vp, vp, vp, vp, i64, i64, f32, cint, vp, vp]
+    lib.mbd_swiglu.argtypes = [vp, vp, i64, i64, vp]
+    lib.mbd_swiglu_quant_fp8.argtypes = [vp, vp, i64, i64, cint, vp, vp]
+    for fn in ("mbd_fused_add_rmsnorm", "mbd_fused_add_rmsnorm_quant_fp8", "mbd_swiglu", "mbd_swiglu_quant_fp8"):
+        getattr(lib, fn).restype = cint
+    return lib
+
+
+_LIB: Optional[ctypes.CDLL] = None
+
+
+def get_lib() -> ctypes.CDLL:
+    """The loaded libmbd.so (loaded on first use; ImportError if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        _LIB = _load()
+    return _LIB
+
+
+def __getattr__(name: str):
+    if name == "lib":
+        return get_lib()
+    raise AttributeError(name)
+
+
+def header_functions() -> List[str]:
+    """Names of the functions include/mbd.h declares."""
+    with open(HEADER_PATH) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mbd_[a-z0-9_]+)\s*\(", text)))
+
+
+def _ptr(a: Any) -> Optional[int]:
+    if a is None:
+        return None
+    if isinstance(a, int):
+        return a
+    dp = getattr(a, "data_ptr", None)
+    if dp is not None:
+        return int(dp())
+    raise TypeError(f"expected a tensor or an integer device pointer, got {type(a).__name__}")
+
+
+def _mode(mode: Any) -> int:
+    """'static' / 'dynamic' or the integer enum value (passed through unchanged for the library to check)."""
+    return MODES[mode] if isinstance(mode, str) else int(mode)
+
+
+def _stream(stream: Any) -> Optional[int]:
+    if stream is None:
+        try:
+            import torch
+            if torch.cuda.is_available() and torch.cuda.is_initialized():
+                return int(torch.cuda.current_stream().cuda_stream)
+        except ImportError:
+            pass
+        return None
+    if isinstance(stream, int):
+        return stream
+    return int(getattr(stream, "cuda_stream"))
+
+
+def _check(status: int, fn: str) -> None:
+    if status != OK:
+        lib = get_lib()
+        msg = lib.mbd_status_string(status).decode()
+        if status == ERR_CUDA:
+            msg += f" (cudaError {lib.mbd_last_cuda_error()})"
+        raise MbdError(status, f"{fn}: {msg}")
+
+
+def abi_version() -> int:
+    return get_lib().mbd_abi_version()
+
+
+def kernel_launches() -> int:
+    return int(get_lib().mbd_kernel_launches())
+
+
+def fused_add_rmsnorm(out, residual, x, weight, n_tokens: int, hidden: int, eps: float, stream=None) -> None:
+    _check(get_lib().mbd_fused_add_rmsnorm(_ptr(out), _ptr(residual), _ptr(x), _ptr(weight), int(n_tokens),
+                                     int(hidden), float(eps), _stream(stream)), "fused_add_rmsnorm")
+
+
+def fused_add_rmsnorm_quant_fp8(out_q, residual, x, weight, n_tokens: int, hidden: int, eps: float, mode,
+                                scale, stream=None) -> None:
+    _check(get_lib().mbd_fused_add_rmsnorm_quant_fp8(_ptr(out_q), _ptr(residual), _ptr(x), _ptr(weight),
+                                               int(n_tokens), int(hidden), float(eps), _mode(mode),
+                                               _ptr(scale), _stream(stream)), "fused_add_rmsnorm_quant_fp8")
+
+
+def swiglu(out, gate_up, n_tokens: int, inter: int, stream=None) -> None:
+    _check(get_lib().mbd_swiglu(_ptr(out), _ptr(gate_up), int(n_tokens), int(inter), _stream(stream)), "swiglu")
+
+
+def swiglu_quant_fp8(out_q, gate_up, n_tokens: int, inter: int, mode, scale, stream=None) -> None:
+    _check(get_lib().mbd_swiglu_quant_fp8(_ptr(out_q), _ptr(gate_up), int(n_tokens), int(inter), _mode(mode),
+                                    _ptr(scale), _stream(stream)), "swiglu_quant_fp8")

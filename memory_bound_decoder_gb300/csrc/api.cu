@@ -1,0 +1,199 @@
+// C ABI of the fusion library: host-side argument checks, launch-shape selection and dispatch.
+// Every check runs before anything is enqueued; a failing call launches nothing.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/mbd.h"
+#include "launch.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+std::atomic<uint64_t> g_launches{0};
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];  // 0 = not queried yet
+
+int sm_count_of_current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+    int n = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();
+        return 148;
+    }
+    g_sm_count[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Half-open byte ranges [a, a + na) and [b, b + nb) intersect.
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return na > 0 && nb > 0 && x < y + nb && y < x + na;
+}
+
+constexpr int kMaxClusterCtas = 8;   // portable cluster size
+constexpr int kMaxThreads = 512;     // matches __launch_bounds__ of the kernels
+
+// Choose how a launch covers [rows, nvec]. Large batches give each row one CTA (no cluster traffic);
+// small batches split each row over a cluster so that enough SMs pull bytes from HBM at once. A CTA aims
+// for at most 256 threads and picks the fewest vectors per thread that keeps it there.
+bool plan_rows(int64_t rows, int nvec, bool reduces, int sms, mbd::RowPlan* plan) {
+    const int max_cta_vec = 256 * 4;
+    int c = (nvec + max_cta_vec - 1) / max_cta_vec;
+    if (rows < sms) {
+        int want = static_cast<int>((2 * sms + rows - 1) / rows);  // about two CTAs per SM
+        int by_width = (nvec + 31) / 32;                          // keep at least a warp of vectors per CTA
+        if (want > by_width) want = by_width;
+        if (want > c) c = want;
+    }
+    if (reduces && c > kMaxClusterCtas) {
+        c = kMaxClusterCtas;
+    }
+    if (c < 1) c = 1;
+    const int slice = (nvec + c - 1) / c;
+    int vpt = 8;
+    for (int v : {1, 2, 4, 8}) {
+        if ((slice + v - 1) / v <= 256) { vpt = v; break; }
+    }
+    int threads = (slice + vpt - 1) / vpt;
+    threads = (threads + 31) / 32 * 32;
+    if (threads > kMaxThreads) return false;
+    plan->ctas_per_row = c;
+    plan->slice = slice;
+    plan->threads = threads;
+    plan->vpt = vpt;
+    return (rows * c) < (int64_t{1} << 31);
+}
+
+mbd_status finish_launch(cudaError_t e) {
+    if (e != cudaSuccess) {
+        g_last_cuda_error = static_cast<int>(e);
+        (void)cudaGetLastError();
+        return MBD_ERR_CUDA;
+    }
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return MBD_OK;
+}
+
+mbd_status check_width(int64_t n_tokens, int64_t width) {
+    if (n_tokens < 0 || width <= 0) return MBD_ERR_INVALID_ARG;
+    if (width % 8 != 0) return MBD_ERR_MISALIGNED;
+    if (width > (int64_t{1} << 28)) return MBD_ERR_UNSUPPORTED;
+    return MBD_OK;
+}
+
+mbd_status norm_common(void* out, size_t out_elem, void* residual, const void* x, const void* weight,
+                       int64_t n_tokens, int64_t hidden, float eps, float* scale, int mode, bool quant,
+                       cudaStream_t stream) {
+    mbd_status st = check_width(n_tokens, hidden);
+    if (st != MBD_OK) return st;
+    if (!(eps >= 0.0f) || !std::isfinite(eps)) return MBD_ERR_INVALID_ARG;
+    if (quant && mode != MBD_SCALE_STATIC_PER_TENSOR && mode != MBD_SCALE_DYNAMIC_PER_TOKEN)
+        return MBD_ERR_INVALID_ARG;
+    if (hidden > MBD_MAX_REDUCED_WIDTH) return MBD_ERR_UNSUPPORTED;
+    if (n_tokens == 0) return MBD_OK;
+    if (!out || !residual || !x || !weight || (quant && !scale)) return MBD_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(residual, 16) || !aligned(x, 16) || !aligned(weight, 16) ||
+        (quant && !aligned(scale, 4)))
+        return MBD_ERR_MISALIGNED;
+    const size_t act = static_cast<size_t>(n_tokens) * static_cast<size_t>(hidden) * 2;
+    const size_t outb = static_cast<size_t>(n_tokens) * static_cast<size_t>(hidden) * out_elem;
+    const size_t wb = static_cast<size_t>(hidden) * 2;
+    const bool dyn = quant && mode == MBD_SCALE_DYNAMIC_PER_TOKEN;
+    const size_t sb = quant ? (dyn ? static_cast<size_t>(n_tokens) * 4 : 4) : 0;
+    if (overlap(residual, act, x, act) || overlap(residual, act, weight, wb)) return MBD_ERR_INVALID_ARG;
+    if (overlap(out, outb, residual, act) || overlap(out, outb, weight, wb)) return MBD_ERR_INVALID_ARG;
+    // out may alias x exactly (bf16 only); any other overlap with x is rejected
+    if (overlap(out, outb, x, act) && !(!quant && out == x)) return MBD_ERR_INVALID_ARG;
+    if (dyn && (overlap(scale, sb, out, outb) || overlap(scale, sb, residual, act) ||
+                overlap(scale, sb, x, act) || overlap(scale, sb, weight, wb)))
+        return MBD_ERR_INVALID_ARG;
+    if (quant && !dyn && overlap(scale, sb, out, outb)) return MBD_ERR_INVALID_ARG;
+
+    mbd::RowPlan plan;
+    if (!plan_rows(n_tokens, static_cast<int>(hidden / 8), true, sm_count_of_current_device(), &plan))
+        return MBD_ERR_UNSUPPORTED;
+    mbd::NormParams p{x, residual, weight, out, scale, n_tokens, static_cast<int>(hidden / 8),
+                      static_cast<int>(hidden), eps};
+    const mbd::Epilogue ep = !quant ? mbd::kBf16 : (dyn ? mbd::kFp8Dynamic : mbd::kFp8Static);
+    return finish_launch(mbd::launch_add_rmsnorm(p, ep, plan, stream));
+}
+
+mbd_status swiglu_common(void* out, size_t out_elem, const void* gate_up, int64_t n_tokens, int64_t inter,
+                         float* scale, int mode, bool quant, cudaStream_t stream) {
+    mbd_status st = check_width(n_tokens, inter);
+    if (st != MBD_OK) return st;
+    if (quant && mode != MBD_SCALE_STATIC_PER_TENSOR && mode != MBD_SCALE_DYNAMIC_PER_TOKEN)
+        return MBD_ERR_INVALID_ARG;
+    const bool dyn = quant && mode == MBD_SCALE_DYNAMIC_PER_TOKEN;
+    if (dyn && inter > MBD_MAX_REDUCED_WIDTH) return MBD_ERR_UNSUPPORTED;
+    if (n_tokens == 0) return MBD_OK;
+    if (!out || !gate_up || (quant && !scale)) return MBD_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(gate_up, 16) || (quant && !aligned(scale, 4))) return MBD_ERR_MISALIGNED;
+    const size_t inb = static_cast<size_t>(n_tokens) * static_cast<size_t>(inter) * 4;
+    const size_t outb = static_cast<size_t>(n_tokens) * static_cast<size_t>(inter) * out_elem;
+    const size_t sb = quant ? (dyn ? static_cast<size_t>(n_tokens) * 4 : 4) : 0;
+    if (overlap(out, outb, gate_up, inb)) return MBD_ERR_INVALID_ARG;
+    if (quant && overlap(scale, sb, out, outb)) return MBD_ERR_INVALID_ARG;
+    if (dyn && overlap(scale, sb, gate_up, inb)) return MBD_ERR_INVALID_ARG;
+
+    mbd::RowPlan plan;
+    if (!plan_rows(n_tokens, static_cast<int>(inter / 8), dyn, sm_count_of_current_device(), &plan))
+        return MBD_ERR_UNSUPPORTED;
+    mbd::SwigluParams p{gate_up, out, scale, n_tokens, static_cast<int>(inter / 8)};
+    const mbd::Epilogue ep = !quant ? mbd::kBf16 : (dyn ? mbd::kFp8Dynamic : mbd::kFp8Static);
+    return finish_launch(mbd::launch_swiglu(p, ep, plan, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int mbd_abi_version(void) { return MBD_ABI_VERSION; }
+
+const char* mbd_status_string(int status) {
+    switch (status) {
+        case MBD_OK: return "MBD_OK";
+        case MBD_ERR_INVALID_ARG: return "MBD_ERR_INVALID_ARG: invalid argument";
+        case MBD_ERR_MISALIGNED: return "MBD_ERR_MISALIGNED: pointer or width not aligned to 16 bytes";
+        case MBD_ERR_UNSUPPORTED: return "MBD_ERR_UNSUPPORTED: shape beyond the library's limits";
+        case MBD_ERR_CUDA: return "MBD_ERR_CUDA: kernel launch failed (see mbd_last_cuda_error)";
+        default: return "unknown mbd_status";
+    }
+}
+
+int mbd_last_cuda_error(void) { return g_last_cuda_error; }
+
+uint64_t mbd_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+mbd_status mbd_fused_add_rmsnorm(void* out, void* residual, const void* x, const void* weight,
+                                 int64_t n_tokens, int64_t hidden, float eps, mbd_stream_t stream) {
+    return norm_common(out, 2, residual, x, weight, n_tokens, hidden, eps, nullptr, 0, false,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+mbd_status mbd_fused_add_rmsnorm_quant_fp8(uint8_t* out_q, void* residual, const void* x,
+                                           const void* weight, int64_t n_tokens, int64_t hidden, float eps,
+                                           mbd_scale_mode mode, float* scale, mbd_stream_t stream) {
+    return norm_common(out_q, 1, residual, x, weight, n_tokens, hidden, eps, scale, static_cast<int>(mode),
+                       true, reinterpret_cast<cudaStream_t>(stream));
+}
+
+mbd_status mbd_swiglu(void* out, const void* gate_up, int64_t n_tokens, int64_t inter, mbd_stream_t stream) {
+    return swiglu_common(out, 2, gate_up, n_tokens, inter, nullptr, 0, false,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+mbd_status mbd_swiglu_quant_fp8(uint8_t* out_q, const void* gate_up, int64_t n_tokens, int64_t inter,
+                                mbd_scale_mode mode, float* scale, mbd_stream_t stream) {
+    return swiglu_common(out_q, 1, gate_up, n_tokens, inter, scale, static_cast<int>(mode), true,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

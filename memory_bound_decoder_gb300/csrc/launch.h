@@ -1,0 +1,48 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mbd {
+
+// Output variant of a fused kernel.
+enum Epilogue : int { kBf16 = 0, kFp8Static = 1, kFp8Dynamic = 2 };
+
+// How one launch covers the [rows, nvec] problem (nvec = row width / 8, one 16-byte bf16 vector each):
+// every row is split into `ctas_per_row` slices of `slice` vectors (the last may be shorter), one CTA per
+// slice; a CTA of `threads` threads gives each thread up to `vpt` vectors strided by `threads`.
+// If the epilogue reduces over the row and ctas_per_row > 1, the CTAs of a row form one thread-block
+// cluster and combine their partial results through distributed shared memory.
+struct RowPlan {
+    int ctas_per_row;
+    int slice;
+    int threads;
+    int vpt;  // 1, 2, 4 or 8
+};
+
+struct NormParams {
+    const void* x;
+    void* residual;
+    const void* weight;
+    void* out;       // bf16 [T, H] or uint8 codes [T, H]
+    float* scale;    // static: [1] read; dynamic: [T] written; unused for bf16
+    int64_t rows;
+    int nvec;
+    int hidden;
+    float eps;
+};
+
+struct SwigluParams {
+    const void* gate_up;
+    void* out;       // bf16 [T, I] or uint8 codes [T, I]
+    float* scale;
+    int64_t rows;
+    int nvec;        // I / 8
+};
+
+// Launchers: return the cudaError_t of the launch (cudaSuccess when enqueued).
+cudaError_t launch_add_rmsnorm(const NormParams& p, Epilogue ep, const RowPlan& plan, cudaStream_t s);
+cudaError_t launch_swiglu(const SwigluParams& p, Epilogue ep, const RowPlan& plan, cudaStream_t s);
+
+}  // namespace mbd

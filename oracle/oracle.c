@@ -57,8 +57,8 @@ uint16_t orc_bf16_round(double v) {
  * E == 0 is subnormal (M / 8 * 2^-6), otherwise (1 + M / 8) * 2^(E - 7). */
 static double e4m3_magnitude(int c) {
     int E = c >> 3, M = c & 7;
-    if (E == 0) return ldexp((double)M, -9);
-    return ldexp((double)(8 + M), E - 10);
+    if (E == 0) return (double)M / 512.0;
+    return (double)(8 + M) * (double)(1u << E) / 1024.0; /* exact: small integers and powers of two */
 }
 
 double orc_e4m3_decode(uint8_t code) {

@@ -1,0 +1,107 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports every function the header
+declares, and rejects invalid arguments before touching the device (the checks under test all fail
+before any CUDA call, so fake pointer values are safe here)."""
+import ctypes
+import re
+
+import pytest
+
+import memory_bound_decoder_gb300 as mbd
+from memory_bound_decoder_gb300 import build as mbd_build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mbd_build.build()
+    return mbd.get_lib()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = mbd.header_functions()
+    assert set(names) >= {"mbd_fused_add_rmsnorm", "mbd_fused_add_rmsnorm_quant_fp8", "mbd_swiglu",
+                          "mbd_swiglu_quant_fp8", "mbd_status_string", "mbd_abi_version",
+                          "mbd_last_cuda_error", "mbd_kernel_launches"}
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_binding_names_match_header():
+    for n in mbd.header_functions():
+        short = n[len("mbd_"):]
+        if short in ("status_string", "last_cuda_error"):
+            continue
+        assert hasattr(mbd, short), short
+
+
+def test_version_and_status_strings(lib):
+    assert lib.mbd_abi_version() == 1
+    hdr = open(mbd.HEADER_PATH).read()
+    assert int(re.search(r"#define MBD_ABI_VERSION (\d+)", hdr).group(1)) == 1
+    for code in range(5):
+        assert lib.mbd_status_string(code).decode().startswith("MBD_")
+    assert lib.mbd_status_string(99) == b"unknown mbd_status"
+    assert lib.mbd_last_cuda_error() == 0
+
+
+A = 1 << 20   # a fake, 16-byte aligned "device pointer" (never dereferenced: validation fails first)
+
+
+def _rc(fn, *args):
+    with pytest.raises(mbd.MbdError) as e:
+        fn(*args)
+    return e.value.status
+
+
+def test_zero_tokens_is_a_noop(lib):
+    n0 = mbd.kernel_launches()
+    mbd.fused_add_rmsnorm(None, None, None, None, 0, 4096, 1e-6)
+    mbd.fused_add_rmsnorm_quant_fp8(None, None, None, None, 0, 4096, 1e-6, "dynamic", None)
+    mbd.swiglu(None, None, 0, 14336)
+    mbd.swiglu_quant_fp8(None, None, 0, 14336, "static", None)
+    assert mbd.kernel_launches() == n0
+
+
+def test_invalid_arguments(lib):
+    f = mbd.fused_add_rmsnorm
+    assert _rc(f, A, 2 * A, 3 * A, 4 * A, -1, 64, 1e-6) == mbd.ERR_INVALID_ARG
+    assert _rc(f, A, 2 * A, 3 * A, 4 * A, 4, 0, 1e-6) == mbd.ERR_INVALID_ARG
+    assert _rc(f, A, 2 * A, 3 * A, 4 * A, 4, 64, -1.0) == mbd.ERR_INVALID_ARG
+    assert _rc(f, A, 2 * A, 3 * A, 4 * A, 4, 64, float("nan")) == mbd.ERR_INVALID_ARG
+    assert _rc(f, None, 2 * A, 3 * A, 4 * A, 4, 64, 1e-6) == mbd.ERR_INVALID_ARG
+    assert _rc(f, A, 2 * A, 3 * A, None, 4, 64, 1e-6) == mbd.ERR_INVALID_ARG
+    # overlapping residual and x
+    assert _rc(f, A, 2 * A, 2 * A + 64, 4 * A, 4, 64, 1e-6) == mbd.ERR_INVALID_ARG
+    # out overlapping x without being equal to it
+    assert _rc(f, 3 * A + 16, 2 * A, 3 * A, 4 * A, 4, 64, 1e-6) == mbd.ERR_INVALID_ARG
+    q = mbd.fused_add_rmsnorm_quant_fp8
+    assert _rc(q, A, 2 * A, 3 * A, 4 * A, 4, 64, 1e-6, 7, 5 * A) == mbd.ERR_INVALID_ARG
+    assert _rc(q, A, 2 * A, 3 * A, 4 * A, 4, 64, 1e-6, "static", None) == mbd.ERR_INVALID_ARG
+    assert _rc(q, 3 * A, 2 * A, 3 * A, 4 * A, 4, 64, 1e-6, "static", 5 * A) == mbd.ERR_INVALID_ARG  # out_q == x
+    s = mbd.swiglu
+    assert _rc(s, A, A + 64, 4, 64) == mbd.ERR_INVALID_ARG        # out overlaps gate_up
+    sq = mbd.swiglu_quant_fp8
+    assert _rc(sq, A, 2 * A, 4, 64, "dynamic", A + 8) == mbd.ERR_INVALID_ARG   # scale inside out_q
+
+
+def test_misaligned(lib):
+    f = mbd.fused_add_rmsnorm
+    assert _rc(f, A + 2, 2 * A, 3 * A, 4 * A, 4, 64, 1e-6) == mbd.ERR_MISALIGNED
+    assert _rc(f, A, 2 * A, 3 * A + 8, 4 * A, 4, 64, 1e-6) == mbd.ERR_MISALIGNED
+    assert _rc(f, A, 2 * A, 3 * A, 4 * A, 4, 60, 1e-6) == mbd.ERR_MISALIGNED        # width % 8
+    assert _rc(mbd.swiglu, A, 2 * A, 4, 100) == mbd.ERR_MISALIGNED
+    assert _rc(mbd.swiglu_quant_fp8, A, 2 * A, 4, 64, "dynamic", 5 * A + 2) == mbd.ERR_MISALIGNED
+
+
+def test_unsupported_widths(lib):
+    wide = 262144 + 8
+    assert _rc(mbd.fused_add_rmsnorm, A, 2 * A, 3 * A, 4 * A, 0, wide, 1e-6) == mbd.ERR_UNSUPPORTED
+    assert _rc(mbd.swiglu_quant_fp8, A, 2 * A, 0, wide, "dynamic", 5 * A) == mbd.ERR_UNSUPPORTED
+    # the pure streams have no such limit: zero tokens with a wide row is a no-op
+    mbd.swiglu(None, None, 0, wide)
+    mbd.swiglu_quant_fp8(None, None, 0, wide, "static", None)
+
+
+def test_raw_ctypes_signature(lib):
+    # the C entry points are callable without the Python binding
+    fn = lib.mbd_swiglu
+    assert fn(None, None, ctypes.c_int64(0), ctypes.c_int64(64), None) == 0

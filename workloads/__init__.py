@@ -4,7 +4,9 @@ This module holds no arithmetic of the method itself: it only draws random numbe
 bf16 input type and describes the workload shapes. Both sides (the CUDA path and the CPU oracle) receive
 the same bf16 bit patterns from here.
 
-Recipe (one Philox stream per tensor, keyed by (seed, tensor id)):
+Recipe (counter-style streams: one PCG64 stream per block of ROWS_PER_BLOCK rows of each tensor, keyed by
+(seed, tensor id, salt, block index), so the values do not depend on how many threads fill the tensor and
+any subset of rows can be regenerated on its own):
   * activations x, residual r, gate_up: float32 draws from N(0, sigma^2); optionally each element is
     multiplied, independently with probability p, by an outlier factor k;
   * RMSNorm weight: 1 + 0.1 * N(0, 1);
@@ -15,23 +17,37 @@ no dataset or trained weight is used.
 """
 from __future__ import annotations
 
-from dataclasses import dataclass, field
+import os
+from dataclasses import dataclass
 from typing import Dict, List, Optional, Tuple
 
 import numpy as np
 
-# tensor ids for the per-tensor Philox key
+# tensor ids for the per-tensor stream key
 _TID = {"x": 1, "residual": 2, "weight": 3, "gate_up": 4}
 
 
+ROWS_PER_BLOCK = 8
+_POOL = None
+
+
+def _pool():
+    global _POOL
+    if _POOL is None:
+        import concurrent.futures as cf
+        _POOL = cf.ThreadPoolExecutor(max_workers=max(1, min(32, os.cpu_count() or 1)))
+    return _POOL
+
+
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
-    """Round float32 values to bf16 (nearest, ties to even) and return the 16-bit patterns as uint16."""
-    a = np.ascontiguousarray(a, dtype=np.float32)
-    u = a.view(np.uint32).astype(np.uint64)
-    lsb = (u >> np.uint64(16)) & np.uint64(1)
-    rounded = (u + np.uint64(0x7FFF) + lsb) >> np.uint64(16)
-    out = rounded.astype(np.uint16)
-    nan = np.isnan(a)
+    """Round finite float32 values to bf16 (nearest, ties to even) and return the 16-bit patterns."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    r = u + lsb
+    r += np.uint32(0x7FFF)          # finite patterns stay below 2^32 after the increment
+    r >>= np.uint32(16)
+    out = r.astype(np.uint16)
+    nan = np.isnan(np.asarray(a, np.float32))
     if nan.any():
         out[nan] = np.uint16(0x7FC0)
     return out
@@ -42,26 +58,49 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     return (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
-def _rng(seed: int, tensor: str, salt: int = 0) -> np.random.Generator:
-    return np.random.Generator(np.random.Philox(key=[int(seed), _TID[tensor] * 1000003 + int(salt)]))
+def _block_rng(seed: int, tensor: str, salt: int, block: int) -> np.random.Generator:
+    ss = np.random.SeedSequence(entropy=int(seed), spawn_key=(_TID[tensor], int(salt), int(block)))
+    return np.random.Generator(np.random.PCG64(ss))
 
 
-def normal_bf16(shape: Tuple[int, ...], seed: int, tensor: str, sigma: float = 1.0,
-                outlier_p: float = 0.0, outlier_k: float = 1.0, salt: int = 0) -> np.ndarray:
-    """bf16 bits of N(0, sigma^2) draws, each element independently scaled by outlier_k with prob. outlier_p."""
-    g = _rng(seed, tensor, salt)
+def _fill_block(out2d, seed, tensor, salt, block, sigma, outlier_p, outlier_k, rows_lo, rows_hi):
+    g = _block_rng(seed, tensor, salt, block)
+    shape = (rows_hi - rows_lo, out2d.shape[1])
     v = g.standard_normal(size=shape, dtype=np.float32)
     if sigma != 1.0:
         v *= np.float32(sigma)
     if outlier_p > 0.0:
         m = g.random(size=shape, dtype=np.float32) < np.float32(outlier_p)
         v[m] *= np.float32(outlier_k)
-    return f32_to_bf16_bits(v)
+    out2d[rows_lo:rows_hi] = f32_to_bf16_bits(v)
+
+
+def normal_bf16(shape: Tuple[int, ...], seed: int, tensor: str, sigma: float = 1.0,
+                outlier_p: float = 0.0, outlier_k: float = 1.0, salt: int = 0,
+                rows: Optional[np.ndarray] = None) -> np.ndarray:
+    """bf16 bits of N(0, sigma^2) draws, each element independently scaled by outlier_k with prob. outlier_p.
+    With `rows`, only those rows of the full tensor are returned (identical to slicing the full tensor)."""
+    T, W = (1, shape[0]) if len(shape) == 1 else shape
+    full = np.empty((T, W), np.uint16)
+    blocks = range((T + ROWS_PER_BLOCK - 1) // ROWS_PER_BLOCK)
+    if rows is not None:
+        rows = np.asarray(rows, np.int64)
+        blocks = sorted({int(r) // ROWS_PER_BLOCK for r in rows})
+    jobs = [(full, seed, tensor, salt, b, sigma, outlier_p, outlier_k, b * ROWS_PER_BLOCK,
+             min(T, (b + 1) * ROWS_PER_BLOCK)) for b in blocks]
+    if len(jobs) <= 2:
+        for j in jobs:
+            _fill_block(*j)
+    else:
+        list(_pool().map(lambda j: _fill_block(*j), jobs))
+    if rows is not None:
+        return full[rows]
+    return full.reshape(shape)
 
 
 def weight_bf16(hidden: int, seed: int, salt: int = 0) -> np.ndarray:
     """bf16 bits of an RMSNorm weight 1 + 0.1 * N(0, 1)."""
-    g = _rng(seed, "weight", salt)
+    g = _block_rng(seed, "weight", salt, 0)
     v = np.float32(1.0) + np.float32(0.1) * g.standard_normal(size=(hidden,), dtype=np.float32)
     return f32_to_bf16_bits(v)
 
@@ -86,16 +125,20 @@ class SwigluInputs:
     gate_up: np.ndarray    # [T, 2I] uint16: gate = columns 0..I-1, up = columns I..2I-1
 
 
-def make_norm_inputs(T: int, H: int, seed: int, dist: Dist, eps: float, salt: int = 0) -> NormInputs:
-    x = normal_bf16((T, H), seed, "x", dist.sigma, dist.outlier_p, dist.outlier_k, salt)
-    r = normal_bf16((T, H), seed, "residual", dist.sigma, dist.outlier_p, dist.outlier_k, salt)
+def make_norm_inputs(T: int, H: int, seed: int, dist: Dist, eps: float, salt: int = 0,
+                     rows: Optional[np.ndarray] = None) -> NormInputs:
+    """Inputs of one fused add+RMSNorm call; with `rows`, only those rows of x and residual."""
+    x = normal_bf16((T, H), seed, "x", dist.sigma, dist.outlier_p, dist.outlier_k, salt, rows)
+    r = normal_bf16((T, H), seed, "residual", dist.sigma, dist.outlier_p, dist.outlier_k, salt, rows)
     w = weight_bf16(H, seed, salt)
     return NormInputs(x, r, w, float(eps))
 
 
-def make_swiglu_inputs(T: int, I: int, seed: int, dist: Dist, salt: int = 0) -> SwigluInputs:
+def make_swiglu_inputs(T: int, I: int, seed: int, dist: Dist, salt: int = 0,
+                       rows: Optional[np.ndarray] = None) -> SwigluInputs:
+    """Inputs of one SwiGLU call; with `rows`, only those rows of gate_up."""
     return SwigluInputs(normal_bf16((T, 2 * I), seed, "gate_up", dist.sigma, dist.outlier_p,
-                                    dist.outlier_k, salt))
+                                    dist.outlier_k, salt, rows))
 
 
 # --------------------------------------------------------------------------------------------------
@@ -195,8 +238,8 @@ def llama31_405b_fp8_ragged() -> Workload:
                     "ragged 5120/13824 shapes at 1, 3, 17, 1000 tokens", tuple(calls))
 
 
-def inputs_for(call: Call, seed: int = 0, salt: int = 0):
-    """Seeded inputs of one call (NormInputs or SwigluInputs)."""
+def inputs_for(call: Call, seed: int = 0, salt: int = 0, rows: Optional[np.ndarray] = None):
+    """Seeded inputs of one call (NormInputs or SwigluInputs), optionally only some rows."""
     if call.kind.startswith("add"):
-        return make_norm_inputs(call.T, call.width, seed, call.dist, call.eps, salt)
-    return make_swiglu_inputs(call.T, call.width, seed, call.dist, salt)
+        return make_norm_inputs(call.T, call.width, seed, call.dist, call.eps, salt, rows)
+    return make_swiglu_inputs(call.T, call.width, seed, call.dist, salt, rows)
