@@ -10,14 +10,15 @@
  *
  * Definitions (cited by page title and section):
  *   [TRT] "TensorRT-LLM: Compiling Inference Engines Ahead of Time", section "Fusing operations, measured":
- *         RMSNorm as cast to float, square, mean, add epsilon, reciprocal square root, multiply, cast back,
- *         multiply by the weight; TensorRT-LLM's RMSNorm "adds the residual and normalizes in one kernel";
- *         the gated MLP runs one gate_up_proj matmul followed by a fused swiglu, g / (1 + exp(-g)) * up.
+ *         RMSNorm is the eight-step chain float cast, square, mean, epsilon, reciprocal square root, scaling,
+ *         cast to 16 bits and weight multiply; TensorRT-LLM fuses the residual addition into the same kernel
+ *         as the normalisation; gate and up come out of one stacked projection and a fused SwiGLU kernel
+ *         forms g / (1 + exp(-g)) * up from the two halves.
  *   [FP8] "TensorRT-LLM" architecture walkthrough, "Part V continued: Deep dive: quantization co-designed
- *         with the hardware": FP8 E4M3 activations with light per-tensor or per-block scaling.
+ *         with the hardware": FP8 E4M3 is the activation format, with a scale per tensor or per block.
  *   [VLLM] "Introduction to torch.compile and How It Works with vLLM", section 3, custom compiler passes:
- *         FusedKernel(x) = Quantize(SiLU(x)), the activation and its FP8 quantisation fused into one kernel;
- *         section 4 lists AllReduce + RMSNorm + Quant (FP8) as a further fusion.
+ *         a compiler pass replaces SiLU followed by FP8 quantisation with one fused kernel; section 4 reports
+ *         a fused AllReduce + RMSNorm + FP8 quantisation as well.
  *
  * Conventions shared by every entry point
  *   - All tensor pointers are DEVICE pointers (or managed memory visible to the device), row-major and
@@ -86,6 +87,16 @@ int mbd_last_cuda_error(void);
 
 /* Number of kernels this library has launched in the process so far (all threads, all devices). */
 uint64_t mbd_kernel_launches(void);
+
+/* Device-side error bits. A kernel that splits a row over a thread-block cluster exchanges partial sums
+ * through distributed shared memory and waits for its peers with a bounded wait (about one second); if
+ * the wait ever ran out, the kernel set this bit and returned without writing its outputs. */
+#define MBD_DEVERR_EXCHANGE_TIMEOUT 1u
+
+/* Copy the OR of the library's device error words on the CURRENT device into *flags and, if clear != 0,
+ * reset them. Synchronous (a device-to-host copy on the legacy default stream). Returns MBD_ERR_INVALID_ARG
+ * for a null flags pointer, MBD_ERR_CUDA if the copy fails. */
+mbd_status mbd_device_error_flags(uint32_t* flags, int clear);
 
 /*
  * Fused residual add + RMSNorm [TRT].

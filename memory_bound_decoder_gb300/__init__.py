@@ -43,6 +43,8 @@ def _load() -> ctypes.CDLL:
     lib.mbd_status_string.argtypes, lib.mbd_status_string.restype = [cint], ctypes.c_char_p
     lib.mbd_last_cuda_error.restype = cint
     lib.mbd_kernel_launches.restype = ctypes.c_uint64
+    lib.mbd_device_error_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32), cint]
+    lib.mbd_device_error_flags.restype = cint
     lib.mbd_fused_add_rmsnorm.argtypes = [vp, vp, vp, vp, i64, i64, f32, vp]
     lib.mbd_fused_add_rmsnorm_quant_fp8.argtypes = [vp, vp, vp, vp, i64, i64, f32, cint, vp, vp]
     lib.mbd_swiglu.argtypes = [vp, vp, i64, i64, vp]
@@ -122,6 +124,16 @@ def abi_version() -> int:
 
 def kernel_launches() -> int:
     return int(get_lib().mbd_kernel_launches())
+
+
+DEVERR_EXCHANGE_TIMEOUT = 1
+
+
+def device_error_flags(clear: bool = False) -> int:
+    """OR of the library's device error words on the current device (synchronous)."""
+    v = ctypes.c_uint32(0)
+    _check(get_lib().mbd_device_error_flags(ctypes.byref(v), int(bool(clear))), "device_error_flags")
+    return int(v.value)
 
 
 def fused_add_rmsnorm(out, residual, x, weight, n_tokens: int, hidden: int, eps: float, stream=None) -> None:

@@ -37,7 +37,7 @@ bool overlap(const void* a, size_t na, const void* b, size_t nb) {
     return na > 0 && nb > 0 && x < y + nb && y < x + na;
 }
 
-constexpr int kMaxClusterCtas = 8;   // portable cluster size
+constexpr int kMaxClusterCtas = 8;   // portable cluster size (also the exchange's slot count)
 constexpr int kMaxThreads = 512;     // matches __launch_bounds__ of the kernels
 
 // Choose how a launch covers [rows, nvec]. Large batches give each row one CTA (no cluster traffic);
@@ -171,6 +171,20 @@ const char* mbd_status_string(int status) {
 int mbd_last_cuda_error(void) { return g_last_cuda_error; }
 
 uint64_t mbd_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+mbd_status mbd_device_error_flags(uint32_t* flags, int clear) {
+    if (!flags) return MBD_ERR_INVALID_ARG;
+    unsigned int a = 0, b = 0;
+    cudaError_t e = mbd::device_error_flags_norm(&a, clear != 0);
+    if (e == cudaSuccess) e = mbd::device_error_flags_swiglu(&b, clear != 0);
+    if (e != cudaSuccess) {
+        g_last_cuda_error = static_cast<int>(e);
+        (void)cudaGetLastError();
+        return MBD_ERR_CUDA;
+    }
+    *flags = a | b;
+    return MBD_OK;
+}
 
 mbd_status mbd_fused_add_rmsnorm(void* out, void* residual, const void* x, const void* weight,
                                  int64_t n_tokens, int64_t hidden, float eps, mbd_stream_t stream) {

@@ -77,23 +77,149 @@ __device__ __forceinline__ float cta_allreduce(float v, float* scratch, Op op) {
     return warp_allreduce(t, op);
 }
 
-// Combine the CTA totals of the `nctas` CTAs of this cluster (they all compute the same value, summed in
-// rank order). `slot` is a __shared__ float of this CTA. The caller must cluster-sync again before `slot`
-// is rewritten or before the CTA exits, because other CTAs read it remotely.
-template <class Op>
-__device__ __forceinline__ float cluster_allreduce(float cta_total, float* slot, int nctas, Op op) {
-    if (nctas == 1) return cta_total;
-    cg::cluster_group cluster = cg::this_cluster();
-    if (threadIdx.x == 0) *slot = cta_total;
-    cluster.sync();
-    const int lane = threadIdx.x & 31;
-    float t = 0.0f;
-    if (lane < nctas) t = *cluster.map_shared_rank(slot, lane);
-    return warp_allreduce(t, op);
+// ------------------------------------------------------------------------------------------ cluster exchange
+
+// Device-side error word of each kernel translation unit (internal linkage, one per .cu file), read on
+// the host through mbd_device_error_flags(). Bits: kDevErrExchangeTimeout.
+static __device__ unsigned int g_device_error_flags;
+constexpr unsigned int kDevErrExchangeTimeout = 1u;
+
+// Partial results of the CTAs of one row are exchanged through distributed shared memory: every CTA
+// pushes its 16-byte partial into slot[my_rank] of every peer with st.async, whose completion is counted
+// on the peer's mbarrier (transaction bytes). No cluster-wide release fence is needed, so the exchange
+// does not wait for this CTA's outstanding global stores. A CTA leaves only after its own mbarrier has
+// seen every peer's bytes, so no write can target a CTA that has exited.
+constexpr int kMaxClusterCtas = 8;
+
+struct alignas(16) Exchange {
+    float4 slot[kMaxClusterCtas];
+    unsigned long long mbar;
+};
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ void cluster_sync_if(int nctas) {
-    if (nctas > 1) cg::this_cluster().sync();
+// Call once per CTA, by all threads, before any peer may push (it ends with a cluster barrier).
+__device__ __forceinline__ void exchange_init(Exchange& ex, int nctas) {
+    if (threadIdx.x == 0) {
+        const uint32_t mb = smem_addr(&ex.mbar);
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mb) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb), "r"((nctas - 1) * 16)
+                     : "memory");
+    }
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+// Thread 0 publishes this CTA's partial; lanes of warp 0 push it to the peers in parallel.
+__device__ __forceinline__ void exchange_send(Exchange& ex, float4 v, int my_rank, int nctas) {
+    if (threadIdx.x >= 32) return;
+    const int lane = threadIdx.x;
+    if (lane == 0) ex.slot[my_rank] = v;
+    if (lane < nctas && lane != my_rank) {
+        uint32_t rslot, rbar;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rslot) : "r"(smem_addr(&ex.slot[my_rank])), "r"(lane));
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rbar) : "r"(smem_addr(&ex.mbar)), "r"(lane));
+        asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+                     ::"r"(rslot), "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)), "r"(__float_as_uint(v.z)),
+                       "r"(__float_as_uint(v.w)), "r"(rbar)
+                     : "memory");
+    }
+}
+
+// Wait until every peer's partial has landed (phase 0 of the mbarrier); all threads poll and the result
+// is made CTA-uniform. Gives up after about one second of SM clock, sets kDevErrExchangeTimeout and
+// returns false, so a stuck exchange ends the kernel instead of hanging the GPU.
+__device__ __forceinline__ bool exchange_wait(Exchange& ex) {
+    const uint32_t mb = smem_addr(&ex.mbar);
+    uint32_t done = 0;
+    const long long t0 = clock64();
+    while (true) {
+        asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n selp.u32 %0, 1, 0, p;\n}"
+                     : "=r"(done)
+                     : "r"(mb)
+                     : "memory");
+        if (done) break;
+        if (clock64() - t0 > (2LL << 30)) {
+            atomicOr(&g_device_error_flags, kDevErrExchangeTimeout);
+            break;
+        }
+    }
+    return __syncthreads_and(static_cast<int>(done)) != 0;
+}
+
+// ------------------------------------------------------------------------------------------ PDL
+
+// Programmatic dependent launch: let the next kernel in the stream be scheduled as soon as every CTA of
+// this one has started, and wait for the previous kernel's completion (and memory) before touching global
+// memory. Both are no-ops when the launch did not enable programmatic stream serialization.
+__device__ __forceinline__ void pdl_trigger_and_wait() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ------------------------------------------------------------------------------------------ double-float
+
+// An unevaluated sum hi + lo of two fp32 values (about 48 significant bits), built with Knuth's TwoSum.
+// Only additions appear, so no FMA contraction can change the result; TwoSum returns the exact rounding
+// error in either operand order, which keeps butterfly reductions identical on every lane.
+struct DD {
+    float hi, lo;
+};
+
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+    s = a + b;
+    const float bp = s - a;
+    e = (a - (s - bp)) + (b - bp);
+}
+
+__device__ __forceinline__ void dd_accumulate(DD& acc, float x) {
+    float s, e;
+    two_sum(acc.hi, x, s, e);
+    acc.hi = s;
+    acc.lo += e;
+}
+
+__device__ __forceinline__ DD dd_add(DD a, DD b) {
+    float s, e;
+    two_sum(a.hi, b.hi, s, e);
+    e += a.lo + b.lo;
+    const float hi = s + e;
+    return DD{hi, e - (hi - s)};
+}
+
+// Row statistics of the dynamic-scale norm: the sum of squares as a double-float and max |w * s|.
+struct RowStats {
+    DD sum_sq;
+    float pmax;
+};
+
+__device__ __forceinline__ RowStats combine(RowStats a, RowStats b) {
+    return RowStats{dd_add(a.sum_sq, b.sum_sq), fmaxf(a.pmax, b.pmax)};
+}
+
+__device__ __forceinline__ RowStats shfl_xor(RowStats v, int o) {
+    return RowStats{DD{__shfl_xor_sync(0xffffffffu, v.sum_sq.hi, o), __shfl_xor_sync(0xffffffffu, v.sum_sq.lo, o)},
+                    __shfl_xor_sync(0xffffffffu, v.pmax, o)};
+}
+
+__device__ __forceinline__ RowStats warp_allreduce(RowStats v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = combine(v, shfl_xor(v, o));
+    return v;
+}
+
+// CTA-wide reduction of RowStats; every thread returns the same value. `scratch` holds 32 entries.
+__device__ __forceinline__ RowStats cta_allreduce(RowStats v, RowStats* scratch) {
+    v = warp_allreduce(v);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) scratch[warp] = v;
+    __syncthreads();
+    const int nwarps = (blockDim.x + 31) >> 5;
+    const RowStats zero{DD{0.0f, 0.0f}, 0.0f};
+    return warp_allreduce(lane < nwarps ? scratch[lane] : zero);
 }
 
 }  // namespace mbd

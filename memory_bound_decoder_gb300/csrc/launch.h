@@ -41,8 +41,36 @@ struct SwigluParams {
     int nvec;        // I / 8
 };
 
-// Launchers: return the cudaError_t of the launch (cudaSuccess when enqueued).
+// Launchers: return the cudaError_t of the launch (cudaSuccess when enqueued). Every launch enables
+// programmatic stream serialization; the kernels wait on the previous grid before touching memory.
 cudaError_t launch_add_rmsnorm(const NormParams& p, Epilogue ep, const RowPlan& plan, cudaStream_t s);
 cudaError_t launch_swiglu(const SwigluParams& p, Epilogue ep, const RowPlan& plan, cudaStream_t s);
+
+// Read (and optionally clear) the device error word of each kernel translation unit (synchronous).
+cudaError_t device_error_flags_norm(unsigned int* flags, bool clear);
+cudaError_t device_error_flags_swiglu(unsigned int* flags, bool clear);
+
+// Fill a launch configuration: grid/block, the cluster attribute when cluster > 1, and PDL.
+inline void fill_launch(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int64_t ctas, int threads,
+                        int cluster, cudaStream_t s) {
+    cfg = cudaLaunchConfig_t{};
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    int n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = static_cast<unsigned>(cluster);
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+}
 
 }  // namespace mbd

@@ -1,17 +1,18 @@
 // Fused residual add + RMSNorm (+ FP8 E4M3 epilogue).
 //
 // Definition ("TensorRT-LLM: Compiling Inference Engines Ahead of Time", "Fusing operations, measured"):
-// RMSNorm is the chain cast-to-float, square, mean, add epsilon, reciprocal square root, multiply,
-// cast back, multiply by the weight, and TensorRT-LLM's module adds the residual and normalises in one
-// kernel. Here that whole chain is one pass over HBM: each row is read once (x, residual), the rounded
+// RMSNorm is an eight-step chain (float cast, square, mean, epsilon, reciprocal square root, scaling,
+// cast back, weight), and TensorRT-LLM runs the residual addition inside the normalisation kernel. Here
+// that whole chain is one pass over HBM: each row is read once (x, residual), the rounded
 // sum is written back as the new residual, and the normalised row leaves as bf16 or as E4M3 codes
 // (the Quantize half of the fusions listed in "Introduction to torch.compile and How It Works with
 // vLLM", section 4).
 //
 // Data flow per row slice: 16-byte loads of x and residual into registers -> s = bf16(x + r) (kept packed)
 // -> residual store -> sum of s^2 -> CTA (+cluster) reduction -> inv = 1/sqrt(mean + eps) -> weight loads
-// -> v = s * inv * w -> bf16 store, or E4M3 codes with a static scale, or (dynamic) a second reduction of
-// max |v| followed by recomputing v and storing the codes.
+// -> v = (w * s) * inv -> bf16 store or E4M3 codes with a static scale. The dynamic per-token variant
+// reduces the sum of squares and max |w * s| together (the scale is max |w * s| * inv / 448), then stores
+// the codes from registers.
 #include "common.cuh"
 #include "launch.h"
 
@@ -19,11 +20,28 @@ namespace mbd {
 
 namespace {
 
+// Quantise y = p * (c_hi + c_lo) to E4M3, rounding the double-float product as if it were exact.
+// p * c_hi is split exactly into y_hi + err (FMA); y_lo = err + p * c_lo. Rounding y_hi alone is correct
+// unless y_hi lands exactly on a rounding boundary of the E4M3 grid; every such boundary (and every code
+// value) has its 19 low fp32 mantissa bits clear, so a value of that form is moved one fp32 ulp toward
+// y_hi + y_lo. A one-ulp move cannot cross a boundary that y_hi was not already on.
+__device__ __forceinline__ float exact_side(float p, float c_hi, float c_lo) {
+    const float y_hi = p * c_hi;
+    const float y_lo = fmaf(p, c_hi, -y_hi) + p * c_lo;
+    uint32_t bits = __float_as_uint(y_hi);
+    if ((bits & 0x7FFFFu) == 0u && y_lo != 0.0f && y_hi != 0.0f) bits += ((y_lo > 0.0f) == (y_hi > 0.0f)) ? 1u : 0xFFFFFFFFu;
+    return __uint_as_float(bits);
+}
+
 template <int VPT, int EP>
 __global__ void __launch_bounds__(512) add_rmsnorm_kernel(NormParams p, int ctas_per_row, int slice) {
     __shared__ float red_sum[32];
-    __shared__ float red_max[32];
-    __shared__ float cl_slot[2];
+    __shared__ RowStats red_stats[32];
+    __shared__ Exchange ex;
+    __shared__ float row_const[2];
+    // The weight is an L2 hit; load it up front when registers allow (small rows, latency-bound), else
+    // after the reduction. The dynamic variant needs it before the reduction anyway.
+    constexpr bool kEarlyWeight = EP == kFp8Dynamic || VPT <= 2;
 
     const int64_t row = blockIdx.x / ctas_per_row;
     const int rank = blockIdx.x - static_cast<int>(row * ctas_per_row);
@@ -34,46 +52,65 @@ __global__ void __launch_bounds__(512) add_rmsnorm_kernel(NormParams p, int ctas
     uint4* rr = static_cast<uint4*>(p.residual) + row * p.nvec;
     const uint4* wr = static_cast<const uint4*>(p.weight);
 
-    uint4 sv[VPT];
+    pdl_trigger_and_wait();
+
+    // 1. one pass over HBM: x and residual in, s = bf16(x + r) kept packed in registers and written back
+    uint4 sv[VPT], wv[VPT];
     bool live[VPT];
     {
-        uint4 xv[VPT], rv[VPT];
+        uint4 xv[VPT];
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
             const int c = begin + threadIdx.x + i * blockDim.x;
             live[i] = c < end;
             if (live[i]) {
                 xv[i] = load_stream(xr + c);
-                rv[i] = load_stream(rr + c);
+                sv[i] = load_stream(rr + c);
+                if constexpr (kEarlyWeight) wv[i] = load_cached(wr + c);
             }
         }
-        float ss = 0.0f;
+        if (ctas_per_row > 1) exchange_init(ex, ctas_per_row);   // overlaps the loads in flight
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
             if (!live[i]) continue;
             const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv[i]);
-            const uint32_t* rw = reinterpret_cast<const uint32_t*>(&rv[i]);
             uint32_t* sw = reinterpret_cast<uint32_t*>(&sv[i]);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint32_t packed = pack_bf16x2(bf16_lo(xw[k]) + bf16_lo(rw[k]), bf16_hi(xw[k]) + bf16_hi(rw[k]));
-                sw[k] = packed;
-                const float s0 = bf16_lo(packed), s1 = bf16_hi(packed);
-                ss = fmaf(s0, s0, ss);
-                ss = fmaf(s1, s1, ss);
-            }
+            for (int k = 0; k < 4; ++k)
+                sw[k] = pack_bf16x2(bf16_lo(xw[k]) + bf16_lo(sw[k]), bf16_hi(xw[k]) + bf16_hi(sw[k]));
             store_stream(rr + (begin + threadIdx.x + i * blockDim.x), sv[i]);
         }
+    }
+
+    if constexpr (EP != kFp8Dynamic) {
+        // 2. sum of squares (fp32) -> inv = 1 / sqrt(mean + eps)
+        float ss = 0.0f;
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            if (!live[i]) continue;
+            const uint32_t* sw = reinterpret_cast<const uint32_t*>(&sv[i]);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                ss = fmaf(bf16_lo(sw[k]), bf16_lo(sw[k]), ss);
+                ss = fmaf(bf16_hi(sw[k]), bf16_hi(sw[k]), ss);
+            }
+        }
         ss = cta_allreduce(ss, red_sum, SumOp{});
-        ss = cluster_allreduce(ss, &cl_slot[0], ctas_per_row, SumOp{});
-        // (reuse of `ss` below: the row's sum of squares)
+        if (ctas_per_row > 1) {
+            exchange_send(ex, make_float4(ss, 0.0f, 0.0f, 0.0f), rank, ctas_per_row);
+            if (!exchange_wait(ex)) return;
+            ss = 0.0f;
+            for (int r = 0; r < ctas_per_row; ++r) ss += ex.slot[r].x;   // rank order: same in every CTA
+        }
         const float inv = 1.0f / sqrtf(ss / static_cast<float>(p.hidden) + p.eps);
 
-        uint4 wv[VPT];
+        if constexpr (!kEarlyWeight) {
 #pragma unroll
-        for (int i = 0; i < VPT; ++i)
-            if (live[i]) wv[i] = load_cached(wr + (begin + threadIdx.x + i * blockDim.x));
+            for (int i = 0; i < VPT; ++i)
+                if (live[i]) wv[i] = load_cached(wr + (begin + threadIdx.x + i * blockDim.x));
+        }
 
+        // 3. v = (w * s) * inv; w * s of two bf16 values is exact in fp32
         if constexpr (EP == kBf16) {
             uint4* outr = static_cast<uint4*>(p.out) + row * p.nvec;
 #pragma unroll
@@ -85,52 +122,84 @@ __global__ void __launch_bounds__(512) add_rmsnorm_kernel(NormParams p, int ctas
                 uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    ow[k] = pack_bf16x2(bf16_lo(sw[k]) * inv * bf16_lo(ww[k]), bf16_hi(sw[k]) * inv * bf16_hi(ww[k]));
+                    ow[k] = pack_bf16x2(bf16_lo(sw[k]) * bf16_lo(ww[k]) * inv, bf16_hi(sw[k]) * bf16_hi(ww[k]) * inv);
                 store_stream(outr + (begin + threadIdx.x + i * blockDim.x), o);
             }
-            cluster_sync_if(ctas_per_row);
         } else {
-            float qmul;
-            if constexpr (EP == kFp8Static) {
-                const float sc = __ldg(p.scale);
-                qmul = sc > 0.0f ? 1.0f / sc : 0.0f;
-            } else {
-                float amax = 0.0f;
-#pragma unroll
-                for (int i = 0; i < VPT; ++i) {
-                    if (!live[i]) continue;
-                    const uint32_t* sw = reinterpret_cast<const uint32_t*>(&sv[i]);
-                    const uint32_t* ww = reinterpret_cast<const uint32_t*>(&wv[i]);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        amax = fmaxf(amax, fabsf(bf16_lo(sw[k]) * inv * bf16_lo(ww[k])));
-                        amax = fmaxf(amax, fabsf(bf16_hi(sw[k]) * inv * bf16_hi(ww[k])));
-                    }
-                }
-                amax = cta_allreduce(amax, red_max, MaxOp{});
-                amax = cluster_allreduce(amax, &cl_slot[1], ctas_per_row, MaxOp{});
-                const float sc = amax / 448.0f;
-                qmul = sc > 0.0f ? 1.0f / sc : 0.0f;
-                if (rank == 0 && threadIdx.x == 0) p.scale[row] = sc;
-            }
+            // static per-tensor scale: codes of v / scale
+            const float sc = __ldg(p.scale);
+            const float c = sc > 0.0f ? inv * (1.0f / sc) : 0.0f;
             uint2* outr = reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + row * (int64_t)p.nvec * 8);
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {
                 if (!live[i]) continue;
                 const uint32_t* sw = reinterpret_cast<const uint32_t*>(&sv[i]);
                 const uint32_t* ww = reinterpret_cast<const uint32_t*>(&wv[i]);
-                float v[8];
+                float y[8];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    v[2 * k] = bf16_lo(sw[k]) * inv * bf16_lo(ww[k]) * qmul;
-                    v[2 * k + 1] = bf16_hi(sw[k]) * inv * bf16_hi(ww[k]) * qmul;
+                    y[2 * k] = bf16_lo(sw[k]) * bf16_lo(ww[k]) * c;
+                    y[2 * k + 1] = bf16_hi(sw[k]) * bf16_hi(ww[k]) * c;
                 }
-                uint2 q;
-                q.x = pack_e4m3x4(v[0], v[1], v[2], v[3]);
-                q.y = pack_e4m3x4(v[4], v[5], v[6], v[7]);
-                store_stream(outr + (begin + threadIdx.x + i * blockDim.x), q);
+                store_stream(outr + (begin + threadIdx.x + i * blockDim.x),
+                             make_uint2(pack_e4m3x4(y[0], y[1], y[2], y[3]), pack_e4m3x4(y[4], y[5], y[6], y[7])));
             }
-            cluster_sync_if(ctas_per_row);
+        }
+    } else {
+        // Dynamic per-token scale. The codes are ratios of exact bf16 products, 448 * (w_j s_j) / (w_k s_k),
+        // rescaled by the fp32 rounding of the scale, so exact E4M3 ties are common; resolving them as the
+        // fp64 definition does needs the row constants to ~1e-13: the sum of squares is kept as a
+        // double-float, the per-row constants are formed in fp64 once per CTA, and every element is scaled
+        // with a double-float multiplier.
+        RowStats st{DD{0.0f, 0.0f}, 0.0f};
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            if (!live[i]) continue;
+            const uint32_t* sw = reinterpret_cast<const uint32_t*>(&sv[i]);
+            const uint32_t* ww = reinterpret_cast<const uint32_t*>(&wv[i]);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float s0 = bf16_lo(sw[k]), s1 = bf16_hi(sw[k]);
+                dd_accumulate(st.sum_sq, s0 * s0);   // exact square of a bf16 value
+                dd_accumulate(st.sum_sq, s1 * s1);
+                st.pmax = fmaxf(st.pmax, fmaxf(fabsf(s0 * bf16_lo(ww[k])), fabsf(s1 * bf16_hi(ww[k]))));
+            }
+        }
+        st = cta_allreduce(st, red_stats);
+        if (ctas_per_row > 1) {
+            exchange_send(ex, make_float4(st.sum_sq.hi, st.sum_sq.lo, st.pmax, 0.0f), rank, ctas_per_row);
+            if (!exchange_wait(ex)) return;
+            st = RowStats{DD{ex.slot[0].x, ex.slot[0].y}, ex.slot[0].z};
+            for (int r = 1; r < ctas_per_row; ++r)
+                st = combine(st, RowStats{DD{ex.slot[r].x, ex.slot[r].y}, ex.slot[r].z});
+        }
+        if (threadIdx.x == 0) {
+            const double mean_sq = (static_cast<double>(st.sum_sq.hi) + static_cast<double>(st.sum_sq.lo)) /
+                                   static_cast<double>(p.hidden);
+            const double inv = 1.0 / sqrt(mean_sq + static_cast<double>(p.eps));
+            const float sc = static_cast<float>(static_cast<double>(st.pmax) * inv / 448.0);
+            const double c = sc > 0.0f ? inv / static_cast<double>(sc) : 0.0;
+            const float c_hi = static_cast<float>(c);
+            row_const[0] = c_hi;
+            row_const[1] = static_cast<float>(c - static_cast<double>(c_hi));
+            if (rank == 0) p.scale[row] = sc;
+        }
+        __syncthreads();
+        const float c_hi = row_const[0], c_lo = row_const[1];
+        uint2* outr = reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + row * (int64_t)p.nvec * 8);
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            if (!live[i]) continue;
+            const uint32_t* sw = reinterpret_cast<const uint32_t*>(&sv[i]);
+            const uint32_t* ww = reinterpret_cast<const uint32_t*>(&wv[i]);
+            float y[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                y[2 * k] = exact_side(bf16_lo(sw[k]) * bf16_lo(ww[k]), c_hi, c_lo);
+                y[2 * k + 1] = exact_side(bf16_hi(sw[k]) * bf16_hi(ww[k]), c_hi, c_lo);
+            }
+            store_stream(outr + (begin + threadIdx.x + i * blockDim.x),
+                         make_uint2(pack_e4m3x4(y[0], y[1], y[2], y[3]), pack_e4m3x4(y[4], y[5], y[6], y[7])));
         }
     }
 }
@@ -145,22 +214,22 @@ cudaError_t launch_ep(const NormParams& p, const RowPlan& plan, cudaStream_t s) 
         case 8: kern = add_rmsnorm_kernel<8, EP>; break;
         default: return cudaErrorInvalidValue;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(p.rows * plan.ctas_per_row), 1, 1);
-    cfg.blockDim = dim3(plan.threads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = plan.ctas_per_row;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = plan.ctas_per_row > 1 ? 1 : 0;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    fill_launch(cfg, attr, p.rows * plan.ctas_per_row, plan.threads, plan.ctas_per_row, s);
     return cudaLaunchKernelEx(&cfg, kern, p, plan.ctas_per_row, plan.slice);
 }
 
 }  // namespace
+
+cudaError_t device_error_flags_norm(unsigned int* flags, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(flags, g_device_error_flags, sizeof(unsigned int));
+    if (e == cudaSuccess && clear) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_device_error_flags, &zero, sizeof(unsigned int));
+    }
+    return e;
+}
 
 cudaError_t launch_add_rmsnorm(const NormParams& p, Epilogue ep, const RowPlan& plan, cudaStream_t s) {
     switch (ep) {

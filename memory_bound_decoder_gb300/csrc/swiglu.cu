@@ -1,11 +1,11 @@
 // Fused SwiGLU over the stacked gate_up projection (+ FP8 E4M3 epilogue).
 //
 // Definition ("TensorRT-LLM: Compiling Inference Engines Ahead of Time", "Fusing operations, measured"):
-// the gated MLP runs one gate_up matmul whose row holds gate in its first half and up in its second half,
-// then a swiglu kernel that computes g / (1 + exp(-g)) * up per element, so the [T, I] intermediate is
-// never written and re-read. The FP8 variant is the Quantize(SiLU(x)) fusion of "Introduction to
-// torch.compile and How It Works with vLLM" (section 3, custom compiler passes): the activation is
-// quantised to E4M3 for the next GEMM inside the same pass.
+// gate and up are the two halves of one stacked projection row, combined per element as
+// g / (1 + exp(-g)) * up by a fused kernel, so the [T, I] activation is not written out and read back.
+// The FP8 variant follows the SiLU-plus-quantisation fusion of "Introduction to torch.compile and How It
+// Works with vLLM" (section 3, custom compiler passes): the activation leaves as E4M3 codes for the next
+// GEMM in the same pass.
 //
 // bf16 and static-scale variants are pure streams (no reduction): each CTA owns a slice of one row.
 // The dynamic per-token variant keeps the slice's fp32 products in registers, reduces max |h| over the row
@@ -18,12 +18,30 @@ namespace mbd {
 
 namespace {
 
-__device__ __forceinline__ float silu_times(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+// silu(g) * u = g * u / (1 + e^-g). e^-g = 2^(-g log2 e) is evaluated with the hardware base-2
+// exponential (ex2.approx) on the fp32-rounded argument t, corrected by 2^d ~ 1 + d ln 2 for the rounding
+// residual d = -g log2 e - t (obtained exactly with an FMA plus the low part of log2 e), so the error
+// does not grow with |g|. 1 / (1 + e) uses the hardware reciprocal (rcp.approx). g is clamped at -87
+// (e^87 < FLT_MAX) so e stays finite; below that silu is ~1e-36 either way.
+__device__ __forceinline__ float silu_times(float g, float u) {
+    constexpr float kLog2e = 1.44269502162933349609375f;   // log2(e) rounded to fp32
+    constexpr float kLog2eLo = 1.925963033500011e-08f;     // log2(e) - kLog2e
+    constexpr float kLn2 = 0.693147182464599609375f;
+    const float gc = fmaxf(g, -87.0f);
+    const float t = gc * -kLog2e;
+    const float d = fmaf(gc, -kLog2eLo, fmaf(gc, -kLog2e, -t));
+    float e;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(t));
+    e = fmaf(e, d * kLn2, e);
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+    return g * r * u;
+}
 
 template <int VPT, int EP>
 __global__ void __launch_bounds__(512) swiglu_kernel(SwigluParams p, int ctas_per_row, int slice) {
     __shared__ float red_max[32];
-    __shared__ float cl_slot[1];
+    __shared__ Exchange ex;
 
     const int64_t row = blockIdx.x / ctas_per_row;
     const int rank = blockIdx.x - static_cast<int>(row * ctas_per_row);
@@ -32,6 +50,8 @@ __global__ void __launch_bounds__(512) swiglu_kernel(SwigluParams p, int ctas_pe
 
     const uint4* gr = static_cast<const uint4*>(p.gate_up) + row * (int64_t)p.nvec * 2;
     const uint4* ur = gr + p.nvec;
+
+    pdl_trigger_and_wait();
 
     uint4 gv[VPT], uv[VPT];
     bool live[VPT];
@@ -43,6 +63,9 @@ __global__ void __launch_bounds__(512) swiglu_kernel(SwigluParams p, int ctas_pe
             gv[i] = load_stream(gr + c);
             uv[i] = load_stream(ur + c);
         }
+    }
+    if constexpr (EP == kFp8Dynamic) {
+        if (ctas_per_row > 1) exchange_init(ex, ctas_per_row);   // overlaps the loads in flight
     }
 
     if constexpr (EP == kBf16) {
@@ -84,7 +107,11 @@ __global__ void __launch_bounds__(512) swiglu_kernel(SwigluParams p, int ctas_pe
         }
         if constexpr (EP == kFp8Dynamic) {
             amax = cta_allreduce(amax, red_max, MaxOp{});
-            amax = cluster_allreduce(amax, &cl_slot[0], ctas_per_row, MaxOp{});
+            if (ctas_per_row > 1) {
+                exchange_send(ex, make_float4(amax, 0.0f, 0.0f, 0.0f), rank, ctas_per_row);
+                if (!exchange_wait(ex)) return;
+                for (int r = 0; r < ctas_per_row; ++r) amax = fmaxf(amax, ex.slot[r].x);
+            }
             const float sc = amax / 448.0f;
             qmul = sc > 0.0f ? 1.0f / sc : 0.0f;
             if (rank == 0 && threadIdx.x == 0) p.scale[row] = sc;
@@ -97,7 +124,6 @@ __global__ void __launch_bounds__(512) swiglu_kernel(SwigluParams p, int ctas_pe
             q.y = pack_e4m3x4(h[i][4] * qmul, h[i][5] * qmul, h[i][6] * qmul, h[i][7] * qmul);
             store_stream(outr + (begin + threadIdx.x + i * blockDim.x), q);
         }
-        if constexpr (EP == kFp8Dynamic) cluster_sync_if(ctas_per_row);
     }
 }
 
@@ -111,22 +137,23 @@ cudaError_t launch_ep(const SwigluParams& p, const RowPlan& plan, cudaStream_t s
         case 8: kern = swiglu_kernel<8, EP>; break;
         default: return cudaErrorInvalidValue;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(p.rows * plan.ctas_per_row), 1, 1);
-    cfg.blockDim = dim3(plan.threads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = plan.ctas_per_row;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = (EP == kFp8Dynamic && plan.ctas_per_row > 1) ? 1 : 0;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    fill_launch(cfg, attr, p.rows * plan.ctas_per_row, plan.threads,
+                EP == kFp8Dynamic ? plan.ctas_per_row : 1, s);
     return cudaLaunchKernelEx(&cfg, kern, p, plan.ctas_per_row, plan.slice);
 }
 
 }  // namespace
+
+cudaError_t device_error_flags_swiglu(unsigned int* flags, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(flags, g_device_error_flags, sizeof(unsigned int));
+    if (e == cudaSuccess && clear) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_device_error_flags, &zero, sizeof(unsigned int));
+    }
+    return e;
+}
 
 cudaError_t launch_swiglu(const SwigluParams& p, Epilogue ep, const RowPlan& plan, cudaStream_t s) {
     switch (ep) {

@@ -7,15 +7,14 @@
  *
  * Sources (cited by page title and section):
  *  [P1] "TensorRT-LLM: Compiling Inference Engines Ahead of Time", section "Fusing operations, measured":
- *       RMSNorm is cast to float, square, mean, add epsilon, reciprocal square root, multiply, cast back,
- *       multiply by the weight; TensorRT-LLM's RMSNorm adds the residual and normalises in one kernel;
- *       the gated MLP is down(silu(gate(x)) * up(x)) with gate and up produced by one stacked matmul and
- *       a swiglu kernel computing g / (1 + exp(-g)) * up per element.
+ *       the RMSNorm chain (float cast, square, mean, epsilon, reciprocal square root, scaling, cast back,
+ *       weight) with the residual addition fused in front of it; the gated MLP takes gate and up from one
+ *       stacked projection and combines them per element as g / (1 + exp(-g)) * up.
  *  [P2] "TensorRT-LLM" architecture walkthrough, "Part V continued: Deep dive: quantization co-designed
- *       with the hardware": FP8 E4M3 for activations, with light per-tensor or per-block scaling
- *       (format defined by Micikevicius et al., "FP8 Formats for Deep Learning").
- *  [P5] "Introduction to torch.compile and How It Works with vLLM", section 3 (custom passes):
- *       FusedKernel(x) = Quantize(SiLU(x)), the activation followed by FP8 quantisation in one kernel.
+ *       with the hardware": activations in FP8 E4M3 with a per-tensor or per-block scale (the format is
+ *       the one of Micikevicius et al., "FP8 Formats for Deep Learning").
+ *  [P5] "Introduction to torch.compile and How It Works with vLLM", section 3 (custom passes): the SiLU
+ *       activation and the FP8 quantisation that follows it are rewritten into a single fused kernel.
  *
  * Conventions: bf16 values are passed as their 16-bit patterns (uint16_t), row-major. Every function
  * processes rows independently, so a caller may pass pointers offset to any row with a smaller T.

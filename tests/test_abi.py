@@ -20,7 +20,7 @@ def test_exports_every_declared_symbol(lib):
     names = mbd.header_functions()
     assert set(names) >= {"mbd_fused_add_rmsnorm", "mbd_fused_add_rmsnorm_quant_fp8", "mbd_swiglu",
                           "mbd_swiglu_quant_fp8", "mbd_status_string", "mbd_abi_version",
-                          "mbd_last_cuda_error", "mbd_kernel_launches"}
+                          "mbd_last_cuda_error", "mbd_kernel_launches", "mbd_device_error_flags"}
     for n in names:
         assert hasattr(lib, n), n
 
@@ -99,6 +99,10 @@ def test_unsupported_widths(lib):
     # the pure streams have no such limit: zero tokens with a wide row is a no-op
     mbd.swiglu(None, None, 0, wide)
     mbd.swiglu_quant_fp8(None, None, 0, wide, "static", None)
+
+
+def test_device_error_flags_rejects_null(lib):
+    assert lib.mbd_device_error_flags(None, 0) == mbd.ERR_INVALID_ARG
 
 
 def test_raw_ctypes_signature(lib):
