@@ -27,6 +27,13 @@ __device__ __forceinline__ uint4 load_cached(const uint4* p) { return __ldg(p); 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// Both halves of a bf16x2 word as a float2 (exact).
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+__device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
+
 // Round two fp32 values to bf16 (nearest even) and pack them (lo -> low half).
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
@@ -44,6 +51,9 @@ __device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
 __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
     return pack_e4m3x2(a, b) | (pack_e4m3x2(c, d) << 16);
 }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float2 v) { return pack_bf16x2(v.x, v.y); }
+__device__ __forceinline__ uint32_t pack_e4m3x4(float2 a, float2 b) { return pack_e4m3x4(a.x, a.y, b.x, b.y); }
 
 // ------------------------------------------------------------------------------------------ reductions
 
@@ -180,6 +190,20 @@ __device__ __forceinline__ void dd_accumulate(DD& acc, float x) {
     two_sum(acc.hi, x, s, e);
     acc.hi = s;
     acc.lo += e;
+}
+
+// Two independent double-float accumulators advanced with packed fp32x2 additions (lanes x and y).
+struct DD2 {
+    float2 hi, lo;
+};
+
+__device__ __forceinline__ void dd_accumulate(DD2& acc, float2 x) {
+    const float2 s = __fadd2_rn(acc.hi, x);
+    const float2 bp = __fadd2_rn(s, make_float2(-acc.hi.x, -acc.hi.y));
+    const float2 t = __fadd2_rn(s, make_float2(-bp.x, -bp.y));
+    const float2 e = __fadd2_rn(__fadd2_rn(acc.hi, make_float2(-t.x, -t.y)), __fadd2_rn(x, make_float2(-bp.x, -bp.y)));
+    acc.hi = s;
+    acc.lo = __fadd2_rn(acc.lo, e);
 }
 
 __device__ __forceinline__ DD dd_add(DD a, DD b) {

@@ -25,12 +25,16 @@ namespace {
 // unless y_hi lands exactly on a rounding boundary of the E4M3 grid; every such boundary (and every code
 // value) has its 19 low fp32 mantissa bits clear, so a value of that form is moved one fp32 ulp toward
 // y_hi + y_lo. A one-ulp move cannot cross a boundary that y_hi was not already on.
-__device__ __forceinline__ float exact_side(float p, float c_hi, float c_lo) {
-    const float y_hi = p * c_hi;
-    const float y_lo = fmaf(p, c_hi, -y_hi) + p * c_lo;
+__device__ __forceinline__ float nudge(float y_hi, float y_lo) {
     uint32_t bits = __float_as_uint(y_hi);
     if ((bits & 0x7FFFFu) == 0u && y_lo != 0.0f && y_hi != 0.0f) bits += ((y_lo > 0.0f) == (y_hi > 0.0f)) ? 1u : 0xFFFFFFFFu;
     return __uint_as_float(bits);
+}
+
+__device__ __forceinline__ float2 exact_side(float2 p, float c_hi, float c_lo) {
+    const float2 y_hi = __fmul2_rn(p, f2(c_hi));
+    const float2 y_lo = __ffma2_rn(p, f2(c_lo), __ffma2_rn(p, f2(c_hi), make_float2(-y_hi.x, -y_hi.y)));
+    return make_float2(nudge(y_hi.x, y_lo.x), nudge(y_hi.y, y_lo.y));
 }
 
 template <int VPT, int EP>
@@ -76,26 +80,25 @@ __global__ void __launch_bounds__(512) add_rmsnorm_kernel(NormParams p, int ctas
             const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv[i]);
             uint32_t* sw = reinterpret_cast<uint32_t*>(&sv[i]);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                sw[k] = pack_bf16x2(bf16_lo(xw[k]) + bf16_lo(sw[k]), bf16_hi(xw[k]) + bf16_hi(sw[k]));
+            for (int k = 0; k < 4; ++k) sw[k] = pack_bf16x2(__fadd2_rn(bf16x2_to_float2(xw[k]), bf16x2_to_float2(sw[k])));
             store_stream(rr + (begin + threadIdx.x + i * blockDim.x), sv[i]);
         }
     }
 
     if constexpr (EP != kFp8Dynamic) {
         // 2. sum of squares (fp32) -> inv = 1 / sqrt(mean + eps)
-        float ss = 0.0f;
+        float2 ss2 = f2(0.0f);
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
             if (!live[i]) continue;
             const uint32_t* sw = reinterpret_cast<const uint32_t*>(&sv[i]);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                ss = fmaf(bf16_lo(sw[k]), bf16_lo(sw[k]), ss);
-                ss = fmaf(bf16_hi(sw[k]), bf16_hi(sw[k]), ss);
+                const float2 s2 = bf16x2_to_float2(sw[k]);
+                ss2 = __ffma2_rn(s2, s2, ss2);
             }
         }
-        ss = cta_allreduce(ss, red_sum, SumOp{});
+        float ss = cta_allreduce(ss2.x + ss2.y, red_sum, SumOp{});
         if (ctas_per_row > 1) {
             exchange_send(ex, make_float4(ss, 0.0f, 0.0f, 0.0f), rank, ctas_per_row);
             if (!exchange_wait(ex)) return;
@@ -122,7 +125,7 @@ __global__ void __launch_bounds__(512) add_rmsnorm_kernel(NormParams p, int ctas
                 uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    ow[k] = pack_bf16x2(bf16_lo(sw[k]) * bf16_lo(ww[k]) * inv, bf16_hi(sw[k]) * bf16_hi(ww[k]) * inv);
+                    ow[k] = pack_bf16x2(__fmul2_rn(__fmul2_rn(bf16x2_to_float2(sw[k]), bf16x2_to_float2(ww[k])), f2(inv)));
                 store_stream(outr + (begin + threadIdx.x + i * blockDim.x), o);
             }
         } else {
@@ -135,14 +138,12 @@ __global__ void __launch_bounds__(512) add_rmsnorm_kernel(NormParams p, int ctas
                 if (!live[i]) continue;
                 const uint32_t* sw = reinterpret_cast<const uint32_t*>(&sv[i]);
                 const uint32_t* ww = reinterpret_cast<const uint32_t*>(&wv[i]);
-                float y[8];
+                float2 y[4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    y[2 * k] = bf16_lo(sw[k]) * bf16_lo(ww[k]) * c;
-                    y[2 * k + 1] = bf16_hi(sw[k]) * bf16_hi(ww[k]) * c;
-                }
+                for (int k = 0; k < 4; ++k)
+                    y[k] = __fmul2_rn(__fmul2_rn(bf16x2_to_float2(sw[k]), bf16x2_to_float2(ww[k])), f2(c));
                 store_stream(outr + (begin + threadIdx.x + i * blockDim.x),
-                             make_uint2(pack_e4m3x4(y[0], y[1], y[2], y[3]), pack_e4m3x4(y[4], y[5], y[6], y[7])));
+                             make_uint2(pack_e4m3x4(y[0], y[1]), pack_e4m3x4(y[2], y[3])));
             }
         }
     } else {
@@ -151,7 +152,8 @@ __global__ void __launch_bounds__(512) add_rmsnorm_kernel(NormParams p, int ctas
         // fp64 definition does needs the row constants to ~1e-13: the sum of squares is kept as a
         // double-float, the per-row constants are formed in fp64 once per CTA, and every element is scaled
         // with a double-float multiplier.
-        RowStats st{DD{0.0f, 0.0f}, 0.0f};
+        DD2 acc{f2(0.0f), f2(0.0f)};
+        float pmax = 0.0f;
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
             if (!live[i]) continue;
@@ -159,12 +161,13 @@ __global__ void __launch_bounds__(512) add_rmsnorm_kernel(NormParams p, int ctas
             const uint32_t* ww = reinterpret_cast<const uint32_t*>(&wv[i]);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const float s0 = bf16_lo(sw[k]), s1 = bf16_hi(sw[k]);
-                dd_accumulate(st.sum_sq, s0 * s0);   // exact square of a bf16 value
-                dd_accumulate(st.sum_sq, s1 * s1);
-                st.pmax = fmaxf(st.pmax, fmaxf(fabsf(s0 * bf16_lo(ww[k])), fabsf(s1 * bf16_hi(ww[k]))));
+                const float2 s2 = bf16x2_to_float2(sw[k]);
+                dd_accumulate(acc, __fmul2_rn(s2, s2));   // exact squares of bf16 values
+                const float2 p2 = __fmul2_rn(s2, bf16x2_to_float2(ww[k]));
+                pmax = fmaxf(pmax, fmaxf(fabsf(p2.x), fabsf(p2.y)));
             }
         }
+        RowStats st{dd_add(DD{acc.hi.x, acc.lo.x}, DD{acc.hi.y, acc.lo.y}), pmax};
         st = cta_allreduce(st, red_stats);
         if (ctas_per_row > 1) {
             exchange_send(ex, make_float4(st.sum_sq.hi, st.sum_sq.lo, st.pmax, 0.0f), rank, ctas_per_row);
@@ -192,14 +195,12 @@ __global__ void __launch_bounds__(512) add_rmsnorm_kernel(NormParams p, int ctas
             if (!live[i]) continue;
             const uint32_t* sw = reinterpret_cast<const uint32_t*>(&sv[i]);
             const uint32_t* ww = reinterpret_cast<const uint32_t*>(&wv[i]);
-            float y[8];
+            float2 y[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                y[2 * k] = exact_side(bf16_lo(sw[k]) * bf16_lo(ww[k]), c_hi, c_lo);
-                y[2 * k + 1] = exact_side(bf16_hi(sw[k]) * bf16_hi(ww[k]), c_hi, c_lo);
-            }
+            for (int k = 0; k < 4; ++k)
+                y[k] = exact_side(__fmul2_rn(bf16x2_to_float2(sw[k]), bf16x2_to_float2(ww[k])), c_hi, c_lo);
             store_stream(outr + (begin + threadIdx.x + i * blockDim.x),
-                         make_uint2(pack_e4m3x4(y[0], y[1], y[2], y[3]), pack_e4m3x4(y[4], y[5], y[6], y[7])));
+                         make_uint2(pack_e4m3x4(y[0], y[1]), pack_e4m3x4(y[2], y[3])));
         }
     }
 }

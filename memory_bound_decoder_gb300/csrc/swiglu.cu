@@ -18,24 +18,36 @@ namespace mbd {
 
 namespace {
 
-// silu(g) * u = g * u / (1 + e^-g). e^-g = 2^(-g log2 e) is evaluated with the hardware base-2
-// exponential (ex2.approx) on the fp32-rounded argument t, corrected by 2^d ~ 1 + d ln 2 for the rounding
-// residual d = -g log2 e - t (obtained exactly with an FMA plus the low part of log2 e), so the error
-// does not grow with |g|. 1 / (1 + e) uses the hardware reciprocal (rcp.approx). g is clamped at -87
-// (e^87 < FLT_MAX) so e stays finite; below that silu is ~1e-36 either way.
-__device__ __forceinline__ float silu_times(float g, float u) {
+// silu(g) * u = g * u / (1 + e^-g) for a pair of elements, with packed fp32x2 arithmetic (FFMA2/FMUL2/
+// FADD2) around the two hardware transcendentals. e^-g = 2^(-g log2 e) comes from the base-2 exponential
+// (ex2.approx) of the fp32-rounded argument t, corrected by 2^d ~ 1 + d ln 2 for the rounding residual
+// d = -g log2 e - t (exact through an FMA plus the low part of log2 e), so the error does not grow with |g|;
+// 1 / (1 + e) comes from the hardware reciprocal (rcp.approx). g is clamped at -87 (e^87 < FLT_MAX) so e
+// stays finite; below that silu is ~1e-36 either way.
+__device__ __forceinline__ float ex2_approx(float t) {
+    float e;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(t));
+    return e;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ float2 silu_times(float2 g, float2 u) {
     constexpr float kLog2e = 1.44269502162933349609375f;   // log2(e) rounded to fp32
     constexpr float kLog2eLo = 1.925963033500011e-08f;     // log2(e) - kLog2e
     constexpr float kLn2 = 0.693147182464599609375f;
-    const float gc = fmaxf(g, -87.0f);
-    const float t = gc * -kLog2e;
-    const float d = fmaf(gc, -kLog2eLo, fmaf(gc, -kLog2e, -t));
-    float e;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(t));
-    e = fmaf(e, d * kLn2, e);
-    float r;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
-    return g * r * u;
+    const float2 gc = make_float2(fmaxf(g.x, -87.0f), fmaxf(g.y, -87.0f));
+    const float2 t = __fmul2_rn(gc, f2(-kLog2e));
+    const float2 d = __ffma2_rn(gc, f2(-kLog2eLo), __ffma2_rn(gc, f2(-kLog2e), make_float2(-t.x, -t.y)));
+    float2 e = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+    e = __ffma2_rn(e, __fmul2_rn(d, f2(kLn2)), e);
+    const float2 den = __fadd2_rn(e, f2(1.0f));
+    const float2 r = make_float2(rcp_approx(den.x), rcp_approx(den.y));
+    return __fmul2_rn(__fmul2_rn(g, r), u);
 }
 
 template <int VPT, int EP>
@@ -78,14 +90,12 @@ __global__ void __launch_bounds__(512) swiglu_kernel(SwigluParams p, int ctas_pe
             uint4 o;
             uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                ow[k] = pack_bf16x2(silu_times(bf16_lo(gw[k]), bf16_lo(uw[k])),
-                                    silu_times(bf16_hi(gw[k]), bf16_hi(uw[k])));
+            for (int k = 0; k < 4; ++k) ow[k] = pack_bf16x2(silu_times(bf16x2_to_float2(gw[k]), bf16x2_to_float2(uw[k])));
             store_stream(outr + (begin + threadIdx.x + i * blockDim.x), o);
         }
     } else {
         uint2* outr = reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + row * (int64_t)p.nvec * 8);
-        float h[VPT][8];
+        float2 h[VPT][4];
         float qmul;
         if constexpr (EP == kFp8Static) {
             const float sc = __ldg(p.scale);
@@ -99,10 +109,8 @@ __global__ void __launch_bounds__(512) swiglu_kernel(SwigluParams p, int ctas_pe
             const uint32_t* uw = reinterpret_cast<const uint32_t*>(&uv[i]);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                h[i][2 * k] = silu_times(bf16_lo(gw[k]), bf16_lo(uw[k]));
-                h[i][2 * k + 1] = silu_times(bf16_hi(gw[k]), bf16_hi(uw[k]));
-                if constexpr (EP == kFp8Dynamic)
-                    amax = fmaxf(amax, fmaxf(fabsf(h[i][2 * k]), fabsf(h[i][2 * k + 1])));
+                h[i][k] = silu_times(bf16x2_to_float2(gw[k]), bf16x2_to_float2(uw[k]));
+                if constexpr (EP == kFp8Dynamic) amax = fmaxf(amax, fmaxf(fabsf(h[i][k].x), fabsf(h[i][k].y)));
             }
         }
         if constexpr (EP == kFp8Dynamic) {
@@ -119,9 +127,10 @@ __global__ void __launch_bounds__(512) swiglu_kernel(SwigluParams p, int ctas_pe
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
             if (!live[i]) continue;
+            const float2 q2 = f2(qmul);
             uint2 q;
-            q.x = pack_e4m3x4(h[i][0] * qmul, h[i][1] * qmul, h[i][2] * qmul, h[i][3] * qmul);
-            q.y = pack_e4m3x4(h[i][4] * qmul, h[i][5] * qmul, h[i][6] * qmul, h[i][7] * qmul);
+            q.x = pack_e4m3x4(__fmul2_rn(h[i][0], q2), __fmul2_rn(h[i][1], q2));
+            q.y = pack_e4m3x4(__fmul2_rn(h[i][2], q2), __fmul2_rn(h[i][3], q2));
             store_stream(outr + (begin + threadIdx.x + i * blockDim.x), q);
         }
     }
