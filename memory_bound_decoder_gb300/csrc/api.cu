@@ -3,9 +3,8 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
-#include <mutex>
 
-#include "../../include/mbd.h"
+#include "mbd.h"
 #include "launch.h"
 
 namespace {
@@ -40,29 +39,57 @@ bool overlap(const void* a, size_t na, const void* b, size_t nb) {
 constexpr int kMaxClusterCtas = 8;   // portable cluster size (also the exchange's slot count)
 constexpr int kMaxThreads = 512;     // matches __launch_bounds__ of the kernels
 
-// Choose how a launch covers [rows, nvec]. Large batches give each row one CTA (no cluster traffic);
-// small batches split each row over a cluster so that enough SMs pull bytes from HBM at once. A CTA aims
-// for at most 256 threads and picks the fewest vectors per thread that keeps it there.
-bool plan_rows(int64_t rows, int nvec, bool reduces, int sms, mbd::RowPlan* plan) {
-    const int max_cta_vec = 256 * 4;
-    int c = (nvec + max_cta_vec - 1) / max_cta_vec;
+// What a launch reduces over each row: the norm's sum of squares, the dynamic SwiGLU's max |h|, or
+// nothing (pure streams, whose row slices are independent CTAs without a cluster).
+enum class Shape { kNorm, kRowMax, kStream };
+
+int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// Launch shape, chosen from a sweep of CTAs per row x vectors per thread x threads on GB300 (back-to-back
+// launches, inputs larger than L2):
+//  - at least one row per SM (large batches):
+//      norm: one CTA per row while the row fits 512 threads x 4 vectors (hidden <= 16384), the fewest
+//            vectors per thread (>= 2) that keep the CTA at <= 512 threads -- no cluster exchange at all;
+//      dynamic SwiGLU: rows cut into about 512-vector slices over a cluster of up to 8 CTAs, 2 vectors per
+//            thread (many small CTAs hide the latency of the amax exchange);
+//      streams: slices of <= 1024 vectors, <= 256 threads.
+//  - fewer rows than SMs (decode): each row is split further so that about two CTAs per SM pull bytes
+//    at once; rows that reduce keep to one cluster of at most 8 CTAs.
+bool plan_rows(int64_t rows, int nvec, Shape shape, int sms, mbd::RowPlan* plan) {
+    const bool reduces = shape != Shape::kStream;
+    int c;
+    if (shape == Shape::kNorm) {
+        c = cdiv(nvec, 2048);
+    } else if (shape == Shape::kRowMax) {
+        c = cdiv(nvec, 512);
+    } else {
+        c = cdiv(nvec, 1024);
+    }
+    int min_vpt = shape == Shape::kStream ? 1 : 2;
+    int max_threads = shape == Shape::kStream ? 256 : kMaxThreads;
     if (rows < sms) {
         int want = static_cast<int>((2 * sms + rows - 1) / rows);  // about two CTAs per SM
-        int by_width = (nvec + 31) / 32;                          // keep at least a warp of vectors per CTA
+        int by_width = cdiv(nvec, 32);                              // keep at least a warp of vectors per CTA
         if (want > by_width) want = by_width;
         if (want > c) c = want;
+        min_vpt = 1;
+        max_threads = 256;
     }
-    if (reduces && c > kMaxClusterCtas) {
-        c = kMaxClusterCtas;
-    }
+    if (reduces && c > kMaxClusterCtas) c = kMaxClusterCtas;
     if (c < 1) c = 1;
-    const int slice = (nvec + c - 1) / c;
-    int vpt = 8;
+    const int slice = cdiv(nvec, c);
+    c = cdiv(nvec, slice);  // no empty slice
+    int vpt = 0;
     for (int v : {1, 2, 4, 8}) {
-        if ((slice + v - 1) / v <= 256) { vpt = v; break; }
+        if (v >= min_vpt && cdiv(slice, v) <= max_threads) {
+            vpt = v;
+            break;
+        }
     }
-    int threads = (slice + vpt - 1) / vpt;
-    threads = (threads + 31) / 32 * 32;
+    if (vpt == 0) {  // very wide rows: 8 vectors per thread and as many threads as needed
+        vpt = 8;
+    }
+    int threads = cdiv(cdiv(slice, vpt), 32) * 32;
     if (threads > kMaxThreads) return false;
     plan->ctas_per_row = c;
     plan->slice = slice;
@@ -117,7 +144,7 @@ mbd_status norm_common(void* out, size_t out_elem, void* residual, const void* x
     if (quant && !dyn && overlap(scale, sb, out, outb)) return MBD_ERR_INVALID_ARG;
 
     mbd::RowPlan plan;
-    if (!plan_rows(n_tokens, static_cast<int>(hidden / 8), true, sm_count_of_current_device(), &plan))
+    if (!plan_rows(n_tokens, static_cast<int>(hidden / 8), Shape::kNorm, sm_count_of_current_device(), &plan))
         return MBD_ERR_UNSUPPORTED;
     mbd::NormParams p{x, residual, weight, out, scale, n_tokens, static_cast<int>(hidden / 8),
                       static_cast<int>(hidden), eps};
@@ -144,7 +171,8 @@ mbd_status swiglu_common(void* out, size_t out_elem, const void* gate_up, int64_
     if (dyn && overlap(scale, sb, gate_up, inb)) return MBD_ERR_INVALID_ARG;
 
     mbd::RowPlan plan;
-    if (!plan_rows(n_tokens, static_cast<int>(inter / 8), dyn, sm_count_of_current_device(), &plan))
+    if (!plan_rows(n_tokens, static_cast<int>(inter / 8), dyn ? Shape::kRowMax : Shape::kStream,
+                   sm_count_of_current_device(), &plan))
         return MBD_ERR_UNSUPPORTED;
     mbd::SwigluParams p{gate_up, out, scale, n_tokens, static_cast<int>(inter / 8)};
     const mbd::Epilogue ep = !quant ? mbd::kBf16 : (dyn ? mbd::kFp8Dynamic : mbd::kFp8Static);

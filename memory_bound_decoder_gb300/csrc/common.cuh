@@ -93,6 +93,8 @@ __device__ __forceinline__ float cta_allreduce(float v, float* scratch, Op op) {
 // the host through mbd_device_error_flags(). Bits: kDevErrExchangeTimeout.
 static __device__ unsigned int g_device_error_flags;
 constexpr unsigned int kDevErrExchangeTimeout = 1u;
+// Bound of every spin-wait, in SM clock cycles (about one second at 2 GHz).
+constexpr long long kWaitLimitCycles = 2LL << 30;
 
 // Partial results of the CTAs of one row are exchanged through distributed shared memory: every CTA
 // pushes its 16-byte partial into slot[my_rank] of every peer with st.async, whose completion is counted
@@ -152,7 +154,7 @@ __device__ __forceinline__ bool exchange_wait(Exchange& ex) {
                      : "r"(mb)
                      : "memory");
         if (done) break;
-        if (clock64() - t0 > (2LL << 30)) {
+        if (clock64() - t0 > kWaitLimitCycles) {
             atomicOr(&g_device_error_flags, kDevErrExchangeTimeout);
             break;
         }

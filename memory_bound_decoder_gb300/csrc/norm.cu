@@ -207,6 +207,8 @@ __global__ void __launch_bounds__(512) add_rmsnorm_kernel(NormParams p, int ctas
 
 template <int EP>
 cudaError_t launch_ep(const NormParams& p, const RowPlan& plan, cudaStream_t s) {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
     void (*kern)(NormParams, int, int) = nullptr;
     switch (plan.vpt) {
         case 1: kern = add_rmsnorm_kernel<1, EP>; break;
@@ -215,8 +217,6 @@ cudaError_t launch_ep(const NormParams& p, const RowPlan& plan, cudaStream_t s) 
         case 8: kern = add_rmsnorm_kernel<8, EP>; break;
         default: return cudaErrorInvalidValue;
     }
-    cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[2];
     fill_launch(cfg, attr, p.rows * plan.ctas_per_row, plan.threads, plan.ctas_per_row, s);
     return cudaLaunchKernelEx(&cfg, kern, p, plan.ctas_per_row, plan.slice);
 }

@@ -138,6 +138,9 @@ __global__ void __launch_bounds__(512) swiglu_kernel(SwigluParams p, int ctas_pe
 
 template <int EP>
 cudaError_t launch_ep(const SwigluParams& p, const RowPlan& plan, cudaStream_t s) {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    const int cluster = EP == kFp8Dynamic ? plan.ctas_per_row : 1;
     void (*kern)(SwigluParams, int, int) = nullptr;
     switch (plan.vpt) {
         case 1: kern = swiglu_kernel<1, EP>; break;
@@ -146,10 +149,7 @@ cudaError_t launch_ep(const SwigluParams& p, const RowPlan& plan, cudaStream_t s
         case 8: kern = swiglu_kernel<8, EP>; break;
         default: return cudaErrorInvalidValue;
     }
-    cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[2];
-    fill_launch(cfg, attr, p.rows * plan.ctas_per_row, plan.threads,
-                EP == kFp8Dynamic ? plan.ctas_per_row : 1, s);
+    fill_launch(cfg, attr, p.rows * plan.ctas_per_row, plan.threads, cluster, s);
     return cudaLaunchKernelEx(&cfg, kern, p, plan.ctas_per_row, plan.slice);
 }
 

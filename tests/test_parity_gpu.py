@@ -131,10 +131,13 @@ def check_swiglu(inp, ep, mode=None, static_scale=0.05, rows=None, **kw):
 
 # ------------------------------------------------------------------------------------------------ small / ragged
 
+# The first rows use the direct (one launch wave) form; shapes with at least two units per SM use the
+# persistent pipelined form: (320, 5000) ragged slices, (400, 32768) a row split over a 2-CTA cluster,
+# (304, 53248) a dynamic SwiGLU row over a 4-CTA cluster, (500, 3000) ragged chunks.
 NORM_SHAPES = [(16, 1536), (1, 1536), (3, 5120), (17, 5120), (7, 8), (5, 24), (33, 520), (2, 1000),
-               (64, 4096), (4, 16384), (300, 1536), (2, 262144)]
+               (64, 4096), (4, 16384), (300, 1536), (2, 262144), (320, 5000), (400, 32768), (1200, 1536)]
 SWIGLU_SHAPES = [(16, 8960), (1, 13824), (3, 13824), (17, 13824), (5, 8), (9, 24), (3, 1000), (2, 53248),
-                 (200, 8960), (1, 262144)]
+                 (200, 8960), (1, 262144), (400, 13824), (304, 53248), (500, 3000), (700, 256)]
 EPS = [("bf16", None), ("q8", "static"), ("q8", "dynamic")]
 
 
