@@ -98,6 +98,13 @@ uint64_t mbd_kernel_launches(void);
  * for a null flags pointer, MBD_ERR_CUDA if the copy fails. */
 mbd_status mbd_device_error_flags(uint32_t* flags, int clear);
 
+/* Self-test of the failure path (no counterpart on the source pages): launches one warp that waits on an
+ * mbarrier which nothing will ever complete, with a wait limit of limit_cycles SM clock cycles
+ * (1 <= limit_cycles <= 2^31, about one second at 2 GHz). The wait runs out, the kernel sets
+ * MBD_DEVERR_EXCHANGE_TIMEOUT and returns; the context stays usable. Returns MBD_ERR_INVALID_ARG for a
+ * limit out of range. Asynchronous on `stream` like every launch. */
+mbd_status mbd_selftest_bounded_wait(uint64_t limit_cycles, mbd_stream_t stream);
+
 /*
  * Fused residual add + RMSNorm [TRT].
  *   For every row t < n_tokens and column j < hidden:

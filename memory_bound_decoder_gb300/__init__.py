@@ -45,6 +45,8 @@ def _load() -> ctypes.CDLL:
     lib.mbd_kernel_launches.restype = ctypes.c_uint64
     lib.mbd_device_error_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32), cint]
     lib.mbd_device_error_flags.restype = cint
+    lib.mbd_selftest_bounded_wait.argtypes = [ctypes.c_uint64, vp]
+    lib.mbd_selftest_bounded_wait.restype = cint
     lib.mbd_fused_add_rmsnorm.argtypes = [vp, vp, vp, vp, i64, i64, f32, vp]
     lib.mbd_fused_add_rmsnorm_quant_fp8.argtypes = [vp, vp, vp, vp, i64, i64, f32, cint, vp, vp]
     lib.mbd_swiglu.argtypes = [vp, vp, i64, i64, vp]
@@ -134,6 +136,11 @@ def device_error_flags(clear: bool = False) -> int:
     v = ctypes.c_uint32(0)
     _check(get_lib().mbd_device_error_flags(ctypes.byref(v), int(bool(clear))), "device_error_flags")
     return int(v.value)
+
+
+def selftest_bounded_wait(limit_cycles: int, stream=None) -> None:
+    """Launch the self-test kernel whose wait can only time out (sets DEVERR_EXCHANGE_TIMEOUT)."""
+    _check(get_lib().mbd_selftest_bounded_wait(int(limit_cycles), _stream(stream)), "selftest_bounded_wait")
 
 
 def fused_add_rmsnorm(out, residual, x, weight, n_tokens: int, hidden: int, eps: float, stream=None) -> None:

@@ -202,16 +202,24 @@ uint64_t mbd_kernel_launches(void) { return g_launches.load(std::memory_order_re
 
 mbd_status mbd_device_error_flags(uint32_t* flags, int clear) {
     if (!flags) return MBD_ERR_INVALID_ARG;
-    unsigned int a = 0, b = 0;
+    unsigned int a = 0, b = 0, c = 0;
     cudaError_t e = mbd::device_error_flags_norm(&a, clear != 0);
     if (e == cudaSuccess) e = mbd::device_error_flags_swiglu(&b, clear != 0);
+    if (e == cudaSuccess) e = mbd::device_error_flags_selftest(&c, clear != 0);
     if (e != cudaSuccess) {
         g_last_cuda_error = static_cast<int>(e);
         (void)cudaGetLastError();
         return MBD_ERR_CUDA;
     }
-    *flags = a | b;
+    *flags = a | b | c;
     return MBD_OK;
+}
+
+mbd_status mbd_selftest_bounded_wait(uint64_t limit_cycles, mbd_stream_t stream) {
+    if (limit_cycles == 0 || limit_cycles > (uint64_t{1} << 31)) return MBD_ERR_INVALID_ARG;
+    const cudaError_t e =
+        mbd::launch_bounded_wait_probe(static_cast<long long>(limit_cycles), reinterpret_cast<cudaStream_t>(stream));
+    return finish_launch(e);
 }
 
 mbd_status mbd_fused_add_rmsnorm(void* out, void* residual, const void* x, const void* weight,

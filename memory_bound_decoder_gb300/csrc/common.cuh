@@ -55,38 +55,6 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
 __device__ __forceinline__ uint32_t pack_bf16x2(float2 v) { return pack_bf16x2(v.x, v.y); }
 __device__ __forceinline__ uint32_t pack_e4m3x4(float2 a, float2 b) { return pack_e4m3x4(a.x, a.y, b.x, b.y); }
 
-// ------------------------------------------------------------------------------------------ reductions
-
-struct SumOp {
-    __device__ __forceinline__ float operator()(float a, float b) const { return a + b; }
-};
-struct MaxOp {
-    __device__ __forceinline__ float operator()(float a, float b) const { return fmaxf(a, b); }
-};
-
-// Butterfly (xor) reduction: every lane ends with the same value because each step combines the same
-// two operands on both partner lanes.
-template <class Op>
-__device__ __forceinline__ float warp_allreduce(float v, Op op) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-
-// CTA-wide reduction; every thread returns the same total. Inputs are sums or magnitudes (>= 0), so 0
-// is the identity for both operators. `scratch` holds one float per warp and may be
-// reused only after a __syncthreads() that follows this call.
-template <class Op>
-__device__ __forceinline__ float cta_allreduce(float v, float* scratch, Op op) {
-    v = warp_allreduce(v, op);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (lane == 0) scratch[warp] = v;
-    __syncthreads();
-    const int nwarps = (blockDim.x + 31) >> 5;
-    float t = lane < nwarps ? scratch[lane] : 0.0f;
-    return warp_allreduce(t, op);
-}
-
 // ------------------------------------------------------------------------------------------ cluster exchange
 
 // Device-side error word of each kernel translation unit (internal linkage, one per .cu file), read on
@@ -125,10 +93,10 @@ __device__ __forceinline__ void exchange_init(Exchange& ex, int nctas) {
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
-// Thread 0 publishes this CTA's partial; lanes of warp 0 push it to the peers in parallel.
+// Called by warp 0 only: lane 0 publishes this CTA's partial in its own slot, lanes 0..nctas-1 push it
+// into the same slot of every peer.
 __device__ __forceinline__ void exchange_send(Exchange& ex, float4 v, int my_rank, int nctas) {
-    if (threadIdx.x >= 32) return;
-    const int lane = threadIdx.x;
+    const int lane = threadIdx.x & 31;
     if (lane == 0) ex.slot[my_rank] = v;
     if (lane < nctas && lane != my_rank) {
         uint32_t rslot, rbar;
@@ -141,25 +109,86 @@ __device__ __forceinline__ void exchange_send(Exchange& ex, float4 v, int my_ran
     }
 }
 
-// Wait until every peer's partial has landed (phase 0 of the mbarrier); all threads poll and the result
-// is made CTA-uniform. Gives up after about one second of SM clock, sets kDevErrExchangeTimeout and
-// returns false, so a stuck exchange ends the kernel instead of hanging the GPU.
-__device__ __forceinline__ bool exchange_wait(Exchange& ex) {
-    const uint32_t mb = smem_addr(&ex.mbar);
+// Called by warp 0 only: lane 0 polls the mbarrier until every peer's bytes have landed (phase 0), then
+// the warp synchronises so that all its lanes may read slot[]. Gives up after kWaitLimitCycles, sets
+// kDevErrExchangeTimeout and returns false on every lane.
+__device__ __forceinline__ bool exchange_wait_warp(Exchange& ex, long long limit = kWaitLimitCycles) {
     uint32_t done = 0;
-    const long long t0 = clock64();
-    while (true) {
-        asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n selp.u32 %0, 1, 0, p;\n}"
-                     : "=r"(done)
-                     : "r"(mb)
-                     : "memory");
-        if (done) break;
-        if (clock64() - t0 > kWaitLimitCycles) {
-            atomicOr(&g_device_error_flags, kDevErrExchangeTimeout);
-            break;
+    if ((threadIdx.x & 31) == 0) {
+        const uint32_t mb = smem_addr(&ex.mbar);
+        const long long t0 = clock64();
+        while (true) {
+            asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n selp.u32 %0, 1, 0, p;\n}"
+                         : "=r"(done)
+                         : "r"(mb)
+                         : "memory");
+            if (done || clock64() - t0 > limit) break;
+        }
+        if (!done) atomicOr(&g_device_error_flags, kDevErrExchangeTimeout);
+    }
+    __syncwarp();
+    return __shfl_sync(0xffffffffu, done, 0) != 0;
+}
+
+// ------------------------------------------------------------------------------------------ row reduction
+
+// Partial results reduced over a row. Each provides combine (commutative in its exact result, so a
+// butterfly leaves every lane identical), shuffles, and packing into the 16-byte exchange slot.
+struct PSum {
+    float v;
+    __device__ __forceinline__ static PSum combine(PSum a, PSum b) { return PSum{a.v + b.v}; }
+    __device__ __forceinline__ PSum shfl_xor(int o) const { return PSum{__shfl_xor_sync(0xffffffffu, v, o)}; }
+    __device__ __forceinline__ float4 pack() const { return make_float4(v, 0.0f, 0.0f, 0.0f); }
+    __device__ __forceinline__ static PSum unpack(float4 f) { return PSum{f.x}; }
+    __device__ __forceinline__ static PSum zero() { return PSum{0.0f}; }
+};
+
+struct PMax {   // of magnitudes (>= 0)
+    float v;
+    __device__ __forceinline__ static PMax combine(PMax a, PMax b) { return PMax{fmaxf(a.v, b.v)}; }
+    __device__ __forceinline__ PMax shfl_xor(int o) const { return PMax{__shfl_xor_sync(0xffffffffu, v, o)}; }
+    __device__ __forceinline__ float4 pack() const { return make_float4(v, 0.0f, 0.0f, 0.0f); }
+    __device__ __forceinline__ static PMax unpack(float4 f) { return PMax{f.x}; }
+    __device__ __forceinline__ static PMax zero() { return PMax{0.0f}; }
+};
+
+template <class P>
+__device__ __forceinline__ P warp_allreduce_p(P v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = P::combine(v, v.shfl_xor(o));
+    return v;
+}
+
+// Reduce one value per thread over the whole row. Every warp reduces its lanes; warp 0 combines the warps
+// and, when the row spans a cluster, pushes the CTA's partial to the peers and combines theirs in rank
+// order (the same order in every CTA, so all CTAs of the row get identical bits); then `fin` runs on warp 0
+// lane 0 with the row total and may publish derived constants to shared memory before the closing barrier.
+// The other warps issue nothing while they wait at the two CTA barriers. Returns false (in every thread)
+// if the cluster exchange timed out.
+template <class P, class Fin>
+__device__ __forceinline__ bool row_reduce(P mine, P* warp_part, Exchange& ex, int rank, int nctas, int* ok_flag,
+                                           Fin fin) {
+    mine = warp_allreduce_p(mine);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) warp_part[warp] = mine;
+    __syncthreads();
+    if (warp == 0) {
+        const int nwarps = (blockDim.x + 31) >> 5;
+        P t = warp_allreduce_p(lane < nwarps ? warp_part[lane] : P::zero());
+        bool ok = true;
+        if (nctas > 1) {
+            exchange_send(ex, t.pack(), rank, nctas);
+            ok = exchange_wait_warp(ex);
+            t = P::unpack(ex.slot[0]);
+            for (int r = 1; r < nctas; ++r) t = P::combine(t, P::unpack(ex.slot[r]));
+        }
+        if (lane == 0) {
+            *ok_flag = ok;
+            if (ok) fin(t);
         }
     }
-    return __syncthreads_and(static_cast<int>(done)) != 0;
+    __syncthreads();
+    return *ok_flag != 0;
 }
 
 // ------------------------------------------------------------------------------------------ PDL
@@ -220,32 +249,18 @@ __device__ __forceinline__ DD dd_add(DD a, DD b) {
 struct RowStats {
     DD sum_sq;
     float pmax;
+    __device__ __forceinline__ static RowStats combine(RowStats a, RowStats b);
+    __device__ __forceinline__ RowStats shfl_xor(int o) const {
+        return RowStats{DD{__shfl_xor_sync(0xffffffffu, sum_sq.hi, o), __shfl_xor_sync(0xffffffffu, sum_sq.lo, o)},
+                        __shfl_xor_sync(0xffffffffu, pmax, o)};
+    }
+    __device__ __forceinline__ float4 pack() const { return make_float4(sum_sq.hi, sum_sq.lo, pmax, 0.0f); }
+    __device__ __forceinline__ static RowStats unpack(float4 f) { return RowStats{DD{f.x, f.y}, f.z}; }
+    __device__ __forceinline__ static RowStats zero() { return RowStats{DD{0.0f, 0.0f}, 0.0f}; }
 };
 
-__device__ __forceinline__ RowStats combine(RowStats a, RowStats b) {
+__device__ __forceinline__ RowStats RowStats::combine(RowStats a, RowStats b) {
     return RowStats{dd_add(a.sum_sq, b.sum_sq), fmaxf(a.pmax, b.pmax)};
-}
-
-__device__ __forceinline__ RowStats shfl_xor(RowStats v, int o) {
-    return RowStats{DD{__shfl_xor_sync(0xffffffffu, v.sum_sq.hi, o), __shfl_xor_sync(0xffffffffu, v.sum_sq.lo, o)},
-                    __shfl_xor_sync(0xffffffffu, v.pmax, o)};
-}
-
-__device__ __forceinline__ RowStats warp_allreduce(RowStats v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = combine(v, shfl_xor(v, o));
-    return v;
-}
-
-// CTA-wide reduction of RowStats; every thread returns the same value. `scratch` holds 32 entries.
-__device__ __forceinline__ RowStats cta_allreduce(RowStats v, RowStats* scratch) {
-    v = warp_allreduce(v);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (lane == 0) scratch[warp] = v;
-    __syncthreads();
-    const int nwarps = (blockDim.x + 31) >> 5;
-    const RowStats zero{DD{0.0f, 0.0f}, 0.0f};
-    return warp_allreduce(lane < nwarps ? scratch[lane] : zero);
 }
 
 }  // namespace mbd

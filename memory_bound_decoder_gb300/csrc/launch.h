@@ -49,6 +49,10 @@ cudaError_t launch_swiglu(const SwigluParams& p, Epilogue ep, const RowPlan& pla
 // Read (and optionally clear) the device error word of each kernel translation unit (synchronous).
 cudaError_t device_error_flags_norm(unsigned int* flags, bool clear);
 cudaError_t device_error_flags_swiglu(unsigned int* flags, bool clear);
+cudaError_t device_error_flags_selftest(unsigned int* flags, bool clear);
+
+// Launch the bounded-wait self-test kernel (one warp).
+cudaError_t launch_bounded_wait_probe(long long limit_cycles, cudaStream_t s);
 
 // Fill a launch configuration: grid/block, the cluster attribute when cluster > 1, and PDL.
 inline void fill_launch(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int64_t ctas, int threads,

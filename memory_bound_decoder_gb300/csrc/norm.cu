@@ -39,10 +39,11 @@ __device__ __forceinline__ float2 exact_side(float2 p, float c_hi, float c_lo) {
 
 template <int VPT, int EP>
 __global__ void __launch_bounds__(512) add_rmsnorm_kernel(NormParams p, int ctas_per_row, int slice) {
-    __shared__ float red_sum[32];
-    __shared__ RowStats red_stats[32];
+    __shared__ PSum part_sum[32];
+    __shared__ RowStats part_stats[32];
     __shared__ Exchange ex;
     __shared__ float row_const[2];
+    __shared__ int ok_flag;
     // The weight is an L2 hit; load it up front when registers allow (small rows, latency-bound), else
     // after the reduction. The dynamic variant needs it before the reduction anyway.
     constexpr bool kEarlyWeight = EP == kFp8Dynamic || VPT <= 2;
@@ -98,14 +99,11 @@ __global__ void __launch_bounds__(512) add_rmsnorm_kernel(NormParams p, int ctas
                 ss2 = __ffma2_rn(s2, s2, ss2);
             }
         }
-        float ss = cta_allreduce(ss2.x + ss2.y, red_sum, SumOp{});
-        if (ctas_per_row > 1) {
-            exchange_send(ex, make_float4(ss, 0.0f, 0.0f, 0.0f), rank, ctas_per_row);
-            if (!exchange_wait(ex)) return;
-            ss = 0.0f;
-            for (int r = 0; r < ctas_per_row; ++r) ss += ex.slot[r].x;   // rank order: same in every CTA
-        }
-        const float inv = 1.0f / sqrtf(ss / static_cast<float>(p.hidden) + p.eps);
+        if (!row_reduce(PSum{ss2.x + ss2.y}, part_sum, ex, rank, ctas_per_row, &ok_flag, [&](PSum t) {
+                row_const[0] = 1.0f / sqrtf(t.v / static_cast<float>(p.hidden) + p.eps);
+            }))
+            return;
+        const float inv = row_const[0];
 
         if constexpr (!kEarlyWeight) {
 #pragma unroll
@@ -167,27 +165,19 @@ __global__ void __launch_bounds__(512) add_rmsnorm_kernel(NormParams p, int ctas
                 pmax = fmaxf(pmax, fmaxf(fabsf(p2.x), fabsf(p2.y)));
             }
         }
-        RowStats st{dd_add(DD{acc.hi.x, acc.lo.x}, DD{acc.hi.y, acc.lo.y}), pmax};
-        st = cta_allreduce(st, red_stats);
-        if (ctas_per_row > 1) {
-            exchange_send(ex, make_float4(st.sum_sq.hi, st.sum_sq.lo, st.pmax, 0.0f), rank, ctas_per_row);
-            if (!exchange_wait(ex)) return;
-            st = RowStats{DD{ex.slot[0].x, ex.slot[0].y}, ex.slot[0].z};
-            for (int r = 1; r < ctas_per_row; ++r)
-                st = combine(st, RowStats{DD{ex.slot[r].x, ex.slot[r].y}, ex.slot[r].z});
-        }
-        if (threadIdx.x == 0) {
-            const double mean_sq = (static_cast<double>(st.sum_sq.hi) + static_cast<double>(st.sum_sq.lo)) /
-                                   static_cast<double>(p.hidden);
-            const double inv = 1.0 / sqrt(mean_sq + static_cast<double>(p.eps));
-            const float sc = static_cast<float>(static_cast<double>(st.pmax) * inv / 448.0);
-            const double c = sc > 0.0f ? inv / static_cast<double>(sc) : 0.0;
-            const float c_hi = static_cast<float>(c);
-            row_const[0] = c_hi;
-            row_const[1] = static_cast<float>(c - static_cast<double>(c_hi));
-            if (rank == 0) p.scale[row] = sc;
-        }
-        __syncthreads();
+        const RowStats mine{dd_add(DD{acc.hi.x, acc.lo.x}, DD{acc.hi.y, acc.lo.y}), pmax};
+        if (!row_reduce(mine, part_stats, ex, rank, ctas_per_row, &ok_flag, [&](RowStats st) {
+                const double mean_sq = (static_cast<double>(st.sum_sq.hi) + static_cast<double>(st.sum_sq.lo)) /
+                                       static_cast<double>(p.hidden);
+                const double inv = 1.0 / sqrt(mean_sq + static_cast<double>(p.eps));
+                const float sc = static_cast<float>(static_cast<double>(st.pmax) * inv / 448.0);
+                const double c = sc > 0.0f ? inv / static_cast<double>(sc) : 0.0;
+                const float c_hi = static_cast<float>(c);
+                row_const[0] = c_hi;
+                row_const[1] = static_cast<float>(c - static_cast<double>(c_hi));
+                if (rank == 0) p.scale[row] = sc;
+            }))
+            return;
         const float c_hi = row_const[0], c_lo = row_const[1];
         uint2* outr = reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + row * (int64_t)p.nvec * 8);
 #pragma unroll

@@ -52,8 +52,10 @@ __device__ __forceinline__ float2 silu_times(float2 g, float2 u) {
 
 template <int VPT, int EP>
 __global__ void __launch_bounds__(512) swiglu_kernel(SwigluParams p, int ctas_per_row, int slice) {
-    __shared__ float red_max[32];
+    __shared__ PMax part_max[32];
     __shared__ Exchange ex;
+    __shared__ float row_qmul;
+    __shared__ int ok_flag;
 
     const int64_t row = blockIdx.x / ctas_per_row;
     const int rank = blockIdx.x - static_cast<int>(row * ctas_per_row);
@@ -114,15 +116,13 @@ __global__ void __launch_bounds__(512) swiglu_kernel(SwigluParams p, int ctas_pe
             }
         }
         if constexpr (EP == kFp8Dynamic) {
-            amax = cta_allreduce(amax, red_max, MaxOp{});
-            if (ctas_per_row > 1) {
-                exchange_send(ex, make_float4(amax, 0.0f, 0.0f, 0.0f), rank, ctas_per_row);
-                if (!exchange_wait(ex)) return;
-                for (int r = 0; r < ctas_per_row; ++r) amax = fmaxf(amax, ex.slot[r].x);
-            }
-            const float sc = amax / 448.0f;
-            qmul = sc > 0.0f ? 1.0f / sc : 0.0f;
-            if (rank == 0 && threadIdx.x == 0) p.scale[row] = sc;
+            if (!row_reduce(PMax{amax}, part_max, ex, rank, ctas_per_row, &ok_flag, [&](PMax t) {
+                    const float sc = t.v / 448.0f;
+                    row_qmul = sc > 0.0f ? 1.0f / sc : 0.0f;
+                    if (rank == 0) p.scale[row] = sc;
+                }))
+                return;
+            qmul = row_qmul;
         }
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {

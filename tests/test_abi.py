@@ -105,6 +105,11 @@ def test_device_error_flags_rejects_null(lib):
     assert lib.mbd_device_error_flags(None, 0) == mbd.ERR_INVALID_ARG
 
 
+def test_selftest_limit_validated(lib):
+    assert _rc(mbd.selftest_bounded_wait, 0) == mbd.ERR_INVALID_ARG
+    assert _rc(mbd.selftest_bounded_wait, (1 << 31) + 1) == mbd.ERR_INVALID_ARG
+
+
 def test_raw_ctypes_signature(lib):
     # the C entry points are callable without the Python binding
     fn = lib.mbd_swiglu
