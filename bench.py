@@ -41,7 +41,12 @@ DEFAULT_WORKLOAD = "llama3.1-405b_fp8_T2048+ragged"
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel, from the ncu capture
 # summarised under profiles/; valid only while the CUDA sources hash to `csrc_sha256`.
-TRAFFIC: Dict[str, Dict] = {}
+TRAFFIC: Dict[str, Dict] = {
+    # profiles/swiglu_q8_dynamic_T2048_I53248.md
+    "swiglu_q8_dynamic_T2048_I53248": {"bytes": 516177152, "csrc_sha256": "4db943e5aa83d84a61ed488720469f49bdc4898b15866e694590ed5e160a4c43"},
+    # profiles/add_rmsnorm_q8_static_T2048_H16384.md
+    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 177876992, "csrc_sha256": "4db943e5aa83d84a61ed488720469f49bdc4898b15866e694590ed5e160a4c43"},
+}
 
 
 def log(*a):
@@ -234,6 +239,25 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(inside), "basis": basis}
 
 
+# ------------------------------------------------------------------------------------------------ ranks
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Maximum of a per-rank value over all ranks (the slowest rank sets the job's time); identity
+    without a process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_rate(bytes_per_step: int, steps: int, world: int, ms: float) -> float:
+    """Whole-job GB/s: every rank processes its own full step (weak scaling), timed by the slowest rank."""
+    return bytes_per_step * steps * world / (ms / 1e3) / 1e9
+
+
 # ------------------------------------------------------------------------------------------------ GPU arm
 
 class DeviceCall:
@@ -394,10 +418,7 @@ def run_mine(args, work: wl.Workload, rank: int, world: int, local_rank: int) ->
     clocks = clock.stop(t0, t1) if clock else None
     dom_ms = statistics.mean(a.elapsed_time(b) for a, b in dom_ev)
 
-    if world > 1:
-        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dev)
 
     # end-to-end leg through the same public entry points, host buffers, copies inside the timed region
     e2e = None
@@ -421,12 +442,8 @@ def run_mine(args, work: wl.Workload, rank: int, world: int, local_rank: int) ->
                         ht.copy_(dt_, non_blocking=True)
             e1.record(stream)
         torch.cuda.synchronize(dev)
-        e_ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": round(step_bytes * ke * world / (e_ms / 1e3) / 1e9, 3), "unit": UNIT,
+        e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
+        e2e = {"value": round(aggregate_rate(step_bytes, ke, world, e_ms), 3), "unit": UNIT,
                "h2d_bytes_per_step": sum(d.bytes_in() for d in dcalls),
                "d2h_bytes_per_step": sum(d.bytes_out() for d in dcalls),
                "steps": ke, "ms_per_step": round(e_ms / ke, 4),
@@ -456,7 +473,7 @@ def run_mine(args, work: wl.Workload, rank: int, world: int, local_rank: int) ->
                         "tokens_per_s": round(d.call.T / (ms / 1e3), 1), "bytes": b, "launches_per_step": len(idx)})
     tokens = work.tokens()
     result = {
-        "metric": METRIC, "value": round(step_bytes * args.steps * world / (elapsed_ms / 1e3) / 1e9, 3),
+        "metric": METRIC, "value": round(aggregate_rate(step_bytes, args.steps, world, elapsed_ms), 3),
         "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(elapsed_ms / args.steps, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
