@@ -46,35 +46,38 @@ enum class Shape { kNorm, kRowMax, kStream };
 int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 // Launch shape, chosen from a sweep of CTAs per row x vectors per thread x threads on GB300 (back-to-back
-// launches, inputs larger than L2):
+// launches; inputs larger than L2 for the large batches):
 //  - at least one row per SM (large batches):
 //      norm: one CTA per row while the row fits 512 threads x 4 vectors (hidden <= 16384), the fewest
 //            vectors per thread (>= 2) that keep the CTA at <= 512 threads -- no cluster exchange at all;
-//      dynamic SwiGLU: rows cut into about 512-vector slices over a cluster of up to 8 CTAs, 2 vectors per
-//            thread (many small CTAs hide the latency of the amax exchange);
+//      dynamic SwiGLU: rows cut into slices of about 576 vectors over a cluster of at most 7 CTAs,
+//            2 vectors per thread (clusters of 7 beat 8 at every width measured);
 //      streams: slices of <= 1024 vectors, <= 256 threads.
-//  - fewer rows than SMs (decode): each row is split further so that about two CTAs per SM pull bytes
-//    at once; rows that reduce keep to one cluster of at most 8 CTAs.
+//  - fewer rows than SMs (decode): latency-bound. Rows that reduce are cut into slices of about 256
+//    (norm) or 288 (dynamic SwiGLU) vectors -- more CTAs per row only add exchange latency; streams are
+//    split until about two CTAs per SM pull bytes at once. At most 256 threads per CTA.
 bool plan_rows(int64_t rows, int nvec, Shape shape, int sms, mbd::RowPlan* plan) {
+    *plan = mbd::RowPlan{};
     const bool reduces = shape != Shape::kStream;
+    const bool small = rows < sms;
     int c;
     if (shape == Shape::kNorm) {
-        c = cdiv(nvec, 2048);
+        c = cdiv(nvec, small ? 256 : 2048);
     } else if (shape == Shape::kRowMax) {
-        c = cdiv(nvec, 512);
+        c = cdiv(nvec, small ? 288 : 576);
+        if (c > 7) c = 7;
     } else {
         c = cdiv(nvec, 1024);
+        if (small) {
+            int want = static_cast<int>((2 * sms + rows - 1) / rows);  // about two CTAs per SM
+            const int by_width = cdiv(nvec, 32);                        // at least a warp of vectors per CTA
+            if (want > by_width) want = by_width;
+            if (want > c) c = want;
+        }
     }
-    int min_vpt = shape == Shape::kStream ? 1 : 2;
-    int max_threads = shape == Shape::kStream ? 256 : kMaxThreads;
-    if (rows < sms) {
-        int want = static_cast<int>((2 * sms + rows - 1) / rows);  // about two CTAs per SM
-        int by_width = cdiv(nvec, 32);                              // keep at least a warp of vectors per CTA
-        if (want > by_width) want = by_width;
-        if (want > c) c = want;
-        min_vpt = 1;
-        max_threads = 256;
-    }
+    const int min_vpt = (shape == Shape::kStream || small) ? 1 : 2;
+    const int max_threads = (shape == Shape::kStream || small) ? 256 : kMaxThreads;
+    if (c < cdiv(nvec, 8 * kMaxThreads)) c = cdiv(nvec, 8 * kMaxThreads);   // widest rows: 8 x 512 per CTA
     if (reduces && c > kMaxClusterCtas) c = kMaxClusterCtas;
     if (c < 1) c = 1;
     const int slice = cdiv(nvec, c);
@@ -86,10 +89,8 @@ bool plan_rows(int64_t rows, int nvec, Shape shape, int sms, mbd::RowPlan* plan)
             break;
         }
     }
-    if (vpt == 0) {  // very wide rows: 8 vectors per thread and as many threads as needed
-        vpt = 8;
-    }
-    int threads = cdiv(cdiv(slice, vpt), 32) * 32;
+    if (vpt == 0) vpt = 8;  // very wide rows: 8 vectors per thread and as many threads as needed
+    const int threads = cdiv(cdiv(slice, vpt), 32) * 32;
     if (threads > kMaxThreads) return false;
     plan->ctas_per_row = c;
     plan->slice = slice;

@@ -69,7 +69,7 @@ constexpr long long kWaitLimitCycles = 2LL << 30;
 // on the peer's mbarrier (transaction bytes). No cluster-wide release fence is needed, so the exchange
 // does not wait for this CTA's outstanding global stores. A CTA leaves only after its own mbarrier has
 // seen every peer's bytes, so no write can target a CTA that has exited.
-constexpr int kMaxClusterCtas = 8;
+constexpr int kMaxClusterCtas = 8;   // portable cluster size
 
 struct alignas(16) Exchange {
     float4 slot[kMaxClusterCtas];

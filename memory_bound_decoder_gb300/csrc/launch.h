@@ -21,6 +21,7 @@ struct RowPlan {
     int vpt;  // 1, 2, 4 or 8
 };
 
+
 struct NormParams {
     const void* x;
     void* residual;
