@@ -96,6 +96,7 @@ bool plan_rows(int64_t rows, int nvec, Shape shape, int sms, mbd::RowPlan* plan)
     plan->slice = slice;
     plan->threads = threads;
     plan->vpt = vpt;
+    plan->prefetch = small ? 1 : 0;
     return (rows * c) < (int64_t{1} << 31);
 }
 

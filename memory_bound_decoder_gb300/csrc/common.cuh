@@ -193,13 +193,19 @@ __device__ __forceinline__ bool row_reduce(P mine, P* warp_part, Exchange& ex, i
 
 // ------------------------------------------------------------------------------------------ PDL
 
-// Programmatic dependent launch: let the next kernel in the stream be scheduled as soon as every CTA of
-// this one has started, and wait for the previous kernel's completion (and memory) before touching global
-// memory. Both are no-ops when the launch did not enable programmatic stream serialization.
-__device__ __forceinline__ void pdl_trigger_and_wait() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
+// Programmatic dependent launch: pdl_trigger lets the next kernel in the stream be scheduled as soon as
+// every CTA of this one has started; pdl_wait blocks until the previous kernel has completed and its memory
+// is visible, and must precede every global load or store. Both are no-ops when the launch did not enable
+// programmatic stream serialization.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Warm L2 with a 16-byte vector this thread will load after pdl_wait. A prefetch returns no data, and L2 is
+// the point of coherence for global memory, so the load that follows the wait still observes every write
+// of the previous kernel; issuing it early only overlaps the HBM latency with the previous kernel's tail.
+// Used for small (single-wave, latency-bound) launches only: in a multi-wave launch most CTAs pass the wait
+// at once and the prefetch would just double their L2 requests.
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 
 // ------------------------------------------------------------------------------------------ double-float
 

@@ -18,7 +18,8 @@ struct RowPlan {
     int ctas_per_row;
     int slice;
     int threads;
-    int vpt;  // 1, 2, 4 or 8
+    int vpt;       // 1, 2, 4 or 8
+    int prefetch;  // 1: single-wave launch, warm L2 with the inputs before waiting on the previous kernel
 };
 
 

@@ -38,7 +38,7 @@ __device__ __forceinline__ float2 exact_side(float2 p, float c_hi, float c_lo) {
 }
 
 template <int VPT, int EP>
-__global__ void __launch_bounds__(512) add_rmsnorm_kernel(NormParams p, int ctas_per_row, int slice) {
+__global__ void __launch_bounds__(512) add_rmsnorm_kernel(NormParams p, int ctas_per_row, int slice, int prefetch) {
     __shared__ PSum part_sum[32];
     __shared__ RowStats part_stats[32];
     __shared__ Exchange ex;
@@ -57,7 +57,18 @@ __global__ void __launch_bounds__(512) add_rmsnorm_kernel(NormParams p, int ctas
     uint4* rr = static_cast<uint4*>(p.residual) + row * p.nvec;
     const uint4* wr = static_cast<const uint4*>(p.weight);
 
-    pdl_trigger_and_wait();
+    pdl_trigger();
+    if (prefetch) {
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int c = begin + threadIdx.x + i * blockDim.x;
+        if (c < end) {
+            prefetch_l2(xr + c);
+            prefetch_l2(rr + c);
+        }
+    }
+    }
+    pdl_wait();
 
     // 1. one pass over HBM: x and residual in, s = bf16(x + r) kept packed in registers and written back
     uint4 sv[VPT], wv[VPT];
@@ -199,7 +210,7 @@ template <int EP>
 cudaError_t launch_ep(const NormParams& p, const RowPlan& plan, cudaStream_t s) {
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
-    void (*kern)(NormParams, int, int) = nullptr;
+    void (*kern)(NormParams, int, int, int) = nullptr;
     switch (plan.vpt) {
         case 1: kern = add_rmsnorm_kernel<1, EP>; break;
         case 2: kern = add_rmsnorm_kernel<2, EP>; break;
@@ -208,7 +219,7 @@ cudaError_t launch_ep(const NormParams& p, const RowPlan& plan, cudaStream_t s) 
         default: return cudaErrorInvalidValue;
     }
     fill_launch(cfg, attr, p.rows * plan.ctas_per_row, plan.threads, plan.ctas_per_row, s);
-    return cudaLaunchKernelEx(&cfg, kern, p, plan.ctas_per_row, plan.slice);
+    return cudaLaunchKernelEx(&cfg, kern, p, plan.ctas_per_row, plan.slice, plan.prefetch);
 }
 
 }  // namespace

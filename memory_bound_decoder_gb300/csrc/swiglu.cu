@@ -51,7 +51,7 @@ __device__ __forceinline__ float2 silu_times(float2 g, float2 u) {
 }
 
 template <int VPT, int EP>
-__global__ void __launch_bounds__(512) swiglu_kernel(SwigluParams p, int ctas_per_row, int slice) {
+__global__ void __launch_bounds__(512) swiglu_kernel(SwigluParams p, int ctas_per_row, int slice, int prefetch) {
     __shared__ PMax part_max[32];
     __shared__ Exchange ex;
     __shared__ float row_qmul;
@@ -65,7 +65,18 @@ __global__ void __launch_bounds__(512) swiglu_kernel(SwigluParams p, int ctas_pe
     const uint4* gr = static_cast<const uint4*>(p.gate_up) + row * (int64_t)p.nvec * 2;
     const uint4* ur = gr + p.nvec;
 
-    pdl_trigger_and_wait();
+    pdl_trigger();
+    if (prefetch) {
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int c = begin + threadIdx.x + i * blockDim.x;
+        if (c < end) {
+            prefetch_l2(gr + c);
+            prefetch_l2(ur + c);
+        }
+    }
+    }
+    pdl_wait();
 
     uint4 gv[VPT], uv[VPT];
     bool live[VPT];
@@ -141,7 +152,7 @@ cudaError_t launch_ep(const SwigluParams& p, const RowPlan& plan, cudaStream_t s
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
     const int cluster = EP == kFp8Dynamic ? plan.ctas_per_row : 1;
-    void (*kern)(SwigluParams, int, int) = nullptr;
+    void (*kern)(SwigluParams, int, int, int) = nullptr;
     switch (plan.vpt) {
         case 1: kern = swiglu_kernel<1, EP>; break;
         case 2: kern = swiglu_kernel<2, EP>; break;
@@ -150,7 +161,7 @@ cudaError_t launch_ep(const SwigluParams& p, const RowPlan& plan, cudaStream_t s
         default: return cudaErrorInvalidValue;
     }
     fill_launch(cfg, attr, p.rows * plan.ctas_per_row, plan.threads, cluster, s);
-    return cudaLaunchKernelEx(&cfg, kern, p, plan.ctas_per_row, plan.slice);
+    return cudaLaunchKernelEx(&cfg, kern, p, plan.ctas_per_row, plan.slice, plan.prefetch);
 }
 
 }  // namespace
