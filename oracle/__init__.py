@@ -55,9 +55,14 @@ def _load():
         lib.orc_silu.argtypes, lib.orc_silu.restype = [ctypes.c_double], ctypes.c_double
         lib.orc_add_rmsnorm.argtypes = [u16p, u16p, u16p, i64, i64, f32, u16p, f64p, u16p]
         lib.orc_add_rmsnorm_quant_fp8.argtypes = [u16p, u16p, u16p, i64, i64, f32, cint, f32p, u16p, u8p, f64p]
+        u16pp = ctypes.POINTER(u16p)
+        lib.orc_allreduce_add_rmsnorm.argtypes = [u16pp, cint, u16p, u16p, i64, i64, f32, u16p, f64p, u16p]
+        lib.orc_allreduce_add_rmsnorm_quant_fp8.argtypes = [u16pp, cint, u16p, u16p, i64, i64, f32, cint, f32p,
+                                                            u16p, u8p, f64p]
         lib.orc_swiglu.argtypes = [u16p, i64, i64, f64p, u16p]
         lib.orc_swiglu_quant_fp8.argtypes = [u16p, i64, i64, cint, f32p, u8p, f64p]
-        for fn in ("orc_add_rmsnorm", "orc_add_rmsnorm_quant_fp8", "orc_swiglu", "orc_swiglu_quant_fp8"):
+        for fn in ("orc_add_rmsnorm", "orc_add_rmsnorm_quant_fp8", "orc_swiglu", "orc_swiglu_quant_fp8",
+                   "orc_allreduce_add_rmsnorm", "orc_allreduce_add_rmsnorm_quant_fp8"):
             getattr(lib, fn).restype = cint
         _lib = lib
         return lib
@@ -129,6 +134,46 @@ def add_rmsnorm_quant_fp8(x: np.ndarray, r: np.ndarray, w: np.ndarray, eps: floa
     _check(_load().orc_add_rmsnorm_quant_fp8(_p(x, u16), _p(r, u16), _p(w, u16), T, H, float(eps),
                                              MODES[mode], _p(scale, f32), _p(res, u16), _p(q, u8),
                                              _p(v, f64)), "add_rmsnorm_quant_fp8")
+    return res, q, (scale if mode == "static" else scale[:T]), v
+
+
+def _partials_arg(partials):
+    arrs = [np.ascontiguousarray(p, np.uint16) for p in partials]
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    arr_t = u16p * len(arrs)
+    return arrs, arr_t(*[a.ctypes.data_as(u16p) for a in arrs])
+
+
+def allreduce_add_rmsnorm(partials, r: np.ndarray, w: np.ndarray, eps: float, want_v: bool = True):
+    """x = bf16(sum of partials), then add + RMSNorm. Returns (residual_out, out, v or None)."""
+    arrs, parr = _partials_arg(partials)
+    r = np.ascontiguousarray(r, np.uint16)
+    w = np.ascontiguousarray(w, np.uint16)
+    T, H = r.shape
+    res = np.empty((T, H), np.uint16)
+    out = np.empty((T, H), np.uint16)
+    v = np.empty((T, H), np.float64) if want_v else None
+    u16, f64 = ctypes.c_uint16, ctypes.c_double
+    _check(_load().orc_allreduce_add_rmsnorm(parr, len(arrs), _p(r, u16), _p(w, u16), T, H, float(eps),
+                                             _p(res, u16), _p(v, f64), _p(out, u16)), "allreduce_add_rmsnorm")
+    return res, out, v
+
+
+def allreduce_add_rmsnorm_quant_fp8(partials, r: np.ndarray, w: np.ndarray, eps: float, mode: str,
+                                    static_scale: float = 0.0, want_v: bool = True):
+    """Returns (residual_out, q, scale ([1] static / [T] dynamic), v or None)."""
+    arrs, parr = _partials_arg(partials)
+    r = np.ascontiguousarray(r, np.uint16)
+    w = np.ascontiguousarray(w, np.uint16)
+    T, H = r.shape
+    res = np.empty((T, H), np.uint16)
+    q = np.empty((T, H), np.uint8)
+    scale = np.array([static_scale], np.float32) if mode == "static" else np.zeros((max(T, 1),), np.float32)
+    v = np.empty((T, H), np.float64) if want_v else None
+    u16, u8, f32, f64 = ctypes.c_uint16, ctypes.c_uint8, ctypes.c_float, ctypes.c_double
+    _check(_load().orc_allreduce_add_rmsnorm_quant_fp8(parr, len(arrs), _p(r, u16), _p(w, u16), T, H, float(eps),
+                                                       MODES[mode], _p(scale, f32), _p(res, u16), _p(q, u8),
+                                                       _p(v, f64)), "allreduce_add_rmsnorm_quant_fp8")
     return res, q, (scale if mode == "static" else scale[:T]), v
 
 

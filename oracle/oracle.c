@@ -162,6 +162,57 @@ int orc_add_rmsnorm_quant_fp8(const uint16_t* x, const uint16_t* r, const uint16
     return 0;
 }
 
+/* ---------------------------------------------------------------- AllReduce half + add + RMSNorm */
+
+/* x row t = bf16 of the exact sum of the partials' row t. */
+static void reduce_partials(const uint16_t* const* partials, int n, int64_t t, int64_t H, uint16_t* x_row) {
+    for (int64_t j = 0; j < H; ++j) {
+        double sum = 0.0;
+        for (int k = 0; k < n; ++k) sum += orc_bf16_to_double(partials[k][t * H + j]);
+        x_row[j] = orc_bf16_round(sum);
+    }
+}
+
+static int check_partials(const uint16_t* const* partials, int n, int64_t T) {
+    if (n < 1 || n > 8) return -1;
+    if (T > 0 && !partials) return -1;
+    for (int k = 0; T > 0 && k < n; ++k)
+        if (!partials[k]) return -1;
+    return 0;
+}
+
+int orc_allreduce_add_rmsnorm(const uint16_t* const* partials, int n, const uint16_t* r, const uint16_t* w,
+                              int64_t T, int64_t H, float eps, uint16_t* residual_out, double* v_out,
+                              uint16_t* out) {
+    if (T < 0 || H <= 0 || check_partials(partials, n, T) != 0) return -1;
+    uint16_t* x_row = (uint16_t*)malloc((size_t)H * sizeof(uint16_t));
+    if (!x_row) return -1;
+    int rc = 0;
+    for (int64_t t = 0; t < T && rc == 0; ++t) {
+        reduce_partials(partials, n, t, H, x_row);
+        rc = orc_add_rmsnorm(x_row, r + t * H, w, 1, H, eps, residual_out + t * H, v_out ? v_out + t * H : NULL,
+                             out ? out + t * H : NULL);
+    }
+    free(x_row);
+    return rc;
+}
+
+int orc_allreduce_add_rmsnorm_quant_fp8(const uint16_t* const* partials, int n, const uint16_t* r,
+                                        const uint16_t* w, int64_t T, int64_t H, float eps, int mode,
+                                        float* scale, uint16_t* residual_out, uint8_t* q_out, double* v_out) {
+    if (T < 0 || H <= 0 || check_partials(partials, n, T) != 0 || (mode != 0 && mode != 1)) return -1;
+    uint16_t* x_row = (uint16_t*)malloc((size_t)H * sizeof(uint16_t));
+    if (!x_row) return -1;
+    int rc = 0;
+    for (int64_t t = 0; t < T && rc == 0; ++t) {
+        reduce_partials(partials, n, t, H, x_row);
+        rc = orc_add_rmsnorm_quant_fp8(x_row, r + t * H, w, 1, H, eps, mode, mode == 0 ? scale : scale + t,
+                                       residual_out + t * H, q_out + t * H, v_out ? v_out + t * H : NULL);
+    }
+    free(x_row);
+    return rc;
+}
+
 /* ---------------------------------------------------------------- SwiGLU */
 
 int orc_swiglu(const uint16_t* gate_up, int64_t T, int64_t I, double* h_out, uint16_t* out) {

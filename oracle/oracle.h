@@ -14,7 +14,8 @@
  *       with the hardware": activations in FP8 E4M3 with a per-tensor or per-block scale (the format is
  *       the one of Micikevicius et al., "FP8 Formats for Deep Learning").
  *  [P5] "Introduction to torch.compile and How It Works with vLLM", section 3 (custom passes): the SiLU
- *       activation and the FP8 quantisation that follows it are rewritten into a single fused kernel.
+ *       activation and the FP8 quantisation that follows it are rewritten into a single fused kernel;
+ *       section 4 reports AllReduce + RMSNorm (+ FP8 quantisation) fused as well.
  *
  * Conventions: bf16 values are passed as their 16-bit patterns (uint16_t), row-major. Every function
  * processes rows independently, so a caller may pass pointers offset to any row with a smaller T.
@@ -57,6 +58,19 @@ int orc_add_rmsnorm(const uint16_t* x, const uint16_t* r, const uint16_t* w, int
 int orc_add_rmsnorm_quant_fp8(const uint16_t* x, const uint16_t* r, const uint16_t* w, int64_t T,
                               int64_t H, float eps, int mode, float* scale, uint16_t* residual_out,
                               uint8_t* q_out, double* v_out);
+
+/* The single-GPU half of the AllReduce + RMSNorm fusion [P5 s.4]: n partial activations (one per
+ * tensor-parallel rank) are reduced to x = bf16(sum_k partial_k) -- the exact sum rounded once, what a
+ * bf16 all-reduce hands to the next kernel -- and x then goes through the fused residual add + RMSNorm
+ * above. The sum is carried in double: exact whenever the partials' exponents span fewer than ~45 bits
+ * (every generated input), otherwise within 2^-53 relative. partials is an array of n row-major [T, H]
+ * bf16 tensors, 1 <= n <= 8; n == 1 gives exactly orc_add_rmsnorm. */
+int orc_allreduce_add_rmsnorm(const uint16_t* const* partials, int n, const uint16_t* r, const uint16_t* w,
+                              int64_t T, int64_t H, float eps, uint16_t* residual_out, double* v_out,
+                              uint16_t* out);
+int orc_allreduce_add_rmsnorm_quant_fp8(const uint16_t* const* partials, int n, const uint16_t* r,
+                                        const uint16_t* w, int64_t T, int64_t H, float eps, int mode,
+                                        float* scale, uint16_t* residual_out, uint8_t* q_out, double* v_out);
 
 /* SwiGLU over a stacked gate_up row [P1]: h[t,j] = silu(gu[t,j]) * gu[t,I+j], computed in fp64 with no
  * rounding of silu(g) before the product. h_out (exact) and out (bf16 of h) may be NULL. */

@@ -327,3 +327,57 @@ def test_empty_and_invalid_arguments(orc):
     assert res.shape == (0, 16)
     out, h = orc.swiglu(np.zeros((0, 32), np.uint16))
     assert out.shape == (0, 16)
+
+
+# ------------------------------------------------------------------------------------------------ AllReduce half
+
+def _partials(k, T, H, seed, dist=wl.C5_ACT):
+    return [wl.normal_bf16((T, H), seed, "x", dist.sigma, dist.outlier_p, dist.outlier_k, salt=100 + j)
+            for j in range(k)]
+
+
+def test_allreduce_single_partial_is_the_plain_fused_norm(orc):
+    inp = wl.make_norm_inputs(6, 1000, 3, wl.C5_ACT, 1e-5)
+    a = orc.allreduce_add_rmsnorm([inp.x], inp.residual, inp.weight, 1e-5)
+    b = orc.add_rmsnorm(inp.x, inp.residual, inp.weight, 1e-5)
+    for u, v in zip(a, b):
+        np.testing.assert_array_equal(u, v)
+    aq = orc.allreduce_add_rmsnorm_quant_fp8([inp.x], inp.residual, inp.weight, 1e-5, "dynamic")
+    bq = orc.add_rmsnorm_quant_fp8(inp.x, inp.residual, inp.weight, 1e-5, "dynamic")
+    for u, v in zip(aq, bq):
+        np.testing.assert_array_equal(u, v)
+
+
+def test_allreduce_sum_is_exact_and_order_free(orc):
+    T, H = 5, 640
+    ps = _partials(4, T, H, 9)
+    r = wl.normal_bf16((T, H), 9, "residual")
+    w = wl.weight_bf16(H, 9)
+    res, out, v = orc.allreduce_add_rmsnorm(ps, r, w, 1e-5)
+    res2, out2, v2 = orc.allreduce_add_rmsnorm(ps[::-1], r, w, 1e-5)
+    np.testing.assert_array_equal(res, res2)
+    np.testing.assert_array_equal(v, v2)
+    # x is the exact sum rounded once (independent rational rounding), then the plain fused norm
+    vals = [bf16_vals(p) for p in ps]
+    x = np.empty((T, H), np.uint16)
+    for t in range(T):
+        for j in range(H):
+            x[t, j] = _exact_bf16_round(sum(Fraction(float(a[t, j])) for a in vals))
+    res3, out3, v3 = orc.add_rmsnorm(x, r, w, 1e-5)
+    np.testing.assert_array_equal(res, res3)
+    np.testing.assert_array_equal(v, v3)
+    # and against PyTorch: where the float64 sum is exact in float32, torch's bf16 cast rounds it once
+    s64 = sum(vals)
+    exact32 = s64.astype(np.float32).astype(np.float64) == s64
+    tx = torch.from_numpy(s64.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert exact32.mean() > 0.99
+    np.testing.assert_array_equal(x[exact32], tx[exact32])
+
+
+def test_allreduce_rejects_bad_partial_counts(orc):
+    r = np.zeros((2, 16), np.uint16)
+    w = np.zeros(16, np.uint16)
+    with pytest.raises(ValueError):
+        orc.allreduce_add_rmsnorm([], r, w, 1e-6)
+    with pytest.raises(ValueError):
+        orc.allreduce_add_rmsnorm([r] * 9, r, w, 1e-6)
