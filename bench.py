@@ -54,7 +54,8 @@ def log(*a):
 
 
 def workloads_by_key() -> Dict[str, wl.Workload]:
-    ws = [wl.qwen_t16(), wl.llama3_8b_prefill(), wl.llama3_70b_fp8(), wl.llama31_405b_fp8_ragged()]
+    ws = [wl.qwen_t16(), wl.llama3_8b_prefill(), wl.llama3_70b_fp8(), wl.llama31_405b_fp8_ragged(),
+          wl.llama31_405b_tp8_allreduce_norm()]
     ws += wl.qwen_decode_sweep()
     return {w.key: w for w in ws}
 
@@ -91,7 +92,12 @@ def measured_peak():
 def oracle_run_call(call: wl.Call, inp) -> None:
     import oracle
     oracle.build()
-    if call.kind == "add_rmsnorm":
+    if call.kind == "allreduce_rmsnorm":
+        oracle.allreduce_add_rmsnorm(inp.partials, inp.residual, inp.weight, call.eps, want_v=False)
+    elif call.kind == "allreduce_rmsnorm_q8":
+        oracle.allreduce_add_rmsnorm_quant_fp8(inp.partials, inp.residual, inp.weight, call.eps, call.mode,
+                                               call.static_scale, want_v=False)
+    elif call.kind == "add_rmsnorm":
         oracle.add_rmsnorm(inp.x, inp.residual, inp.weight, call.eps, want_v=False)
     elif call.kind == "add_rmsnorm_q8":
         oracle.add_rmsnorm_quant_fp8(inp.x, inp.residual, inp.weight, call.eps, call.mode, call.static_scale,
@@ -110,7 +116,9 @@ def _split(call: wl.Call, inp, nchunks: int):
     for a, b in zip(bounds[:-1], bounds[1:]):
         if b <= a:
             continue
-        if call.kind.startswith("add"):
+        if call.kind.startswith("allreduce"):
+            out.append(wl.PartialNormInputs([q[a:b] for q in inp.partials], inp.residual[a:b], inp.weight, inp.eps))
+        elif call.kind.startswith("add"):
             out.append(wl.NormInputs(inp.x[a:b], inp.residual[a:b], inp.weight, inp.eps))
         else:
             out.append(wl.SwigluInputs(inp.gate_up[a:b]))
@@ -131,7 +139,8 @@ class OracleSample:
             n = max(1, int(round(call.T * frac)))
             rows = np.unique(np.linspace(0, call.T - 1, n).round().astype(np.int64))
             inp = wl.inputs_for(call, seed=seed, salt=ci, rows=rows)
-            sub = wl.Call(call.kind, len(rows), call.width, call.dist, call.eps, call.mode, call.static_scale)
+            sub = wl.Call(call.kind, len(rows), call.width, call.dist, call.eps, call.mode, call.static_scale,
+                          call.partials)
             self.items.append((sub, _split(sub, inp, threads)))
             self.bytes += sub.algorithmic_bytes() * work.layers
             self.rows += len(rows)
@@ -160,7 +169,7 @@ def calibrate_fraction(work: wl.Workload, threads: int, target_s: float) -> floa
     for ci, call in enumerate(work.calls):
         rows = np.array([0], np.int64)
         inp = wl.inputs_for(call, seed=0, salt=ci, rows=rows)
-        one = wl.Call(call.kind, 1, call.width, call.dist, call.eps, call.mode, call.static_scale)
+        one = wl.Call(call.kind, 1, call.width, call.dist, call.eps, call.mode, call.static_scale, call.partials)
         t = time.perf_counter()
         oracle_run_call(one, inp)
         full_s += (time.perf_counter() - t) * call.T * work.layers
@@ -270,7 +279,31 @@ class DeviceCall:
         u16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16))
         self.h2d = []   # (device tensor, pinned host tensor): activation inputs copied in by the e2e leg
         self.d2h = []   # (device tensor, pinned host tensor): outputs copied back by the e2e leg
-        if call.kind.startswith("add"):
+        if call.kind.startswith("allreduce"):
+            self.ps = [u16(q).to(dev) for q in inp.partials]
+            self.res = u16(inp.residual).to(dev)
+            self.w = u16(inp.weight).to(dev)
+            self.h2d += [(t, u16(q).pin_memory()) for t, q in zip(self.ps, inp.partials)]
+            self.h2d.append((self.res, u16(inp.residual).pin_memory()))
+            lib = mbd.get_lib()
+            import ctypes
+            self._parr = (ctypes.c_void_p * len(self.ps))(*[t.data_ptr() for t in self.ps])
+            if call.kind == "allreduce_rmsnorm":
+                self.out = torch.empty((T, W), dtype=torch.int16, device=dev)
+                self.fn = lib.mbd_fused_allreduce_add_rmsnorm
+                self.args = [self.out.data_ptr(), self.res.data_ptr(), self._parr, len(self.ps), self.w.data_ptr(),
+                             T, W, call.eps]
+            else:
+                self.out = torch.empty((T, W), dtype=torch.uint8, device=dev)
+                self.scale = (torch.tensor([call.static_scale], dtype=torch.float32, device=dev)
+                              if call.mode == "static" else torch.zeros((T,), dtype=torch.float32, device=dev))
+                self.fn = lib.mbd_fused_allreduce_add_rmsnorm_quant_fp8
+                self.args = [self.out.data_ptr(), self.res.data_ptr(), self._parr, len(self.ps), self.w.data_ptr(),
+                             T, W, call.eps, mbd.MODES[call.mode], self.scale.data_ptr()]
+                if call.mode == "dynamic":
+                    self.d2h.append((self.scale, torch.empty_like(self.scale, device="cpu").pin_memory()))
+            self.d2h.append((self.res, torch.empty_like(self.res, device="cpu").pin_memory()))
+        elif call.kind.startswith("add"):
             self.x = u16(inp.x).to(dev)
             self.res = shared_residual if shared_residual is not None else u16(inp.residual).to(dev)
             self.w = u16(inp.weight).to(dev)
@@ -313,6 +346,8 @@ class DeviceCall:
         args = list(self.args)
         if self.call.kind in ("add_rmsnorm", "add_rmsnorm_q8"):
             args[6] = ctypes.c_float(args[6])
+        elif self.call.kind.startswith("allreduce"):
+            args[7] = ctypes.c_float(args[7])
         self.bound = tuple(args) + (stream_handle,)
 
     def launch(self):

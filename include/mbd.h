@@ -137,6 +137,31 @@ mbd_status mbd_fused_add_rmsnorm_quant_fp8(uint8_t* out_q, void* residual, const
                                            const void* weight, int64_t n_tokens, int64_t hidden, float eps,
                                            mbd_scale_mode mode, float* scale, mbd_stream_t stream);
 
+/* Largest number of partial activations of the all-reduce entry points below. */
+#define MBD_MAX_PARTIALS 8
+
+/*
+ * The single-GPU half of AllReduce + RMSNorm [VLLM] section 4 (fused AllReduce + RMSNorm, with or without
+ * FP8 quantisation): n_partials partial activations -- one per tensor-parallel rank, already gathered on
+ * this GPU -- are reduced and fed to the fused residual add + RMSNorm, in one pass:
+ *     x[t,j] = bf16(sum_k partials[k][t,j])   (the exact sum rounded once: what a bf16 all-reduce delivers)
+ * then everything as in mbd_fused_add_rmsnorm (bf16 out) / mbd_fused_add_rmsnorm_quant_fp8 (E4M3 codes).
+ * With n_partials == 1 the results are bit-identical to those entry points.
+ *   partials   : HOST array of n_partials DEVICE pointers, each [n_tokens, hidden] bf16, 16-byte aligned,
+ *                read only; 1 <= n_partials <= MBD_MAX_PARTIALS. They may repeat or overlap each other but
+ *                not residual, weight, out (bf16 out may be exactly partials[0]) or a dynamic scale.
+ *   other arguments and errors: as for the plain entry points. Limit: hidden <= 32768 (one 8-element vector
+ *   of exact partial sums per thread, at most 8 CTAs of 512 threads per row); wider rows return
+ *   MBD_ERR_UNSUPPORTED.
+ */
+mbd_status mbd_fused_allreduce_add_rmsnorm(void* out, void* residual, const void* const* partials, int n_partials,
+                                           const void* weight, int64_t n_tokens, int64_t hidden, float eps,
+                                           mbd_stream_t stream);
+mbd_status mbd_fused_allreduce_add_rmsnorm_quant_fp8(uint8_t* out_q, void* residual, const void* const* partials,
+                                                     int n_partials, const void* weight, int64_t n_tokens,
+                                                     int64_t hidden, float eps, mbd_scale_mode mode, float* scale,
+                                                     mbd_stream_t stream);
+
 /*
  * SwiGLU over the stacked gate_up projection [TRT].
  *   gate_up : [n_tokens, 2 * inter] bf16, read; columns 0..inter-1 are gate, inter..2*inter-1 are up.

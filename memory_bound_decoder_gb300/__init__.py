@@ -49,9 +49,13 @@ def _load() -> ctypes.CDLL:
     lib.mbd_selftest_bounded_wait.restype = cint
     lib.mbd_fused_add_rmsnorm.argtypes = [vp, vp, vp, vp, i64, i64, f32, vp]
     lib.mbd_fused_add_rmsnorm_quant_fp8.argtypes = [vp, vp, vp, vp, i64, i64, f32, cint, vp, vp]
+    lib.mbd_fused_allreduce_add_rmsnorm.argtypes = [vp, vp, ctypes.POINTER(vp), cint, vp, i64, i64, f32, vp]
+    lib.mbd_fused_allreduce_add_rmsnorm_quant_fp8.argtypes = [vp, vp, ctypes.POINTER(vp), cint, vp, i64, i64, f32,
+                                                              cint, vp, vp]
     lib.mbd_swiglu.argtypes = [vp, vp, i64, i64, vp]
     lib.mbd_swiglu_quant_fp8.argtypes = [vp, vp, i64, i64, cint, vp, vp]
-    for fn in ("mbd_fused_add_rmsnorm", "mbd_fused_add_rmsnorm_quant_fp8", "mbd_swiglu", "mbd_swiglu_quant_fp8"):
+    for fn in ("mbd_fused_add_rmsnorm", "mbd_fused_add_rmsnorm_quant_fp8", "mbd_swiglu", "mbd_swiglu_quant_fp8",
+               "mbd_fused_allreduce_add_rmsnorm", "mbd_fused_allreduce_add_rmsnorm_quant_fp8"):
         getattr(lib, fn).restype = cint
     return lib
 
@@ -153,6 +157,31 @@ def fused_add_rmsnorm_quant_fp8(out_q, residual, x, weight, n_tokens: int, hidde
     _check(get_lib().mbd_fused_add_rmsnorm_quant_fp8(_ptr(out_q), _ptr(residual), _ptr(x), _ptr(weight),
                                                int(n_tokens), int(hidden), float(eps), _mode(mode),
                                                _ptr(scale), _stream(stream)), "fused_add_rmsnorm_quant_fp8")
+
+
+def _ptr_array(items) -> Any:
+    if items is None:
+        return None
+    vals = [_ptr(a) for a in items]
+    return (ctypes.c_void_p * max(1, len(vals)))(*vals)
+
+
+def fused_allreduce_add_rmsnorm(out, residual, partials, weight, n_tokens: int, hidden: int, eps: float,
+                                stream=None) -> None:
+    """`partials`: a sequence of tensors or device pointers (the C entry point gets a host pointer array)."""
+    n = len(partials) if partials is not None else 0
+    _check(get_lib().mbd_fused_allreduce_add_rmsnorm(_ptr(out), _ptr(residual), _ptr_array(partials), n, _ptr(weight),
+                                                     int(n_tokens), int(hidden), float(eps), _stream(stream)),
+           "fused_allreduce_add_rmsnorm")
+
+
+def fused_allreduce_add_rmsnorm_quant_fp8(out_q, residual, partials, weight, n_tokens: int, hidden: int, eps: float,
+                                          mode, scale, stream=None) -> None:
+    n = len(partials) if partials is not None else 0
+    _check(get_lib().mbd_fused_allreduce_add_rmsnorm_quant_fp8(_ptr(out_q), _ptr(residual), _ptr_array(partials), n,
+                                                               _ptr(weight), int(n_tokens), int(hidden), float(eps),
+                                                               _mode(mode), _ptr(scale), _stream(stream)),
+           "fused_allreduce_add_rmsnorm_quant_fp8")
 
 
 def swiglu(out, gate_up, n_tokens: int, inter: int, stream=None) -> None:

@@ -41,7 +41,7 @@ constexpr int kMaxThreads = 512;     // matches __launch_bounds__ of the kernels
 
 // What a launch reduces over each row: the norm's sum of squares, the dynamic SwiGLU's max |h|, or
 // nothing (pure streams, whose row slices are independent CTAs without a cluster).
-enum class Shape { kNorm, kRowMax, kStream };
+enum class Shape { kNorm, kNormPartials, kRowMax, kStream };
 
 int cdiv(int a, int b) { return (a + b - 1) / b; }
 
@@ -52,7 +52,8 @@ int cdiv(int a, int b) { return (a + b - 1) / b; }
 //            vectors per thread (>= 2) that keep the CTA at <= 512 threads -- no cluster exchange at all;
 //      dynamic SwiGLU: rows cut into slices of about 576 vectors over a cluster of at most 7 CTAs,
 //            2 vectors per thread (clusters of 7 beat 8 at every width measured);
-//      streams: slices of <= 1024 vectors, <= 256 threads.
+//      streams: slices of <= 1024 vectors, <= 256 threads;
+//      norm over partial activations: one vector per thread, ~128-vector slices over up to 8 CTAs.
 //  - fewer rows than SMs (decode): latency-bound. Rows that reduce are cut into slices of about 256
 //    (norm) or 288 (dynamic SwiGLU) vectors -- more CTAs per row only add exchange latency; streams are
 //    split until about two CTAs per SM pull bytes at once. At most 256 threads per CTA.
@@ -63,6 +64,8 @@ bool plan_rows(int64_t rows, int nvec, Shape shape, int sms, mbd::RowPlan* plan)
     int c;
     if (shape == Shape::kNorm) {
         c = cdiv(nvec, small ? 256 : 2048);
+    } else if (shape == Shape::kNormPartials) {   // one vector per thread (all partials' loads in flight)
+        c = cdiv(nvec, small ? 256 : 128);         // small CTAs: 8 x 256 threads beat 4 x 512 at H 16384
     } else if (shape == Shape::kRowMax) {
         c = cdiv(nvec, small ? 288 : 576);
         if (c > 7) c = 7;
@@ -77,19 +80,21 @@ bool plan_rows(int64_t rows, int nvec, Shape shape, int sms, mbd::RowPlan* plan)
     }
     const int min_vpt = (shape == Shape::kStream || small) ? 1 : 2;
     const int max_threads = (shape == Shape::kStream || small) ? 256 : kMaxThreads;
-    if (c < cdiv(nvec, 8 * kMaxThreads)) c = cdiv(nvec, 8 * kMaxThreads);   // widest rows: 8 x 512 per CTA
+    const int widest = (shape == Shape::kNormPartials ? 1 : 8) * kMaxThreads;  // vectors one CTA can take
+    if (c < cdiv(nvec, widest)) c = cdiv(nvec, widest);
     if (reduces && c > kMaxClusterCtas) c = kMaxClusterCtas;
     if (c < 1) c = 1;
     const int slice = cdiv(nvec, c);
     c = cdiv(nvec, slice);  // no empty slice
+    const int max_vpt = shape == Shape::kNormPartials ? 1 : 8;
     int vpt = 0;
     for (int v : {1, 2, 4, 8}) {
-        if (v >= min_vpt && cdiv(slice, v) <= max_threads) {
+        if (v >= min_vpt && v <= max_vpt && cdiv(slice, v) <= max_threads) {
             vpt = v;
             break;
         }
     }
-    if (vpt == 0) vpt = 8;  // very wide rows: 8 vectors per thread and as many threads as needed
+    if (vpt == 0) vpt = max_vpt;  // very wide rows: as many threads as needed
     const int threads = cdiv(cdiv(slice, vpt), 32) * 32;
     if (threads > kMaxThreads) return false;
     plan->ctas_per_row = c;
@@ -119,14 +124,16 @@ mbd_status check_width(int64_t n_tokens, int64_t width) {
 
 mbd_status norm_common(void* out, size_t out_elem, void* residual, const void* x, const void* weight,
                        int64_t n_tokens, int64_t hidden, float eps, float* scale, int mode, bool quant,
-                       cudaStream_t stream) {
+                       cudaStream_t stream, const void* const* partials = nullptr, int n_partials = 0) {
     mbd_status st = check_width(n_tokens, hidden);
     if (st != MBD_OK) return st;
     if (!(eps >= 0.0f) || !std::isfinite(eps)) return MBD_ERR_INVALID_ARG;
     if (quant && mode != MBD_SCALE_STATIC_PER_TENSOR && mode != MBD_SCALE_DYNAMIC_PER_TOKEN)
         return MBD_ERR_INVALID_ARG;
     if (hidden > MBD_MAX_REDUCED_WIDTH) return MBD_ERR_UNSUPPORTED;
+    if (partials && (n_partials < 1 || n_partials > MBD_MAX_PARTIALS)) return MBD_ERR_INVALID_ARG;
     if (n_tokens == 0) return MBD_OK;
+    if (partials) x = partials[0];   // validated below like x; the others are checked in the loop
     if (!out || !residual || !x || !weight || (quant && !scale)) return MBD_ERR_INVALID_ARG;
     if (!aligned(out, 16) || !aligned(residual, 16) || !aligned(x, 16) || !aligned(weight, 16) ||
         (quant && !aligned(scale, 4)))
@@ -144,12 +151,31 @@ mbd_status norm_common(void* out, size_t out_elem, void* residual, const void* x
                 overlap(scale, sb, x, act) || overlap(scale, sb, weight, wb)))
         return MBD_ERR_INVALID_ARG;
     if (quant && !dyn && overlap(scale, sb, out, outb)) return MBD_ERR_INVALID_ARG;
+    for (int k = 1; partials && k < n_partials; ++k) {   // partial 0 was checked as x above
+        const void* pk = partials[k];
+        if (!pk) return MBD_ERR_INVALID_ARG;
+        if (!aligned(pk, 16)) return MBD_ERR_MISALIGNED;
+        if (overlap(pk, act, residual, act) || overlap(pk, act, weight, wb) || overlap(pk, act, out, outb) ||
+            (dyn && overlap(pk, act, scale, sb)))
+            return MBD_ERR_INVALID_ARG;
+    }
 
     mbd::RowPlan plan;
-    if (!plan_rows(n_tokens, static_cast<int>(hidden / 8), Shape::kNorm, sm_count_of_current_device(), &plan))
+    if (!plan_rows(n_tokens, static_cast<int>(hidden / 8), partials ? Shape::kNormPartials : Shape::kNorm,
+                   sm_count_of_current_device(), &plan))
         return MBD_ERR_UNSUPPORTED;
-    mbd::NormParams p{x, residual, weight, out, scale, n_tokens, static_cast<int>(hidden / 8),
-                      static_cast<int>(hidden), eps};
+    mbd::NormParams p{};
+    p.x = x;
+    p.n_partials = partials ? n_partials : 0;
+    for (int k = 0; k < p.n_partials; ++k) p.partials[k] = partials[k];
+    p.residual = residual;
+    p.weight = weight;
+    p.out = out;
+    p.scale = scale;
+    p.rows = n_tokens;
+    p.nvec = static_cast<int>(hidden / 8);
+    p.hidden = static_cast<int>(hidden);
+    p.eps = eps;
     const mbd::Epilogue ep = !quant ? mbd::kBf16 : (dyn ? mbd::kFp8Dynamic : mbd::kFp8Static);
     return finish_launch(mbd::launch_add_rmsnorm(p, ep, plan, stream));
 }
@@ -235,6 +261,23 @@ mbd_status mbd_fused_add_rmsnorm_quant_fp8(uint8_t* out_q, void* residual, const
                                            mbd_scale_mode mode, float* scale, mbd_stream_t stream) {
     return norm_common(out_q, 1, residual, x, weight, n_tokens, hidden, eps, scale, static_cast<int>(mode),
                        true, reinterpret_cast<cudaStream_t>(stream));
+}
+
+mbd_status mbd_fused_allreduce_add_rmsnorm(void* out, void* residual, const void* const* partials, int n_partials,
+                                           const void* weight, int64_t n_tokens, int64_t hidden, float eps,
+                                           mbd_stream_t stream) {
+    if (n_partials < 1 || n_partials > MBD_MAX_PARTIALS || (n_tokens > 0 && !partials)) return MBD_ERR_INVALID_ARG;
+    return norm_common(out, 2, residual, nullptr, weight, n_tokens, hidden, eps, nullptr, 0, false,
+                       reinterpret_cast<cudaStream_t>(stream), partials ? partials : nullptr, n_partials);
+}
+
+mbd_status mbd_fused_allreduce_add_rmsnorm_quant_fp8(uint8_t* out_q, void* residual, const void* const* partials,
+                                                     int n_partials, const void* weight, int64_t n_tokens,
+                                                     int64_t hidden, float eps, mbd_scale_mode mode, float* scale,
+                                                     mbd_stream_t stream) {
+    if (n_partials < 1 || n_partials > MBD_MAX_PARTIALS || (n_tokens > 0 && !partials)) return MBD_ERR_INVALID_ARG;
+    return norm_common(out_q, 1, residual, nullptr, weight, n_tokens, hidden, eps, scale, static_cast<int>(mode),
+                       true, reinterpret_cast<cudaStream_t>(stream), partials, n_partials);
 }
 
 mbd_status mbd_swiglu(void* out, const void* gate_up, int64_t n_tokens, int64_t inter, mbd_stream_t stream) {

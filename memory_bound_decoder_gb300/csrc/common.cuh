@@ -243,6 +243,17 @@ __device__ __forceinline__ void dd_accumulate(DD2& acc, float2 x) {
     acc.lo = __fadd2_rn(acc.lo, e);
 }
 
+// Round the double-float pair (hi + lo) in each lane to bf16 as if it were exact: renormalise so that
+// hi = fl(hi + lo), then, if hi sits exactly on a bf16 rounding boundary (low 16 bits 0x8000), move it one
+// fp32 ulp toward lo. A value off the boundary rounds the same with or without lo.
+__device__ __forceinline__ float dd_nudge_bf16(float hi, float lo) {
+    const float s = hi + lo;
+    const float e = lo - (s - hi);   // exact remainder (|lo| small against hi)
+    uint32_t bits = __float_as_uint(s);
+    if ((bits & 0xFFFFu) == 0x8000u && e != 0.0f && s != 0.0f) bits += ((e > 0.0f) == (s > 0.0f)) ? 1u : 0xFFFFFFFFu;
+    return __uint_as_float(bits);
+}
+
 __device__ __forceinline__ DD dd_add(DD a, DD b) {
     float s, e;
     two_sum(a.hi, b.hi, s, e);

@@ -23,8 +23,12 @@ struct RowPlan {
 };
 
 
+constexpr int kMaxPartials = 8;
+
 struct NormParams {
-    const void* x;
+    const void* x;                          // unused when n_partials > 0
+    const void* partials[kMaxPartials];     // x = bf16(sum of the n_partials tensors) when n_partials > 0
+    int n_partials;
     void* residual;
     const void* weight;
     void* out;       // bf16 [T, H] or uint8 codes [T, H]

@@ -37,8 +37,37 @@ __device__ __forceinline__ float2 exact_side(float2 p, float c_hi, float c_lo) {
     return make_float2(nudge(y_hi.x, y_lo.x), nudge(y_hi.y, y_lo.y));
 }
 
-template <int VPT, int EP>
-__global__ void __launch_bounds__(512) add_rmsnorm_kernel(NormParams p, int ctas_per_row, int slice, int prefetch) {
+// Sum the partial activations of this thread's vector exactly (packed double-float accumulation) and round
+// once to bf16: the reduced activation x of the all-reduce half. All the partials' loads are issued before
+// the first is used, so the vector costs one memory round trip.
+__device__ __forceinline__ uint4 reduce_partials(const NormParams& p, int64_t row, int c) {
+    uint4 pv[kMaxPartials];
+#pragma unroll
+    for (int k = 0; k < kMaxPartials; ++k)
+        if (k < p.n_partials) pv[k] = load_stream(static_cast<const uint4*>(p.partials[k]) + row * p.nvec + c);
+    DD2 acc[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[q] = DD2{f2(0.0f), f2(0.0f)};
+#pragma unroll
+    for (int k = 0; k < kMaxPartials; ++k) {
+        if (k >= p.n_partials) break;
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(&pv[k]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dd_accumulate(acc[q], bf16x2_to_float2(w[q]));
+    }
+    uint4 x;
+    uint32_t* xw = reinterpret_cast<uint32_t*>(&x);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        xw[q] = pack_bf16x2(dd_nudge_bf16(acc[q].hi.x, acc[q].lo.x), dd_nudge_bf16(acc[q].hi.y, acc[q].lo.y));
+    return x;
+}
+
+// The partial-sum form asks for two 512-thread CTAs per SM (<= 64 registers): its eight loads in flight
+// per vector would otherwise leave one CTA, a quarter of the SM's warps.
+template <int VPT, int EP, bool ALLRED>
+__global__ void __launch_bounds__(512, ALLRED ? 2 : 1) add_rmsnorm_kernel(NormParams p, int ctas_per_row, int slice,
+                                                                        int prefetch) {
     __shared__ PSum part_sum[32];
     __shared__ RowStats part_stats[32];
     __shared__ Exchange ex;
@@ -60,13 +89,16 @@ __global__ void __launch_bounds__(512) add_rmsnorm_kernel(NormParams p, int ctas
     pdl_trigger();
     if (prefetch) {
 #pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-        const int c = begin + threadIdx.x + i * blockDim.x;
-        if (c < end) {
-            prefetch_l2(xr + c);
+        for (int i = 0; i < VPT; ++i) {
+            const int c = begin + threadIdx.x + i * blockDim.x;
+            if (c >= end) continue;
             prefetch_l2(rr + c);
+            if constexpr (ALLRED) {
+                for (int k = 0; k < p.n_partials; ++k) prefetch_l2(static_cast<const uint4*>(p.partials[k]) + row * p.nvec + c);
+            } else {
+                prefetch_l2(xr + c);
+            }
         }
-    }
     }
     pdl_wait();
 
@@ -80,10 +112,15 @@ __global__ void __launch_bounds__(512) add_rmsnorm_kernel(NormParams p, int ctas
             const int c = begin + threadIdx.x + i * blockDim.x;
             live[i] = c < end;
             if (live[i]) {
-                xv[i] = load_stream(xr + c);
+                if constexpr (!ALLRED) xv[i] = load_stream(xr + c);
                 sv[i] = load_stream(rr + c);
                 if constexpr (kEarlyWeight) wv[i] = load_cached(wr + c);
             }
+        }
+        if constexpr (ALLRED) {
+#pragma unroll
+            for (int i = 0; i < VPT; ++i)
+                if (live[i]) xv[i] = reduce_partials(p, row, begin + threadIdx.x + i * blockDim.x);
         }
         if (ctas_per_row > 1) exchange_init(ex, ctas_per_row);   // overlaps the loads in flight
 #pragma unroll
@@ -211,12 +248,17 @@ cudaError_t launch_ep(const NormParams& p, const RowPlan& plan, cudaStream_t s) 
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
     void (*kern)(NormParams, int, int, int) = nullptr;
-    switch (plan.vpt) {
-        case 1: kern = add_rmsnorm_kernel<1, EP>; break;
-        case 2: kern = add_rmsnorm_kernel<2, EP>; break;
-        case 4: kern = add_rmsnorm_kernel<4, EP>; break;
-        case 8: kern = add_rmsnorm_kernel<8, EP>; break;
-        default: return cudaErrorInvalidValue;
+    if (p.n_partials > 0) {
+        if (plan.vpt != 1) return cudaErrorInvalidValue;
+        kern = add_rmsnorm_kernel<1, EP, true>;
+    } else {
+        switch (plan.vpt) {
+            case 1: kern = add_rmsnorm_kernel<1, EP, false>; break;
+            case 2: kern = add_rmsnorm_kernel<2, EP, false>; break;
+            case 4: kern = add_rmsnorm_kernel<4, EP, false>; break;
+            case 8: kern = add_rmsnorm_kernel<8, EP, false>; break;
+            default: return cudaErrorInvalidValue;
+        }
     }
     fill_launch(cfg, attr, p.rows * plan.ctas_per_row, plan.threads, plan.ctas_per_row, s);
     return cudaLaunchKernelEx(&cfg, kern, p, plan.ctas_per_row, plan.slice, plan.prefetch);

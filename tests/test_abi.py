@@ -101,6 +101,23 @@ def test_unsupported_widths(lib):
     mbd.swiglu_quant_fp8(None, None, 0, wide, "static", None)
 
 
+def test_allreduce_argument_checks(lib):
+    f = mbd.fused_allreduce_add_rmsnorm
+    assert _rc(f, A, 2 * A, [], 4 * A, 4, 64, 1e-6) == mbd.ERR_INVALID_ARG                  # no partial
+    assert _rc(f, A, 2 * A, [3 * A] * 9, 4 * A, 4, 64, 1e-6) == mbd.ERR_INVALID_ARG          # too many
+    assert _rc(f, A, 2 * A, [3 * A, None], 4 * A, 4, 64, 1e-6) == mbd.ERR_INVALID_ARG        # null partial
+    assert _rc(f, A, 2 * A, [3 * A, 5 * A + 8], 4 * A, 4, 64, 1e-6) == mbd.ERR_MISALIGNED    # misaligned
+    assert _rc(f, A, 2 * A, [3 * A, 2 * A + 64], 4 * A, 4, 64, 1e-6) == mbd.ERR_INVALID_ARG  # overlaps residual
+    assert _rc(f, A, 2 * A, [3 * A, A], 4 * A, 4, 64, 1e-6) == mbd.ERR_INVALID_ARG           # partial 1 is out
+    q = mbd.fused_allreduce_add_rmsnorm_quant_fp8
+    assert _rc(q, A, 2 * A, [3 * A], 4 * A, 4, 64, 1e-6, "dynamic", 3 * A + 4) == mbd.ERR_INVALID_ARG
+    # the partial sums hold their accumulators in registers: at most 8 x 512 vectors per row
+    assert _rc(f, A, 2 * A, [3 * A], 4 * A, 1, 32768 + 8, 1e-6) == mbd.ERR_UNSUPPORTED
+    n0 = mbd.kernel_launches()
+    f(None, None, [None, None], None, 0, 64, 1e-6)     # zero tokens: a no-op
+    assert mbd.kernel_launches() == n0
+
+
 def test_device_error_flags_rejects_null(lib):
     assert lib.mbd_device_error_flags(None, 0) == mbd.ERR_INVALID_ARG
 

@@ -148,19 +148,25 @@ def make_swiglu_inputs(T: int, I: int, seed: int, dist: Dist, salt: int = 0,
 
 @dataclass(frozen=True)
 class Call:
-    kind: str
+    kind: str                  # add_rmsnorm[_q8] | allreduce_rmsnorm[_q8] | swiglu[_q8]
     T: int
     width: int                 # H for the norm, I for SwiGLU
     dist: Dist
     eps: float = 1e-6
     mode: Optional[str] = None
     static_scale: float = 0.05
+    partials: int = 0          # allreduce_rmsnorm: number of partial activations
+
+    @property
+    def is_norm(self) -> bool:
+        return self.kind.startswith("add") or self.kind.startswith("allreduce")
 
     @property
     def name(self) -> str:
         m = f"_{self.mode}" if self.mode else ""
-        w = "H" if self.kind.startswith("add") else "I"
-        return f"{self.kind}{m}_T{self.T}_{w}{self.width}"
+        k = f"_k{self.partials}" if self.partials else ""
+        w = "H" if self.is_norm else "I"
+        return f"{self.kind}{m}{k}_T{self.T}_{w}{self.width}"
 
     def algorithmic_bytes(self) -> int:
         """Minimum HBM bytes of one call: every input read once, every output written once."""
@@ -169,6 +175,10 @@ class Call:
             return 8 * T * W + 2 * W
         if self.kind == "add_rmsnorm_q8":
             return 7 * T * W + 2 * W + (4 * T if self.mode == "dynamic" else 4)
+        if self.kind == "allreduce_rmsnorm":       # k partials + residual in, out + residual out
+            return (2 * self.partials + 6) * T * W + 2 * W
+        if self.kind == "allreduce_rmsnorm_q8":
+            return (2 * self.partials + 5) * T * W + 2 * W + (4 * T if self.mode == "dynamic" else 4)
         if self.kind == "swiglu":
             return 6 * T * W
         if self.kind == "swiglu_q8":
@@ -238,8 +248,37 @@ def llama31_405b_fp8_ragged() -> Workload:
                     "ragged 5120/13824 shapes at 1, 3, 17, 1000 tokens", tuple(calls))
 
 
+@dataclass
+class PartialNormInputs:
+    partials: List[np.ndarray]   # k x [T, H] uint16
+    residual: np.ndarray
+    weight: np.ndarray
+    eps: float
+
+
+def make_partial_norm_inputs(k: int, T: int, H: int, seed: int, dist: Dist, eps: float, salt: int = 0,
+                             rows: Optional[np.ndarray] = None) -> PartialNormInputs:
+    """k partial activations (independent streams), a residual and a weight."""
+    ps = [normal_bf16((T, H), seed, "x", dist.sigma, dist.outlier_p, dist.outlier_k, salt * 16 + 1 + j, rows)
+          for j in range(k)]
+    r = normal_bf16((T, H), seed, "residual", dist.sigma, dist.outlier_p, dist.outlier_k, salt, rows)
+    return PartialNormInputs(ps, r, weight_bf16(H, seed, salt), float(eps))
+
+
+def llama31_405b_tp8_allreduce_norm() -> Workload:
+    """The all-reduce half of AllReduce + RMSNorm for a Llama-3.1-405B-shaped layer split over 8
+    tensor-parallel ranks: 8 partial activations per token reduced, added to the residual and normalised,
+    to E4M3 with the static scale and to bf16."""
+    return Workload("llama3.1-405b_tp8_allreduce_norm_T2048", "Llama-3.1-405B-shaped all-reduce half + add + "
+                    "RMSNorm, 8 partials, 2048 tokens",
+                    (Call("allreduce_rmsnorm_q8", 2048, 16384, C5_ACT, 1e-5, "static", partials=8),
+                     Call("allreduce_rmsnorm", 2048, 16384, C5_ACT, 1e-5, partials=8)))
+
+
 def inputs_for(call: Call, seed: int = 0, salt: int = 0, rows: Optional[np.ndarray] = None):
-    """Seeded inputs of one call (NormInputs or SwigluInputs), optionally only some rows."""
+    """Seeded inputs of one call (NormInputs, PartialNormInputs or SwigluInputs), optionally only some rows."""
+    if call.kind.startswith("allreduce"):
+        return make_partial_norm_inputs(call.partials, call.T, call.width, seed, call.dist, call.eps, salt, rows)
     if call.kind.startswith("add"):
         return make_norm_inputs(call.T, call.width, seed, call.dist, call.eps, salt, rows)
     return make_swiglu_inputs(call.T, call.width, seed, call.dist, salt, rows)
