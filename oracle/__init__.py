@@ -53,6 +53,10 @@ def _load():
         lib.orc_e4m3_decode.argtypes, lib.orc_e4m3_decode.restype = [ctypes.c_uint8], ctypes.c_double
         lib.orc_e4m3_encode.argtypes, lib.orc_e4m3_encode.restype = [ctypes.c_double], ctypes.c_uint8
         lib.orc_silu.argtypes, lib.orc_silu.restype = [ctypes.c_double], ctypes.c_double
+        lib.orc_e2m1_decode.argtypes, lib.orc_e2m1_decode.restype = [ctypes.c_uint8], ctypes.c_double
+        lib.orc_e2m1_encode.argtypes, lib.orc_e2m1_encode.restype = [ctypes.c_double], ctypes.c_uint8
+        lib.orc_add_rmsnorm_quant_nvfp4.argtypes = [u16p, u16p, u16p, i64, i64, f32, f32, u16p, u8p, u8p, f64p]
+        lib.orc_swiglu_quant_nvfp4.argtypes = [u16p, i64, i64, f32, u8p, u8p, f64p]
         lib.orc_add_rmsnorm.argtypes = [u16p, u16p, u16p, i64, i64, f32, u16p, f64p, u16p]
         lib.orc_add_rmsnorm_quant_fp8.argtypes = [u16p, u16p, u16p, i64, i64, f32, cint, f32p, u16p, u8p, f64p]
         u16pp = ctypes.POINTER(u16p)
@@ -62,7 +66,8 @@ def _load():
         lib.orc_swiglu.argtypes = [u16p, i64, i64, f64p, u16p]
         lib.orc_swiglu_quant_fp8.argtypes = [u16p, i64, i64, cint, f32p, u8p, f64p]
         for fn in ("orc_add_rmsnorm", "orc_add_rmsnorm_quant_fp8", "orc_swiglu", "orc_swiglu_quant_fp8",
-                   "orc_allreduce_add_rmsnorm", "orc_allreduce_add_rmsnorm_quant_fp8"):
+                   "orc_allreduce_add_rmsnorm", "orc_allreduce_add_rmsnorm_quant_fp8",
+                   "orc_add_rmsnorm_quant_nvfp4", "orc_swiglu_quant_nvfp4"):
             getattr(lib, fn).restype = cint
         _lib = lib
         return lib
@@ -97,6 +102,44 @@ def e4m3_decode(code: int) -> float:
 
 def e4m3_encode(v: float) -> int:
     return int(_load().orc_e4m3_encode(float(v)))
+
+
+def e2m1_decode(code: int) -> float:
+    return _load().orc_e2m1_decode(int(code))
+
+
+def e2m1_encode(v: float) -> int:
+    return int(_load().orc_e2m1_encode(float(v)))
+
+
+def add_rmsnorm_quant_nvfp4(x, r, w, eps: float, tensor_scale: float, want_v: bool = True):
+    """Returns (residual_out [T,H] u16, q packed [T,H/2] u8, sf [T,H/16] u8 E4M3, v or None)."""
+    x = np.ascontiguousarray(x, np.uint16)
+    r = np.ascontiguousarray(r, np.uint16)
+    w = np.ascontiguousarray(w, np.uint16)
+    T, H = x.shape
+    res = np.empty((T, H), np.uint16)
+    q = np.empty((T, H // 2), np.uint8)
+    sf = np.empty((T, H // 16), np.uint8)
+    v = np.empty((T, H), np.float64) if want_v else None
+    u16, u8, f64 = ctypes.c_uint16, ctypes.c_uint8, ctypes.c_double
+    _check(_load().orc_add_rmsnorm_quant_nvfp4(_p(x, u16), _p(r, u16), _p(w, u16), T, H, float(eps),
+                                               float(tensor_scale), _p(res, u16), _p(q, u8), _p(sf, u8), _p(v, f64)),
+           "add_rmsnorm_quant_nvfp4")
+    return res, q, sf, v
+
+
+def swiglu_quant_nvfp4(gate_up, tensor_scale: float, want_h: bool = True):
+    """Returns (q packed [T,I/2] u8, sf [T,I/16] u8 E4M3, h or None)."""
+    gu = np.ascontiguousarray(gate_up, np.uint16)
+    T, I2 = gu.shape
+    I = I2 // 2
+    q = np.empty((T, I // 2), np.uint8)
+    sf = np.empty((T, I // 16), np.uint8)
+    h = np.empty((T, I), np.float64) if want_h else None
+    _check(_load().orc_swiglu_quant_nvfp4(_p(gu, ctypes.c_uint16), T, I, float(tensor_scale), _p(q, ctypes.c_uint8),
+                                          _p(sf, ctypes.c_uint8), _p(h, ctypes.c_double)), "swiglu_quant_nvfp4")
+    return q, sf, h
 
 
 def silu(g: float) -> float:

@@ -86,6 +86,58 @@ uint8_t orc_e4m3_encode(double v) {
     return (uint8_t)(sign | best);
 }
 
+/* ---------------------------------------------------------------- E2M1 (NVFP4 element) */
+
+/* magnitude of code c in [0, 7]: exponent field E = c >> 1, mantissa M = c & 1; E == 0 is subnormal
+ * (M / 2), otherwise (1 + M / 2) * 2^(E - 1). */
+static double e2m1_magnitude(int c) {
+    int E = c >> 1, M = c & 1;
+    if (E == 0) return 0.5 * (double)M;
+    return (1.0 + 0.5 * (double)M) * (double)(1 << (E - 1));
+}
+
+double orc_e2m1_decode(uint8_t code) {
+    double m = e2m1_magnitude(code & 7);
+    return (code & 8) ? -m : m;
+}
+
+uint8_t orc_e2m1_encode(double v) {
+    if (isnan(v)) return 7;   /* no NaN in E2M1; not generated */
+    uint8_t sign = signbit(v) ? (uint8_t)8 : (uint8_t)0;
+    double a = fabs(v);
+    int best = 7;
+    if (a < 6.0) {
+        double best_d = INFINITY;
+        for (int c = 0; c <= 7; ++c) {
+            double d = fabs(a - e2m1_magnitude(c));
+            if (d < best_d || (d == best_d && (c & 1) == 0)) {
+                best = c;
+                best_d = d;
+            }
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+/* NVFP4 of one row of exact values: block scales sf[n/16], codes packed two per byte. */
+static void nvfp4_row(const double* v, int64_t n, float S, uint8_t* q, uint8_t* sf) {
+    for (int64_t b = 0; b < n / 16; ++b) {
+        double amax = 0.0;
+        for (int j = 0; j < 16; ++j) {
+            double a = fabs(v[b * 16 + j]);
+            if (a > amax) amax = a;
+        }
+        uint8_t code = orc_e4m3_encode(amax / (6.0 * (double)S));
+        sf[b] = code;
+        double scale = orc_e4m3_decode(code) * (double)S;
+        for (int j = 0; j < 16; j += 2) {
+            uint8_t lo = scale == 0.0 ? (uint8_t)0 : orc_e2m1_encode(v[b * 16 + j] / scale);
+            uint8_t hi = scale == 0.0 ? (uint8_t)0 : orc_e2m1_encode(v[b * 16 + j + 1] / scale);
+            q[(b * 16 + j) / 2] = (uint8_t)(lo | (hi << 4));
+        }
+    }
+}
+
 /* ---------------------------------------------------------------- SiLU */
 
 double orc_silu(double g) { return g / (1.0 + exp(-g)); }
@@ -162,6 +214,24 @@ int orc_add_rmsnorm_quant_fp8(const uint16_t* x, const uint16_t* r, const uint16
     return 0;
 }
 
+int orc_add_rmsnorm_quant_nvfp4(const uint16_t* x, const uint16_t* r, const uint16_t* w, int64_t T, int64_t H,
+                                float eps, float tensor_scale, uint16_t* residual_out, uint8_t* q_out,
+                                uint8_t* sf_out, double* v_out) {
+    if (T < 0 || H <= 0 || H % 16 != 0 || !(tensor_scale > 0.0f)) return -1;
+    if (T > 0 && (!x || !r || !w || !residual_out || !q_out || !sf_out)) return -1;
+    double* row = (double*)malloc((size_t)H * sizeof(double));
+    if (!row) return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        uint16_t* sr = residual_out + t * H;
+        double inv = add_and_inv_rms(x + t * H, r + t * H, H, eps, sr);
+        for (int64_t j = 0; j < H; ++j) row[j] = normed(sr, w, j, inv);
+        nvfp4_row(row, H, tensor_scale, q_out + t * (H / 2), sf_out + t * (H / 16));
+        if (v_out) memcpy(v_out + t * H, row, (size_t)H * sizeof(double));
+    }
+    free(row);
+    return 0;
+}
+
 /* ---------------------------------------------------------------- AllReduce half + add + RMSNorm */
 
 /* x row t = bf16 of the exact sum of the partials' row t. */
@@ -227,6 +297,21 @@ int orc_swiglu(const uint16_t* gate_up, int64_t T, int64_t I, double* h_out, uin
             if (out) out[t * I + j] = orc_bf16_round(h);
         }
     }
+    return 0;
+}
+
+int orc_swiglu_quant_nvfp4(const uint16_t* gate_up, int64_t T, int64_t I, float tensor_scale, uint8_t* q_out,
+                           uint8_t* sf_out, double* h_out) {
+    if (T < 0 || I <= 0 || I % 16 != 0 || !(tensor_scale > 0.0f)) return -1;
+    if (T > 0 && (!gate_up || !q_out || !sf_out)) return -1;
+    double* row = (double*)malloc((size_t)I * sizeof(double));
+    if (!row) return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        orc_swiglu(gate_up + t * 2 * I, 1, I, row, NULL);
+        nvfp4_row(row, I, tensor_scale, q_out + t * (I / 2), sf_out + t * (I / 16));
+        if (h_out) memcpy(h_out + t * I, row, (size_t)I * sizeof(double));
+    }
+    free(row);
     return 0;
 }
 

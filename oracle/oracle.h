@@ -12,7 +12,8 @@
  *       stacked projection and combines them per element as g / (1 + exp(-g)) * up.
  *  [P2] "TensorRT-LLM" architecture walkthrough, "Part V continued: Deep dive: quantization co-designed
  *       with the hardware": activations in FP8 E4M3 with a per-tensor or per-block scale (the format is
- *       the one of Micikevicius et al., "FP8 Formats for Deep Learning").
+ *       the one of Micikevicius et al., "FP8 Formats for Deep Learning"); its NVFP4 paragraph gives the
+ *       Blackwell 4-bit format (E2M1 elements, an E4M3 scale per 16 of them, an fp32 scale per tensor).
  *  [P5] "Introduction to torch.compile and How It Works with vLLM", section 3 (custom passes): the SiLU
  *       activation and the FP8 quantisation that follows it are rewritten into a single fused kernel;
  *       section 4 reports AllReduce + RMSNorm (+ FP8 quantisation) fused as well.
@@ -40,6 +41,13 @@ uint16_t orc_bf16_round(double v);
  * even code, magnitudes above 448 saturate to 448, the sign bit is set for negative inputs. */
 double orc_e4m3_decode(uint8_t code);
 uint8_t orc_e4m3_encode(double v);
+
+/* E2M1, the NVFP4 element format [P2, NVFP4 paragraph]: a 4-bit float with a sign bit, 2 exponent bits and
+ * 1 mantissa bit whose largest magnitude is 6. With exponent bias 1, codes 0..7 stand for 0, 0.5, 1, 1.5, 2,
+ * 3, 4, 6 and bit 3 is the sign. encode: nearest magnitude by exhaustive search, ties to the even code,
+ * anything above 6 saturates to 6, and the sign is kept on a zero. */
+double orc_e2m1_decode(uint8_t code);
+uint8_t orc_e2m1_encode(double v);
 
 /* SiLU [P1]: g / (1 + exp(-g)). */
 double orc_silu(double g);
@@ -71,6 +79,19 @@ int orc_allreduce_add_rmsnorm(const uint16_t* const* partials, int n, const uint
 int orc_allreduce_add_rmsnorm_quant_fp8(const uint16_t* const* partials, int n, const uint16_t* r,
                                         const uint16_t* w, int64_t T, int64_t H, float eps, int mode,
                                         float* scale, uint16_t* residual_out, uint8_t* q_out, double* v_out);
+
+/* NVFP4 quantisation [P2, NVFP4 paragraph: each run of 16 consecutive E2M1 elements carries an E4M3 scale and
+ * the tensor as a whole an fp32 scale], applied to the unrounded row values v (the norm's v or SwiGLU's h). With S the per-tensor fp32 scale
+ * (read, > 0) and amax_b the largest |v| of 16-element block b:
+ *     sf_b = E4M3(amax_b / (6 S))                 (the block scale, so that amax_b maps to about 6)
+ *     q_j  = E2M1(v_j / (dec(sf_b) S))             (0 when dec(sf_b) == 0)
+ * and v_j ~ dec(q_j) * dec(sf_b) * S. Outputs: q packed two codes per byte, element 2i in the low nibble,
+ * [T, W/2]; sf [T, W/16] E4M3 codes, row-major. The width must be a multiple of 16. */
+int orc_add_rmsnorm_quant_nvfp4(const uint16_t* x, const uint16_t* r, const uint16_t* w, int64_t T, int64_t H,
+                                float eps, float tensor_scale, uint16_t* residual_out, uint8_t* q_out,
+                                uint8_t* sf_out, double* v_out);
+int orc_swiglu_quant_nvfp4(const uint16_t* gate_up, int64_t T, int64_t I, float tensor_scale, uint8_t* q_out,
+                           uint8_t* sf_out, double* h_out);
 
 /* SwiGLU over a stacked gate_up row [P1]: h[t,j] = silu(gu[t,j]) * gu[t,I+j], computed in fp64 with no
  * rounding of silu(g) before the product. h_out (exact) and out (bf16 of h) may be NULL. */

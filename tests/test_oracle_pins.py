@@ -381,3 +381,86 @@ def test_allreduce_rejects_bad_partial_counts(orc):
         orc.allreduce_add_rmsnorm([], r, w, 1e-6)
     with pytest.raises(ValueError):
         orc.allreduce_add_rmsnorm([r] * 9, r, w, 1e-6)
+
+
+# ------------------------------------------------------------------------------------------------ NVFP4
+
+def test_e2m1_golden_anchors(orc):
+    for value, code, *_ in _golden("e2m1_anchors.txt"):
+        assert orc.e2m1_encode(float(value)) == int(code, 16), value
+
+
+def test_e2m1_every_midpoint_and_neighbours(orc):
+    mags = [orc.e2m1_decode(c) for c in range(8)]
+    assert mags == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert all(orc.e2m1_decode(c | 8) == -mags[c] for c in range(1, 8))
+    for c in range(7):
+        mid = (mags[c] + mags[c + 1]) / 2
+        even = c if c % 2 == 0 else c + 1
+        assert orc.e2m1_encode(mid) == even
+        assert orc.e2m1_encode(-mid) == 8 | even
+        assert orc.e2m1_encode(math.nextafter(mid, 0.0)) == c
+        assert orc.e2m1_encode(math.nextafter(mid, math.inf)) == c + 1
+
+
+def _unpack_e2m1(q):
+    """Test-side unpacking of packed E2M1 codes (low nibble first) to codes and values, from the format's
+    definition: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6, sign in bit 3."""
+    codes = np.stack([q & 0xF, q >> 4], axis=-1).reshape(q.shape[0], -1)
+    mag_tab = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    return codes, np.where(codes & 8, -1.0, 1.0) * mag_tab[codes & 7]
+
+
+def test_nvfp4_block_structure(orc):
+    T, H, S = 6, 512, 0.02
+    inp = wl.make_norm_inputs(T, H, 5, wl.C5_ACT, 1e-5)
+    res, q, sf, v = orc.add_rmsnorm_quant_nvfp4(inp.x, inp.residual, inp.weight, 1e-5, S)
+    res0, _, v0 = orc.add_rmsnorm(inp.x, inp.residual, inp.weight, 1e-5)
+    np.testing.assert_array_equal(res, res0)
+    np.testing.assert_array_equal(v, v0)
+    codes, vals = _unpack_e2m1(q)
+    blk_scale = np.array([[orc.e4m3_decode(int(c)) for c in row] for row in sf]) * float(np.float32(S))
+    deq = vals * np.repeat(blk_scale, 16, axis=1)
+    amax = np.abs(v).reshape(T, H // 16, 16).max(axis=2)
+    # the block scale is the E4M3 rounding of amax / (6 S): within one E4M3 half-step (<= 1/16 relative)
+    target = amax / (6 * float(np.float32(S)))
+    np.testing.assert_array_less(np.abs(blk_scale / float(np.float32(S)) - target), target / 16 + 2.0 ** -10)
+    # every element sits within half an E2M1 step of its exact value (steps are <= 2 units of the block scale)
+    step = np.repeat(blk_scale, 16, axis=1) * np.where(np.abs(v) / np.repeat(blk_scale, 16, axis=1) < 2, 0.5,
+                                                        np.where(np.abs(v) / np.repeat(blk_scale, 16, axis=1) < 4, 1.0, 2.0))
+    sat = np.abs(v) > 6 * np.repeat(blk_scale, 16, axis=1)
+    assert (np.abs(deq - v)[~sat] <= step[~sat] / 2 * (1 + 1e-12)).all()
+    # with a normal E4M3 block scale (relative error <= 1/16) the block maximum lands in [6/(1+1/16),
+    # 6/(1-1/16)] = [5.65, 6.4], above the 4/6 midpoint: it always takes code +-6
+    j = np.abs(v).reshape(T, H // 16, 16).argmax(axis=2)
+    top = np.take_along_axis(codes.reshape(T, H // 16, 16), j[..., None], axis=2)[..., 0]
+    normal = (sf & 0x78) != 0
+    assert normal.mean() > 0.99
+    assert ((top & 7) == 7)[normal].all()
+    sign = np.take_along_axis(v.reshape(T, H // 16, 16), j[..., None], axis=2)[..., 0] < 0
+    assert ((top >> 3) == sign)[normal].all()
+
+
+def test_nvfp4_codes_vs_exact_rational(orc):
+    T, I, S = 3, 64, 0.01
+    inp = wl.make_swiglu_inputs(T, I, 7, wl.C5_ACT)
+    q, sf, h = orc.swiglu_quant_nvfp4(inp.gate_up, S)
+    Sf = Fraction(float(np.float32(S)))
+    mags = [Fraction(0), Fraction(1, 2), Fraction(1), Fraction(3, 2), Fraction(2), Fraction(3), Fraction(4), Fraction(6)]
+    for t in range(T):
+        for b in range(I // 16):
+            blk = [Fraction(float(x)) for x in h[t, b * 16:(b + 1) * 16]]
+            amax = max(abs(x) for x in blk)
+            assert sf[t, b] == orc.e4m3_encode(float(amax / (6 * Sf)))
+            scale = Fraction(orc.e4m3_decode(int(sf[t, b]))) * Sf
+            for j, x in enumerate(blk):
+                code = (q[t, (b * 16 + j) // 2] >> (4 * (j % 2))) & 0xF
+                a = abs(x) / scale
+                if a >= 6:
+                    want = 7
+                else:
+                    d = [abs(a - m) for m in mags]
+                    best = min(range(8), key=lambda c: (d[c], c % 2))
+                    want = best
+                assert code & 7 == want
+                assert (code >> 3) == (1 if x < 0 else 0)   # the sign is kept, also on a rounded zero
