@@ -42,10 +42,14 @@ DEFAULT_WORKLOAD = "llama3.1-405b_fp8_T2048+ragged"
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel, from the ncu capture
 # summarised under profiles/; valid only while the CUDA sources hash to `csrc_sha256`.
 TRAFFIC: Dict[str, Dict] = {
+    # profiles/add_rmsnorm_nvfp4_T2048_H16384.md
+    "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 166616064, "csrc_sha256": "300ffd8e7514eafd264ff7f3e83740b746e756e7516b0fbb43c994f1cd3a598e"},
+    # profiles/swiglu_nvfp4_T2048_I53248.md
+    "swiglu_nvfp4_T2048_I53248": {"bytes": 468434688, "csrc_sha256": "c0ab45a98838c8ba65209886e452fae93c9f27647759ac2613f6204cf04e51ca"},
     # profiles/swiglu_q8_dynamic_T2048_I53248.md
-    "swiglu_q8_dynamic_T2048_I53248": {"bytes": 515822592, "csrc_sha256": "3b2556376086f6653d8ed67fbc09c4c4e78561d310bcbf383302f971f4ccca47"},
+    "swiglu_q8_dynamic_T2048_I53248": {"bytes": 516052736, "csrc_sha256": "300ffd8e7514eafd264ff7f3e83740b746e756e7516b0fbb43c994f1cd3a598e"},
     # profiles/add_rmsnorm_q8_static_T2048_H16384.md
-    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 177734400, "csrc_sha256": "3b2556376086f6653d8ed67fbc09c4c4e78561d310bcbf383302f971f4ccca47"},
+    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 177788416, "csrc_sha256": "300ffd8e7514eafd264ff7f3e83740b746e756e7516b0fbb43c994f1cd3a598e"},
 }
 
 
@@ -55,7 +59,7 @@ def log(*a):
 
 def workloads_by_key() -> Dict[str, wl.Workload]:
     ws = [wl.qwen_t16(), wl.llama3_8b_prefill(), wl.llama3_70b_fp8(), wl.llama31_405b_fp8_ragged(),
-          wl.llama31_405b_tp8_allreduce_norm()]
+          wl.llama31_405b_tp8_allreduce_norm(), wl.llama31_405b_nvfp4()]
     ws += wl.qwen_decode_sweep()
     return {w.key: w for w in ws}
 
@@ -102,8 +106,12 @@ def oracle_run_call(call: wl.Call, inp) -> None:
     elif call.kind == "add_rmsnorm_q8":
         oracle.add_rmsnorm_quant_fp8(inp.x, inp.residual, inp.weight, call.eps, call.mode, call.static_scale,
                                      want_v=False)
+    elif call.kind == "add_rmsnorm_nvfp4":
+        oracle.add_rmsnorm_quant_nvfp4(inp.x, inp.residual, inp.weight, call.eps, call.static_scale, want_v=False)
     elif call.kind == "swiglu":
         oracle.swiglu(inp.gate_up, want_h=False)
+    elif call.kind == "swiglu_nvfp4":
+        oracle.swiglu_quant_nvfp4(inp.gate_up, call.static_scale, want_h=False)
     else:
         oracle.swiglu_quant_fp8(inp.gate_up, call.mode, call.static_scale, want_h=False)
 
@@ -313,6 +321,14 @@ class DeviceCall:
                 self.fn = mbd.get_lib().mbd_fused_add_rmsnorm
                 self.args = [self.out.data_ptr(), self.res.data_ptr(), self.x.data_ptr(), self.w.data_ptr(),
                              T, W, call.eps]
+            elif call.kind == "add_rmsnorm_nvfp4":
+                self.out = torch.empty((T, W // 2), dtype=torch.uint8, device=dev)
+                self.sf = torch.empty((T, W // 16), dtype=torch.uint8, device=dev)
+                self.scale = torch.tensor([call.static_scale], dtype=torch.float32, device=dev)
+                self.fn = mbd.get_lib().mbd_fused_add_rmsnorm_quant_nvfp4
+                self.args = [self.out.data_ptr(), self.sf.data_ptr(), self.res.data_ptr(), self.x.data_ptr(),
+                             self.w.data_ptr(), T, W, call.eps, self.scale.data_ptr()]
+                self.d2h.append((self.sf, torch.empty_like(self.sf, device="cpu").pin_memory()))
             else:
                 self.out = torch.empty((T, W), dtype=torch.uint8, device=dev)
                 self.scale = (torch.tensor([call.static_scale], dtype=torch.float32, device=dev)
@@ -330,6 +346,13 @@ class DeviceCall:
                 self.out = torch.empty((T, W), dtype=torch.int16, device=dev)
                 self.fn = mbd.get_lib().mbd_swiglu
                 self.args = [self.out.data_ptr(), self.gu.data_ptr(), T, W]
+            elif call.kind == "swiglu_nvfp4":
+                self.out = torch.empty((T, W // 2), dtype=torch.uint8, device=dev)
+                self.sf = torch.empty((T, W // 16), dtype=torch.uint8, device=dev)
+                self.scale = torch.tensor([call.static_scale], dtype=torch.float32, device=dev)
+                self.fn = mbd.get_lib().mbd_swiglu_quant_nvfp4
+                self.args = [self.out.data_ptr(), self.sf.data_ptr(), self.gu.data_ptr(), T, W, self.scale.data_ptr()]
+                self.d2h.append((self.sf, torch.empty_like(self.sf, device="cpu").pin_memory()))
             else:
                 self.out = torch.empty((T, W), dtype=torch.uint8, device=dev)
                 self.scale = (torch.tensor([call.static_scale], dtype=torch.float32, device=dev)
@@ -346,7 +369,7 @@ class DeviceCall:
         args = list(self.args)
         if self.call.kind in ("add_rmsnorm", "add_rmsnorm_q8"):
             args[6] = ctypes.c_float(args[6])
-        elif self.call.kind.startswith("allreduce"):
+        elif self.call.kind.startswith("allreduce") or self.call.kind == "add_rmsnorm_nvfp4":
             args[7] = ctypes.c_float(args[7])
         self.bound = tuple(args) + (stream_handle,)
 

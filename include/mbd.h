@@ -7,6 +7,10 @@
  *   mbd_fused_add_rmsnorm_quant_fp8  the same, writing FP8 E4M3 codes of the normalised row instead of bf16
  *   mbd_swiglu                       out = silu(gate) * up over a stacked gate_up row
  *   mbd_swiglu_quant_fp8             FP8 E4M3 codes of silu(gate) * up
+ *   mbd_fused_add_rmsnorm_quant_nvfp4, mbd_swiglu_quant_nvfp4
+ *                                    the norm / SwiGLU with an NVFP4 epilogue (E2M1 codes, E4M3 block scales)
+ *   mbd_fused_allreduce_add_rmsnorm[_quant_fp8]
+ *                                    the norm fed by n partial activations summed on the way in
  *
  * Definitions (cited by page title and section):
  *   [TRT] "TensorRT-LLM: Compiling Inference Engines Ahead of Time", section "Fusing operations, measured":
@@ -16,6 +20,9 @@
  *         forms g / (1 + exp(-g)) * up from the two halves.
  *   [FP8] "TensorRT-LLM" architecture walkthrough, "Part V continued: Deep dive: quantization co-designed
  *         with the hardware": FP8 E4M3 is the activation format, with a scale per tensor or per block.
+ *   [FP4] same section, NVFP4 paragraph: Blackwell's 4-bit format stores E2M1 elements (sign, 2 exponent bits,
+ *         1 mantissa bit, largest magnitude 6); every 16 consecutive elements carry an E4M3 scale and the
+ *         tensor an fp32 scale, about 4.5 bits per element in all.
  *   [VLLM] "Introduction to torch.compile and How It Works with vLLM", section 3, custom compiler passes:
  *         a compiler pass replaces SiLU followed by FP8 quantisation with one fused kernel; section 4 reports
  *         a fused AllReduce + RMSNorm + FP8 quantisation as well.
@@ -75,8 +82,8 @@ typedef enum {
  * mbd_swiglu_quant_fp8 in dynamic mode); wider rows return MBD_ERR_UNSUPPORTED. */
 #define MBD_MAX_REDUCED_WIDTH 262144
 
-/* ABI version of this header (bumped on any signature change). */
-#define MBD_ABI_VERSION 1
+/* ABI version of this header (bumped on any signature change or added entry point). */
+#define MBD_ABI_VERSION 2
 int mbd_abi_version(void);
 
 /* Static, human-readable name of a status code (never NULL). */
@@ -179,6 +186,33 @@ mbd_status mbd_swiglu(void* out, const void* gate_up, int64_t n_tokens, int64_t 
  */
 mbd_status mbd_swiglu_quant_fp8(uint8_t* out_q, const void* gate_up, int64_t n_tokens, int64_t inter,
                                 mbd_scale_mode mode, float* scale, mbd_stream_t stream);
+
+/*
+ * NVFP4 epilogues [FP4] of the fused residual add + RMSNorm and of SwiGLU. The row values v (the norm's
+ * v[t,j] = weight[j] * s[t,j] * inv_t, SwiGLU's h[t,j], both fp32, not rounded) are cut into blocks of 16
+ * consecutive elements; with S = *tensor_scale and amax_b the largest |v| of block b:
+ *     out_sf[t,b]  = e4m3(amax_b / (6 S))                    block scale, so that amax_b maps to about 6
+ *     code[t,j]    = e2m1(v[t,j] / (dec(out_sf[t,b]) S))     0 where the block scale is 0
+ * e2m1 rounds to nearest even among 0, 0.5, 1, 1.5, 2, 3, 4, 6, saturates at 6 and keeps the sign (also on
+ * a zero); the value is v ~ dec(code) * dec(out_sf) * S. The fp32 arithmetic (the divisions by 6 S and S
+ * folded into per-row constants, 1 / dec(out_sf) from the hardware reciprocal) sits within a few ulps of
+ * the exact ratios, so a value within that distance of a rounding midpoint may round the other way.
+ *   out_q        : [n_tokens, width / 2] uint8, written: element 2i in the low nibble of byte i, 2i + 1 in
+ *                  the high nibble, bit 3 of a nibble the sign. 16-byte aligned.
+ *   out_sf       : [n_tokens, width / 16] uint8 E4M3 block scales, written, row-major (no tensor-core
+ *                  swizzle). Any alignment.
+ *   tensor_scale : ONE fp32 value S, read on the device, 4-byte aligned; usable range 2^-64 <= S <= 2^64.
+ *                  Anything else (0, negative, NaN, infinite, or outside that range) gives all-zero block
+ *                  scales and codes.
+ *   Other arguments as in mbd_fused_add_rmsnorm / mbd_swiglu. out_q, out_sf and tensor_scale must not
+ *   overlap anything written; tensor_scale may overlap inputs. width (hidden or inter) must be a multiple of
+ *   16 elements, else MBD_ERR_MISALIGNED; the norm's limit is hidden <= MBD_MAX_REDUCED_WIDTH.
+ */
+mbd_status mbd_fused_add_rmsnorm_quant_nvfp4(uint8_t* out_q, uint8_t* out_sf, void* residual, const void* x,
+                                             const void* weight, int64_t n_tokens, int64_t hidden, float eps,
+                                             const float* tensor_scale, mbd_stream_t stream);
+mbd_status mbd_swiglu_quant_nvfp4(uint8_t* out_q, uint8_t* out_sf, const void* gate_up, int64_t n_tokens,
+                                  int64_t inter, const float* tensor_scale, mbd_stream_t stream);
 
 #ifdef __cplusplus
 }

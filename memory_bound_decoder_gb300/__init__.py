@@ -54,8 +54,11 @@ def _load() -> ctypes.CDLL:
                                                               cint, vp, vp]
     lib.mbd_swiglu.argtypes = [vp, vp, i64, i64, vp]
     lib.mbd_swiglu_quant_fp8.argtypes = [vp, vp, i64, i64, cint, vp, vp]
+    lib.mbd_fused_add_rmsnorm_quant_nvfp4.argtypes = [vp, vp, vp, vp, vp, i64, i64, f32, vp, vp]
+    lib.mbd_swiglu_quant_nvfp4.argtypes = [vp, vp, vp, i64, i64, vp, vp]
     for fn in ("mbd_fused_add_rmsnorm", "mbd_fused_add_rmsnorm_quant_fp8", "mbd_swiglu", "mbd_swiglu_quant_fp8",
-               "mbd_fused_allreduce_add_rmsnorm", "mbd_fused_allreduce_add_rmsnorm_quant_fp8"):
+               "mbd_fused_allreduce_add_rmsnorm", "mbd_fused_allreduce_add_rmsnorm_quant_fp8",
+               "mbd_fused_add_rmsnorm_quant_nvfp4", "mbd_swiglu_quant_nvfp4"):
         getattr(lib, fn).restype = cint
     return lib
 
@@ -159,6 +162,14 @@ def fused_add_rmsnorm_quant_fp8(out_q, residual, x, weight, n_tokens: int, hidde
                                                _ptr(scale), _stream(stream)), "fused_add_rmsnorm_quant_fp8")
 
 
+def fused_add_rmsnorm_quant_nvfp4(out_q, out_sf, residual, x, weight, n_tokens: int, hidden: int, eps: float,
+                                  tensor_scale, stream=None) -> None:
+    _check(get_lib().mbd_fused_add_rmsnorm_quant_nvfp4(_ptr(out_q), _ptr(out_sf), _ptr(residual), _ptr(x),
+                                                       _ptr(weight), int(n_tokens), int(hidden), float(eps),
+                                                       _ptr(tensor_scale), _stream(stream)),
+           "fused_add_rmsnorm_quant_nvfp4")
+
+
 def _ptr_array(items) -> Any:
     if items is None:
         return None
@@ -191,3 +202,8 @@ def swiglu(out, gate_up, n_tokens: int, inter: int, stream=None) -> None:
 def swiglu_quant_fp8(out_q, gate_up, n_tokens: int, inter: int, mode, scale, stream=None) -> None:
     _check(get_lib().mbd_swiglu_quant_fp8(_ptr(out_q), _ptr(gate_up), int(n_tokens), int(inter), _mode(mode),
                                     _ptr(scale), _stream(stream)), "swiglu_quant_fp8")
+
+
+def swiglu_quant_nvfp4(out_q, out_sf, gate_up, n_tokens: int, inter: int, tensor_scale, stream=None) -> None:
+    _check(get_lib().mbd_swiglu_quant_nvfp4(_ptr(out_q), _ptr(out_sf), _ptr(gate_up), int(n_tokens), int(inter),
+                                            _ptr(tensor_scale), _stream(stream)), "swiglu_quant_nvfp4")

@@ -53,11 +53,16 @@ int cdiv(int a, int b) { return (a + b - 1) / b; }
 //      dynamic SwiGLU: rows cut into slices of about 576 vectors over a cluster of at most 7 CTAs,
 //            2 vectors per thread (clusters of 7 beat 8 at every width measured);
 //      streams: slices of <= 1024 vectors, <= 256 threads;
+//      NVFP4 (more work per vector): the norm takes 4 vectors per thread (34.6 vs 43.0 us at T 4096,
+//            H 8192), the SwiGLU stream ~448-vector slices at 2 vectors per thread (76.8 vs 81.5 us at
+//            T 2048, I 53248; 80.7 vs 87.3 us at T 4096, I 28672);
 //      norm over partial activations: one vector per thread, ~128-vector slices over up to 8 CTAs.
 //  - fewer rows than SMs (decode): latency-bound. Rows that reduce are cut into slices of about 256
 //    (norm) or 288 (dynamic SwiGLU) vectors -- more CTAs per row only add exchange latency; streams are
 //    split until about two CTAs per SM pull bytes at once. At most 256 threads per CTA.
-bool plan_rows(int64_t rows, int nvec, Shape shape, int sms, mbd::RowPlan* plan) {
+// `pairs` (NVFP4): slices of an even number of vectors, so that every 16-element block lies in one CTA, in
+// neighbouring lanes.
+bool plan_rows(int64_t rows, int nvec, Shape shape, int sms, bool pairs, mbd::RowPlan* plan) {
     *plan = mbd::RowPlan{};
     const bool reduces = shape != Shape::kStream;
     const bool small = rows < sms;
@@ -70,7 +75,7 @@ bool plan_rows(int64_t rows, int nvec, Shape shape, int sms, mbd::RowPlan* plan)
         c = cdiv(nvec, small ? 288 : 576);
         if (c > 7) c = 7;
     } else {
-        c = cdiv(nvec, 1024);
+        c = cdiv(nvec, pairs ? 448 : 1024);
         if (small) {
             int want = static_cast<int>((2 * sms + rows - 1) / rows);  // about two CTAs per SM
             const int by_width = cdiv(nvec, 32);                        // at least a warp of vectors per CTA
@@ -78,13 +83,15 @@ bool plan_rows(int64_t rows, int nvec, Shape shape, int sms, mbd::RowPlan* plan)
             if (want > c) c = want;
         }
     }
-    const int min_vpt = (shape == Shape::kStream || small) ? 1 : 2;
+    int min_vpt = (shape == Shape::kStream || small) ? 1 : 2;
+    if (pairs && !small) min_vpt = shape == Shape::kNorm ? 4 : 2;
     const int max_threads = (shape == Shape::kStream || small) ? 256 : kMaxThreads;
     const int widest = (shape == Shape::kNormPartials ? 1 : 8) * kMaxThreads;  // vectors one CTA can take
     if (c < cdiv(nvec, widest)) c = cdiv(nvec, widest);
     if (reduces && c > kMaxClusterCtas) c = kMaxClusterCtas;
     if (c < 1) c = 1;
-    const int slice = cdiv(nvec, c);
+    int slice = cdiv(nvec, c);
+    if (pairs && (slice & 1)) ++slice;
     c = cdiv(nvec, slice);  // no empty slice
     const int max_vpt = shape == Shape::kNormPartials ? 1 : 8;
     int vpt = 0;
@@ -102,7 +109,7 @@ bool plan_rows(int64_t rows, int nvec, Shape shape, int sms, mbd::RowPlan* plan)
     plan->threads = threads;
     plan->vpt = vpt;
     plan->prefetch = small ? 1 : 0;
-    return (rows * c) < (int64_t{1} << 31);
+    return rows <= mbd::kMaxGridYZ * mbd::kMaxGridYZ;
 }
 
 mbd_status finish_launch(cudaError_t e) {
@@ -122,47 +129,66 @@ mbd_status check_width(int64_t n_tokens, int64_t width) {
     return MBD_OK;
 }
 
-mbd_status norm_common(void* out, size_t out_elem, void* residual, const void* x, const void* weight,
-                       int64_t n_tokens, int64_t hidden, float eps, float* scale, int mode, bool quant,
+// Output bytes of T x width elements under an epilogue: bf16 2, E4M3 1, packed E2M1 1/2 per element.
+size_t out_bytes(mbd::Epilogue ep, int64_t n_tokens, int64_t width) {
+    const size_t n = static_cast<size_t>(n_tokens) * static_cast<size_t>(width);
+    return ep == mbd::kBf16 ? 2 * n : (ep == mbd::kNvfp4 ? n / 2 : n);
+}
+
+// The FP8 epilogue of a scale mode, false for an unknown mode.
+bool fp8_epilogue(int mode, mbd::Epilogue* ep) {
+    if (mode == MBD_SCALE_STATIC_PER_TENSOR) *ep = mbd::kFp8Static;
+    else if (mode == MBD_SCALE_DYNAMIC_PER_TOKEN) *ep = mbd::kFp8Dynamic;
+    else return false;
+    return true;
+}
+
+mbd_status norm_common(void* out, uint8_t* out_sf, mbd::Epilogue ep, void* residual, const void* x,
+                       const void* weight, int64_t n_tokens, int64_t hidden, float eps, float* scale,
                        cudaStream_t stream, const void* const* partials = nullptr, int n_partials = 0) {
     mbd_status st = check_width(n_tokens, hidden);
     if (st != MBD_OK) return st;
+    const bool quant = ep != mbd::kBf16, dyn = ep == mbd::kFp8Dynamic, fp4 = ep == mbd::kNvfp4;
+    if (fp4 && hidden % 16 != 0) return MBD_ERR_MISALIGNED;
     if (!(eps >= 0.0f) || !std::isfinite(eps)) return MBD_ERR_INVALID_ARG;
-    if (quant && mode != MBD_SCALE_STATIC_PER_TENSOR && mode != MBD_SCALE_DYNAMIC_PER_TOKEN)
-        return MBD_ERR_INVALID_ARG;
     if (hidden > MBD_MAX_REDUCED_WIDTH) return MBD_ERR_UNSUPPORTED;
     if (partials && (n_partials < 1 || n_partials > MBD_MAX_PARTIALS)) return MBD_ERR_INVALID_ARG;
     if (n_tokens == 0) return MBD_OK;
     if (partials) x = partials[0];   // validated below like x; the others are checked in the loop
-    if (!out || !residual || !x || !weight || (quant && !scale)) return MBD_ERR_INVALID_ARG;
+    if (!out || !residual || !x || !weight || (quant && !scale) || (fp4 && !out_sf)) return MBD_ERR_INVALID_ARG;
     if (!aligned(out, 16) || !aligned(residual, 16) || !aligned(x, 16) || !aligned(weight, 16) ||
         (quant && !aligned(scale, 4)))
         return MBD_ERR_MISALIGNED;
     const size_t act = static_cast<size_t>(n_tokens) * static_cast<size_t>(hidden) * 2;
-    const size_t outb = static_cast<size_t>(n_tokens) * static_cast<size_t>(hidden) * out_elem;
+    const size_t outb = out_bytes(ep, n_tokens, hidden);
+    const size_t sfb = fp4 ? static_cast<size_t>(n_tokens) * static_cast<size_t>(hidden / 16) : 0;
     const size_t wb = static_cast<size_t>(hidden) * 2;
-    const bool dyn = quant && mode == MBD_SCALE_DYNAMIC_PER_TOKEN;
     const size_t sb = quant ? (dyn ? static_cast<size_t>(n_tokens) * 4 : 4) : 0;
     if (overlap(residual, act, x, act) || overlap(residual, act, weight, wb)) return MBD_ERR_INVALID_ARG;
     if (overlap(out, outb, residual, act) || overlap(out, outb, weight, wb)) return MBD_ERR_INVALID_ARG;
     // out may alias x exactly (bf16 only); any other overlap with x is rejected
     if (overlap(out, outb, x, act) && !(!quant && out == x)) return MBD_ERR_INVALID_ARG;
+    if (fp4 && (overlap(out_sf, sfb, out, outb) || overlap(out_sf, sfb, residual, act) ||
+                overlap(out_sf, sfb, x, act) || overlap(out_sf, sfb, weight, wb) || overlap(out_sf, sfb, scale, sb)))
+        return MBD_ERR_INVALID_ARG;
     if (dyn && (overlap(scale, sb, out, outb) || overlap(scale, sb, residual, act) ||
                 overlap(scale, sb, x, act) || overlap(scale, sb, weight, wb)))
         return MBD_ERR_INVALID_ARG;
-    if (quant && !dyn && overlap(scale, sb, out, outb)) return MBD_ERR_INVALID_ARG;
+    // a read-only scale (FP8 static, NVFP4) may share memory with the inputs but not with what is written
+    if (quant && !dyn && (overlap(scale, sb, out, outb) || overlap(scale, sb, residual, act)))
+        return MBD_ERR_INVALID_ARG;
     for (int k = 1; partials && k < n_partials; ++k) {   // partial 0 was checked as x above
         const void* pk = partials[k];
         if (!pk) return MBD_ERR_INVALID_ARG;
         if (!aligned(pk, 16)) return MBD_ERR_MISALIGNED;
         if (overlap(pk, act, residual, act) || overlap(pk, act, weight, wb) || overlap(pk, act, out, outb) ||
-            (dyn && overlap(pk, act, scale, sb)))
+            (dyn && overlap(pk, act, scale, sb)) || (fp4 && overlap(pk, act, out_sf, sfb)))
             return MBD_ERR_INVALID_ARG;
     }
 
     mbd::RowPlan plan;
     if (!plan_rows(n_tokens, static_cast<int>(hidden / 8), partials ? Shape::kNormPartials : Shape::kNorm,
-                   sm_count_of_current_device(), &plan))
+                   sm_count_of_current_device(), fp4, &plan))
         return MBD_ERR_UNSUPPORTED;
     mbd::NormParams p{};
     p.x = x;
@@ -171,39 +197,41 @@ mbd_status norm_common(void* out, size_t out_elem, void* residual, const void* x
     p.residual = residual;
     p.weight = weight;
     p.out = out;
+    p.out_sf = out_sf;
     p.scale = scale;
     p.rows = n_tokens;
     p.nvec = static_cast<int>(hidden / 8);
     p.hidden = static_cast<int>(hidden);
     p.eps = eps;
-    const mbd::Epilogue ep = !quant ? mbd::kBf16 : (dyn ? mbd::kFp8Dynamic : mbd::kFp8Static);
     return finish_launch(mbd::launch_add_rmsnorm(p, ep, plan, stream));
 }
 
-mbd_status swiglu_common(void* out, size_t out_elem, const void* gate_up, int64_t n_tokens, int64_t inter,
-                         float* scale, int mode, bool quant, cudaStream_t stream) {
+mbd_status swiglu_common(void* out, uint8_t* out_sf, mbd::Epilogue ep, const void* gate_up, int64_t n_tokens,
+                         int64_t inter, float* scale, cudaStream_t stream) {
     mbd_status st = check_width(n_tokens, inter);
     if (st != MBD_OK) return st;
-    if (quant && mode != MBD_SCALE_STATIC_PER_TENSOR && mode != MBD_SCALE_DYNAMIC_PER_TOKEN)
-        return MBD_ERR_INVALID_ARG;
-    const bool dyn = quant && mode == MBD_SCALE_DYNAMIC_PER_TOKEN;
+    const bool quant = ep != mbd::kBf16, dyn = ep == mbd::kFp8Dynamic, fp4 = ep == mbd::kNvfp4;
+    if (fp4 && inter % 16 != 0) return MBD_ERR_MISALIGNED;
     if (dyn && inter > MBD_MAX_REDUCED_WIDTH) return MBD_ERR_UNSUPPORTED;
     if (n_tokens == 0) return MBD_OK;
-    if (!out || !gate_up || (quant && !scale)) return MBD_ERR_INVALID_ARG;
+    if (!out || !gate_up || (quant && !scale) || (fp4 && !out_sf)) return MBD_ERR_INVALID_ARG;
     if (!aligned(out, 16) || !aligned(gate_up, 16) || (quant && !aligned(scale, 4))) return MBD_ERR_MISALIGNED;
     const size_t inb = static_cast<size_t>(n_tokens) * static_cast<size_t>(inter) * 4;
-    const size_t outb = static_cast<size_t>(n_tokens) * static_cast<size_t>(inter) * out_elem;
+    const size_t outb = out_bytes(ep, n_tokens, inter);
+    const size_t sfb = fp4 ? static_cast<size_t>(n_tokens) * static_cast<size_t>(inter / 16) : 0;
     const size_t sb = quant ? (dyn ? static_cast<size_t>(n_tokens) * 4 : 4) : 0;
     if (overlap(out, outb, gate_up, inb)) return MBD_ERR_INVALID_ARG;
     if (quant && overlap(scale, sb, out, outb)) return MBD_ERR_INVALID_ARG;
     if (dyn && overlap(scale, sb, gate_up, inb)) return MBD_ERR_INVALID_ARG;
+    if (fp4 && (overlap(out_sf, sfb, out, outb) || overlap(out_sf, sfb, gate_up, inb) ||
+                overlap(out_sf, sfb, scale, sb)))
+        return MBD_ERR_INVALID_ARG;
 
     mbd::RowPlan plan;
     if (!plan_rows(n_tokens, static_cast<int>(inter / 8), dyn ? Shape::kRowMax : Shape::kStream,
-                   sm_count_of_current_device(), &plan))
+                   sm_count_of_current_device(), fp4, &plan))
         return MBD_ERR_UNSUPPORTED;
-    mbd::SwigluParams p{gate_up, out, scale, n_tokens, static_cast<int>(inter / 8)};
-    const mbd::Epilogue ep = !quant ? mbd::kBf16 : (dyn ? mbd::kFp8Dynamic : mbd::kFp8Static);
+    mbd::SwigluParams p{gate_up, out, scale, n_tokens, static_cast<int>(inter / 8), out_sf};
     return finish_launch(mbd::launch_swiglu(p, ep, plan, stream));
 }
 
@@ -252,23 +280,32 @@ mbd_status mbd_selftest_bounded_wait(uint64_t limit_cycles, mbd_stream_t stream)
 
 mbd_status mbd_fused_add_rmsnorm(void* out, void* residual, const void* x, const void* weight,
                                  int64_t n_tokens, int64_t hidden, float eps, mbd_stream_t stream) {
-    return norm_common(out, 2, residual, x, weight, n_tokens, hidden, eps, nullptr, 0, false,
+    return norm_common(out, nullptr, mbd::kBf16, residual, x, weight, n_tokens, hidden, eps, nullptr,
                        reinterpret_cast<cudaStream_t>(stream));
 }
 
 mbd_status mbd_fused_add_rmsnorm_quant_fp8(uint8_t* out_q, void* residual, const void* x,
                                            const void* weight, int64_t n_tokens, int64_t hidden, float eps,
                                            mbd_scale_mode mode, float* scale, mbd_stream_t stream) {
-    return norm_common(out_q, 1, residual, x, weight, n_tokens, hidden, eps, scale, static_cast<int>(mode),
-                       true, reinterpret_cast<cudaStream_t>(stream));
+    mbd::Epilogue ep;
+    if (!fp8_epilogue(static_cast<int>(mode), &ep)) return MBD_ERR_INVALID_ARG;
+    return norm_common(out_q, nullptr, ep, residual, x, weight, n_tokens, hidden, eps, scale,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+mbd_status mbd_fused_add_rmsnorm_quant_nvfp4(uint8_t* out_q, uint8_t* out_sf, void* residual, const void* x,
+                                             const void* weight, int64_t n_tokens, int64_t hidden, float eps,
+                                             const float* tensor_scale, mbd_stream_t stream) {
+    return norm_common(out_q, out_sf, mbd::kNvfp4, residual, x, weight, n_tokens, hidden, eps,
+                       const_cast<float*>(tensor_scale), reinterpret_cast<cudaStream_t>(stream));
 }
 
 mbd_status mbd_fused_allreduce_add_rmsnorm(void* out, void* residual, const void* const* partials, int n_partials,
                                            const void* weight, int64_t n_tokens, int64_t hidden, float eps,
                                            mbd_stream_t stream) {
     if (n_partials < 1 || n_partials > MBD_MAX_PARTIALS || (n_tokens > 0 && !partials)) return MBD_ERR_INVALID_ARG;
-    return norm_common(out, 2, residual, nullptr, weight, n_tokens, hidden, eps, nullptr, 0, false,
-                       reinterpret_cast<cudaStream_t>(stream), partials ? partials : nullptr, n_partials);
+    return norm_common(out, nullptr, mbd::kBf16, residual, nullptr, weight, n_tokens, hidden, eps, nullptr,
+                       reinterpret_cast<cudaStream_t>(stream), partials, n_partials);
 }
 
 mbd_status mbd_fused_allreduce_add_rmsnorm_quant_fp8(uint8_t* out_q, void* residual, const void* const* partials,
@@ -276,18 +313,27 @@ mbd_status mbd_fused_allreduce_add_rmsnorm_quant_fp8(uint8_t* out_q, void* resid
                                                      int64_t hidden, float eps, mbd_scale_mode mode, float* scale,
                                                      mbd_stream_t stream) {
     if (n_partials < 1 || n_partials > MBD_MAX_PARTIALS || (n_tokens > 0 && !partials)) return MBD_ERR_INVALID_ARG;
-    return norm_common(out_q, 1, residual, nullptr, weight, n_tokens, hidden, eps, scale, static_cast<int>(mode),
-                       true, reinterpret_cast<cudaStream_t>(stream), partials, n_partials);
+    mbd::Epilogue ep;
+    if (!fp8_epilogue(static_cast<int>(mode), &ep)) return MBD_ERR_INVALID_ARG;
+    return norm_common(out_q, nullptr, ep, residual, nullptr, weight, n_tokens, hidden, eps, scale,
+                       reinterpret_cast<cudaStream_t>(stream), partials, n_partials);
 }
 
 mbd_status mbd_swiglu(void* out, const void* gate_up, int64_t n_tokens, int64_t inter, mbd_stream_t stream) {
-    return swiglu_common(out, 2, gate_up, n_tokens, inter, nullptr, 0, false,
+    return swiglu_common(out, nullptr, mbd::kBf16, gate_up, n_tokens, inter, nullptr,
                          reinterpret_cast<cudaStream_t>(stream));
 }
 
 mbd_status mbd_swiglu_quant_fp8(uint8_t* out_q, const void* gate_up, int64_t n_tokens, int64_t inter,
                                 mbd_scale_mode mode, float* scale, mbd_stream_t stream) {
-    return swiglu_common(out_q, 1, gate_up, n_tokens, inter, scale, static_cast<int>(mode), true,
+    mbd::Epilogue ep;
+    if (!fp8_epilogue(static_cast<int>(mode), &ep)) return MBD_ERR_INVALID_ARG;
+    return swiglu_common(out_q, nullptr, ep, gate_up, n_tokens, inter, scale, reinterpret_cast<cudaStream_t>(stream));
+}
+
+mbd_status mbd_swiglu_quant_nvfp4(uint8_t* out_q, uint8_t* out_sf, const void* gate_up, int64_t n_tokens,
+                                  int64_t inter, const float* tensor_scale, mbd_stream_t stream) {
+    return swiglu_common(out_q, out_sf, mbd::kNvfp4, gate_up, n_tokens, inter, const_cast<float*>(tensor_scale),
                          reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -19,6 +19,7 @@ namespace cg = cooperative_groups;
 __device__ __forceinline__ uint4 load_stream(const uint4* p) { return __ldcs(p); }
 __device__ __forceinline__ void store_stream(uint4* p, const uint4& v) { __stcs(p, v); }
 __device__ __forceinline__ void store_stream(uint2* p, const uint2& v) { __stcs(p, v); }
+__device__ __forceinline__ void store_stream(unsigned int* p, unsigned int v) { __stcs(p, v); }
 __device__ __forceinline__ uint4 load_cached(const uint4* p) { return __ldg(p); }
 
 // ------------------------------------------------------------------------------------------ bf16 / e4m3
@@ -54,6 +55,83 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float2 v) { return pack_bf16x2(v.x, v.y); }
 __device__ __forceinline__ uint32_t pack_e4m3x4(float2 a, float2 b) { return pack_e4m3x4(a.x, a.y, b.x, b.y); }
+
+// ------------------------------------------------------------------------------------------ NVFP4
+
+// Eight fp32 values to E2M1 (nearest even, saturating to +-6), packed into one word: element 0 in the
+// lowest nibble, so element 2i lands in the low nibble of byte i once stored.
+__device__ __forceinline__ uint32_t pack_e2m1x8(float2 a, float2 b, float2 c, float2 d) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q3, %8, %7;\n\t"
+        "mov.b32 %0, {q0, q1, q2, q3};\n\t}"
+        : "=r"(r)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y), "f"(d.x), "f"(d.y));
+    return r;
+}
+
+// Value of an E4M3 code (low byte of `code`) through the hardware conversion E4M3 -> f16 -> f32 (exact).
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<unsigned short>(code & 0xffu)));
+    float f;
+    asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(static_cast<unsigned short>(h2 & 0xffffu)));
+    return f;
+}
+
+__device__ __forceinline__ float rcp_approx_ftz(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// The per-tensor fp32 scale S of an NVFP4 output, read once per thread. S outside [2^-64, 2^64] (or not a
+// number) counts as unusable and gives zero block scales and zero codes everywhere.
+__device__ __forceinline__ float nvfp4_tensor_scale(const float* scale) {
+    const float s = __ldg(scale);
+    return (s >= 0x1p-64f && s <= 0x1p64f) ? s : 0.0f;
+}
+
+// Row constants of the NVFP4 epilogue for row values v = y * vmul under the tensor scale S (0 when
+// unusable): k = vmul / (6 S) turns a block maximum of |y| into the block scale's argument, and
+// ms = vmul / S turns y into v / S. Two IEEE divisions per thread, none per element.
+struct Nvfp4Row {
+    float k;
+    float ms;
+};
+
+__device__ __forceinline__ Nvfp4Row nvfp4_row(float vmul, float s) {
+    if (s == 0.0f) return Nvfp4Row{0.0f, 0.0f};
+    return Nvfp4Row{vmul / (6.0f * s), vmul / s};
+}
+
+// The same for vmul == 1 through correctly rounded reciprocals (equal to 1 / x, cheaper than a division).
+__device__ __forceinline__ Nvfp4Row nvfp4_unit_row(float s) {
+    if (s == 0.0f) return Nvfp4Row{0.0f, 0.0f};
+    return Nvfp4Row{__frcp_rn(6.0f * s), __frcp_rn(s)};
+}
+
+// NVFP4 epilogue of one 16-byte vector: eight values y that form half of a 16-element block whose other
+// half sits in the neighbouring lane (lane ^ 1). Every lane of the warp must call it (the block maximum is
+// shared through a shuffle); a lane without a vector passes zeros. With v = y * vmul:
+//     sf   = E4M3(max |v| / (6 S))            = cvt(max |y| * k)
+//     code = E2M1(v / (dec(sf) S))            = cvt(y * (ms * (1 / dec(sf))))
+// and zero codes when sf is zero. 1 / dec(sf) comes from rcp.approx (within an ulp); with the products the
+// code arguments sit within a few ulps of the exact ratios. Returns the packed codes; *sf gets the scale.
+__device__ __forceinline__ uint32_t nvfp4_encode(const float2 (&y)[4], const Nvfp4Row& r, uint32_t* sf) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) amax = fmaxf(amax, fmaxf(fabsf(y[k].x), fabsf(y[k].y)));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    const uint32_t code = pack_e4m3x2(amax * r.k, 0.0f) & 0xffu;
+    *sf = code;
+    const float2 m = f2(r.ms * rcp_approx_ftz(e4m3_value(code)));
+    const uint32_t q = pack_e2m1x8(__fmul2_rn(y[0], m), __fmul2_rn(y[1], m), __fmul2_rn(y[2], m), __fmul2_rn(y[3], m));
+    return code != 0u ? q : 0u;
+}
 
 // ------------------------------------------------------------------------------------------ cluster exchange
 

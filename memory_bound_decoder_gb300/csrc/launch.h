@@ -7,13 +7,14 @@
 namespace mbd {
 
 // Output variant of a fused kernel.
-enum Epilogue : int { kBf16 = 0, kFp8Static = 1, kFp8Dynamic = 2 };
+enum Epilogue : int { kBf16 = 0, kFp8Static = 1, kFp8Dynamic = 2, kNvfp4 = 3 };
 
 // How one launch covers the [rows, nvec] problem (nvec = row width / 8, one 16-byte bf16 vector each):
 // every row is split into `ctas_per_row` slices of `slice` vectors (the last may be shorter), one CTA per
 // slice; a CTA of `threads` threads gives each thread up to `vpt` vectors strided by `threads`.
 // If the epilogue reduces over the row and ctas_per_row > 1, the CTAs of a row form one thread-block
-// cluster and combine their partial results through distributed shared memory.
+// cluster and combine their partial results through distributed shared memory. The NVFP4 epilogue needs
+// even slices, so that the two vectors of every 16-element block sit in neighbouring lanes of one warp.
 struct RowPlan {
     int ctas_per_row;
     int slice;
@@ -31,8 +32,9 @@ struct NormParams {
     int n_partials;
     void* residual;
     const void* weight;
-    void* out;       // bf16 [T, H] or uint8 codes [T, H]
-    float* scale;    // static: [1] read; dynamic: [T] written; unused for bf16
+    void* out;       // bf16 [T, H], E4M3 codes [T, H] or packed E2M1 codes [T, H / 2]
+    uint8_t* out_sf; // NVFP4 block scales [T, H / 16] (E4M3); unused otherwise
+    float* scale;    // FP8 static and NVFP4: [1] read; FP8 dynamic: [T] written; unused for bf16
     int64_t rows;
     int nvec;
     int hidden;
@@ -41,10 +43,11 @@ struct NormParams {
 
 struct SwigluParams {
     const void* gate_up;
-    void* out;       // bf16 [T, I] or uint8 codes [T, I]
-    float* scale;
+    void* out;       // bf16 [T, I], E4M3 codes [T, I] or packed E2M1 codes [T, I / 2]
+    float* scale;    // as in NormParams
     int64_t rows;
     int nvec;        // I / 8
+    uint8_t* out_sf; // NVFP4 block scales [T, I / 16]
 };
 
 // Launchers: return the cudaError_t of the launch (cudaSuccess when enqueued). Every launch enables
@@ -60,11 +63,18 @@ cudaError_t device_error_flags_selftest(unsigned int* flags, bool clear);
 // Launch the bounded-wait self-test kernel (one warp).
 cudaError_t launch_bounded_wait_probe(long long limit_cycles, cudaStream_t s);
 
-// Fill a launch configuration: grid/block, the cluster attribute when cluster > 1, and PDL.
-inline void fill_launch(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int64_t ctas, int threads,
-                        int cluster, cudaStream_t s) {
+// Largest grid extent in y and z: rows are laid out over (y, z), so a launch covers up to kMaxGridYZ^2 rows.
+constexpr int64_t kMaxGridYZ = 65535;
+
+// Fill a launch configuration: a grid of (ctas_per_row, gy, gz) CTAs with gy * gz >= rows (row index
+// y + gy * z, so no CTA divides to find its row; CTAs past the last row return at once), the cluster
+// attribute (cluster along x, one row per cluster) when cluster > 1, and PDL.
+inline void fill_launch(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int64_t rows, int ctas_per_row,
+                        int threads, int cluster, cudaStream_t s) {
     cfg = cudaLaunchConfig_t{};
-    cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
+    const int64_t gy = rows < kMaxGridYZ ? rows : kMaxGridYZ;
+    const int64_t gz = (rows + gy - 1) / gy;
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas_per_row), static_cast<unsigned>(gy), static_cast<unsigned>(gz));
     cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
@@ -81,6 +91,11 @@ inline void fill_launch(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int6
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
+}
+
+// Row of this CTA under fill_launch's grid, and its rank (slice) within the row.
+__device__ __forceinline__ int64_t launch_row() {
+    return static_cast<int64_t>(blockIdx.y) + static_cast<int64_t>(gridDim.y) * blockIdx.z;
 }
 
 }  // namespace mbd

@@ -1,4 +1,4 @@
-// Fused residual add + RMSNorm (+ FP8 E4M3 epilogue).
+// Fused residual add + RMSNorm (+ FP8 E4M3 or NVFP4 epilogue).
 //
 // Definition ("TensorRT-LLM: Compiling Inference Engines Ahead of Time", "Fusing operations, measured"):
 // RMSNorm is an eight-step chain (float cast, square, mean, epsilon, reciprocal square root, scaling,
@@ -10,7 +10,9 @@
 //
 // Data flow per row slice: 16-byte loads of x and residual into registers -> s = bf16(x + r) (kept packed)
 // -> residual store -> sum of s^2 -> CTA (+cluster) reduction -> inv = 1/sqrt(mean + eps) -> weight loads
-// -> v = (w * s) * inv -> bf16 store or E4M3 codes with a static scale. The dynamic per-token variant
+// -> v = (w * s) * inv -> bf16 store, E4M3 codes with a static scale, or NVFP4 (E2M1 codes under an E4M3
+// scale per 16 elements and the fp32 tensor scale, the Blackwell 4-bit format described in the TensorRT-LLM
+// walkthrough, Part V, quantization co-designed with the hardware). The dynamic per-token variant
 // reduces the sum of squares and max |w * s| together (the scale is max |w * s| * inv / 448), then stores
 // the codes from registers.
 #include "common.cuh"
@@ -77,8 +79,9 @@ __global__ void __launch_bounds__(512, ALLRED ? 2 : 1) add_rmsnorm_kernel(NormPa
     // after the reduction. The dynamic variant needs it before the reduction anyway.
     constexpr bool kEarlyWeight = EP == kFp8Dynamic || VPT <= 2;
 
-    const int64_t row = blockIdx.x / ctas_per_row;
-    const int rank = blockIdx.x - static_cast<int>(row * ctas_per_row);
+    const int64_t row = launch_row();
+    if (row >= p.rows) return;   // past the last row (the whole cluster shares the row)
+    const int rank = static_cast<int>(blockIdx.x);
     const int begin = rank * slice;
     const int end = min(begin + slice, p.nvec);
 
@@ -174,6 +177,27 @@ __global__ void __launch_bounds__(512, ALLRED ? 2 : 1) add_rmsnorm_kernel(NormPa
                     ow[k] = pack_bf16x2(__fmul2_rn(__fmul2_rn(bf16x2_to_float2(sw[k]), bf16x2_to_float2(ww[k])), f2(inv)));
                 store_stream(outr + (begin + threadIdx.x + i * blockDim.x), o);
             }
+        } else if constexpr (EP == kNvfp4) {
+            // NVFP4: block scales over 16 elements (this vector and the neighbouring lane's), E2M1 codes of
+            // v = (w * s) * inv scaled by the block's decoded scale times the tensor scale.
+            const Nvfp4Row nr = nvfp4_row(inv, nvfp4_tensor_scale(p.scale));
+            unsigned int* qr = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(p.out) + row * (int64_t)p.nvec * 4);
+            uint8_t* sfr = p.out_sf + row * (int64_t)(p.nvec / 2);
+#pragma unroll
+            for (int i = 0; i < VPT; ++i) {
+                float2 y[4];
+                const uint32_t* sw = reinterpret_cast<const uint32_t*>(&sv[i]);
+                const uint32_t* ww = reinterpret_cast<const uint32_t*>(&wv[i]);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    y[k] = live[i] ? __fmul2_rn(bf16x2_to_float2(sw[k]), bf16x2_to_float2(ww[k])) : f2(0.0f);
+                uint32_t sf;
+                const uint32_t q = nvfp4_encode(y, nr, &sf);   // whole warp (block max by shuffle)
+                if (!live[i]) continue;
+                const int c = begin + threadIdx.x + i * blockDim.x;
+                store_stream(qr + c, q);
+                if ((threadIdx.x & 1) == 0) sfr[c >> 1] = static_cast<uint8_t>(sf);
+            }
         } else {
             // static per-tensor scale: codes of v / scale
             const float sc = __ldg(p.scale);
@@ -260,7 +284,7 @@ cudaError_t launch_ep(const NormParams& p, const RowPlan& plan, cudaStream_t s) 
             default: return cudaErrorInvalidValue;
         }
     }
-    fill_launch(cfg, attr, p.rows * plan.ctas_per_row, plan.threads, plan.ctas_per_row, s);
+    fill_launch(cfg, attr, p.rows, plan.ctas_per_row, plan.threads, plan.ctas_per_row, s);
     return cudaLaunchKernelEx(&cfg, kern, p, plan.ctas_per_row, plan.slice, plan.prefetch);
 }
 
@@ -280,6 +304,7 @@ cudaError_t launch_add_rmsnorm(const NormParams& p, Epilogue ep, const RowPlan& 
         case kBf16: return launch_ep<kBf16>(p, plan, s);
         case kFp8Static: return launch_ep<kFp8Static>(p, plan, s);
         case kFp8Dynamic: return launch_ep<kFp8Dynamic>(p, plan, s);
+        case kNvfp4: return launch_ep<kNvfp4>(p, plan, s);
     }
     return cudaErrorInvalidValue;
 }

@@ -217,7 +217,7 @@ int orc_add_rmsnorm_quant_fp8(const uint16_t* x, const uint16_t* r, const uint16
 int orc_add_rmsnorm_quant_nvfp4(const uint16_t* x, const uint16_t* r, const uint16_t* w, int64_t T, int64_t H,
                                 float eps, float tensor_scale, uint16_t* residual_out, uint8_t* q_out,
                                 uint8_t* sf_out, double* v_out) {
-    if (T < 0 || H <= 0 || H % 16 != 0 || !(tensor_scale > 0.0f)) return -1;
+    if (T < 0 || H <= 0 || H % 16 != 0 || !(tensor_scale > 0.0f) || isinf(tensor_scale)) return -1;
     if (T > 0 && (!x || !r || !w || !residual_out || !q_out || !sf_out)) return -1;
     double* row = (double*)malloc((size_t)H * sizeof(double));
     if (!row) return -1;
@@ -302,7 +302,7 @@ int orc_swiglu(const uint16_t* gate_up, int64_t T, int64_t I, double* h_out, uin
 
 int orc_swiglu_quant_nvfp4(const uint16_t* gate_up, int64_t T, int64_t I, float tensor_scale, uint8_t* q_out,
                            uint8_t* sf_out, double* h_out) {
-    if (T < 0 || I <= 0 || I % 16 != 0 || !(tensor_scale > 0.0f)) return -1;
+    if (T < 0 || I <= 0 || I % 16 != 0 || !(tensor_scale > 0.0f) || isinf(tensor_scale)) return -1;
     if (T > 0 && (!gate_up || !q_out || !sf_out)) return -1;
     double* row = (double*)malloc((size_t)I * sizeof(double));
     if (!row) return -1;

@@ -82,7 +82,7 @@ int orc_allreduce_add_rmsnorm_quant_fp8(const uint16_t* const* partials, int n, 
 
 /* NVFP4 quantisation [P2, NVFP4 paragraph: each run of 16 consecutive E2M1 elements carries an E4M3 scale and
  * the tensor as a whole an fp32 scale], applied to the unrounded row values v (the norm's v or SwiGLU's h). With S the per-tensor fp32 scale
- * (read, > 0) and amax_b the largest |v| of 16-element block b:
+ * (read; finite and > 0, else the call fails) and amax_b the largest |v| of 16-element block b:
  *     sf_b = E4M3(amax_b / (6 S))                 (the block scale, so that amax_b maps to about 6)
  *     q_j  = E2M1(v_j / (dec(sf_b) S))             (0 when dec(sf_b) == 0)
  * and v_j ~ dec(q_j) * dec(sf_b) * S. Outputs: q packed two codes per byte, element 2i in the low nibble,

@@ -7,6 +7,10 @@ Tolerances (stated for this library's outputs):
   * E4M3 codes: equal, except at most 0.1% of the elements, each of which may differ by one code step
     (adjacent magnitude; +0 and -0 are the same code);
   * dynamic scales: within 1e-6 relative (zero exactly when the oracle's is zero).
+  * NVFP4: block scales (E4M3 codes) as E4M3 codes above; E2M1 codes of a block whose scale matches the
+    oracle's: equal except at most 0.1% one step apart (+0 and -0 the same); a block whose scale is one step
+    off: its codes equal the oracle's encoding of the exact values under the GPU's block scale, with the same
+    budget.
 """
 from __future__ import annotations
 
@@ -51,6 +55,34 @@ def check_codes(gpu_q: np.ndarray, ref_q: np.ndarray, what: str = "") -> float:
     # the budget is a fraction of the elements; tiny tensors may carry one near-tie flip
     assert frac <= CODE_BUDGET or (d != 0).sum() <= 1, f"{what}: {frac:.2e} of codes differ (> {CODE_BUDGET})"
     return frac
+
+
+def unpack_e2m1(q: np.ndarray) -> np.ndarray:
+    """[rows, W/2] packed bytes -> [rows, W] 4-bit codes (element 2i from the low nibble of byte i)."""
+    return np.stack([q & 0xF, q >> 4], axis=-1).reshape(q.shape[0], -1)
+
+
+def check_nvfp4(q_g: np.ndarray, sf_g: np.ndarray, q_o: np.ndarray, sf_o: np.ndarray, v: np.ndarray,
+                tensor_scale: float, orc, what: str = "") -> dict:
+    """Compare the GPU's NVFP4 output with the oracle's (rule in the module docstring)."""
+    sf_frac = check_codes(sf_g, sf_o, f"{what} block scales")
+    cg, co = unpack_e2m1(q_g).astype(np.int32), unpack_e2m1(q_o).astype(np.int32)
+    T, W = cg.shape
+    same = np.repeat(sf_g == sf_o, 16, axis=1)
+    # blocks whose scale differs: the oracle's codes under the GPU's scale (few elements; one call each)
+    if (~same).any():
+        S = float(np.float32(tensor_scale))
+        for t, j in zip(*np.nonzero(~same)):
+            sc = orc.e4m3_decode(int(sf_g[t, j // 16])) * S
+            co[t, j] = 0 if sc == 0.0 else orc.e2m1_encode(float(v[t, j]) / sc)
+    signed = lambda c: np.where(c & 8, -(c & 7), c & 7)
+    d = np.abs(signed(cg) - signed(co))
+    assert d.max(initial=0) <= 1, f"{what}: an E2M1 code differs by {int(d.max())} steps"
+    # a zero keeps its sign: -0 (0x8) and +0 must match except where the step rule above allows
+    bad_zero = ((cg & 7) == 0) & ((co & 7) == 0) & (cg != co)
+    frac = float(((d != 0) | bad_zero).mean()) if d.size else 0.0
+    assert frac <= CODE_BUDGET or ((d != 0) | bad_zero).sum() <= 1, f"{what}: {frac:.2e} of E2M1 codes differ"
+    return {"sf_diff": sf_frac, "code_diff": frac, "blocks_rescaled": float((~same).mean()) / 1.0 if same.size else 0.0}
 
 
 def check_scales(gpu_s: np.ndarray, ref_s: np.ndarray, what: str = "") -> float:

@@ -34,9 +34,9 @@ def test_binding_names_match_header():
 
 
 def test_version_and_status_strings(lib):
-    assert lib.mbd_abi_version() == 1
+    assert lib.mbd_abi_version() == 2
     hdr = open(mbd.HEADER_PATH).read()
-    assert int(re.search(r"#define MBD_ABI_VERSION (\d+)", hdr).group(1)) == 1
+    assert int(re.search(r"#define MBD_ABI_VERSION (\d+)", hdr).group(1)) == 2
     for code in range(5):
         assert lib.mbd_status_string(code).decode().startswith("MBD_")
     assert lib.mbd_status_string(99) == b"unknown mbd_status"
@@ -131,3 +131,31 @@ def test_raw_ctypes_signature(lib):
     # the C entry points are callable without the Python binding
     fn = lib.mbd_swiglu
     assert fn(None, None, ctypes.c_int64(0), ctypes.c_int64(64), None) == 0
+
+
+def test_nvfp4_argument_checks(lib):
+    n0 = mbd.kernel_launches()
+    mbd.fused_add_rmsnorm_quant_nvfp4(None, None, None, None, None, 0, 4096, 1e-6, None)
+    mbd.swiglu_quant_nvfp4(None, None, None, 0, 14336, None)
+    assert mbd.kernel_launches() == n0
+    f = mbd.fused_add_rmsnorm_quant_nvfp4
+    # width a multiple of 8 but not of 16: a 16-element block would straddle rows
+    assert _rc(f, A, 6 * A, 2 * A, 3 * A, 4 * A, 4, 72, 1e-6, 5 * A) == mbd.ERR_MISALIGNED
+    assert _rc(f, A, None, 2 * A, 3 * A, 4 * A, 4, 64, 1e-6, 5 * A) == mbd.ERR_INVALID_ARG     # no block scales
+    assert _rc(f, A, 6 * A, 2 * A, 3 * A, 4 * A, 4, 64, 1e-6, None) == mbd.ERR_INVALID_ARG     # no tensor scale
+    assert _rc(f, A + 4, 6 * A, 2 * A, 3 * A, 4 * A, 4, 64, 1e-6, 5 * A) == mbd.ERR_MISALIGNED
+    assert _rc(f, A, 6 * A, 2 * A, 3 * A, 4 * A, 4, 64, 1e-6, 5 * A + 2) == mbd.ERR_MISALIGNED
+    # codes take T * H / 2 = 128 bytes: block scales starting inside them overlap
+    assert _rc(f, A, A + 120, 2 * A, 3 * A, 4 * A, 4, 64, 1e-6, 5 * A) == mbd.ERR_INVALID_ARG
+    assert _rc(f, A, A + 128, 2 * A, 3 * A, 4 * A, 4, 64, 1e-6, A + 124) == mbd.ERR_INVALID_ARG  # scale in codes
+    assert _rc(f, A, 6 * A, 2 * A, 3 * A, 4 * A, 4, 64, 1e-6, 6 * A + 12) == mbd.ERR_INVALID_ARG  # scale in sf
+    assert _rc(f, A, 6 * A, 2 * A, 3 * A, 4 * A, 4, 64, 1e-6, 2 * A + 8) == mbd.ERR_INVALID_ARG  # scale in residual
+    assert _rc(f, A, 2 * A + 8, 2 * A, 3 * A, 4 * A, 4, 64, 1e-6, 5 * A) == mbd.ERR_INVALID_ARG  # sf in residual
+    assert _rc(f, A, 6 * A, 2 * A, 3 * A, 4 * A, 0, 262144 + 16, 1e-6, 5 * A) == mbd.ERR_UNSUPPORTED
+    s = mbd.swiglu_quant_nvfp4
+    assert _rc(s, A, 6 * A, 2 * A, 4, 72, 5 * A) == mbd.ERR_MISALIGNED
+    assert _rc(s, A, 2 * A + 16, 2 * A, 4, 64, 5 * A) == mbd.ERR_INVALID_ARG        # sf inside gate_up
+    assert _rc(s, A, A + 64, 2 * A, 4, 64, 5 * A) == mbd.ERR_INVALID_ARG            # sf inside codes
+    assert _rc(s, A, 6 * A, 2 * A, 4, 64, None) == mbd.ERR_INVALID_ARG
+    # a pure stream: no width limit beyond the 2^28 sanity bound
+    s(None, None, None, 0, 262144 + 16, None)

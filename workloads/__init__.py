@@ -143,12 +143,14 @@ def make_swiglu_inputs(T: int, I: int, seed: int, dist: Dist, salt: int = 0,
 
 # --------------------------------------------------------------------------------------------------
 # Workload descriptions. A "call" is one invocation of one entry point on one shape.
-# kind: "add_rmsnorm" | "add_rmsnorm_q8" | "swiglu" | "swiglu_q8"; mode: None | "static" | "dynamic"
+# kind: "add_rmsnorm" | "add_rmsnorm_q8" | "add_rmsnorm_nvfp4" | "swiglu" | "swiglu_q8" | "swiglu_nvfp4" |
+# "allreduce_rmsnorm[_q8]"; mode: None | "static" | "dynamic" (FP8 only). static_scale is the FP8 static scale
+# or the NVFP4 per-tensor scale.
 # --------------------------------------------------------------------------------------------------
 
 @dataclass(frozen=True)
 class Call:
-    kind: str                  # add_rmsnorm[_q8] | allreduce_rmsnorm[_q8] | swiglu[_q8]
+    kind: str                  # add_rmsnorm[_q8|_nvfp4] | allreduce_rmsnorm[_q8] | swiglu[_q8|_nvfp4]
     T: int
     width: int                 # H for the norm, I for SwiGLU
     dist: Dist
@@ -179,10 +181,14 @@ class Call:
             return (2 * self.partials + 6) * T * W + 2 * W
         if self.kind == "allreduce_rmsnorm_q8":
             return (2 * self.partials + 5) * T * W + 2 * W + (4 * T if self.mode == "dynamic" else 4)
+        if self.kind == "add_rmsnorm_nvfp4":     # codes W/2 + block scales W/16 bytes per row, S read
+            return 6 * T * W + T * W // 2 + T * W // 16 + 2 * W + 4
         if self.kind == "swiglu":
             return 6 * T * W
         if self.kind == "swiglu_q8":
             return 5 * T * W + (4 * T if self.mode == "dynamic" else 4)
+        if self.kind == "swiglu_nvfp4":
+            return 4 * T * W + T * W // 2 + T * W // 16 + 4
         raise ValueError(self.kind)
 
 
@@ -246,6 +252,20 @@ def llama31_405b_fp8_ragged() -> Workload:
         calls += _all_four(T, 5120, 13824, C5_ACT, 1e-5)
     return Workload("llama3.1-405b_fp8_T2048+ragged", "Llama-3.1-405B-shaped FP8 path (2048 tokens) plus "
                     "ragged 5120/13824 shapes at 1, 3, 17, 1000 tokens", tuple(calls))
+
+
+# Per-tensor NVFP4 scales of the 405B-shaped C5 activations, calibrated as the tensor's amax / (6 * 448)
+# (amax ~82 for the normalised rows, ~461 for the SwiGLU output at 2048 tokens): block scales then stay
+# within E4M3's normal range.
+NVFP4_SCALE_NORM_C5 = 0.03
+NVFP4_SCALE_SWIGLU_C5 = 0.17
+
+
+def llama31_405b_nvfp4() -> Workload:
+    """The 405B-shaped prefill batch with the Blackwell 4-bit epilogue on both fusions."""
+    return Workload("llama3.1-405b_nvfp4_T2048", "Llama-3.1-405B-shaped NVFP4 path, 2048 tokens",
+                    (Call("add_rmsnorm_nvfp4", 2048, 16384, C5_ACT, 1e-5, static_scale=NVFP4_SCALE_NORM_C5),
+                     Call("swiglu_nvfp4", 2048, 53248, C5_ACT, static_scale=NVFP4_SCALE_SWIGLU_C5)))
 
 
 @dataclass
