@@ -373,6 +373,24 @@ class DeviceCall:
             args[7] = ctypes.c_float(args[7])
         self.bound = tuple(args) + (stream_handle,)
 
+    def op(self):
+        """This call as a program op (mbd_op), or None for kinds a program does not take."""
+        m, c = self.mbd, self.call
+        T, W = c.T, c.width
+        if c.kind == "add_rmsnorm":
+            return m.op_add_rmsnorm(self.out, self.res, self.x, self.w, T, W, c.eps)
+        if c.kind == "add_rmsnorm_q8":
+            return m.op_add_rmsnorm_quant_fp8(self.out, self.res, self.x, self.w, T, W, c.eps, c.mode, self.scale)
+        if c.kind == "add_rmsnorm_nvfp4":
+            return m.op_add_rmsnorm_quant_nvfp4(self.out, self.sf, self.res, self.x, self.w, T, W, c.eps, self.scale)
+        if c.kind == "swiglu":
+            return m.op_swiglu(self.out, self.gu, T, W)
+        if c.kind == "swiglu_q8":
+            return m.op_swiglu_quant_fp8(self.out, self.gu, T, W, c.mode, self.scale)
+        if c.kind == "swiglu_nvfp4":
+            return m.op_swiglu_quant_nvfp4(self.out, self.sf, self.gu, T, W, self.scale)
+        return None
+
     def launch(self):
         rc = self.fn(*self.bound)
         if rc != 0:
@@ -439,6 +457,111 @@ def run_e2e(torch, dcalls: List[DeviceCall], kstream, dev, steps: int, step_byte
                     "stream of every output; per-call events pipeline the three"}
 
 
+def build_device_calls(torch, mbd, work: wl.Workload, seed: int, rank: int, dev) -> List[DeviceCall]:
+    """Device buffers of every launch of one step. Layers repeat the calls with fresh inputs; in a multi-layer
+    step every norm of one token count updates one shared residual, as a decoder's layers do."""
+    dcalls: List[DeviceCall] = []
+    residual_by_T: Dict[int, object] = {}
+    for layer in range(work.layers):
+        for ci, call in enumerate(work.calls):
+            salt = layer * 64 + ci + 1000 * rank
+            inp = wl.inputs_for(call, seed=seed, salt=salt)
+            shared = None
+            if work.layers > 1 and call.kind.startswith("add"):
+                if call.T not in residual_by_T:
+                    residual_by_T[call.T] = torch.from_numpy(inp.residual.view(np.int16)).to(dev)
+                shared = residual_by_T[call.T]
+            dcalls.append(DeviceCall(torch, mbd, call, inp, dev, shared))
+    return dcalls
+
+
+def run_decode_table(args) -> Dict:
+    """Decode-step latency of the Qwen2.5-1.5B-shaped sweep (28 layers x (add + RMSNorm, add + RMSNorm,
+    SwiGLU) per token count), launched three ways: one C-ABI call per op, the same calls replayed from a CUDA
+    graph, and programs (mbd_run_program, at most 128 ops each: the 84 ops of one token count are one persistent
+    launch)."""
+    import torch
+    import memory_bound_decoder_gb300 as mbd
+    from memory_bound_decoder_gb300 import build as mbd_build
+    mbd_build.build()
+    lib = mbd.get_lib()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    table, modes = {}, ("calls", "graph", "program")
+    launches = {}
+    for work in wl.qwen_decode_sweep():
+        T = work.calls[0].T
+        dcalls = build_device_calls(torch, mbd, work, args.seed, 0, dev)
+        stream = torch.cuda.Stream(device=dev)
+        handle = int(stream.cuda_stream)
+        for d in dcalls:
+            d.bind(handle)
+        ops = [d.op() for d in dcalls]
+        progs = [mbd.program_array(ops[i:i + mbd.MAX_PROGRAM_OPS]) for i in range(0, len(ops), mbd.MAX_PROGRAM_OPS)]
+
+        def run_calls():
+            for d in dcalls:
+                d.launch()
+
+        def run_program():
+            for arr, n in progs:
+                rc = lib.mbd_run_program(arr, n, handle)
+                if rc != 0:
+                    raise RuntimeError(lib.mbd_status_string(rc).decode())
+
+        with torch.cuda.stream(stream):
+            run_calls()
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        graph_error = None
+        try:
+            with torch.cuda.graph(graph, stream=stream):
+                run_calls()
+            torch.cuda.synchronize(dev)
+        except RuntimeError as e:   # reported in the line instead of a graph time
+            graph_error = str(e).splitlines()[0]
+            torch.cuda.synchronize(dev)
+        fns = {"calls": run_calls, "graph": graph.replay, "program": run_program}
+        row = {}
+        for mode in modes:
+            if mode == "graph" and graph_error:
+                row[mode] = None
+                row["graph_error"] = graph_error
+                continue
+            fn = fns[mode]
+            with torch.cuda.stream(stream):
+                for _ in range(args.warmup):
+                    fn()
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            n0 = mbd.kernel_launches()
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for _ in range(args.steps):
+                    fn()
+                e1.record(stream)
+            torch.cuda.synchronize(dev)
+            launches[(T, mode)] = (mbd.kernel_launches() - n0) // args.steps
+            ms = e0.elapsed_time(e1) / args.steps
+            row[mode] = round(ms * 1e3 / work.layers, 3)
+        row["program_GBps"] = round(work.algorithmic_bytes() / (row["program"] * work.layers / 1e6) / 1e9, 1)
+        row["launches_per_step"] = {"calls": launches[(T, "calls")], "graph": len(dcalls),
+                                    "program": launches[(T, "program")]}
+        table[str(T)] = row
+        log(f"[decode] T={T}: {row}")
+        del dcalls, progs, graph
+        torch.cuda.empty_cache()
+    mean_prog = statistics.mean(r["program"] for r in table.values())
+    return {"metric": "decode-step latency per layer, Qwen2.5-1.5B shapes (28 layers of 2 add+RMSNorm + 1 SwiGLU)",
+            "value": round(mean_prog, 3), "unit": "us/layer (mean over token counts, program launch)",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": False,
+            "data": "synthetic", "dtype": "f32",
+            "config": {"workload": "qwen2.5-1.5b_decode_sweep", "hidden": 1536, "intermediate": 8960, "layers": 28,
+                       "tokens": [int(t) for t in table], "modes": list(modes),
+                       "l2": "decode buffers below T~64 are L2-resident between steps: these are latencies"},
+            "table": table}
+
+
 def run_mine(args, work: wl.Workload, rank: int, world: int, local_rank: int) -> Optional[Dict]:
     import torch
     import memory_bound_decoder_gb300 as mbd
@@ -454,18 +577,7 @@ def run_mine(args, work: wl.Workload, rank: int, world: int, local_rank: int) ->
     l2_bytes = int(getattr(props, "L2_cache_size", 0)) or 126 * 2 ** 20
 
     t_gen = time.perf_counter()
-    dcalls: List[DeviceCall] = []
-    residual_by_T: Dict[int, object] = {}
-    for layer in range(work.layers):
-        for ci, call in enumerate(work.calls):
-            salt = layer * 64 + ci + 1000 * rank
-            inp = wl.inputs_for(call, seed=args.seed, salt=salt)
-            shared = None
-            if work.layers > 1 and call.kind.startswith("add"):
-                if call.T not in residual_by_T:
-                    residual_by_T[call.T] = torch.from_numpy(inp.residual.view(np.int16)).to(dev)
-                shared = residual_by_T[call.T]
-            dcalls.append(DeviceCall(torch, mbd, call, inp, dev, shared))
+    dcalls = build_device_calls(torch, mbd, work, args.seed, rank, dev)
     log(f"[bench] rank {rank}: inputs for {len(dcalls)} launches ready in {time.perf_counter() - t_gen:.1f}s")
 
     stream = torch.cuda.Stream(device=dev)
@@ -602,6 +714,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=1.0, help="target wall time of the oracle sample")
+    ap.add_argument("--decode-table", action="store_true",
+                    help="time the Qwen decode sweep as per-op calls, a CUDA graph and programs (one JSON line)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -609,6 +723,10 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.decode_table and args.impl == "mine":
+        if rank == 0:
+            print(json.dumps(run_decode_table(args)), flush=True)
+        return 0
     work = decode_sweep_workload() if args.workload == "qwen2.5-1.5b_decode_sweep" else workloads_by_key()[args.workload]
     if args.calls:
         keep = set(args.calls.split(","))

@@ -11,6 +11,7 @@
  *                                    the norm / SwiGLU with an NVFP4 epilogue (E2M1 codes, E4M3 block scales)
  *   mbd_fused_allreduce_add_rmsnorm[_quant_fp8]
  *                                    the norm fed by n partial activations summed on the way in
+ *   mbd_run_program                  a list of the above operations as ONE persistent kernel launch
  *
  * Definitions (cited by page title and section):
  *   [TRT] "TensorRT-LLM: Compiling Inference Engines Ahead of Time", section "Fusing operations, measured":
@@ -83,7 +84,7 @@ typedef enum {
 #define MBD_MAX_REDUCED_WIDTH 262144
 
 /* ABI version of this header (bumped on any signature change or added entry point). */
-#define MBD_ABI_VERSION 2
+#define MBD_ABI_VERSION 3
 int mbd_abi_version(void);
 
 /* Static, human-readable name of a status code (never NULL). */
@@ -213,6 +214,70 @@ mbd_status mbd_fused_add_rmsnorm_quant_nvfp4(uint8_t* out_q, uint8_t* out_sf, vo
                                              const float* tensor_scale, mbd_stream_t stream);
 mbd_status mbd_swiglu_quant_nvfp4(uint8_t* out_q, uint8_t* out_sf, const void* gate_up, int64_t n_tokens,
                                   int64_t inter, const float* tensor_scale, mbd_stream_t stream);
+
+/*
+ * Programs: several operations in one persistent kernel launch. No counterpart on the source pages as an
+ * API; it is this library's form of the launch-overhead remedies they discuss: [TRT] "Fusing operations,
+ * measured" notes that on a data-center GPU issuing the kernels can take longer than running them, and
+ * "Leaving the engine behind" lists CUDA graphs captured per batch size for decoding; [VLLM] section 5
+ * plans a single kernel for a whole forward pass.
+ *
+ * Each op is one call of the entry points above, described by value. Every op's n_tokens rows are
+ * independent: row t of an op reads and writes only row t of its tensors (plus the shared weight and a
+ * static scale). The program therefore gives the results of calling the ops one after another on
+ * `stream`, provided every buffer that two ops share, with one of them writing it, is the SAME tensor in
+ * both: the same pointer and the same row layout (same n_tokens and bytes per row) -- typically the
+ * residual that consecutive norms update, or an output that a later op reads in place. Ops linked that way
+ * form a chain whose rows run op after op inside one CTA; ops that share nothing with another op are spread
+ * over all CTAs. Sharing that is not row-aligned (a different pointer into the same memory, a different
+ * row layout, a dynamic scale read as a static scale) returns MBD_ERR_UNSUPPORTED.
+ */
+typedef enum {
+    MBD_OP_ADD_RMSNORM = 0,              /* mbd_fused_add_rmsnorm: in = x, out bf16 */
+    MBD_OP_ADD_RMSNORM_QUANT_FP8 = 1,    /* mbd_fused_add_rmsnorm_quant_fp8: mode, scale */
+    MBD_OP_ADD_RMSNORM_QUANT_NVFP4 = 2,  /* mbd_fused_add_rmsnorm_quant_nvfp4: out_sf, scale = tensor scale */
+    MBD_OP_SWIGLU = 3,                   /* mbd_swiglu: in = gate_up */
+    MBD_OP_SWIGLU_QUANT_FP8 = 4,         /* mbd_swiglu_quant_fp8: mode, scale */
+    MBD_OP_SWIGLU_QUANT_NVFP4 = 5        /* mbd_swiglu_quant_nvfp4: out_sf, scale = tensor scale */
+} mbd_op_kind;
+
+/* One operation of a program: the arguments of its entry point (unused fields are ignored). */
+typedef struct {
+    int32_t kind;           /* mbd_op_kind */
+    int32_t mode;           /* FP8 ops: mbd_scale_mode */
+    int64_t n_tokens;
+    int64_t width;          /* hidden (norms) or inter (SwiGLU) */
+    float eps;              /* norms */
+    int32_t reserved;       /* must be 0 */
+    void* out;              /* bf16, E4M3 codes or packed E2M1 codes */
+    uint8_t* out_sf;        /* NVFP4 block scales */
+    void* residual;         /* norms */
+    const void* in;         /* norms: x; SwiGLU: gate_up */
+    const void* weight;     /* norms */
+    float* scale;           /* FP8 scale ([1] read or [n_tokens] written), or the NVFP4 tensor scale ([1] read) */
+} mbd_op;
+
+/* Largest number of ops in one program. */
+#define MBD_MAX_PROGRAM_OPS 128
+/* Largest hidden size of a norm in a program: one CTA of 256 threads holds the row, 4 vectors per thread.
+ * SwiGLU rows of any width run in chunks (a dynamic FP8 row wider than the CTA holds takes two passes:
+ * the row maximum, then the codes from the same inputs, read again from L2). */
+#define MBD_MAX_PROGRAM_WIDTH 8192
+
+/*
+ * Run ops[0..n_ops) as one persistent kernel on `stream`.
+ *   ops    : HOST array of n_ops descriptors, read during the call only (the schedule travels in the kernel's
+ *            parameters; nothing is allocated or copied beforehand).
+ *   n_ops  : 0 (no-op) .. MBD_MAX_PROGRAM_OPS.
+ * Each op is validated exactly as its entry point validates it (and the same status is returned, nothing
+ * launched). Besides: an unknown kind or a non-zero `reserved` gives MBD_ERR_INVALID_ARG; a norm wider
+ * than MBD_MAX_PROGRAM_WIDTH, sharing that is not row-aligned, or epilogues outside the compiled sets
+ * gives MBD_ERR_UNSUPPORTED. The compiled sets (norm epilogues / SwiGLU epilogues): bf16 / bf16, FP8
+ * static / FP8 dynamic, NVFP4 / NVFP4. Ops with n_tokens == 0 are skipped; if nothing remains, nothing is launched.
+ * Reductions run inside one CTA per row (no cluster), so sums may round differently from the single-call
+ * entry points in their last bit; every result keeps the tolerances stated for those entry points.
+ */
+mbd_status mbd_run_program(const mbd_op* ops, int n_ops, mbd_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -33,6 +33,23 @@ class MbdError(RuntimeError):
         self.status = status
 
 
+class Op(ctypes.Structure):
+    """One operation of a program (the C struct mbd_op)."""
+    _fields_ = [("kind", ctypes.c_int32), ("mode", ctypes.c_int32), ("n_tokens", ctypes.c_int64),
+                ("width", ctypes.c_int64), ("eps", ctypes.c_float), ("reserved", ctypes.c_int32),
+                ("out", ctypes.c_void_p), ("out_sf", ctypes.c_void_p), ("residual", ctypes.c_void_p),
+                ("in_", ctypes.c_void_p), ("weight", ctypes.c_void_p), ("scale", ctypes.c_void_p)]
+
+
+OP_ADD_RMSNORM = 0
+OP_ADD_RMSNORM_QUANT_FP8 = 1
+OP_ADD_RMSNORM_QUANT_NVFP4 = 2
+OP_SWIGLU = 3
+OP_SWIGLU_QUANT_FP8 = 4
+OP_SWIGLU_QUANT_NVFP4 = 5
+MAX_PROGRAM_OPS = 128
+
+
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is missing: build it with memory_bound_decoder_gb300.build.build() "
@@ -56,9 +73,10 @@ def _load() -> ctypes.CDLL:
     lib.mbd_swiglu_quant_fp8.argtypes = [vp, vp, i64, i64, cint, vp, vp]
     lib.mbd_fused_add_rmsnorm_quant_nvfp4.argtypes = [vp, vp, vp, vp, vp, i64, i64, f32, vp, vp]
     lib.mbd_swiglu_quant_nvfp4.argtypes = [vp, vp, vp, i64, i64, vp, vp]
+    lib.mbd_run_program.argtypes = [ctypes.POINTER(Op), cint, vp]
     for fn in ("mbd_fused_add_rmsnorm", "mbd_fused_add_rmsnorm_quant_fp8", "mbd_swiglu", "mbd_swiglu_quant_fp8",
                "mbd_fused_allreduce_add_rmsnorm", "mbd_fused_allreduce_add_rmsnorm_quant_fp8",
-               "mbd_fused_add_rmsnorm_quant_nvfp4", "mbd_swiglu_quant_nvfp4"):
+               "mbd_fused_add_rmsnorm_quant_nvfp4", "mbd_swiglu_quant_nvfp4", "mbd_run_program"):
         getattr(lib, fn).restype = cint
     return lib
 
@@ -207,3 +225,48 @@ def swiglu_quant_fp8(out_q, gate_up, n_tokens: int, inter: int, mode, scale, str
 def swiglu_quant_nvfp4(out_q, out_sf, gate_up, n_tokens: int, inter: int, tensor_scale, stream=None) -> None:
     _check(get_lib().mbd_swiglu_quant_nvfp4(_ptr(out_q), _ptr(out_sf), _ptr(gate_up), int(n_tokens), int(inter),
                                             _ptr(tensor_scale), _stream(stream)), "swiglu_quant_nvfp4")
+
+
+# ------------------------------------------------------------------------------------------------ programs
+
+def op_add_rmsnorm(out, residual, x, weight, n_tokens: int, hidden: int, eps: float) -> Op:
+    return Op(OP_ADD_RMSNORM, 0, int(n_tokens), int(hidden), float(eps), 0, _ptr(out), None, _ptr(residual),
+              _ptr(x), _ptr(weight), None)
+
+
+def op_add_rmsnorm_quant_fp8(out_q, residual, x, weight, n_tokens: int, hidden: int, eps: float, mode,
+                             scale) -> Op:
+    return Op(OP_ADD_RMSNORM_QUANT_FP8, _mode(mode), int(n_tokens), int(hidden), float(eps), 0, _ptr(out_q), None,
+              _ptr(residual), _ptr(x), _ptr(weight), _ptr(scale))
+
+
+def op_add_rmsnorm_quant_nvfp4(out_q, out_sf, residual, x, weight, n_tokens: int, hidden: int, eps: float,
+                               tensor_scale) -> Op:
+    return Op(OP_ADD_RMSNORM_QUANT_NVFP4, 0, int(n_tokens), int(hidden), float(eps), 0, _ptr(out_q), _ptr(out_sf),
+              _ptr(residual), _ptr(x), _ptr(weight), _ptr(tensor_scale))
+
+
+def op_swiglu(out, gate_up, n_tokens: int, inter: int) -> Op:
+    return Op(OP_SWIGLU, 0, int(n_tokens), int(inter), 0.0, 0, _ptr(out), None, None, _ptr(gate_up), None, None)
+
+
+def op_swiglu_quant_fp8(out_q, gate_up, n_tokens: int, inter: int, mode, scale) -> Op:
+    return Op(OP_SWIGLU_QUANT_FP8, _mode(mode), int(n_tokens), int(inter), 0.0, 0, _ptr(out_q), None, None,
+              _ptr(gate_up), None, _ptr(scale))
+
+
+def op_swiglu_quant_nvfp4(out_q, out_sf, gate_up, n_tokens: int, inter: int, tensor_scale) -> Op:
+    return Op(OP_SWIGLU_QUANT_NVFP4, 0, int(n_tokens), int(inter), 0.0, 0, _ptr(out_q), _ptr(out_sf), None,
+              _ptr(gate_up), None, _ptr(tensor_scale))
+
+
+def program_array(ops) -> Any:
+    """A ctypes array of Op for mbd_run_program (keep it alive while launching it repeatedly)."""
+    ops = list(ops)
+    return (Op * max(1, len(ops)))(*ops), len(ops)
+
+
+def run_program(ops, stream=None) -> None:
+    """Run a list of Op (or a program_array result) as one persistent kernel launch."""
+    arr, n = ops if isinstance(ops, tuple) else program_array(ops)
+    _check(get_lib().mbd_run_program(arr if n else None, n, _stream(stream)), "run_program")

@@ -18,8 +18,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libmbd.so")
-SOURCES = ["api.cu", "norm.cu", "swiglu.cu", "selftest.cu"]
-HEADERS = ["common.cuh", "launch.h"]
+SOURCES = ["api.cu", "norm.cu", "swiglu.cu", "program.cu", "selftest.cu"]
+HEADERS = ["common.cuh", "launch.h", "norm_impl.cuh", "swiglu_impl.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

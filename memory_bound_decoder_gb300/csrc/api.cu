@@ -2,6 +2,7 @@
 // Every check runs before anything is enqueued; a failing call launches nothing.
 #include <atomic>
 #include <cmath>
+#include <cstddef>
 #include <cstdint>
 
 #include "mbd.h"
@@ -143,9 +144,11 @@ bool fp8_epilogue(int mode, mbd::Epilogue* ep) {
     return true;
 }
 
-mbd_status norm_common(void* out, uint8_t* out_sf, mbd::Epilogue ep, void* residual, const void* x,
-                       const void* weight, int64_t n_tokens, int64_t hidden, float eps, float* scale,
-                       cudaStream_t stream, const void* const* partials = nullptr, int n_partials = 0) {
+// Every host-side check of one norm call, then its kernel parameters in *p (p->rows == 0: nothing to do).
+mbd_status norm_prepare(void* out, uint8_t* out_sf, mbd::Epilogue ep, void* residual, const void* x,
+                        const void* weight, int64_t n_tokens, int64_t hidden, float eps, float* scale,
+                        const void* const* partials, int n_partials, mbd::NormParams* p) {
+    *p = mbd::NormParams{};
     mbd_status st = check_width(n_tokens, hidden);
     if (st != MBD_OK) return st;
     const bool quant = ep != mbd::kBf16, dyn = ep == mbd::kFp8Dynamic, fp4 = ep == mbd::kNvfp4;
@@ -186,28 +189,38 @@ mbd_status norm_common(void* out, uint8_t* out_sf, mbd::Epilogue ep, void* resid
             return MBD_ERR_INVALID_ARG;
     }
 
+    p->x = x;
+    p->n_partials = partials ? n_partials : 0;
+    for (int k = 0; k < p->n_partials; ++k) p->partials[k] = partials[k];
+    p->residual = residual;
+    p->weight = weight;
+    p->out = out;
+    p->out_sf = out_sf;
+    p->scale = scale;
+    p->rows = n_tokens;
+    p->nvec = static_cast<int>(hidden / 8);
+    p->hidden = static_cast<int>(hidden);
+    p->eps = eps;
+    return MBD_OK;
+}
+
+mbd_status norm_common(void* out, uint8_t* out_sf, mbd::Epilogue ep, void* residual, const void* x,
+                       const void* weight, int64_t n_tokens, int64_t hidden, float eps, float* scale,
+                       cudaStream_t stream, const void* const* partials = nullptr, int n_partials = 0) {
+    mbd::NormParams p;
+    const mbd_status st =
+        norm_prepare(out, out_sf, ep, residual, x, weight, n_tokens, hidden, eps, scale, partials, n_partials, &p);
+    if (st != MBD_OK || p.rows == 0) return st;
     mbd::RowPlan plan;
-    if (!plan_rows(n_tokens, static_cast<int>(hidden / 8), partials ? Shape::kNormPartials : Shape::kNorm,
-                   sm_count_of_current_device(), fp4, &plan))
+    if (!plan_rows(p.rows, p.nvec, partials ? Shape::kNormPartials : Shape::kNorm, sm_count_of_current_device(),
+                   ep == mbd::kNvfp4, &plan))
         return MBD_ERR_UNSUPPORTED;
-    mbd::NormParams p{};
-    p.x = x;
-    p.n_partials = partials ? n_partials : 0;
-    for (int k = 0; k < p.n_partials; ++k) p.partials[k] = partials[k];
-    p.residual = residual;
-    p.weight = weight;
-    p.out = out;
-    p.out_sf = out_sf;
-    p.scale = scale;
-    p.rows = n_tokens;
-    p.nvec = static_cast<int>(hidden / 8);
-    p.hidden = static_cast<int>(hidden);
-    p.eps = eps;
     return finish_launch(mbd::launch_add_rmsnorm(p, ep, plan, stream));
 }
 
-mbd_status swiglu_common(void* out, uint8_t* out_sf, mbd::Epilogue ep, const void* gate_up, int64_t n_tokens,
-                         int64_t inter, float* scale, cudaStream_t stream) {
+mbd_status swiglu_prepare(void* out, uint8_t* out_sf, mbd::Epilogue ep, const void* gate_up, int64_t n_tokens,
+                          int64_t inter, float* scale, mbd::SwigluParams* p) {
+    *p = mbd::SwigluParams{};
     mbd_status st = check_width(n_tokens, inter);
     if (st != MBD_OK) return st;
     const bool quant = ep != mbd::kBf16, dyn = ep == mbd::kFp8Dynamic, fp4 = ep == mbd::kNvfp4;
@@ -227,12 +240,207 @@ mbd_status swiglu_common(void* out, uint8_t* out_sf, mbd::Epilogue ep, const voi
                 overlap(out_sf, sfb, scale, sb)))
         return MBD_ERR_INVALID_ARG;
 
+    *p = mbd::SwigluParams{gate_up, out, scale, n_tokens, static_cast<int>(inter / 8), out_sf};
+    return MBD_OK;
+}
+
+mbd_status swiglu_common(void* out, uint8_t* out_sf, mbd::Epilogue ep, const void* gate_up, int64_t n_tokens,
+                         int64_t inter, float* scale, cudaStream_t stream) {
+    mbd::SwigluParams p;
+    const mbd_status st = swiglu_prepare(out, out_sf, ep, gate_up, n_tokens, inter, scale, &p);
+    if (st != MBD_OK || p.rows == 0) return st;
     mbd::RowPlan plan;
-    if (!plan_rows(n_tokens, static_cast<int>(inter / 8), dyn ? Shape::kRowMax : Shape::kStream,
-                   sm_count_of_current_device(), fp4, &plan))
+    if (!plan_rows(p.rows, p.nvec, ep == mbd::kFp8Dynamic ? Shape::kRowMax : Shape::kStream,
+                   sm_count_of_current_device(), ep == mbd::kNvfp4, &plan))
         return MBD_ERR_UNSUPPORTED;
-    mbd::SwigluParams p{gate_up, out, scale, n_tokens, static_cast<int>(inter / 8), out_sf};
     return finish_launch(mbd::launch_swiglu(p, ep, plan, stream));
+}
+
+// ------------------------------------------------------------------------------------------ programs
+
+static_assert(sizeof(mbd::ProgramParams) <= 32764, "program parameters exceed the kernel parameter limit");
+static_assert(mbd::kMaxProgramOps == MBD_MAX_PROGRAM_OPS, "program op limit");
+static_assert(sizeof(mbd_op) == 80 && offsetof(mbd_op, out) == 32 && offsetof(mbd_op, scale) == 72, "mbd_op layout");
+
+// A byte range an op touches: row-wise ranges (row_bytes > 0) hold `rows` rows of row_bytes each.
+struct Region {
+    const void* ptr;
+    size_t bytes;
+    bool write;
+    size_t row_bytes;
+    int64_t rows;
+};
+
+struct OpInfo {
+    Region reg[6];
+    int nreg;
+    bool holds_row;   // reduces over its row: the whole row stays in one CTA
+};
+
+void add_region(OpInfo& o, const void* ptr, size_t bytes, bool write, size_t row_bytes, int64_t rows) {
+    if (ptr && bytes) o.reg[o.nreg++] = Region{ptr, bytes, write, row_bytes, rows};
+}
+
+int find_root(int* parent, int i) {
+    while (parent[i] != i) i = parent[i] = parent[parent[i]];
+    return i;
+}
+
+// The ops' regions conflict (overlap, one of them written); ok == false if they do so other than as the
+// same row-wise tensor.
+bool conflicts(const OpInfo& a, const OpInfo& b, bool* ok) {
+    bool any = false;
+    *ok = true;
+    for (int i = 0; i < a.nreg; ++i)
+        for (int j = 0; j < b.nreg; ++j) {
+            const Region &x = a.reg[i], &y = b.reg[j];
+            if (!(x.write || y.write) || !overlap(x.ptr, x.bytes, y.ptr, y.bytes)) continue;
+            any = true;
+            if (!(x.row_bytes > 0 && x.ptr == y.ptr && x.row_bytes == y.row_bytes && x.rows == y.rows)) *ok = false;
+        }
+    return any;
+}
+
+// Resident program CTAs per SM, queried once per device, vectors per thread and variant.
+std::atomic<int> g_prog_ctas[kMaxDevices][3][mbd::kProgramVariants];
+
+int program_ctas_per_sm_cached(int vpt, int variant) {
+    int dev = 0;
+    const int vi = vpt == 1 ? 0 : (vpt == 2 ? 1 : 2);
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        (void)cudaGetLastError();
+        return mbd::program_ctas_per_sm(vpt, variant);
+    }
+    int n = g_prog_ctas[dev][vi][variant].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+    n = mbd::program_ctas_per_sm(vpt, variant);
+    if (n > 0) g_prog_ctas[dev][vi][variant].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+mbd_status run_program(const mbd_op* ops, int n_ops, cudaStream_t stream) {
+    if (n_ops < 0 || n_ops > MBD_MAX_PROGRAM_OPS || (n_ops > 0 && !ops)) return MBD_ERR_INVALID_ARG;
+    mbd::ProgramParams P{};
+    OpInfo info[MBD_MAX_PROGRAM_OPS];
+    bool active[MBD_MAX_PROGRAM_OPS] = {};
+    int norm_mask = 0, swiglu_mask = 0, max_held_nvec = 0;
+    for (int i = 0; i < n_ops; ++i) {
+        const mbd_op& o = ops[i];
+        if (o.reserved != 0 || o.kind < MBD_OP_ADD_RMSNORM || o.kind > MBD_OP_SWIGLU_QUANT_NVFP4) return MBD_ERR_INVALID_ARG;
+        const bool is_norm = o.kind <= MBD_OP_ADD_RMSNORM_QUANT_NVFP4;
+        const int sub = is_norm ? o.kind : o.kind - MBD_OP_SWIGLU;   // 0 bf16, 1 FP8, 2 NVFP4
+        mbd::Epilogue ep = sub == 0 ? mbd::kBf16 : mbd::kNvfp4;
+        if (sub == 1 && !fp8_epilogue(o.mode, &ep)) return MBD_ERR_INVALID_ARG;
+        mbd::ProgOp& po = P.ops[i];
+        OpInfo& in = info[i];
+        in.nreg = 0;
+        const size_t W = static_cast<size_t>(o.width);
+        if (is_norm) {
+            mbd::NormParams np;
+            const mbd_status st = norm_prepare(o.out, o.out_sf, ep, o.residual, o.in, o.weight, o.n_tokens, o.width,
+                                               o.eps, o.scale, nullptr, 0, &np);
+            if (st != MBD_OK) return st;
+            if (np.rows == 0) continue;
+            po = mbd::ProgOp{np.x, np.residual, np.weight, np.out, np.out_sf, np.scale, np.rows, mbd::kOpNorm,
+                             ep, np.nvec, np.hidden, np.eps, 0};
+            add_region(in, o.in, np.rows * W * 2, false, W * 2, np.rows);
+            add_region(in, o.residual, np.rows * W * 2, true, W * 2, np.rows);
+            add_region(in, o.weight, W * 2, false, 0, 0);
+            in.holds_row = true;
+            norm_mask |= 1 << ep;
+        } else {
+            mbd::SwigluParams sp;
+            const mbd_status st = swiglu_prepare(o.out, o.out_sf, ep, o.in, o.n_tokens, o.width, o.scale, &sp);
+            if (st != MBD_OK) return st;
+            if (sp.rows == 0) continue;
+            po = mbd::ProgOp{sp.gate_up, nullptr, nullptr, sp.out, sp.out_sf, sp.scale, sp.rows, mbd::kOpSwiglu, ep,
+                             sp.nvec, static_cast<int>(o.width), 0.0f, 0};
+            add_region(in, o.in, sp.rows * W * 4, false, W * 4, sp.rows);
+            in.holds_row = false;   // streams run in chunks; a wide dynamic row takes two passes
+            swiglu_mask |= 1 << ep;
+        }
+        const int64_t T = po.rows;
+        const size_t out_row = ep == mbd::kBf16 ? 2 * W : (ep == mbd::kNvfp4 ? W / 2 : W);
+        add_region(in, o.out, T * out_row, true, out_row, T);
+        if (ep == mbd::kNvfp4) add_region(in, o.out_sf, T * (W / 16), true, W / 16, T);
+        if (ep == mbd::kFp8Dynamic) add_region(in, o.scale, T * 4, true, 4, T);
+        else if (ep != mbd::kBf16) add_region(in, o.scale, 4, false, 0, 0);
+        if (in.holds_row && po.nvec > max_held_nvec) max_held_nvec = po.nvec;
+        active[i] = true;
+    }
+    // ops linked by a shared, written buffer form chains (union-find)
+    int parent[MBD_MAX_PROGRAM_OPS];
+    for (int i = 0; i < n_ops; ++i) parent[i] = i;
+    for (int i = 0; i < n_ops; ++i)
+        for (int j = i + 1; j < n_ops; ++j) {
+            if (!active[i] || !active[j]) continue;
+            bool ok;
+            if (!conflicts(info[i], info[j], &ok)) continue;
+            if (!ok) return MBD_ERR_UNSUPPORTED;
+            parent[find_root(parent, j)] = find_root(parent, i);
+        }
+    int size[MBD_MAX_PROGRAM_OPS] = {};
+    for (int i = 0; i < n_ops; ++i)
+        if (active[i]) ++size[find_root(parent, i)];
+    if (max_held_nvec > MBD_MAX_PROGRAM_WIDTH / 8) return MBD_ERR_UNSUPPORTED;
+    const int vpt = max_held_nvec <= mbd::kProgramThreads ? 1 : (max_held_nvec <= 2 * mbd::kProgramThreads ? 2 : 4);
+    const int variant = mbd::program_variant(norm_mask, swiglu_mask);
+    if (variant < 0) return MBD_ERR_UNSUPPORTED;
+    P.chunk_vecs = mbd::kProgramThreads * vpt;
+
+    // chains in the order of their first op, each op after the ops before it in the list
+    int order_len = 0;
+    int64_t warm_row_bytes = 0;
+    for (int r = 0; r < n_ops; ++r) {
+        if (!active[r] || find_root(parent, r) != r) continue;
+        if (size[r] > 1) {
+            P.group_begin[P.n_groups] = order_len;
+            P.group_items[P.n_groups] = P.n_chain_items;
+            for (int i = r; i < n_ops; ++i) {
+                if (!active[i] || find_root(parent, i) != r) continue;
+                // warm this op's row inputs unless an earlier op of the chain writes them
+                mbd::ProgOp& po = P.ops[i];
+                bool in_written = false, res_written = false;
+                for (int k = P.group_begin[P.n_groups]; k < order_len; ++k)
+                    for (int q = 0; q < info[P.chain_order[k]].nreg; ++q) {
+                        const Region& w = info[P.chain_order[k]].reg[q];
+                        if (!w.write) continue;
+                        in_written |= overlap(w.ptr, w.bytes, po.in, static_cast<size_t>(po.rows) * po.nvec *
+                                                                         (po.cls == mbd::kOpNorm ? 16 : 32));
+                        if (po.residual)
+                            res_written |= overlap(w.ptr, w.bytes, po.residual, static_cast<size_t>(po.rows) * po.nvec * 16);
+                    }
+                po.prefetch = (in_written ? 0 : 1) | ((po.residual && !res_written) ? 2 : 0);
+                warm_row_bytes += (in_written ? 0 : int64_t{po.nvec} * (po.cls == mbd::kOpNorm ? 16 : 32)) +
+                                  ((po.residual && !res_written) ? int64_t{po.nvec} * 16 : 0);
+                P.chain_order[order_len++] = i;
+            }
+            P.n_chain_items += P.ops[r].rows;
+            ++P.n_groups;
+        } else {
+            P.free_op[P.n_free] = r;
+            P.free_chunks[P.n_free] = (info[r].holds_row || P.ops[r].ep == mbd::kFp8Dynamic)
+                                          ? 1 : cdiv(P.ops[r].nvec, P.chunk_vecs);
+            P.free_items[P.n_free] = P.n_free_items;
+            P.n_free_items += P.ops[r].rows * P.free_chunks[P.n_free];
+            ++P.n_free;
+        }
+    }
+    P.group_begin[P.n_groups] = order_len;
+    P.group_items[P.n_groups] = P.n_chain_items;
+    P.free_items[P.n_free] = P.n_free_items;
+    const int64_t items = P.n_chain_items + P.n_free_items;
+    if (items == 0) return MBD_OK;
+    const int per_sm = program_ctas_per_sm_cached(vpt, variant);
+    if (per_sm <= 0) {
+        g_last_cuda_error = static_cast<int>(cudaErrorInvalidConfiguration);
+        return MBD_ERR_CUDA;
+    }
+    const int64_t slots = int64_t{sm_count_of_current_device()} * per_sm;
+    const int grid = static_cast<int>(items < slots ? items : slots);
+    // warm the chains' row inputs only while the rows in flight fit well inside L2 (a quarter of 126 MiB)
+    P.prefetch_chains = warm_row_bytes * (P.n_chain_items < grid ? P.n_chain_items : grid) <= (int64_t{32} << 20);
+    return finish_launch(mbd::launch_program(P, vpt, variant, grid, stream));
 }
 
 }  // namespace
@@ -262,12 +470,14 @@ mbd_status mbd_device_error_flags(uint32_t* flags, int clear) {
     cudaError_t e = mbd::device_error_flags_norm(&a, clear != 0);
     if (e == cudaSuccess) e = mbd::device_error_flags_swiglu(&b, clear != 0);
     if (e == cudaSuccess) e = mbd::device_error_flags_selftest(&c, clear != 0);
+    unsigned int d = 0;
+    if (e == cudaSuccess) e = mbd::device_error_flags_program(&d, clear != 0);
     if (e != cudaSuccess) {
         g_last_cuda_error = static_cast<int>(e);
         (void)cudaGetLastError();
         return MBD_ERR_CUDA;
     }
-    *flags = a | b | c;
+    *flags = a | b | c | d;
     return MBD_OK;
 }
 
@@ -335,6 +545,10 @@ mbd_status mbd_swiglu_quant_nvfp4(uint8_t* out_q, uint8_t* out_sf, const void* g
                                   int64_t inter, const float* tensor_scale, mbd_stream_t stream) {
     return swiglu_common(out_q, out_sf, mbd::kNvfp4, gate_up, n_tokens, inter, const_cast<float*>(tensor_scale),
                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+mbd_status mbd_run_program(const mbd_op* ops, int n_ops, mbd_stream_t stream) {
+    return run_program(ops, n_ops, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -50,6 +50,60 @@ struct SwigluParams {
     uint8_t* out_sf; // NVFP4 block scales [T, I / 16]
 };
 
+// ------------------------------------------------------------------------------------------ programs
+
+constexpr int kMaxProgramOps = 128;     // MBD_MAX_PROGRAM_OPS
+constexpr int kProgramThreads = 256;    // CTA size of the program kernel
+constexpr int kMaxProgramGroups = kMaxProgramOps / 2;
+
+enum OpClass : int { kOpNorm = 0, kOpSwiglu = 1 };
+
+// One op of a program, as the kernel sees it.
+struct ProgOp {
+    const void* in;      // x (norm) or gate_up (SwiGLU)
+    void* residual;      // norm
+    const void* weight;  // norm
+    void* out;
+    uint8_t* out_sf;     // NVFP4 block scales
+    float* scale;
+    int64_t rows;
+    int cls;             // OpClass
+    int ep;              // Epilogue
+    int nvec;            // width / 8
+    int hidden;          // width
+    float eps;
+    int prefetch;        // chain ops: bit 0 warm `in`, bit 1 warm `residual` (row inputs no earlier op writes)
+};
+
+// The whole schedule, passed by value as the kernel's parameters (about 14 KB).
+// Chain items: (group g, row t) for t < rows of g; the CTA runs every op of g on row t in list order.
+// Free items: (free op f, row t, chunk k); ops that hold their row have one chunk per row.
+struct ProgramParams {
+    int n_groups;
+    int n_free;
+    int chunk_vecs;                             // vectors of one stream chunk (kProgramThreads * vpt)
+    int prefetch_chains;                        // warm each chain row's external inputs first
+    int64_t n_chain_items;
+    int64_t n_free_items;
+    int chain_order[kMaxProgramOps];            // op indices, group by group, each in list order
+    int group_begin[kMaxProgramGroups + 1];     // group g: chain_order[group_begin[g] .. group_begin[g + 1])
+    int64_t group_items[kMaxProgramGroups + 1]; // prefix sums of the groups' rows
+    int free_op[kMaxProgramOps];
+    int free_chunks[kMaxProgramOps];            // items per row of free op f
+    int64_t free_items[kMaxProgramOps + 1];     // prefix sums of rows * chunks
+    ProgOp ops[kMaxProgramOps];
+};
+
+// Compiled program-kernel variants, each for a set of norm and SwiGLU epilogues (bit e = Epilogue e).
+constexpr int kProgramVariants = 3;
+// The first variant that covers the given epilogue sets, or -1.
+int program_variant(int norm_mask, int swiglu_mask);
+// Program kernel `variant` for `vpt` vectors per thread (1, 2 or 4) on `grid` CTAs of kProgramThreads.
+cudaError_t launch_program(const ProgramParams& p, int vpt, int variant, int grid, cudaStream_t s);
+// Resident program CTAs per SM (occupancy query; 0 on error).
+int program_ctas_per_sm(int vpt, int variant);
+cudaError_t device_error_flags_program(unsigned int* flags, bool clear);
+
 // Launchers: return the cudaError_t of the launch (cudaSuccess when enqueued). Every launch enables
 // programmatic stream serialization; the kernels wait on the previous grid before touching memory.
 cudaError_t launch_add_rmsnorm(const NormParams& p, Epilogue ep, const RowPlan& plan, cudaStream_t s);

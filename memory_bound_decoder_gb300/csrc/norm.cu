@@ -15,256 +15,27 @@
 // walkthrough, Part V, quantization co-designed with the hardware). The dynamic per-token variant
 // reduces the sum of squares and max |w * s| together (the scale is max |w * s| * inv / 448), then stores
 // the codes from registers.
-#include "common.cuh"
-#include "launch.h"
+#include "norm_impl.cuh"
 
 namespace mbd {
 
 namespace {
 
-// Quantise y = p * (c_hi + c_lo) to E4M3, rounding the double-float product as if it were exact.
-// p * c_hi is split exactly into y_hi + err (FMA); y_lo = err + p * c_lo. Rounding y_hi alone is correct
-// unless y_hi lands exactly on a rounding boundary of the E4M3 grid; every such boundary (and every code
-// value) has its 19 low fp32 mantissa bits clear, so a value of that form is moved one fp32 ulp toward
-// y_hi + y_lo. A one-ulp move cannot cross a boundary that y_hi was not already on.
-__device__ __forceinline__ float nudge(float y_hi, float y_lo) {
-    uint32_t bits = __float_as_uint(y_hi);
-    if ((bits & 0x7FFFFu) == 0u && y_lo != 0.0f && y_hi != 0.0f) bits += ((y_lo > 0.0f) == (y_hi > 0.0f)) ? 1u : 0xFFFFFFFFu;
-    return __uint_as_float(bits);
-}
-
-__device__ __forceinline__ float2 exact_side(float2 p, float c_hi, float c_lo) {
-    const float2 y_hi = __fmul2_rn(p, f2(c_hi));
-    const float2 y_lo = __ffma2_rn(p, f2(c_lo), __ffma2_rn(p, f2(c_hi), make_float2(-y_hi.x, -y_hi.y)));
-    return make_float2(nudge(y_hi.x, y_lo.x), nudge(y_hi.y, y_lo.y));
-}
-
-// Sum the partial activations of this thread's vector exactly (packed double-float accumulation) and round
-// once to bf16: the reduced activation x of the all-reduce half. All the partials' loads are issued before
-// the first is used, so the vector costs one memory round trip.
-__device__ __forceinline__ uint4 reduce_partials(const NormParams& p, int64_t row, int c) {
-    uint4 pv[kMaxPartials];
-#pragma unroll
-    for (int k = 0; k < kMaxPartials; ++k)
-        if (k < p.n_partials) pv[k] = load_stream(static_cast<const uint4*>(p.partials[k]) + row * p.nvec + c);
-    DD2 acc[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) acc[q] = DD2{f2(0.0f), f2(0.0f)};
-#pragma unroll
-    for (int k = 0; k < kMaxPartials; ++k) {
-        if (k >= p.n_partials) break;
-        const uint32_t* w = reinterpret_cast<const uint32_t*>(&pv[k]);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) dd_accumulate(acc[q], bf16x2_to_float2(w[q]));
-    }
-    uint4 x;
-    uint32_t* xw = reinterpret_cast<uint32_t*>(&x);
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-        xw[q] = pack_bf16x2(dd_nudge_bf16(acc[q].hi.x, acc[q].lo.x), dd_nudge_bf16(acc[q].hi.y, acc[q].lo.y));
-    return x;
-}
-
 // The partial-sum form asks for two 512-thread CTAs per SM (<= 64 registers): its eight loads in flight
 // per vector would otherwise leave one CTA, a quarter of the SM's warps.
 template <int VPT, int EP, bool ALLRED>
-__global__ void __launch_bounds__(512, ALLRED ? 2 : 1) add_rmsnorm_kernel(NormParams p, int ctas_per_row, int slice,
+__global__ void __launch_bounds__(512, ALLRED ? 2 : 1) add_rmsnorm_kernel(const __grid_constant__ NormParams p, int ctas_per_row, int slice,
                                                                         int prefetch) {
-    __shared__ PSum part_sum[32];
-    __shared__ RowStats part_stats[32];
-    __shared__ Exchange ex;
-    __shared__ float row_const[2];
-    __shared__ int ok_flag;
-    // The weight is an L2 hit; load it up front when registers allow (small rows, latency-bound), else
-    // after the reduction. The dynamic variant needs it before the reduction anyway.
-    constexpr bool kEarlyWeight = EP == kFp8Dynamic || VPT <= 2;
-
+    __shared__ NormSmem sm;
     const int64_t row = launch_row();
     if (row >= p.rows) return;   // past the last row (the whole cluster shares the row)
     const int rank = static_cast<int>(blockIdx.x);
     const int begin = rank * slice;
     const int end = min(begin + slice, p.nvec);
-
-    const uint4* xr = static_cast<const uint4*>(p.x) + row * p.nvec;
-    uint4* rr = static_cast<uint4*>(p.residual) + row * p.nvec;
-    const uint4* wr = static_cast<const uint4*>(p.weight);
-
     pdl_trigger();
-    if (prefetch) {
-#pragma unroll
-        for (int i = 0; i < VPT; ++i) {
-            const int c = begin + threadIdx.x + i * blockDim.x;
-            if (c >= end) continue;
-            prefetch_l2(rr + c);
-            if constexpr (ALLRED) {
-                for (int k = 0; k < p.n_partials; ++k) prefetch_l2(static_cast<const uint4*>(p.partials[k]) + row * p.nvec + c);
-            } else {
-                prefetch_l2(xr + c);
-            }
-        }
-    }
+    if (prefetch) norm_prefetch<VPT, ALLRED>(p, row, begin, end);
     pdl_wait();
-
-    // 1. one pass over HBM: x and residual in, s = bf16(x + r) kept packed in registers and written back
-    uint4 sv[VPT], wv[VPT];
-    bool live[VPT];
-    {
-        uint4 xv[VPT];
-#pragma unroll
-        for (int i = 0; i < VPT; ++i) {
-            const int c = begin + threadIdx.x + i * blockDim.x;
-            live[i] = c < end;
-            if (live[i]) {
-                if constexpr (!ALLRED) xv[i] = load_stream(xr + c);
-                sv[i] = load_stream(rr + c);
-                if constexpr (kEarlyWeight) wv[i] = load_cached(wr + c);
-            }
-        }
-        if constexpr (ALLRED) {
-#pragma unroll
-            for (int i = 0; i < VPT; ++i)
-                if (live[i]) xv[i] = reduce_partials(p, row, begin + threadIdx.x + i * blockDim.x);
-        }
-        if (ctas_per_row > 1) exchange_init(ex, ctas_per_row);   // overlaps the loads in flight
-#pragma unroll
-        for (int i = 0; i < VPT; ++i) {
-            if (!live[i]) continue;
-            const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv[i]);
-            uint32_t* sw = reinterpret_cast<uint32_t*>(&sv[i]);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) sw[k] = pack_bf16x2(__fadd2_rn(bf16x2_to_float2(xw[k]), bf16x2_to_float2(sw[k])));
-            store_stream(rr + (begin + threadIdx.x + i * blockDim.x), sv[i]);
-        }
-    }
-
-    if constexpr (EP != kFp8Dynamic) {
-        // 2. sum of squares (fp32) -> inv = 1 / sqrt(mean + eps)
-        float2 ss2 = f2(0.0f);
-#pragma unroll
-        for (int i = 0; i < VPT; ++i) {
-            if (!live[i]) continue;
-            const uint32_t* sw = reinterpret_cast<const uint32_t*>(&sv[i]);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float2 s2 = bf16x2_to_float2(sw[k]);
-                ss2 = __ffma2_rn(s2, s2, ss2);
-            }
-        }
-        if (!row_reduce(PSum{ss2.x + ss2.y}, part_sum, ex, rank, ctas_per_row, &ok_flag, [&](PSum t) {
-                row_const[0] = 1.0f / sqrtf(t.v / static_cast<float>(p.hidden) + p.eps);
-            }))
-            return;
-        const float inv = row_const[0];
-
-        if constexpr (!kEarlyWeight) {
-#pragma unroll
-            for (int i = 0; i < VPT; ++i)
-                if (live[i]) wv[i] = load_cached(wr + (begin + threadIdx.x + i * blockDim.x));
-        }
-
-        // 3. v = (w * s) * inv; w * s of two bf16 values is exact in fp32
-        if constexpr (EP == kBf16) {
-            uint4* outr = static_cast<uint4*>(p.out) + row * p.nvec;
-#pragma unroll
-            for (int i = 0; i < VPT; ++i) {
-                if (!live[i]) continue;
-                const uint32_t* sw = reinterpret_cast<const uint32_t*>(&sv[i]);
-                const uint32_t* ww = reinterpret_cast<const uint32_t*>(&wv[i]);
-                uint4 o;
-                uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    ow[k] = pack_bf16x2(__fmul2_rn(__fmul2_rn(bf16x2_to_float2(sw[k]), bf16x2_to_float2(ww[k])), f2(inv)));
-                store_stream(outr + (begin + threadIdx.x + i * blockDim.x), o);
-            }
-        } else if constexpr (EP == kNvfp4) {
-            // NVFP4: block scales over 16 elements (this vector and the neighbouring lane's), E2M1 codes of
-            // v = (w * s) * inv scaled by the block's decoded scale times the tensor scale.
-            const Nvfp4Row nr = nvfp4_row(inv, nvfp4_tensor_scale(p.scale));
-            unsigned int* qr = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(p.out) + row * (int64_t)p.nvec * 4);
-            uint8_t* sfr = p.out_sf + row * (int64_t)(p.nvec / 2);
-#pragma unroll
-            for (int i = 0; i < VPT; ++i) {
-                float2 y[4];
-                const uint32_t* sw = reinterpret_cast<const uint32_t*>(&sv[i]);
-                const uint32_t* ww = reinterpret_cast<const uint32_t*>(&wv[i]);
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    y[k] = live[i] ? __fmul2_rn(bf16x2_to_float2(sw[k]), bf16x2_to_float2(ww[k])) : f2(0.0f);
-                uint32_t sf;
-                const uint32_t q = nvfp4_encode(y, nr, &sf);   // whole warp (block max by shuffle)
-                if (!live[i]) continue;
-                const int c = begin + threadIdx.x + i * blockDim.x;
-                store_stream(qr + c, q);
-                if ((threadIdx.x & 1) == 0) sfr[c >> 1] = static_cast<uint8_t>(sf);
-            }
-        } else {
-            // static per-tensor scale: codes of v / scale
-            const float sc = __ldg(p.scale);
-            const float c = sc > 0.0f ? inv * (1.0f / sc) : 0.0f;
-            uint2* outr = reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + row * (int64_t)p.nvec * 8);
-#pragma unroll
-            for (int i = 0; i < VPT; ++i) {
-                if (!live[i]) continue;
-                const uint32_t* sw = reinterpret_cast<const uint32_t*>(&sv[i]);
-                const uint32_t* ww = reinterpret_cast<const uint32_t*>(&wv[i]);
-                float2 y[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    y[k] = __fmul2_rn(__fmul2_rn(bf16x2_to_float2(sw[k]), bf16x2_to_float2(ww[k])), f2(c));
-                store_stream(outr + (begin + threadIdx.x + i * blockDim.x),
-                             make_uint2(pack_e4m3x4(y[0], y[1]), pack_e4m3x4(y[2], y[3])));
-            }
-        }
-    } else {
-        // Dynamic per-token scale. The codes are ratios of exact bf16 products, 448 * (w_j s_j) / (w_k s_k),
-        // rescaled by the fp32 rounding of the scale, so exact E4M3 ties are common; resolving them as the
-        // fp64 definition does needs the row constants to ~1e-13: the sum of squares is kept as a
-        // double-float, the per-row constants are formed in fp64 once per CTA, and every element is scaled
-        // with a double-float multiplier.
-        DD2 acc{f2(0.0f), f2(0.0f)};
-        float pmax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < VPT; ++i) {
-            if (!live[i]) continue;
-            const uint32_t* sw = reinterpret_cast<const uint32_t*>(&sv[i]);
-            const uint32_t* ww = reinterpret_cast<const uint32_t*>(&wv[i]);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float2 s2 = bf16x2_to_float2(sw[k]);
-                dd_accumulate(acc, __fmul2_rn(s2, s2));   // exact squares of bf16 values
-                const float2 p2 = __fmul2_rn(s2, bf16x2_to_float2(ww[k]));
-                pmax = fmaxf(pmax, fmaxf(fabsf(p2.x), fabsf(p2.y)));
-            }
-        }
-        const RowStats mine{dd_add(DD{acc.hi.x, acc.lo.x}, DD{acc.hi.y, acc.lo.y}), pmax};
-        if (!row_reduce(mine, part_stats, ex, rank, ctas_per_row, &ok_flag, [&](RowStats st) {
-                const double mean_sq = (static_cast<double>(st.sum_sq.hi) + static_cast<double>(st.sum_sq.lo)) /
-                                       static_cast<double>(p.hidden);
-                const double inv = 1.0 / sqrt(mean_sq + static_cast<double>(p.eps));
-                const float sc = static_cast<float>(static_cast<double>(st.pmax) * inv / 448.0);
-                const double c = sc > 0.0f ? inv / static_cast<double>(sc) : 0.0;
-                const float c_hi = static_cast<float>(c);
-                row_const[0] = c_hi;
-                row_const[1] = static_cast<float>(c - static_cast<double>(c_hi));
-                if (rank == 0) p.scale[row] = sc;
-            }))
-            return;
-        const float c_hi = row_const[0], c_lo = row_const[1];
-        uint2* outr = reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + row * (int64_t)p.nvec * 8);
-#pragma unroll
-        for (int i = 0; i < VPT; ++i) {
-            if (!live[i]) continue;
-            const uint32_t* sw = reinterpret_cast<const uint32_t*>(&sv[i]);
-            const uint32_t* ww = reinterpret_cast<const uint32_t*>(&wv[i]);
-            float2 y[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                y[k] = exact_side(__fmul2_rn(bf16x2_to_float2(sw[k]), bf16x2_to_float2(ww[k])), c_hi, c_lo);
-            store_stream(outr + (begin + threadIdx.x + i * blockDim.x),
-                         make_uint2(pack_e4m3x4(y[0], y[1]), pack_e4m3x4(y[2], y[3])));
-        }
-    }
+    norm_row_slice<VPT, EP, ALLRED>(p, row, rank, ctas_per_row, begin, end, sm);
 }
 
 template <int EP>

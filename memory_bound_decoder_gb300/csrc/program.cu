@@ -1,0 +1,265 @@
+// Persistent program kernel: a list of fused norm / SwiGLU ops in one launch.
+//
+// Every op maps row t of its inputs to row t of its outputs, so a list of ops can run row by row: ops that
+// share a buffer (the residual that consecutive norms update, an output read in place later) form a chain,
+// and one CTA runs a chain's ops on one row in list order, with a CTA barrier between ops so that each op
+// sees the previous op's stores; no grid-wide synchronisation and no scratch memory are needed. Ops that
+// share nothing are split into (row, chunk) items spread over the other CTAs. The per-row arithmetic is the
+// same device code as the one-launch-per-call kernels (norm_row_slice, swiglu_row_slice), with the whole
+// row in one CTA (no cluster).
+//
+// This is the launch-overhead remedy in kernel form ("TensorRT-LLM: Compiling Inference Engines Ahead of
+// Time", "Fusing operations, measured" and "Leaving the engine behind": issuing many small kernels costs
+// more than running them, hence CUDA graphs for decoding; "Introduction to torch.compile and How It Works
+// with vLLM", section 5: one kernel for a whole forward pass).
+#include "norm_impl.cuh"
+#include "swiglu_impl.cuh"
+
+namespace mbd {
+
+namespace {
+
+struct ProgSmem {
+    NormSmem norm;
+    SwigluSmem swiglu;
+};
+
+// Epilogue sets of a program kernel variant: bit e set = epilogue e compiled in. Each variant carries only
+// the epilogues it can meet, which keeps its registers near those of the one-launch-per-call kernels.
+constexpr int bit(int ep) { return 1 << ep; }
+
+template <int V, int NM>
+__device__ __forceinline__ void run_norm_row(const ProgOp& op, int64_t row, ProgSmem& sm) {
+    NormParams np;
+    np.x = op.in;
+    np.n_partials = 0;
+    np.residual = op.residual;
+    np.weight = op.weight;
+    np.out = op.out;
+    np.out_sf = op.out_sf;
+    np.scale = op.scale;
+    np.rows = op.rows;
+    np.nvec = op.nvec;
+    np.hidden = op.hidden;
+    np.eps = op.eps;
+    if constexpr ((NM & bit(kBf16)) != 0) {
+        if (op.ep == kBf16) return norm_row_slice<V, kBf16, false>(np, row, 0, 1, 0, op.nvec, sm.norm);
+    }
+    if constexpr ((NM & bit(kFp8Static)) != 0) {
+        if (op.ep == kFp8Static) return norm_row_slice<V, kFp8Static, false>(np, row, 0, 1, 0, op.nvec, sm.norm);
+    }
+    if constexpr ((NM & bit(kFp8Dynamic)) != 0) {
+        if (op.ep == kFp8Dynamic) return norm_row_slice<V, kFp8Dynamic, false>(np, row, 0, 1, 0, op.nvec, sm.norm);
+    }
+    if constexpr ((NM & bit(kNvfp4)) != 0) {
+        if (op.ep == kNvfp4) return norm_row_slice<V, kNvfp4, false>(np, row, 0, 1, 0, op.nvec, sm.norm);
+    }
+}
+
+// Vectors [begin, end) of one SwiGLU row (end - begin <= kProgramThreads * V; the whole row for the
+// dynamic epilogue, which reduces over it, when it fits).
+template <int V, int SM>
+__device__ __forceinline__ void run_swiglu_part(const ProgOp& op, int64_t row, int begin, int end, ProgSmem& sm) {
+    SwigluParams sp{op.in, op.out, op.scale, op.rows, op.nvec, op.out_sf};
+    if constexpr ((SM & bit(kBf16)) != 0) {
+        if (op.ep == kBf16) return swiglu_row_slice<V, kBf16>(sp, row, 0, 1, begin, end, sm.swiglu);
+    }
+    if constexpr ((SM & bit(kFp8Static)) != 0) {
+        if (op.ep == kFp8Static) return swiglu_row_slice<V, kFp8Static>(sp, row, 0, 1, begin, end, sm.swiglu);
+    }
+    if constexpr ((SM & bit(kFp8Dynamic)) != 0) {
+        if (op.ep == kFp8Dynamic) return swiglu_row_slice<V, kFp8Dynamic>(sp, row, 0, 1, begin, end, sm.swiglu);
+    }
+    if constexpr ((SM & bit(kNvfp4)) != 0) {
+        if (op.ep == kNvfp4) return swiglu_row_slice<V, kNvfp4>(sp, row, 0, 1, begin, end, sm.swiglu);
+    }
+}
+
+// A dynamic FP8 SwiGLU row: one pass from registers when it fits the CTA, else two passes (max, then codes).
+template <int V, int SM>
+__device__ __forceinline__ void run_swiglu_dynamic_row(const ProgOp& op, int64_t row, int chunk_vecs, ProgSmem& sm) {
+    if constexpr ((SM & bit(kFp8Dynamic)) != 0) {
+        if (op.nvec <= chunk_vecs) return run_swiglu_part<V, SM>(op, row, 0, op.nvec, sm);
+        SwigluParams sp{op.in, op.out, op.scale, op.rows, op.nvec, op.out_sf};
+        swiglu_dynamic_two_pass<1>(sp, row, sm.swiglu);   // one vector per thread per step: few registers
+    }
+}
+
+__device__ __forceinline__ void warm_row(const void* base, int64_t row, int nvec) {
+    const uint4* r = static_cast<const uint4*>(base) + row * nvec;
+    for (int c = threadIdx.x; c < nvec; c += blockDim.x) prefetch_l2(r + c);
+}
+
+template <int V, int NM, int SM>
+__device__ void run_chain_item(const ProgramParams& P, int64_t item, ProgSmem& sm) {
+    int g = 0;
+    while (g + 1 < P.n_groups && P.group_items[g + 1] <= item) ++g;
+    const int64_t row = item - P.group_items[g];
+    const int k0 = P.group_begin[g], k1 = P.group_begin[g + 1];
+    if (P.prefetch_chains) {
+        for (int k = k0; k < k1; ++k) {
+            const ProgOp& op = P.ops[P.chain_order[k]];
+            const int in_vecs = op.cls == kOpNorm ? op.nvec : 2 * op.nvec;
+            if (op.prefetch & 1) warm_row(op.in, row, in_vecs);
+            if (op.prefetch & 2) warm_row(op.residual, row, op.nvec);
+        }
+    }
+    for (int k = k0; k < k1; ++k) {
+        const ProgOp& op = P.ops[P.chain_order[k]];
+        if (op.cls == kOpNorm) {
+            run_norm_row<V, NM>(op, row, sm);
+        } else if (op.ep == kFp8Dynamic) {
+            run_swiglu_dynamic_row<V, SM>(op, row, P.chunk_vecs, sm);
+        } else {
+            for (int b = 0; b < op.nvec; b += P.chunk_vecs) run_swiglu_part<V, SM>(op, row, b, min(b + P.chunk_vecs, op.nvec), sm);
+        }
+        __syncthreads();   // this op's stores are visible to every thread before the next op reads them
+    }
+}
+
+template <int V, int NM, int SM>
+__device__ void run_free_item(const ProgramParams& P, int64_t item, ProgSmem& sm) {
+    int f = 0;
+    while (f + 1 < P.n_free && P.free_items[f + 1] <= item) ++f;
+    const ProgOp& op = P.ops[P.free_op[f]];
+    const int64_t local = item - P.free_items[f];
+    const int chunks = P.free_chunks[f];
+    const int64_t row = local / chunks;
+    const int chunk = static_cast<int>(local - row * chunks);
+    if (op.cls == kOpNorm) {
+        run_norm_row<V, NM>(op, row, sm);
+    } else if (op.ep == kFp8Dynamic) {
+        run_swiglu_dynamic_row<V, SM>(op, row, P.chunk_vecs, sm);
+    } else {
+        const int b = chunks == 1 ? 0 : chunk * P.chunk_vecs;
+        const int e = chunks == 1 ? op.nvec : min(b + P.chunk_vecs, op.nvec);
+        run_swiglu_part<V, SM>(op, row, b, e, sm);
+    }
+}
+
+// Chain items take CTAs 0 .. n_chain - 1 and free items the CTAs after them, so a chain (the critical path
+// of a decode step) shares its CTA with nothing; when there are more chain items than CTAs both kinds are
+// dealt round-robin over the whole grid.
+// Resident CTAs per SM each variant is compiled for (the register cap): the most that leaves it without
+// spills, from ptxas -v (bf16 at 1 vector per thread fits 32 registers; the others need 40 to 128; the FP8
+// variant at 4 vectors per thread keeps a small spill at the 128-register limit).
+constexpr int min_ctas(int v, int nm, int sm) {
+    return sm == bit(kFp8Dynamic) ? (v == 1 ? 4 : 2)   // the dynamic SwiGLU's two-pass form adds registers
+                                  : (v == 1 ? ((nm == bit(kBf16) && sm == bit(kBf16)) ? 8 : 6) : (v == 2 ? 3 : 2));
+}
+
+template <int V, int NM, int SM>
+__global__ void __launch_bounds__(kProgramThreads, min_ctas(V, NM, SM)) program_kernel(const __grid_constant__ ProgramParams P) {
+    __shared__ ProgSmem sm;
+    pdl_trigger();
+    pdl_wait();
+    const int64_t G = gridDim.x, b = blockIdx.x;
+    const int64_t nc = P.n_chain_items, nf = P.n_free_items;
+    if (nc < G) {
+        if (b < nc) {
+            run_chain_item<V, NM, SM>(P, b, sm);
+        } else {
+            for (int64_t j = b - nc; j < nf; j += G - nc) run_free_item<V, NM, SM>(P, j, sm);
+        }
+    } else {
+        for (int64_t i = b; i < nc; i += G) run_chain_item<V, NM, SM>(P, i, sm);
+        for (int64_t j = b; j < nf; j += G) run_free_item<V, NM, SM>(P, j, sm);
+    }
+}
+
+template <int V, int NM, int SM>
+int ctas_per_sm() {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, program_kernel<V, NM, SM>, kProgramThreads, 0) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+template <int V, int NM, int SM>
+cudaError_t launch_variant(const ProgramParams& p, int grid, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = cudaLaunchConfig_t{};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(kProgramThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, program_kernel<V, NM, SM>, p);
+}
+
+// The compiled variants: (norm epilogues, SwiGLU epilogues).
+constexpr int kVariantMasks[kProgramVariants][2] = {
+    {bit(kBf16), bit(kBf16)},                  // bf16 layers
+    {bit(kFp8Static), bit(kFp8Dynamic)},       // FP8: static-scale norm, dynamic-scale SwiGLU
+    {bit(kNvfp4), bit(kNvfp4)},                // NVFP4 layers
+};
+
+template <int V, int K>
+int ctas_of() { return ctas_per_sm<V, kVariantMasks[K][0], kVariantMasks[K][1]>(); }
+
+template <int V, int K>
+cudaError_t launch_of(const ProgramParams& p, int grid, cudaStream_t s) {
+    return launch_variant<V, kVariantMasks[K][0], kVariantMasks[K][1]>(p, grid, s);
+}
+
+template <int V>
+int ctas_v(int variant) {
+    switch (variant) {
+        case 0: return ctas_of<V, 0>();
+        case 1: return ctas_of<V, 1>();
+        case 2: return ctas_of<V, 2>();
+    }
+    return 0;
+}
+
+template <int V>
+cudaError_t launch_v(const ProgramParams& p, int variant, int grid, cudaStream_t s) {
+    switch (variant) {
+        case 0: return launch_of<V, 0>(p, grid, s);
+        case 1: return launch_of<V, 1>(p, grid, s);
+        case 2: return launch_of<V, 2>(p, grid, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+int program_variant(int norm_mask, int swiglu_mask) {
+    for (int k = 0; k < kProgramVariants; ++k)
+        if ((norm_mask & ~kVariantMasks[k][0]) == 0 && (swiglu_mask & ~kVariantMasks[k][1]) == 0) return k;
+    return -1;
+}
+
+int program_ctas_per_sm(int vpt, int variant) {
+    switch (vpt) {
+        case 1: return ctas_v<1>(variant);
+        case 2: return ctas_v<2>(variant);
+        case 4: return ctas_v<4>(variant);
+    }
+    return 0;
+}
+
+cudaError_t launch_program(const ProgramParams& p, int vpt, int variant, int grid, cudaStream_t s) {
+    switch (vpt) {
+        case 1: return launch_v<1>(p, variant, grid, s);
+        case 2: return launch_v<2>(p, variant, grid, s);
+        case 4: return launch_v<4>(p, variant, grid, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t device_error_flags_program(unsigned int* flags, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(flags, g_device_error_flags, sizeof(unsigned int));
+    if (e == cudaSuccess && clear) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_device_error_flags, &zero, sizeof(unsigned int));
+    }
+    return e;
+}
+
+}  // namespace mbd

@@ -34,9 +34,9 @@ def test_binding_names_match_header():
 
 
 def test_version_and_status_strings(lib):
-    assert lib.mbd_abi_version() == 2
+    assert lib.mbd_abi_version() == 3
     hdr = open(mbd.HEADER_PATH).read()
-    assert int(re.search(r"#define MBD_ABI_VERSION (\d+)", hdr).group(1)) == 2
+    assert int(re.search(r"#define MBD_ABI_VERSION (\d+)", hdr).group(1)) == 3
     for code in range(5):
         assert lib.mbd_status_string(code).decode().startswith("MBD_")
     assert lib.mbd_status_string(99) == b"unknown mbd_status"
@@ -159,3 +159,46 @@ def test_nvfp4_argument_checks(lib):
     assert _rc(s, A, 6 * A, 2 * A, 4, 64, None) == mbd.ERR_INVALID_ARG
     # a pure stream: no width limit beyond the 2^28 sanity bound
     s(None, None, None, 0, 262144 + 16, None)
+
+
+def test_program_argument_checks(lib):
+    n0 = mbd.kernel_launches()
+    mbd.run_program([])                                                      # empty program: nothing launched
+    mbd.run_program([mbd.op_swiglu(None, None, 0, 64)])                      # zero-token ops are skipped
+    assert mbd.kernel_launches() == n0
+    H = 64
+    norm = lambda out, res, x, T=4, H=H: mbd.op_add_rmsnorm(out, res, x, 9 * A, T, H, 1e-6)
+    assert _rc(mbd.run_program, [norm(A, 2 * A, 3 * A)] * 129) == mbd.ERR_INVALID_ARG        # too many ops
+    bad = norm(A, 2 * A, 3 * A)
+    bad.kind = 9
+    assert _rc(mbd.run_program, [bad]) == mbd.ERR_INVALID_ARG                                # unknown kind
+    bad = norm(A, 2 * A, 3 * A)
+    bad.reserved = 1
+    assert _rc(mbd.run_program, [bad]) == mbd.ERR_INVALID_ARG
+    bad = mbd.op_add_rmsnorm_quant_fp8(A, 2 * A, 3 * A, 9 * A, 4, H, 1e-6, 7, 5 * A)
+    assert _rc(mbd.run_program, [bad]) == mbd.ERR_INVALID_ARG                                # unknown FP8 mode
+    # each op is validated like its entry point, with the same status
+    assert _rc(mbd.run_program, [norm(A + 2, 2 * A, 3 * A)]) == mbd.ERR_MISALIGNED
+    assert _rc(mbd.run_program, [norm(A, 2 * A, 2 * A + 64)]) == mbd.ERR_INVALID_ARG         # x inside residual
+    # a later op reading a written buffer through another pointer, or with another row layout
+    a, b = norm(A, 2 * A, 3 * A), norm(4 * A, 5 * A, A + 16)
+    assert _rc(mbd.run_program, [a, b]) == mbd.ERR_UNSUPPORTED
+    a, b = norm(A, 2 * A, 3 * A), norm(4 * A, 5 * A, A, T=2, H=2 * H)
+    assert _rc(mbd.run_program, [a, b]) == mbd.ERR_UNSUPPORTED
+    # a dynamic FP8 scale written by one op and read as another op's static scale
+    q1 = mbd.op_add_rmsnorm_quant_fp8(6 * A, 2 * A, 3 * A, 9 * A, 4, H, 1e-6, "dynamic", 7 * A)
+    q2 = mbd.op_add_rmsnorm_quant_fp8(8 * A, 5 * A, 4 * A, 9 * A, 4, H, 1e-6, "static", 7 * A)
+    assert _rc(mbd.run_program, [q1, q2]) == mbd.ERR_UNSUPPORTED
+    # the weight is not a row-wise tensor: writing it in a program is rejected
+    w_writer = mbd.op_add_rmsnorm(9 * A, 5 * A, 4 * A, 13 * A, 4, H, 1e-6)   # its output is the first op's weight
+    assert _rc(mbd.run_program, [norm(A, 2 * A, 3 * A), w_writer]) == mbd.ERR_UNSUPPORTED
+    # a row that must stay in one CTA is limited to MBD_MAX_PROGRAM_WIDTH elements
+    assert _rc(mbd.run_program, [norm(A, 2 * A, 3 * A, T=1, H=8192 + 16)]) == mbd.ERR_UNSUPPORTED
+    # epilogues outside the compiled sets: a bf16 norm with an FP8 SwiGLU
+    s8 = mbd.op_swiglu_quant_fp8(10 * A, 11 * A, 4, H, "dynamic", 12 * A)
+    assert _rc(mbd.run_program, [norm(A, 2 * A, 3 * A), s8]) == mbd.ERR_UNSUPPORTED
+    assert mbd.kernel_launches() == n0
+
+
+def test_program_struct_layout():
+    assert ctypes.sizeof(mbd.Op) == 80 and mbd.Op.out.offset == 32 and mbd.Op.scale.offset == 72
