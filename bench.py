@@ -15,6 +15,7 @@ Diagnostics go to stderr.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import concurrent.futures as cf
 import hashlib
 import json
@@ -294,7 +295,7 @@ class DeviceCall:
             self.h2d += [(t, u16(q).pin_memory()) for t, q in zip(self.ps, inp.partials)]
             self.h2d.append((self.res, u16(inp.residual).pin_memory()))
             lib = mbd.get_lib()
-            import ctypes
+
             self._parr = (ctypes.c_void_p * len(self.ps))(*[t.data_ptr() for t in self.ps])
             if call.kind == "allreduce_rmsnorm":
                 self.out = torch.empty((T, W), dtype=torch.int16, device=dev)
@@ -365,7 +366,7 @@ class DeviceCall:
         self.d2h.append((self.out, torch.empty_like(self.out, device="cpu").pin_memory()))
 
     def bind(self, stream_handle: int):
-        import ctypes
+
         args = list(self.args)
         if self.call.kind in ("add_rmsnorm", "add_rmsnorm_q8"):
             args[6] = ctypes.c_float(args[6])
@@ -478,8 +479,8 @@ def build_device_calls(torch, mbd, work: wl.Workload, seed: int, rank: int, dev)
 def run_decode_table(args) -> Dict:
     """Decode-step latency of the Qwen2.5-1.5B-shaped sweep (28 layers x (add + RMSNorm, add + RMSNorm,
     SwiGLU) per token count), launched three ways: one C-ABI call per op, the same calls replayed from a CUDA
-    graph, and programs (mbd_run_program, at most 128 ops each: the 84 ops of one token count are one persistent
-    launch)."""
+    graph, programs (the 84 ops of one token count as one persistent launch, a plan built once and launched every
+    step), and that launch replayed from a CUDA graph."""
     import torch
     import memory_bound_decoder_gb300 as mbd
     from memory_bound_decoder_gb300 import build as mbd_build
@@ -487,9 +488,10 @@ def run_decode_table(args) -> Dict:
     lib = mbd.get_lib()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    table, modes = {}, ("calls", "graph", "program")
+    table, modes = {}, ("calls", "graph", "program", "program_graph")
     launches = {}
-    for work in wl.qwen_decode_sweep():
+    tokens = tuple(int(t) for t in args.decode_tokens.split(",")) if args.decode_tokens else (1, 2, 4, 8, 32, 64, 128, 256)
+    for work in wl.qwen_decode_sweep(tokens):
         T = work.calls[0].T
         dcalls = build_device_calls(torch, mbd, work, args.seed, 0, dev)
         stream = torch.cuda.Stream(device=dev)
@@ -497,36 +499,44 @@ def run_decode_table(args) -> Dict:
         for d in dcalls:
             d.bind(handle)
         ops = [d.op() for d in dcalls]
-        progs = [mbd.program_array(ops[i:i + mbd.MAX_PROGRAM_OPS]) for i in range(0, len(ops), mbd.MAX_PROGRAM_OPS)]
+        # built once per token count (a decode loop reuses the step's program), launched every step
+        t_b = time.perf_counter()
+        plans = [mbd.program_plan_build(ops[i:i + mbd.MAX_PROGRAM_OPS]) for i in range(0, len(ops), mbd.MAX_PROGRAM_OPS)]
+        build_us = (time.perf_counter() - t_b) * 1e6
 
         def run_calls():
             for d in dcalls:
                 d.launch()
 
+        plan_ptrs = [ctypes.addressof(p.buf) for p in plans]
+
         def run_program():
-            for arr, n in progs:
-                rc = lib.mbd_run_program(arr, n, handle)
+            for pp in plan_ptrs:
+                rc = lib.mbd_program_plan_launch(pp, handle)
                 if rc != 0:
                     raise RuntimeError(lib.mbd_status_string(rc).decode())
 
         with torch.cuda.stream(stream):
             run_calls()
         torch.cuda.synchronize(dev)
-        graph = torch.cuda.CUDAGraph()
-        graph_error = None
-        try:
-            with torch.cuda.graph(graph, stream=stream):
-                run_calls()
-            torch.cuda.synchronize(dev)
-        except RuntimeError as e:   # reported in the line instead of a graph time
-            graph_error = str(e).splitlines()[0]
-            torch.cuda.synchronize(dev)
-        fns = {"calls": run_calls, "graph": graph.replay, "program": run_program}
+        graphs, graph_errors = {}, {}
+        for name, body in (("graph", run_calls), ("program_graph", run_program)):
+            g = torch.cuda.CUDAGraph()
+            try:
+                with torch.cuda.graph(g, stream=stream):
+                    body()
+                torch.cuda.synchronize(dev)
+                graphs[name] = g
+            except RuntimeError as e:   # reported in the line instead of a graph time
+                graph_errors[name] = str(e).splitlines()[0]
+                torch.cuda.synchronize(dev)
+        fns = {"calls": run_calls, "program": run_program}
+        fns.update({k: g.replay for k, g in graphs.items()})
         row = {}
         for mode in modes:
-            if mode == "graph" and graph_error:
+            if mode in graph_errors:
                 row[mode] = None
-                row["graph_error"] = graph_error
+                row[mode + "_error"] = graph_errors[mode]
                 continue
             fn = fns[mode]
             with torch.cuda.stream(stream):
@@ -541,15 +551,16 @@ def run_decode_table(args) -> Dict:
                     fn()
                 e1.record(stream)
             torch.cuda.synchronize(dev)
-            launches[(T, mode)] = (mbd.kernel_launches() - n0) // args.steps
+            launches[(T, mode)] = (mbd.kernel_launches() - n0) // args.steps if "graph" not in mode else None
             ms = e0.elapsed_time(e1) / args.steps
             row[mode] = round(ms * 1e3 / work.layers, 3)
         row["program_GBps"] = round(work.algorithmic_bytes() / (row["program"] * work.layers / 1e6) / 1e9, 1)
         row["launches_per_step"] = {"calls": launches[(T, "calls")], "graph": len(dcalls),
-                                    "program": launches[(T, "program")]}
+                                    "program": launches[(T, "program")], "program_graph": len(plans)}
+        row["plan_build_us"] = round(build_us, 1)
         table[str(T)] = row
         log(f"[decode] T={T}: {row}")
-        del dcalls, progs, graph
+        del dcalls, plans, graphs
         torch.cuda.empty_cache()
     mean_prog = statistics.mean(r["program"] for r in table.values())
     return {"metric": "decode-step latency per layer, Qwen2.5-1.5B shapes (28 layers of 2 add+RMSNorm + 1 SwiGLU)",
@@ -716,6 +727,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=1.0, help="target wall time of the oracle sample")
     ap.add_argument("--decode-table", action="store_true",
                     help="time the Qwen decode sweep as per-op calls, a CUDA graph and programs (one JSON line)")
+    ap.add_argument("--decode-tokens", default="", help="token counts of --decode-table (default 1,2,4,8,32,64,128,256)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -84,7 +84,7 @@ typedef enum {
 #define MBD_MAX_REDUCED_WIDTH 262144
 
 /* ABI version of this header (bumped on any signature change or added entry point). */
-#define MBD_ABI_VERSION 3
+#define MBD_ABI_VERSION 4
 int mbd_abi_version(void);
 
 /* Static, human-readable name of a status code (never NULL). */
@@ -278,6 +278,28 @@ typedef struct {
  * entry points in their last bit; every result keeps the tolerances stated for those entry points.
  */
 mbd_status mbd_run_program(const mbd_op* ops, int n_ops, mbd_stream_t stream);
+
+/*
+ * The same in two steps, for a program that runs many times (every decode step): build validates and
+ * schedules once on the host; launch enqueues the kernel with no further host work beyond the launch
+ * itself. mbd_run_program is build + launch, and checking and scheduling ~100 ops costs tens of
+ * microseconds of host time per call.
+ *   mbd_program_plan : plain caller-owned memory (may be copied, stored or freed; holds no pointer into
+ *                      itself), filled by build. It records the device that was current at build time
+ *                      (launch shapes depend on its SM count) and the ops' device pointers: the tensors must
+ *                      stay where they are while the plan is launched.
+ *   build  : the checks and statuses of mbd_run_program; on failure the plan is left unusable. No kernel
+ *            is launched (device attributes are queried).
+ *   launch : MBD_ERR_INVALID_ARG for a plan that build did not fill, or on a device other than the one it
+ *            was built on; a plan with nothing to do launches nothing and returns MBD_OK.
+ */
+#define MBD_PROGRAM_PLAN_BYTES 16384
+typedef struct {
+    uint64_t opaque[MBD_PROGRAM_PLAN_BYTES / 8];
+} mbd_program_plan;
+
+mbd_status mbd_program_plan_build(const mbd_op* ops, int n_ops, mbd_program_plan* plan);
+mbd_status mbd_program_plan_launch(const mbd_program_plan* plan, mbd_stream_t stream);
 
 #ifdef __cplusplus
 }

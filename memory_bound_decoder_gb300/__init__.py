@@ -48,6 +48,7 @@ OP_SWIGLU = 3
 OP_SWIGLU_QUANT_FP8 = 4
 OP_SWIGLU_QUANT_NVFP4 = 5
 MAX_PROGRAM_OPS = 128
+PROGRAM_PLAN_BYTES = 16384
 
 
 def _load() -> ctypes.CDLL:
@@ -74,9 +75,12 @@ def _load() -> ctypes.CDLL:
     lib.mbd_fused_add_rmsnorm_quant_nvfp4.argtypes = [vp, vp, vp, vp, vp, i64, i64, f32, vp, vp]
     lib.mbd_swiglu_quant_nvfp4.argtypes = [vp, vp, vp, i64, i64, vp, vp]
     lib.mbd_run_program.argtypes = [ctypes.POINTER(Op), cint, vp]
+    lib.mbd_program_plan_build.argtypes = [ctypes.POINTER(Op), cint, vp]
+    lib.mbd_program_plan_launch.argtypes = [vp, vp]
     for fn in ("mbd_fused_add_rmsnorm", "mbd_fused_add_rmsnorm_quant_fp8", "mbd_swiglu", "mbd_swiglu_quant_fp8",
                "mbd_fused_allreduce_add_rmsnorm", "mbd_fused_allreduce_add_rmsnorm_quant_fp8",
-               "mbd_fused_add_rmsnorm_quant_nvfp4", "mbd_swiglu_quant_nvfp4", "mbd_run_program"):
+               "mbd_fused_add_rmsnorm_quant_nvfp4", "mbd_swiglu_quant_nvfp4", "mbd_run_program",
+               "mbd_program_plan_build", "mbd_program_plan_launch"):
         getattr(lib, fn).restype = cint
     return lib
 
@@ -270,3 +274,25 @@ def run_program(ops, stream=None) -> None:
     """Run a list of Op (or a program_array result) as one persistent kernel launch."""
     arr, n = ops if isinstance(ops, tuple) else program_array(ops)
     _check(get_lib().mbd_run_program(arr if n else None, n, _stream(stream)), "run_program")
+
+
+class ProgramPlan:
+    """A built program (the C mbd_program_plan): plain host memory, launched any number of times. Keeps the
+    descriptor array alive with it (the plan itself holds only the ops' device pointers)."""
+
+    def __init__(self, ops):
+        self.buf = (ctypes.c_uint64 * (PROGRAM_PLAN_BYTES // 8))()
+        self.arr, n = program_array(ops)
+        _check(get_lib().mbd_program_plan_build(self.arr if n else None, n, ctypes.addressof(self.buf)),
+               "program_plan_build")
+
+    def launch(self, stream=None) -> None:
+        _check(get_lib().mbd_program_plan_launch(ctypes.addressof(self.buf), _stream(stream)), "program_plan_launch")
+
+
+def program_plan_build(ops) -> ProgramPlan:
+    return ProgramPlan(ops)
+
+
+def program_plan_launch(plan: ProgramPlan, stream=None) -> None:
+    plan.launch(stream)

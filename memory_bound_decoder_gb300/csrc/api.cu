@@ -1,5 +1,6 @@
 // C ABI of the fusion library: host-side argument checks, launch-shape selection and dispatch.
 // Every check runs before anything is enqueued; a failing call launches nothing.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstddef>
@@ -281,24 +282,10 @@ void add_region(OpInfo& o, const void* ptr, size_t bytes, bool write, size_t row
     if (ptr && bytes) o.reg[o.nreg++] = Region{ptr, bytes, write, row_bytes, rows};
 }
 
+// Union-find over op indices; unions keep the smaller index as the root, so a chain's root is its first op.
 int find_root(int* parent, int i) {
     while (parent[i] != i) i = parent[i] = parent[parent[i]];
     return i;
-}
-
-// The ops' regions conflict (overlap, one of them written); ok == false if they do so other than as the
-// same row-wise tensor.
-bool conflicts(const OpInfo& a, const OpInfo& b, bool* ok) {
-    bool any = false;
-    *ok = true;
-    for (int i = 0; i < a.nreg; ++i)
-        for (int j = 0; j < b.nreg; ++j) {
-            const Region &x = a.reg[i], &y = b.reg[j];
-            if (!(x.write || y.write) || !overlap(x.ptr, x.bytes, y.ptr, y.bytes)) continue;
-            any = true;
-            if (!(x.row_bytes > 0 && x.ptr == y.ptr && x.row_bytes == y.row_bytes && x.rows == y.rows)) *ok = false;
-        }
-    return any;
 }
 
 // Resident program CTAs per SM, queried once per device, vectors per thread and variant.
@@ -318,9 +305,25 @@ int program_ctas_per_sm_cached(int vpt, int variant) {
     return n;
 }
 
-mbd_status run_program(const mbd_op* ops, int n_ops, cudaStream_t stream) {
+// A built program: the kernel's parameters and its launch shape, for the device it was built on.
+struct PlanImpl {
+    uint32_t magic;
+    int device;
+    int vpt, variant, grid, pad;
+    mbd::ProgramParams P;
+};
+constexpr uint32_t kPlanMagic = 0x4d424450u;
+static_assert(sizeof(PlanImpl) <= sizeof(mbd_program_plan), "program plan size");
+static_assert(alignof(PlanImpl) <= alignof(mbd_program_plan), "program plan alignment");
+
+mbd_status build_program(const mbd_op* ops, int n_ops, PlanImpl* plan) {
+    if (!plan) return MBD_ERR_INVALID_ARG;
+    plan->magic = 0;
     if (n_ops < 0 || n_ops > MBD_MAX_PROGRAM_OPS || (n_ops > 0 && !ops)) return MBD_ERR_INVALID_ARG;
-    mbd::ProgramParams P{};
+    int device = -1;   // queried once there is something to launch (every check before it is host-only)
+    mbd::ProgramParams& P = plan->P;
+    P = mbd::ProgramParams{};
+    P.n_ops = n_ops;
     OpInfo info[MBD_MAX_PROGRAM_OPS];
     bool active[MBD_MAX_PROGRAM_OPS] = {};
     int norm_mask = 0, swiglu_mask = 0, max_held_nvec = 0;
@@ -368,17 +371,42 @@ mbd_status run_program(const mbd_op* ops, int n_ops, cudaStream_t stream) {
         if (in.holds_row && po.nvec > max_held_nvec) max_held_nvec = po.nvec;
         active[i] = true;
     }
-    // ops linked by a shared, written buffer form chains (union-find)
+    // ops linked by a shared, written buffer form chains (union-find over the overlapping pairs of regions,
+    // found by sorting all regions by start address and sweeping)
     int parent[MBD_MAX_PROGRAM_OPS];
     for (int i = 0; i < n_ops; ++i) parent[i] = i;
+    struct RegRef {
+        uintptr_t lo, hi;
+        int op, reg;
+    };
+    RegRef refs[MBD_MAX_PROGRAM_OPS * 6];
+    int nref = 0;
     for (int i = 0; i < n_ops; ++i)
-        for (int j = i + 1; j < n_ops; ++j) {
-            if (!active[i] || !active[j]) continue;
-            bool ok;
-            if (!conflicts(info[i], info[j], &ok)) continue;
-            if (!ok) return MBD_ERR_UNSUPPORTED;
-            parent[find_root(parent, j)] = find_root(parent, i);
+        for (int q = 0; active[i] && q < info[i].nreg; ++q) {
+            const uintptr_t lo = reinterpret_cast<uintptr_t>(info[i].reg[q].ptr);
+            refs[nref++] = RegRef{lo, lo + info[i].reg[q].bytes, i, q};
         }
+    std::sort(refs, refs + nref, [](const RegRef& a, const RegRef& b) { return a.lo < b.lo; });
+    int open_refs[MBD_MAX_PROGRAM_OPS * 6];
+    int nopen = 0;
+    for (int r = 0; r < nref; ++r) {
+        int keep = 0;   // drop the regions that end before this one starts
+        for (int k = 0; k < nopen; ++k)
+            if (refs[open_refs[k]].hi > refs[r].lo) open_refs[keep++] = open_refs[k];
+        nopen = keep;
+        const Region& y = info[refs[r].op].reg[refs[r].reg];
+        for (int k = 0; k < nopen; ++k) {
+            const RegRef& a = refs[open_refs[k]];
+            if (a.op == refs[r].op) continue;   // within one op: checked by its entry point's rules
+            const Region& x = info[a.op].reg[a.reg];
+            if (!(x.write || y.write)) continue;
+            if (!(x.row_bytes > 0 && x.ptr == y.ptr && x.row_bytes == y.row_bytes && x.rows == y.rows))
+                return MBD_ERR_UNSUPPORTED;
+            const int ra = find_root(parent, a.op), rb = find_root(parent, refs[r].op);
+            parent[ra > rb ? ra : rb] = ra < rb ? ra : rb;   // the root stays the chain's first op
+        }
+        open_refs[nopen++] = r;
+    }
     int size[MBD_MAX_PROGRAM_OPS] = {};
     for (int i = 0; i < n_ops; ++i)
         if (active[i]) ++size[find_root(parent, i)];
@@ -411,6 +439,12 @@ mbd_status run_program(const mbd_op* ops, int n_ops, cudaStream_t stream) {
                             res_written |= overlap(w.ptr, w.bytes, po.residual, static_cast<size_t>(po.rows) * po.nvec * 16);
                     }
                 po.prefetch = (in_written ? 0 : 1) | ((po.residual && !res_written) ? 2 : 0);
+                if (order_len > P.group_begin[P.n_groups]) {   // continues a run of norms on one residual row
+                    const mbd::ProgOp& prev = P.ops[P.chain_order[order_len - 1]];
+                    if (po.cls == mbd::kOpNorm && prev.cls == mbd::kOpNorm && po.residual == prev.residual &&
+                        po.nvec == prev.nvec && po.rows == prev.rows && !in_written)
+                        po.prefetch |= mbd::kContinuesRun;
+                }
                 warm_row_bytes += (in_written ? 0 : int64_t{po.nvec} * (po.cls == mbd::kOpNorm ? 16 : 32)) +
                                   ((po.residual && !res_written) ? int64_t{po.nvec} * 16 : 0);
                 P.chain_order[order_len++] = i;
@@ -430,17 +464,41 @@ mbd_status run_program(const mbd_op* ops, int n_ops, cudaStream_t stream) {
     P.group_items[P.n_groups] = P.n_chain_items;
     P.free_items[P.n_free] = P.n_free_items;
     const int64_t items = P.n_chain_items + P.n_free_items;
-    if (items == 0) return MBD_OK;
-    const int per_sm = program_ctas_per_sm_cached(vpt, variant);
-    if (per_sm <= 0) {
-        g_last_cuda_error = static_cast<int>(cudaErrorInvalidConfiguration);
+    int grid = 0;
+    if (items > 0) {
+        if (cudaGetDevice(&device) != cudaSuccess) {
+            g_last_cuda_error = static_cast<int>(cudaGetLastError());
+            return MBD_ERR_CUDA;
+        }
+        const int per_sm = program_ctas_per_sm_cached(vpt, variant);
+        if (per_sm <= 0) {
+            g_last_cuda_error = static_cast<int>(cudaErrorInvalidConfiguration);
+            return MBD_ERR_CUDA;
+        }
+        const int64_t slots = int64_t{sm_count_of_current_device()} * per_sm;
+        grid = static_cast<int>(items < slots ? items : slots);
+        // warm the chains' row inputs only while the rows in flight fit well inside L2 (a quarter of 126 MiB)
+        P.prefetch_chains = warm_row_bytes * (P.n_chain_items < grid ? P.n_chain_items : grid) <= (int64_t{32} << 20);
+    }
+    plan->device = device;
+    plan->vpt = vpt;
+    plan->variant = variant;
+    plan->grid = grid;
+    plan->pad = 0;
+    plan->magic = kPlanMagic;
+    return MBD_OK;
+}
+
+mbd_status launch_plan(const PlanImpl* plan, cudaStream_t stream) {
+    if (!plan || plan->magic != kPlanMagic) return MBD_ERR_INVALID_ARG;
+    if (plan->grid == 0) return MBD_OK;   // nothing to do
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) {
+        g_last_cuda_error = static_cast<int>(cudaGetLastError());
         return MBD_ERR_CUDA;
     }
-    const int64_t slots = int64_t{sm_count_of_current_device()} * per_sm;
-    const int grid = static_cast<int>(items < slots ? items : slots);
-    // warm the chains' row inputs only while the rows in flight fit well inside L2 (a quarter of 126 MiB)
-    P.prefetch_chains = warm_row_bytes * (P.n_chain_items < grid ? P.n_chain_items : grid) <= (int64_t{32} << 20);
-    return finish_launch(mbd::launch_program(P, vpt, variant, grid, stream));
+    if (device != plan->device) return MBD_ERR_INVALID_ARG;
+    return finish_launch(mbd::launch_program(plan->P, plan->vpt, plan->variant, plan->grid, stream));
 }
 
 }  // namespace
@@ -547,8 +605,19 @@ mbd_status mbd_swiglu_quant_nvfp4(uint8_t* out_q, uint8_t* out_sf, const void* g
                          reinterpret_cast<cudaStream_t>(stream));
 }
 
+mbd_status mbd_program_plan_build(const mbd_op* ops, int n_ops, mbd_program_plan* plan) {
+    return build_program(ops, n_ops, reinterpret_cast<PlanImpl*>(plan));
+}
+
+mbd_status mbd_program_plan_launch(const mbd_program_plan* plan, mbd_stream_t stream) {
+    return launch_plan(reinterpret_cast<const PlanImpl*>(plan), reinterpret_cast<cudaStream_t>(stream));
+}
+
 mbd_status mbd_run_program(const mbd_op* ops, int n_ops, mbd_stream_t stream) {
-    return run_program(ops, n_ops, reinterpret_cast<cudaStream_t>(stream));
+    thread_local PlanImpl plan;   // about 14 KB: kept off the stack, reused by each call of this thread
+    const mbd_status st = build_program(ops, n_ops, &plan);
+    if (st != MBD_OK) return st;
+    return launch_plan(&plan, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

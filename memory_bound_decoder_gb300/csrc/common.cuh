@@ -269,6 +269,22 @@ __device__ __forceinline__ bool row_reduce(P mine, P* warp_part, Exchange& ex, i
     return *ok_flag != 0;
 }
 
+// Total over a row held by ONE CTA, returned to every thread: the warps reduce their lanes, then every
+// thread combines the warp partials in warp order (the same order everywhere, so all threads get identical
+// bits). One CTA barrier. warp_part must not be written again before the CTA has passed another barrier
+// (the callers' next barrier, or the end of the CTA).
+template <class P>
+__device__ __forceinline__ P block_total(P mine, P* warp_part) {
+    mine = warp_allreduce_p(mine);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) warp_part[warp] = mine;
+    __syncthreads();
+    const int nwarps = (blockDim.x + 31) >> 5;
+    P t = warp_part[0];
+    for (int w = 1; w < nwarps; ++w) t = P::combine(t, warp_part[w]);
+    return t;
+}
+
 // ------------------------------------------------------------------------------------------ PDL
 
 // Programmatic dependent launch: pdl_trigger lets the next kernel in the stream be scheduled as soon as

@@ -72,13 +72,17 @@ struct ProgOp {
     int nvec;            // width / 8
     int hidden;          // width
     float eps;
-    int prefetch;        // chain ops: bit 0 warm `in`, bit 1 warm `residual` (row inputs no earlier op writes)
+    int prefetch;        // chain ops: bit 0 warm `in`, bit 1 warm `residual` (row inputs no earlier op writes),
+                         // kContinuesRun: a norm on the previous op's residual row whose x no earlier op writes
 };
+
+constexpr int kContinuesRun = 4;
 
 // The whole schedule, passed by value as the kernel's parameters (about 14 KB).
 // Chain items: (group g, row t) for t < rows of g; the CTA runs every op of g on row t in list order.
 // Free items: (free op f, row t, chunk k); ops that hold their row have one chunk per row.
 struct ProgramParams {
+    int n_ops;                                  // ops[0 .. n_ops) are filled (the kernel copies only those)
     int n_groups;
     int n_free;
     int chunk_vecs;                             // vectors of one stream chunk (kProgramThreads * vpt)

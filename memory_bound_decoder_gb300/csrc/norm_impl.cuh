@@ -81,6 +81,66 @@ __device__ __forceinline__ void norm_prefetch(const NormParams& p, int64_t row, 
     }
 }
 
+// Step 3 of the norm for the bf16, static-FP8 and NVFP4 epilogues: v = (w * s) * inv (w * s of two bf16
+// values is exact in fp32) and its store, for this thread's vectors of one row slice starting at `begin`.
+template <int VPT, int EP>
+__device__ __forceinline__ void norm_store(const NormParams& p, int64_t row, int begin, const uint4 (&sv)[VPT],
+                                           const uint4 (&wv)[VPT], const bool (&live)[VPT], float inv) {
+    if constexpr (EP == kBf16) {
+        uint4* outr = static_cast<uint4*>(p.out) + row * p.nvec;
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            if (!live[i]) continue;
+            const uint32_t* sw = reinterpret_cast<const uint32_t*>(&sv[i]);
+            const uint32_t* ww = reinterpret_cast<const uint32_t*>(&wv[i]);
+            uint4 o;
+            uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                ow[k] = pack_bf16x2(__fmul2_rn(__fmul2_rn(bf16x2_to_float2(sw[k]), bf16x2_to_float2(ww[k])), f2(inv)));
+            store_stream(outr + (begin + threadIdx.x + i * blockDim.x), o);
+        }
+    } else if constexpr (EP == kNvfp4) {
+        // NVFP4: block scales over 16 elements (this vector and the neighbouring lane's), E2M1 codes of
+        // v = (w * s) * inv scaled by the block's decoded scale times the tensor scale.
+        const Nvfp4Row nr = nvfp4_row(inv, nvfp4_tensor_scale(p.scale));
+        unsigned int* qr = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(p.out) + row * (int64_t)p.nvec * 4);
+        uint8_t* sfr = p.out_sf + row * (int64_t)(p.nvec / 2);
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            float2 y[4];
+            const uint32_t* sw = reinterpret_cast<const uint32_t*>(&sv[i]);
+            const uint32_t* ww = reinterpret_cast<const uint32_t*>(&wv[i]);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                y[k] = live[i] ? __fmul2_rn(bf16x2_to_float2(sw[k]), bf16x2_to_float2(ww[k])) : f2(0.0f);
+            uint32_t sf;
+            const uint32_t q = nvfp4_encode(y, nr, &sf);   // whole warp (block max by shuffle)
+            if (!live[i]) continue;
+            const int c = begin + threadIdx.x + i * blockDim.x;
+            store_stream(qr + c, q);
+            if ((threadIdx.x & 1) == 0) sfr[c >> 1] = static_cast<uint8_t>(sf);
+        }
+    } else {
+        // static per-tensor scale: codes of v / scale
+        const float sc = __ldg(p.scale);
+        const float c = sc > 0.0f ? inv * (1.0f / sc) : 0.0f;
+        uint2* outr = reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + row * (int64_t)p.nvec * 8);
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            if (!live[i]) continue;
+            const uint32_t* sw = reinterpret_cast<const uint32_t*>(&sv[i]);
+            const uint32_t* ww = reinterpret_cast<const uint32_t*>(&wv[i]);
+            float2 y[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                y[k] = __fmul2_rn(__fmul2_rn(bf16x2_to_float2(sw[k]), bf16x2_to_float2(ww[k])), f2(c));
+            store_stream(outr + (begin + threadIdx.x + i * blockDim.x),
+                         make_uint2(pack_e4m3x4(y[0], y[1]), pack_e4m3x4(y[2], y[3])));
+        }
+    }
+}
+
 // One CTA's share of one row: vectors [begin, end) of `row` (at most VPT per thread), the CTA being `rank`
 // of the `nctas` CTAs of the row (one thread-block cluster when nctas > 1). Every thread of the CTA calls
 // it. On a cluster-exchange timeout the CTA returns without writing its outputs.
@@ -145,11 +205,17 @@ __device__ __forceinline__ void norm_row_slice(const NormParams& p, int64_t row,
                 ss2 = __ffma2_rn(s2, s2, ss2);
             }
         }
-        if (!row_reduce(PSum{ss2.x + ss2.y}, part_sum, ex, rank, ctas_per_row, &sm.ok_flag, [&](PSum t) {
-                row_const[0] = 1.0f / sqrtf(t.v / static_cast<float>(p.hidden) + p.eps);
-            }))
-            return;
-        const float inv = row_const[0];
+        float inv;
+        if (ctas_per_row == 1) {   // the whole row in this CTA: one barrier, every thread forms inv
+            const PSum t = block_total(PSum{ss2.x + ss2.y}, part_sum);
+            inv = 1.0f / sqrtf(t.v / static_cast<float>(p.hidden) + p.eps);
+        } else {
+            if (!row_reduce(PSum{ss2.x + ss2.y}, part_sum, ex, rank, ctas_per_row, &sm.ok_flag, [&](PSum t) {
+                    row_const[0] = 1.0f / sqrtf(t.v / static_cast<float>(p.hidden) + p.eps);
+                }))
+                return;
+            inv = row_const[0];
+        }
 
         if constexpr (!kEarlyWeight) {
 #pragma unroll
@@ -157,60 +223,7 @@ __device__ __forceinline__ void norm_row_slice(const NormParams& p, int64_t row,
                 if (live[i]) wv[i] = load_cached(wr + (begin + threadIdx.x + i * blockDim.x));
         }
 
-        // 3. v = (w * s) * inv; w * s of two bf16 values is exact in fp32
-        if constexpr (EP == kBf16) {
-            uint4* outr = static_cast<uint4*>(p.out) + row * p.nvec;
-#pragma unroll
-            for (int i = 0; i < VPT; ++i) {
-                if (!live[i]) continue;
-                const uint32_t* sw = reinterpret_cast<const uint32_t*>(&sv[i]);
-                const uint32_t* ww = reinterpret_cast<const uint32_t*>(&wv[i]);
-                uint4 o;
-                uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    ow[k] = pack_bf16x2(__fmul2_rn(__fmul2_rn(bf16x2_to_float2(sw[k]), bf16x2_to_float2(ww[k])), f2(inv)));
-                store_stream(outr + (begin + threadIdx.x + i * blockDim.x), o);
-            }
-        } else if constexpr (EP == kNvfp4) {
-            // NVFP4: block scales over 16 elements (this vector and the neighbouring lane's), E2M1 codes of
-            // v = (w * s) * inv scaled by the block's decoded scale times the tensor scale.
-            const Nvfp4Row nr = nvfp4_row(inv, nvfp4_tensor_scale(p.scale));
-            unsigned int* qr = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(p.out) + row * (int64_t)p.nvec * 4);
-            uint8_t* sfr = p.out_sf + row * (int64_t)(p.nvec / 2);
-#pragma unroll
-            for (int i = 0; i < VPT; ++i) {
-                float2 y[4];
-                const uint32_t* sw = reinterpret_cast<const uint32_t*>(&sv[i]);
-                const uint32_t* ww = reinterpret_cast<const uint32_t*>(&wv[i]);
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    y[k] = live[i] ? __fmul2_rn(bf16x2_to_float2(sw[k]), bf16x2_to_float2(ww[k])) : f2(0.0f);
-                uint32_t sf;
-                const uint32_t q = nvfp4_encode(y, nr, &sf);   // whole warp (block max by shuffle)
-                if (!live[i]) continue;
-                const int c = begin + threadIdx.x + i * blockDim.x;
-                store_stream(qr + c, q);
-                if ((threadIdx.x & 1) == 0) sfr[c >> 1] = static_cast<uint8_t>(sf);
-            }
-        } else {
-            // static per-tensor scale: codes of v / scale
-            const float sc = __ldg(p.scale);
-            const float c = sc > 0.0f ? inv * (1.0f / sc) : 0.0f;
-            uint2* outr = reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + row * (int64_t)p.nvec * 8);
-#pragma unroll
-            for (int i = 0; i < VPT; ++i) {
-                if (!live[i]) continue;
-                const uint32_t* sw = reinterpret_cast<const uint32_t*>(&sv[i]);
-                const uint32_t* ww = reinterpret_cast<const uint32_t*>(&wv[i]);
-                float2 y[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    y[k] = __fmul2_rn(__fmul2_rn(bf16x2_to_float2(sw[k]), bf16x2_to_float2(ww[k])), f2(c));
-                store_stream(outr + (begin + threadIdx.x + i * blockDim.x),
-                             make_uint2(pack_e4m3x4(y[0], y[1]), pack_e4m3x4(y[2], y[3])));
-            }
-        }
+        norm_store<VPT, EP>(p, row, begin, sv, wv, live, inv);
     } else {
         // Dynamic per-token scale. The codes are ratios of exact bf16 products, 448 * (w_j s_j) / (w_k s_k),
         // rescaled by the fp32 rounding of the scale, so exact E4M3 ties are common; resolving them as the

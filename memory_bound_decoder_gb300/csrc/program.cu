@@ -90,22 +90,116 @@ __device__ __forceinline__ void warm_row(const void* base, int64_t row, int nvec
     for (int c = threadIdx.x; c < nvec; c += blockDim.x) prefetch_l2(r + c);
 }
 
+// The one epilogue a mask holds, or -1.
+constexpr int single_ep(int mask) {
+    return mask == bit(kBf16) ? kBf16
+         : mask == bit(kFp8Static) ? kFp8Static
+         : mask == bit(kFp8Dynamic) ? kFp8Dynamic
+         : mask == bit(kNvfp4) ? kNvfp4 : -1;
+}
+
+// A run of consecutive norms of one chain on the same residual row (the layers of a decode step), ops
+// ops[0 .. n), whole rows of one vector per thread. The residual row stays in registers across the run and
+// is stored once at its end: the values in between would be overwritten by the next norm of the run, and
+// no op outside the chain reads that buffer. The next op's x and weight vectors (which no earlier op of the
+// chain writes) are loaded before this op's reduction, so their L2 latency overlaps the reduction and the
+// epilogue instead of adding to them.
+template <int EP>
+__device__ void norm_run(const ProgOp* ops, int n, int64_t row, ProgSmem& sm) {
+    const int nvec = ops[0].nvec;
+    const int c = threadIdx.x;
+    const bool live[1] = {c < nvec};
+    uint4* rr = static_cast<uint4*>(ops[0].residual) + row * nvec + c;
+    uint4 sv[1], xv, wv[1];
+    if (live[0]) {
+        sv[0] = load_cached(rr);
+        xv = load_stream(static_cast<const uint4*>(ops[0].in) + row * nvec + c);
+        wv[0] = load_cached(static_cast<const uint4*>(ops[0].weight) + c);
+    }
+    for (int k = 0; k < n; ++k) {
+        const ProgOp& op = ops[k];
+        float2 ss2 = f2(0.0f);
+        if (live[0]) {
+            const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv);
+            uint32_t* sw = reinterpret_cast<uint32_t*>(&sv[0]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                sw[q] = pack_bf16x2(__fadd2_rn(bf16x2_to_float2(xw[q]), bf16x2_to_float2(sw[q])));
+                const float2 s2 = bf16x2_to_float2(sw[q]);
+                ss2 = __ffma2_rn(s2, s2, ss2);
+            }
+        }
+        uint4 wn;
+        if (k + 1 < n && live[0]) {   // the next op's inputs (x into the spent x registers)
+            xv = load_stream(static_cast<const uint4*>(ops[k + 1].in) + row * nvec + c);
+            wn = load_cached(static_cast<const uint4*>(ops[k + 1].weight) + c);
+        }
+        const PSum t = block_total(PSum{ss2.x + ss2.y}, sm.norm.part_sum);
+        const float inv = 1.0f / sqrtf(t.v / static_cast<float>(op.hidden) + op.eps);
+        NormParams np;
+        np.x = op.in;
+        np.n_partials = 0;
+        np.residual = op.residual;
+        np.weight = op.weight;
+        np.out = op.out;
+        np.out_sf = op.out_sf;
+        np.scale = op.scale;
+        np.rows = op.rows;
+        np.nvec = op.nvec;
+        np.hidden = op.hidden;
+        np.eps = op.eps;
+        norm_store<1, EP>(np, row, 0, sv, wv, live, inv);
+        if (k + 1 < n) wv[0] = wn;
+        __syncthreads();   // the warp partials are read by every thread before the next op writes them
+    }
+    if (live[0]) store_stream(rr, sv[0]);
+}
+
+// A chain CTA's copy of its chain's op descriptors: read in place, every descriptor would be a dynamically
+// indexed constant-bank load on the chain's critical path, once per op.
+struct ChainSmem {
+    ProgOp ops[kMaxProgramOps];
+};
+
 template <int V, int NM, int SM>
-__device__ void run_chain_item(const ProgramParams& P, int64_t item, ProgSmem& sm) {
-    int g = 0;
-    while (g + 1 < P.n_groups && P.group_items[g + 1] <= item) ++g;
+// `g` is the chain of this item's CTA cursor and `held` the chain whose descriptors cs.ops holds (-1: none);
+// both live in registers and every thread of the CTA updates them identically.
+__device__ void run_chain_item(const ProgramParams& P, int64_t item, int& g, int& held, ProgSmem& sm, ChainSmem& cs) {
+    while (g + 1 < P.n_groups && P.group_items[g + 1] <= item) ++g;   // items of a CTA only increase
     const int64_t row = item - P.group_items[g];
-    const int k0 = P.group_begin[g], k1 = P.group_begin[g + 1];
+    const int k0 = P.group_begin[g], n = P.group_begin[g + 1] - k0;
+    if (held != g) {
+        __syncthreads();   // every thread is done with the previous chain's descriptors
+        constexpr int kWords = sizeof(ProgOp) / 4;
+        for (int w = threadIdx.x; w < n * kWords; w += blockDim.x) {
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(&P.ops[P.chain_order[k0 + w / kWords]]);
+            reinterpret_cast<uint32_t*>(cs.ops)[w] = src[w % kWords];
+        }
+        __syncthreads();
+        held = g;
+    }
     if (P.prefetch_chains) {
-        for (int k = k0; k < k1; ++k) {
-            const ProgOp& op = P.ops[P.chain_order[k]];
+        for (int k = 0; k < n; ++k) {
+            const ProgOp& op = cs.ops[k];
             const int in_vecs = op.cls == kOpNorm ? op.nvec : 2 * op.nvec;
             if (op.prefetch & 1) warm_row(op.in, row, in_vecs);
             if (op.prefetch & 2) warm_row(op.residual, row, op.nvec);
         }
     }
-    for (int k = k0; k < k1; ++k) {
-        const ProgOp& op = P.ops[P.chain_order[k]];
+    for (int k = 0; k < n; ++k) {
+        const ProgOp& op = cs.ops[k];
+        if constexpr (V == 1 && single_ep(NM) >= 0 && single_ep(NM) != kFp8Dynamic) {
+            if (op.cls == kOpNorm) {
+                int e = k + 1;
+                while (e < n && (cs.ops[e].prefetch & kContinuesRun)) ++e;
+                if (e - k > 1) {   // ops k .. e - 1 run with the residual row in registers
+                    norm_run<single_ep(NM)>(cs.ops + k, e - k, row, sm);
+                    k = e - 1;
+                    __syncthreads();
+                    continue;
+                }
+            }
+        }
         if (op.cls == kOpNorm) {
             run_norm_row<V, NM>(op, row, sm);
         } else if (op.ep == kFp8Dynamic) {
@@ -118,9 +212,8 @@ __device__ void run_chain_item(const ProgramParams& P, int64_t item, ProgSmem& s
 }
 
 template <int V, int NM, int SM>
-__device__ void run_free_item(const ProgramParams& P, int64_t item, ProgSmem& sm) {
-    int f = 0;
-    while (f + 1 < P.n_free && P.free_items[f + 1] <= item) ++f;
+__device__ void run_free_item(const ProgramParams& P, int64_t item, int& f, ProgSmem& sm) {
+    while (f + 1 < P.n_free && P.free_items[f + 1] <= item) ++f;   // items of a CTA only increase
     const ProgOp& op = P.ops[P.free_op[f]];
     const int64_t local = item - P.free_items[f];
     const int chunks = P.free_chunks[f];
@@ -135,35 +228,38 @@ __device__ void run_free_item(const ProgramParams& P, int64_t item, ProgSmem& sm
         const int e = chunks == 1 ? op.nvec : min(b + P.chunk_vecs, op.nvec);
         run_swiglu_part<V, SM>(op, row, b, e, sm);
     }
+    __syncthreads();   // the next item's reduction may reuse the warp partials
+}
+
+// Resident CTAs per SM each variant is compiled for (the register cap): the most that leaves it without
+// spills, from ptxas -v (40 to 128 registers; the FP8 variant at 4 vectors per thread keeps a small spill
+// at the 128-register limit).
+constexpr int min_ctas(int v, int nm, int sm) {
+    return sm == bit(kFp8Dynamic) ? (v == 1 ? 4 : 2)   // the dynamic SwiGLU's two-pass form adds registers
+                                  : (v == 1 ? ((nm == bit(kBf16) && sm == bit(kBf16)) ? 6 : 5) : (v == 2 ? 3 : 2));
 }
 
 // Chain items take CTAs 0 .. n_chain - 1 and free items the CTAs after them, so a chain (the critical path
 // of a decode step) shares its CTA with nothing; when there are more chain items than CTAs both kinds are
 // dealt round-robin over the whole grid.
-// Resident CTAs per SM each variant is compiled for (the register cap): the most that leaves it without
-// spills, from ptxas -v (bf16 at 1 vector per thread fits 32 registers; the others need 40 to 128; the FP8
-// variant at 4 vectors per thread keeps a small spill at the 128-register limit).
-constexpr int min_ctas(int v, int nm, int sm) {
-    return sm == bit(kFp8Dynamic) ? (v == 1 ? 4 : 2)   // the dynamic SwiGLU's two-pass form adds registers
-                                  : (v == 1 ? ((nm == bit(kBf16) && sm == bit(kBf16)) ? 8 : 6) : (v == 2 ? 3 : 2));
-}
-
 template <int V, int NM, int SM>
 __global__ void __launch_bounds__(kProgramThreads, min_ctas(V, NM, SM)) program_kernel(const __grid_constant__ ProgramParams P) {
     __shared__ ProgSmem sm;
+    __shared__ ChainSmem cs;
     pdl_trigger();
     pdl_wait();
     const int64_t G = gridDim.x, b = blockIdx.x;
     const int64_t nc = P.n_chain_items, nf = P.n_free_items;
+    int g = 0, held = -1, f = 0;
     if (nc < G) {
         if (b < nc) {
-            run_chain_item<V, NM, SM>(P, b, sm);
+            run_chain_item<V, NM, SM>(P, b, g, held, sm, cs);
         } else {
-            for (int64_t j = b - nc; j < nf; j += G - nc) run_free_item<V, NM, SM>(P, j, sm);
+            for (int64_t j = b - nc; j < nf; j += G - nc) run_free_item<V, NM, SM>(P, j, f, sm);
         }
     } else {
-        for (int64_t i = b; i < nc; i += G) run_chain_item<V, NM, SM>(P, i, sm);
-        for (int64_t j = b; j < nf; j += G) run_free_item<V, NM, SM>(P, j, sm);
+        for (int64_t i = b; i < nc; i += G) run_chain_item<V, NM, SM>(P, i, g, held, sm, cs);
+        for (int64_t j = b; j < nf; j += G) run_free_item<V, NM, SM>(P, j, f, sm);
     }
 }
 

@@ -140,13 +140,19 @@ __device__ __forceinline__ void swiglu_row_slice(const SwigluParams p, int64_t r
             }
         }
         if constexpr (EP == kFp8Dynamic) {
-            if (!row_reduce(PMax{amax}, part_max, ex, rank, ctas_per_row, &sm.ok_flag, [&](PMax t) {
-                    const float sc = t.v / 448.0f;
-                    sm.row_qmul = sc > 0.0f ? 1.0f / sc : 0.0f;
-                    if (rank == 0) p.scale[row] = sc;
-                }))
-                return;
-            qmul = sm.row_qmul;
+            if (ctas_per_row == 1) {   // the whole row in this CTA: one barrier, every thread forms the scale
+                const float sc = block_total(PMax{amax}, part_max).v / 448.0f;
+                qmul = sc > 0.0f ? 1.0f / sc : 0.0f;
+                if (threadIdx.x == 0) p.scale[row] = sc;
+            } else {
+                if (!row_reduce(PMax{amax}, part_max, ex, rank, ctas_per_row, &sm.ok_flag, [&](PMax t) {
+                        const float sc = t.v / 448.0f;
+                        sm.row_qmul = sc > 0.0f ? 1.0f / sc : 0.0f;
+                        if (rank == 0) p.scale[row] = sc;
+                    }))
+                    return;
+                qmul = sm.row_qmul;
+            }
         }
         // formed after the reduction: nothing but the products stays live across the exchange
         uint2* outr = reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + row * (int64_t)p.nvec * 8);
@@ -195,13 +201,9 @@ __device__ __forceinline__ void swiglu_dynamic_two_pass(const SwigluParams p, in
             }
         }
     }
-    if (!row_reduce(PMax{amax}, sm.part_max, sm.ex, 0, 1, &sm.ok_flag, [&](PMax t) {
-            const float sc = t.v / 448.0f;
-            sm.row_qmul = sc > 0.0f ? 1.0f / sc : 0.0f;
-            p.scale[row] = sc;
-        }))
-        return;
-    const float2 q2 = f2(sm.row_qmul);
+    const float sc = block_total(PMax{amax}, sm.part_max).v / 448.0f;
+    if (threadIdx.x == 0) p.scale[row] = sc;
+    const float2 q2 = f2(sc > 0.0f ? 1.0f / sc : 0.0f);
     uint2* outr = reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + row * (int64_t)p.nvec * 8);
     for (int b = 0; b < p.nvec; b += step) {
         uint4 gv[VPT], uv[VPT];

@@ -34,9 +34,9 @@ def test_binding_names_match_header():
 
 
 def test_version_and_status_strings(lib):
-    assert lib.mbd_abi_version() == 3
+    assert lib.mbd_abi_version() == 4
     hdr = open(mbd.HEADER_PATH).read()
-    assert int(re.search(r"#define MBD_ABI_VERSION (\d+)", hdr).group(1)) == 3
+    assert int(re.search(r"#define MBD_ABI_VERSION (\d+)", hdr).group(1)) == 4
     for code in range(5):
         assert lib.mbd_status_string(code).decode().startswith("MBD_")
     assert lib.mbd_status_string(99) == b"unknown mbd_status"
@@ -202,3 +202,24 @@ def test_program_argument_checks(lib):
 
 def test_program_struct_layout():
     assert ctypes.sizeof(mbd.Op) == 80 and mbd.Op.out.offset == 32 and mbd.Op.scale.offset == 72
+
+
+def test_program_plan_checks(lib):
+    # build runs every check of mbd_run_program before touching the device
+    H = 64
+    a = mbd.op_add_rmsnorm(A, 2 * A, 3 * A, 9 * A, 4, H, 1e-6)
+    b = mbd.op_add_rmsnorm(4 * A, 5 * A, A + 16, 9 * A, 4, H, 1e-6)
+    with pytest.raises(mbd.MbdError) as e:
+        mbd.program_plan_build([a, b])
+    assert e.value.status == mbd.ERR_UNSUPPORTED
+    with pytest.raises(mbd.MbdError) as e:
+        mbd.program_plan_build([mbd.op_add_rmsnorm(A + 2, 2 * A, 3 * A, 9 * A, 4, H, 1e-6)])
+    assert e.value.status == mbd.ERR_MISALIGNED
+    # a plan build left unfilled (failed) cannot be launched; an empty plan launches nothing
+    buf = (ctypes.c_uint64 * (mbd.PROGRAM_PLAN_BYTES // 8))()
+    assert lib.mbd_program_plan_launch(ctypes.addressof(buf), None) == mbd.ERR_INVALID_ARG
+    assert lib.mbd_program_plan_launch(None, None) == mbd.ERR_INVALID_ARG
+    n0 = mbd.kernel_launches()
+    empty = mbd.program_plan_build([mbd.op_swiglu(None, None, 0, 64)])
+    empty.launch()
+    assert mbd.kernel_launches() == n0

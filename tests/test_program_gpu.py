@@ -277,3 +277,35 @@ def test_program_matches_single_calls():
     for a, b in zip(outs["calls"][1], outs["program"][1]):
         d = np.abs(a.astype(np.int32) - b.astype(np.int32))
         assert d.max() <= 1, "outputs differ by more than one bf16 ulp"
+
+
+def test_plan_built_once_launched_twice():
+    """A plan is built once and launched twice: the second launch sees the residual the first one left, as
+    two decode steps through the same layers would."""
+    mbd = _mbd()
+    T, L, H, I, eps = 3, 4, 1536, 8960, 1e-6
+    res0, layers = decode_layers(T, L, H, I, seed=11)
+    R = dev_u16(torch, res0)
+    ops, keep, outs = [], [R], []
+    for x1, w1, x2, w2, gu in layers:
+        X1, W1, X2, W2, GU = (dev_u16(torch, a) for a in (x1, w1, x2, w2, gu))
+        O1, O2, Y = Guarded(torch, T * H, torch.int16), Guarded(torch, T * H, torch.int16), Guarded(torch, T * I, torch.int16)
+        ops += [mbd.op_add_rmsnorm(O1.view, R.view, X1.view, W1.view, T, H, eps),
+                mbd.op_add_rmsnorm(O2.view, R.view, X2.view, W2.view, T, H, eps), mbd.op_swiglu(Y.view, GU.view, T, I)]
+        keep += [X1, W1, X2, W2, GU]
+        outs.append((O1, O2, Y))
+    plan = mbd.program_plan_build(ops)
+    n0 = mbd.kernel_launches()
+    plan.launch()
+    plan.launch()
+    torch.cuda.synchronize()
+    assert mbd.kernel_launches() - n0 == 2
+    r = res0
+    for step in range(2):
+        for (x1, w1, x2, w2, gu), (O1, O2, Y) in zip(layers, outs):
+            r, _, v1 = orc.add_rmsnorm(x1, r, w1, eps)
+            r, _, v2 = orc.add_rmsnorm(x2, r, w2, eps)
+            if step == 1:
+                check_bf16(u16(O1, (T, H)), v1, "step 2 norm 1")
+                check_bf16(u16(O2, (T, H)), v2, "step 2 norm 2")
+    np.testing.assert_array_equal(u16(R, (T, H)), r, "residual after two launches")
