@@ -480,7 +480,8 @@ def run_decode_table(args) -> Dict:
     """Decode-step latency of the Qwen2.5-1.5B-shaped sweep (28 layers x (add + RMSNorm, add + RMSNorm,
     SwiGLU) per token count), launched three ways: one C-ABI call per op, the same calls replayed from a CUDA
     graph, programs (the 84 ops of one token count as one persistent launch, a plan built once and launched every
-    step), and that launch replayed from a CUDA graph."""
+    step, with its schedule in the launch parameters or uploaded once to device memory), and the by-value launch
+    replayed from a CUDA graph."""
     import torch
     import memory_bound_decoder_gb300 as mbd
     from memory_bound_decoder_gb300 import build as mbd_build
@@ -488,7 +489,7 @@ def run_decode_table(args) -> Dict:
     lib = mbd.get_lib()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    table, modes = {}, ("calls", "graph", "program", "program_graph")
+    table, modes = {}, ("calls", "graph", "program", "program_dev", "program_graph")
     launches = {}
     tokens = tuple(int(t) for t in args.decode_tokens.split(",")) if args.decode_tokens else (1, 2, 4, 8, 32, 64, 128, 256)
     for work in wl.qwen_decode_sweep(tokens):
@@ -509,6 +510,10 @@ def run_decode_table(args) -> Dict:
                 d.launch()
 
         plan_ptrs = [ctypes.addressof(p.buf) for p in plans]
+        scheds = [torch.empty(mbd.program_schedule_bytes(), dtype=torch.uint8, device=dev) for _ in plans]
+        for p, sc in zip(plans, scheds):
+            p.upload(sc, stream)
+        sched_ptrs = [sc.data_ptr() for sc in scheds]
 
         def run_program():
             for pp in plan_ptrs:
@@ -519,6 +524,12 @@ def run_decode_table(args) -> Dict:
         with torch.cuda.stream(stream):
             run_calls()
         torch.cuda.synchronize(dev)
+        def run_program_dev():
+            for pp, sp in zip(plan_ptrs, sched_ptrs):
+                rc = lib.mbd_program_plan_launch_uploaded(pp, sp, handle)
+                if rc != 0:
+                    raise RuntimeError(lib.mbd_status_string(rc).decode())
+
         graphs, graph_errors = {}, {}
         for name, body in (("graph", run_calls), ("program_graph", run_program)):
             g = torch.cuda.CUDAGraph()
@@ -530,7 +541,7 @@ def run_decode_table(args) -> Dict:
             except RuntimeError as e:   # reported in the line instead of a graph time
                 graph_errors[name] = str(e).splitlines()[0]
                 torch.cuda.synchronize(dev)
-        fns = {"calls": run_calls, "program": run_program}
+        fns = {"calls": run_calls, "program": run_program, "program_dev": run_program_dev}
         fns.update({k: g.replay for k, g in graphs.items()})
         row = {}
         for mode in modes:
@@ -556,11 +567,12 @@ def run_decode_table(args) -> Dict:
             row[mode] = round(ms * 1e3 / work.layers, 3)
         row["program_GBps"] = round(work.algorithmic_bytes() / (row["program"] * work.layers / 1e6) / 1e9, 1)
         row["launches_per_step"] = {"calls": launches[(T, "calls")], "graph": len(dcalls),
-                                    "program": launches[(T, "program")], "program_graph": len(plans)}
+                                    "program": launches[(T, "program")], "program_dev": launches[(T, "program_dev")],
+                                    "program_graph": len(plans)}
         row["plan_build_us"] = round(build_us, 1)
         table[str(T)] = row
         log(f"[decode] T={T}: {row}")
-        del dcalls, plans, graphs
+        del dcalls, plans, graphs, scheds
         torch.cuda.empty_cache()
     mean_prog = statistics.mean(r["program"] for r in table.values())
     return {"metric": "decode-step latency per layer, Qwen2.5-1.5B shapes (28 layers of 2 add+RMSNorm + 1 SwiGLU)",

@@ -84,7 +84,7 @@ typedef enum {
 #define MBD_MAX_REDUCED_WIDTH 262144
 
 /* ABI version of this header (bumped on any signature change or added entry point). */
-#define MBD_ABI_VERSION 4
+#define MBD_ABI_VERSION 5
 int mbd_abi_version(void);
 
 /* Static, human-readable name of a status code (never NULL). */
@@ -300,6 +300,26 @@ typedef struct {
 
 mbd_status mbd_program_plan_build(const mbd_op* ops, int n_ops, mbd_program_plan* plan);
 mbd_status mbd_program_plan_launch(const mbd_program_plan* plan, mbd_stream_t stream);
+
+/*
+ * A plan's schedule kept in device memory. mbd_program_plan_launch passes the whole schedule (about 14 KB)
+ * in the kernel parameters, and such a launch costs tens of microseconds of host time; after one upload,
+ * launch_uploaded passes a single pointer.
+ *   mbd_program_schedule_bytes : device bytes a schedule takes (a multiple of 256).
+ *   upload  : one asynchronous host-to-device copy of the plan's schedule into `schedule` (caller-owned
+ *             device memory, 256-byte aligned, at least mbd_program_schedule_bytes() long) on `stream`.
+ *             The plan must stay unchanged until the copy has executed (it may read the plan after the
+ *             call returns). MBD_ERR_INVALID_ARG: an unfilled plan, a null or short buffer;
+ *             MBD_ERR_MISALIGNED: a buffer not 256-byte aligned; MBD_ERR_CUDA: the copy failed.
+ *   launch_uploaded : the kernel reads the schedule from `schedule`, which must hold this plan's upload
+ *             (stream order makes an upload on the same stream visible to the launch). Errors as for
+ *             mbd_program_plan_launch, plus those of the buffer. `schedule` must not be written while the
+ *             kernel runs.
+ */
+size_t mbd_program_schedule_bytes(void);
+mbd_status mbd_program_plan_upload(const mbd_program_plan* plan, void* schedule, size_t schedule_bytes,
+                                   mbd_stream_t stream);
+mbd_status mbd_program_plan_launch_uploaded(const mbd_program_plan* plan, const void* schedule, mbd_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -77,10 +77,14 @@ def _load() -> ctypes.CDLL:
     lib.mbd_run_program.argtypes = [ctypes.POINTER(Op), cint, vp]
     lib.mbd_program_plan_build.argtypes = [ctypes.POINTER(Op), cint, vp]
     lib.mbd_program_plan_launch.argtypes = [vp, vp]
+    lib.mbd_program_schedule_bytes.restype = ctypes.c_size_t
+    lib.mbd_program_plan_upload.argtypes = [vp, vp, ctypes.c_size_t, vp]
+    lib.mbd_program_plan_launch_uploaded.argtypes = [vp, vp, vp]
     for fn in ("mbd_fused_add_rmsnorm", "mbd_fused_add_rmsnorm_quant_fp8", "mbd_swiglu", "mbd_swiglu_quant_fp8",
                "mbd_fused_allreduce_add_rmsnorm", "mbd_fused_allreduce_add_rmsnorm_quant_fp8",
                "mbd_fused_add_rmsnorm_quant_nvfp4", "mbd_swiglu_quant_nvfp4", "mbd_run_program",
-               "mbd_program_plan_build", "mbd_program_plan_launch"):
+               "mbd_program_plan_build", "mbd_program_plan_launch", "mbd_program_plan_upload",
+               "mbd_program_plan_launch_uploaded"):
         getattr(lib, fn).restype = cint
     return lib
 
@@ -288,6 +292,28 @@ class ProgramPlan:
 
     def launch(self, stream=None) -> None:
         _check(get_lib().mbd_program_plan_launch(ctypes.addressof(self.buf), _stream(stream)), "program_plan_launch")
+
+    def upload(self, schedule, stream=None) -> None:
+        """Copy the schedule into device memory `schedule` (a tensor or pointer of program_schedule_bytes())."""
+        nbytes = schedule.numel() * schedule.element_size() if hasattr(schedule, "numel") else program_schedule_bytes()
+        _check(get_lib().mbd_program_plan_upload(ctypes.addressof(self.buf), _ptr(schedule), nbytes, _stream(stream)),
+               "program_plan_upload")
+
+    def launch_uploaded(self, schedule, stream=None) -> None:
+        _check(get_lib().mbd_program_plan_launch_uploaded(ctypes.addressof(self.buf), _ptr(schedule), _stream(stream)),
+               "program_plan_launch_uploaded")
+
+
+def program_schedule_bytes() -> int:
+    return int(get_lib().mbd_program_schedule_bytes())
+
+
+def program_plan_upload(plan: ProgramPlan, schedule, stream=None) -> None:
+    plan.upload(schedule, stream)
+
+
+def program_plan_launch_uploaded(plan: ProgramPlan, schedule, stream=None) -> None:
+    plan.launch_uploaded(schedule, stream)
 
 
 def program_plan_build(ops) -> ProgramPlan:

@@ -498,7 +498,36 @@ mbd_status launch_plan(const PlanImpl* plan, cudaStream_t stream) {
         return MBD_ERR_CUDA;
     }
     if (device != plan->device) return MBD_ERR_INVALID_ARG;
-    return finish_launch(mbd::launch_program(plan->P, plan->vpt, plan->variant, plan->grid, stream));
+    return finish_launch(mbd::launch_program(plan->P, nullptr, plan->vpt, plan->variant, plan->grid, stream));
+}
+
+constexpr size_t kScheduleBytes = (sizeof(mbd::ProgramParams) + 255) & ~size_t{255};
+
+mbd_status upload_plan(const PlanImpl* plan, void* schedule, size_t bytes, cudaStream_t stream) {
+    if (!plan || plan->magic != kPlanMagic || !schedule) return MBD_ERR_INVALID_ARG;
+    if (!aligned(schedule, 256)) return MBD_ERR_MISALIGNED;
+    if (bytes < kScheduleBytes) return MBD_ERR_INVALID_ARG;
+    const cudaError_t e = cudaMemcpyAsync(schedule, &plan->P, sizeof(mbd::ProgramParams), cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) {
+        g_last_cuda_error = static_cast<int>(e);
+        (void)cudaGetLastError();
+        return MBD_ERR_CUDA;
+    }
+    return MBD_OK;
+}
+
+mbd_status launch_uploaded(const PlanImpl* plan, const void* schedule, cudaStream_t stream) {
+    if (!plan || plan->magic != kPlanMagic || !schedule) return MBD_ERR_INVALID_ARG;
+    if (!aligned(schedule, 256)) return MBD_ERR_MISALIGNED;
+    if (plan->grid == 0) return MBD_OK;
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) {
+        g_last_cuda_error = static_cast<int>(cudaGetLastError());
+        return MBD_ERR_CUDA;
+    }
+    if (device != plan->device) return MBD_ERR_INVALID_ARG;
+    return finish_launch(mbd::launch_program(plan->P, static_cast<const mbd::ProgramParams*>(schedule), plan->vpt,
+                                             plan->variant, plan->grid, stream));
 }
 
 }  // namespace
@@ -611,6 +640,18 @@ mbd_status mbd_program_plan_build(const mbd_op* ops, int n_ops, mbd_program_plan
 
 mbd_status mbd_program_plan_launch(const mbd_program_plan* plan, mbd_stream_t stream) {
     return launch_plan(reinterpret_cast<const PlanImpl*>(plan), reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t mbd_program_schedule_bytes(void) { return kScheduleBytes; }
+
+mbd_status mbd_program_plan_upload(const mbd_program_plan* plan, void* schedule, size_t schedule_bytes,
+                                   mbd_stream_t stream) {
+    return upload_plan(reinterpret_cast<const PlanImpl*>(plan), schedule, schedule_bytes,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+mbd_status mbd_program_plan_launch_uploaded(const mbd_program_plan* plan, const void* schedule, mbd_stream_t stream) {
+    return launch_uploaded(reinterpret_cast<const PlanImpl*>(plan), schedule, reinterpret_cast<cudaStream_t>(stream));
 }
 
 mbd_status mbd_run_program(const mbd_op* ops, int n_ops, mbd_stream_t stream) {

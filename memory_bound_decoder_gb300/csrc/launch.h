@@ -102,8 +102,12 @@ struct ProgramParams {
 constexpr int kProgramVariants = 3;
 // The first variant that covers the given epilogue sets, or -1.
 int program_variant(int norm_mask, int swiglu_mask);
-// Program kernel `variant` for `vpt` vectors per thread (1, 2 or 4) on `grid` CTAs of kProgramThreads.
-cudaError_t launch_program(const ProgramParams& p, int vpt, int variant, int grid, cudaStream_t s);
+static_assert(sizeof(ProgOp) % 8 == 0 && sizeof(ProgramParams) % 8 == 0, "schedules are copied in 8-byte words");
+
+// Program kernel `variant` for `vpt` vectors per thread (1, 2 or 4) on `grid` CTAs of kProgramThreads; the
+// schedule `p` by value, or, when `dev` is not null, read from that copy of it in device memory.
+cudaError_t launch_program(const ProgramParams& p, const ProgramParams* dev, int vpt, int variant, int grid,
+                           cudaStream_t s);
 // Resident program CTAs per SM (occupancy query; 0 on error).
 int program_ctas_per_sm(int vpt, int variant);
 cudaError_t device_error_flags_program(unsigned int* flags, bool clear);

@@ -12,6 +12,8 @@
 // Time", "Fusing operations, measured" and "Leaving the engine behind": issuing many small kernels costs
 // more than running them, hence CUDA graphs for decoding; "Introduction to torch.compile and How It Works
 // with vLLM", section 5: one kernel for a whole forward pass).
+#include <cstddef>
+
 #include "norm_impl.cuh"
 #include "swiglu_impl.cuh"
 
@@ -243,11 +245,9 @@ constexpr int min_ctas(int v, int nm, int sm) {
 // of a decode step) shares its CTA with nothing; when there are more chain items than CTAs both kinds are
 // dealt round-robin over the whole grid.
 template <int V, int NM, int SM>
-__global__ void __launch_bounds__(kProgramThreads, min_ctas(V, NM, SM)) program_kernel(const __grid_constant__ ProgramParams P) {
+__device__ __forceinline__ void program_body(const ProgramParams& P) {
     __shared__ ProgSmem sm;
     __shared__ ChainSmem cs;
-    pdl_trigger();
-    pdl_wait();
     const int64_t G = gridDim.x, b = blockIdx.x;
     const int64_t nc = P.n_chain_items, nf = P.n_free_items;
     int g = 0, held = -1, f = 0;
@@ -263,6 +263,34 @@ __global__ void __launch_bounds__(kProgramThreads, min_ctas(V, NM, SM)) program_
     }
 }
 
+// The schedule by value in the kernel parameters (no device memory needed; a launch carries ~14 KB)...
+template <int V, int NM, int SM>
+__global__ void __launch_bounds__(kProgramThreads, min_ctas(V, NM, SM)) program_kernel(const __grid_constant__ ProgramParams P) {
+    pdl_trigger();
+    pdl_wait();
+    program_body<V, NM, SM>(P);
+}
+
+// ... or uploaded by the caller to device memory (a launch carries one pointer). Every CTA first copies the
+// used part of it into shared memory with coalesced loads (one L2 round trip), so that the item lookups and
+// descriptors cost shared-memory latency rather than an L2 round trip each. The upload precedes the launch
+// in stream order and is not a kernel, so the copy may run before the grid dependency wait.
+template <int V, int NM, int SM>
+__global__ void __launch_bounds__(kProgramThreads, min_ctas(V, NM, SM)) program_kernel_dev(const ProgramParams* __restrict__ P) {
+    __shared__ __align__(16) ProgramParams S;
+    pdl_trigger();
+    {
+        const size_t bytes = offsetof(ProgramParams, ops) + static_cast<size_t>(P->n_ops) * sizeof(ProgOp);
+        const int words = static_cast<int>(bytes / 8);
+        const uint2* src = reinterpret_cast<const uint2*>(P);
+        uint2* dst = reinterpret_cast<uint2*>(&S);
+        for (int i = threadIdx.x; i < words; i += blockDim.x) dst[i] = src[i];
+    }
+    __syncthreads();
+    pdl_wait();
+    program_body<V, NM, SM>(S);
+}
+
 template <int V, int NM, int SM>
 int ctas_per_sm() {
     int n = 0;
@@ -274,7 +302,7 @@ int ctas_per_sm() {
 }
 
 template <int V, int NM, int SM>
-cudaError_t launch_variant(const ProgramParams& p, int grid, cudaStream_t s) {
+cudaError_t launch_variant(const ProgramParams& p, const ProgramParams* dev, int grid, cudaStream_t s) {
     cudaLaunchConfig_t cfg = cudaLaunchConfig_t{};
     cudaLaunchAttribute attr[1];
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
@@ -285,6 +313,7 @@ cudaError_t launch_variant(const ProgramParams& p, int grid, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (dev) return cudaLaunchKernelEx(&cfg, program_kernel_dev<V, NM, SM>, dev);
     return cudaLaunchKernelEx(&cfg, program_kernel<V, NM, SM>, p);
 }
 
@@ -299,8 +328,8 @@ template <int V, int K>
 int ctas_of() { return ctas_per_sm<V, kVariantMasks[K][0], kVariantMasks[K][1]>(); }
 
 template <int V, int K>
-cudaError_t launch_of(const ProgramParams& p, int grid, cudaStream_t s) {
-    return launch_variant<V, kVariantMasks[K][0], kVariantMasks[K][1]>(p, grid, s);
+cudaError_t launch_of(const ProgramParams& p, const ProgramParams* dev, int grid, cudaStream_t s) {
+    return launch_variant<V, kVariantMasks[K][0], kVariantMasks[K][1]>(p, dev, grid, s);
 }
 
 template <int V>
@@ -314,11 +343,11 @@ int ctas_v(int variant) {
 }
 
 template <int V>
-cudaError_t launch_v(const ProgramParams& p, int variant, int grid, cudaStream_t s) {
+cudaError_t launch_v(const ProgramParams& p, const ProgramParams* dev, int variant, int grid, cudaStream_t s) {
     switch (variant) {
-        case 0: return launch_of<V, 0>(p, grid, s);
-        case 1: return launch_of<V, 1>(p, grid, s);
-        case 2: return launch_of<V, 2>(p, grid, s);
+        case 0: return launch_of<V, 0>(p, dev, grid, s);
+        case 1: return launch_of<V, 1>(p, dev, grid, s);
+        case 2: return launch_of<V, 2>(p, dev, grid, s);
     }
     return cudaErrorInvalidValue;
 }
@@ -340,11 +369,12 @@ int program_ctas_per_sm(int vpt, int variant) {
     return 0;
 }
 
-cudaError_t launch_program(const ProgramParams& p, int vpt, int variant, int grid, cudaStream_t s) {
+cudaError_t launch_program(const ProgramParams& p, const ProgramParams* dev, int vpt, int variant, int grid,
+                           cudaStream_t s) {
     switch (vpt) {
-        case 1: return launch_v<1>(p, variant, grid, s);
-        case 2: return launch_v<2>(p, variant, grid, s);
-        case 4: return launch_v<4>(p, variant, grid, s);
+        case 1: return launch_v<1>(p, dev, variant, grid, s);
+        case 2: return launch_v<2>(p, dev, variant, grid, s);
+        case 4: return launch_v<4>(p, dev, variant, grid, s);
     }
     return cudaErrorInvalidValue;
 }

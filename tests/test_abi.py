@@ -34,9 +34,9 @@ def test_binding_names_match_header():
 
 
 def test_version_and_status_strings(lib):
-    assert lib.mbd_abi_version() == 4
+    assert lib.mbd_abi_version() == 5
     hdr = open(mbd.HEADER_PATH).read()
-    assert int(re.search(r"#define MBD_ABI_VERSION (\d+)", hdr).group(1)) == 4
+    assert int(re.search(r"#define MBD_ABI_VERSION (\d+)", hdr).group(1)) == 5
     for code in range(5):
         assert lib.mbd_status_string(code).decode().startswith("MBD_")
     assert lib.mbd_status_string(99) == b"unknown mbd_status"
@@ -223,3 +223,18 @@ def test_program_plan_checks(lib):
     empty = mbd.program_plan_build([mbd.op_swiglu(None, None, 0, 64)])
     empty.launch()
     assert mbd.kernel_launches() == n0
+
+
+def test_program_upload_checks(lib):
+    buf = (ctypes.c_uint64 * (mbd.PROGRAM_PLAN_BYTES // 8))()
+    n = mbd.program_schedule_bytes()
+    assert n % 256 == 0 and n >= 8192
+    assert lib.mbd_program_plan_upload(ctypes.addressof(buf), A, n, None) == mbd.ERR_INVALID_ARG   # unfilled plan
+    assert lib.mbd_program_plan_launch_uploaded(ctypes.addressof(buf), A, None) == mbd.ERR_INVALID_ARG
+    empty = mbd.program_plan_build([])
+    pp = ctypes.addressof(empty.buf)
+    assert lib.mbd_program_plan_upload(pp, None, n, None) == mbd.ERR_INVALID_ARG
+    assert lib.mbd_program_plan_upload(pp, A + 16, n, None) == mbd.ERR_MISALIGNED
+    assert lib.mbd_program_plan_upload(pp, A, n - 256, None) == mbd.ERR_INVALID_ARG
+    assert lib.mbd_program_plan_launch_uploaded(pp, A + 16, None) == mbd.ERR_MISALIGNED
+    assert lib.mbd_program_plan_launch_uploaded(pp, A, None) == 0                  # nothing to do: no launch

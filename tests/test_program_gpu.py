@@ -309,3 +309,35 @@ def test_plan_built_once_launched_twice():
                 check_bf16(u16(O1, (T, H)), v1, "step 2 norm 1")
                 check_bf16(u16(O2, (T, H)), v2, "step 2 norm 2")
     np.testing.assert_array_equal(u16(R, (T, H)), r, "residual after two launches")
+
+
+def test_uploaded_schedule_matches_by_value_launch():
+    """The same plan launched twice with its schedule by value and twice from an uploaded copy: identical bits
+    (same kernel body, same schedule)."""
+    mbd = _mbd()
+    T, L, H, I, eps = 5, 6, 1536, 8960, 1e-6
+    res0, layers = decode_layers(T, L, H, I, seed=12)
+    results = []
+    for mode in ("value", "uploaded"):
+        R = dev_u16(torch, res0)
+        ops, keep, outs = [], [R], []
+        for x1, w1, x2, w2, gu in layers:
+            X1, W1, X2, W2, GU = (dev_u16(torch, a) for a in (x1, w1, x2, w2, gu))
+            O1, O2, Y = (torch.empty(T * n, dtype=torch.int16, device="cuda") for n in (H, H, I))
+            ops += [mbd.op_add_rmsnorm(O1, R.view, X1.view, W1.view, T, H, eps),
+                    mbd.op_add_rmsnorm(O2, R.view, X2.view, W2.view, T, H, eps), mbd.op_swiglu(Y, GU.view, T, I)]
+            keep += [X1, W1, X2, W2, GU]
+            outs += [O1, O2, Y]
+        plan = mbd.program_plan_build(ops)
+        if mode == "value":
+            plan.launch()
+            plan.launch()
+        else:
+            sched = torch.empty(mbd.program_schedule_bytes(), dtype=torch.uint8, device="cuda")
+            plan.upload(sched)
+            plan.launch_uploaded(sched)
+            plan.launch_uploaded(sched)
+        torch.cuda.synchronize()
+        results.append([R.numpy(np.uint16)] + [t.cpu().numpy() for t in outs])
+    for a, b in zip(*results):
+        np.testing.assert_array_equal(a, b)
