@@ -489,7 +489,7 @@ def run_decode_table(args) -> Dict:
     lib = mbd.get_lib()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    table, modes = {}, ("calls", "graph", "program", "program_dev", "program_graph")
+    table, modes = {}, ("calls", "graph", "program", "program_dev", "program_static", "program_graph")
     launches = {}
     tokens = tuple(int(t) for t in args.decode_tokens.split(",")) if args.decode_tokens else (1, 2, 4, 8, 32, 64, 128, 256)
     for work in wl.qwen_decode_sweep(tokens):
@@ -530,6 +530,12 @@ def run_decode_table(args) -> Dict:
                 if rc != 0:
                     raise RuntimeError(lib.mbd_status_string(rc).decode())
 
+        def run_program_static():
+            for pp in plan_ptrs:
+                rc = lib.mbd_program_plan_launch_static(pp, handle)
+                if rc != 0:
+                    raise RuntimeError(lib.mbd_status_string(rc).decode())
+
         graphs, graph_errors = {}, {}
         for name, body in (("graph", run_calls), ("program_graph", run_program)):
             g = torch.cuda.CUDAGraph()
@@ -541,7 +547,8 @@ def run_decode_table(args) -> Dict:
             except RuntimeError as e:   # reported in the line instead of a graph time
                 graph_errors[name] = str(e).splitlines()[0]
                 torch.cuda.synchronize(dev)
-        fns = {"calls": run_calls, "program": run_program, "program_dev": run_program_dev}
+        fns = {"calls": run_calls, "program": run_program, "program_dev": run_program_dev,
+               "program_static": run_program_static}
         fns.update({k: g.replay for k, g in graphs.items()})
         row = {}
         for mode in modes:
@@ -568,6 +575,7 @@ def run_decode_table(args) -> Dict:
         row["program_GBps"] = round(work.algorithmic_bytes() / (row["program"] * work.layers / 1e6) / 1e9, 1)
         row["launches_per_step"] = {"calls": launches[(T, "calls")], "graph": len(dcalls),
                                     "program": launches[(T, "program")], "program_dev": launches[(T, "program_dev")],
+                                    "program_static": launches[(T, "program_static")],
                                     "program_graph": len(plans)}
         row["plan_build_us"] = round(build_us, 1)
         table[str(T)] = row

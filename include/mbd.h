@@ -84,7 +84,7 @@ typedef enum {
 #define MBD_MAX_REDUCED_WIDTH 262144
 
 /* ABI version of this header (bumped on any signature change or added entry point). */
-#define MBD_ABI_VERSION 5
+#define MBD_ABI_VERSION 6
 int mbd_abi_version(void);
 
 /* Static, human-readable name of a status code (never NULL). */
@@ -320,6 +320,19 @@ size_t mbd_program_schedule_bytes(void);
 mbd_status mbd_program_plan_upload(const mbd_program_plan* plan, void* schedule, size_t schedule_bytes,
                                    mbd_stream_t stream);
 mbd_status mbd_program_plan_launch_uploaded(const mbd_program_plan* plan, const void* schedule, mbd_stream_t stream);
+
+/*
+ * mbd_program_plan_upload + mbd_program_plan_launch_uploaded without caller memory. No counterpart on the
+ * source pages. The schedule is copied (one asynchronous host-to-device copy on `stream`, as upload does)
+ * into a static buffer of the library: MBD_STATIC_SCHEDULE_BYTES per device, part of the library's device
+ * image, its address looked up once per device. Nothing is allocated (no cudaMalloc or other allocating
+ * call). Each call copies the schedule again, so plans may alternate freely; because the buffer is shared,
+ * calls must not run concurrently on different streams of one device (on one stream they are ordered).
+ * A schedule larger than the buffer returns MBD_ERR_UNSUPPORTED (with this header's limits it always fits).
+ * Other errors as for mbd_program_plan_launch.
+ */
+#define MBD_STATIC_SCHEDULE_BYTES 16384
+mbd_status mbd_program_plan_launch_static(const mbd_program_plan* plan, mbd_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -80,11 +80,12 @@ def _load() -> ctypes.CDLL:
     lib.mbd_program_schedule_bytes.restype = ctypes.c_size_t
     lib.mbd_program_plan_upload.argtypes = [vp, vp, ctypes.c_size_t, vp]
     lib.mbd_program_plan_launch_uploaded.argtypes = [vp, vp, vp]
+    lib.mbd_program_plan_launch_static.argtypes = [vp, vp]
     for fn in ("mbd_fused_add_rmsnorm", "mbd_fused_add_rmsnorm_quant_fp8", "mbd_swiglu", "mbd_swiglu_quant_fp8",
                "mbd_fused_allreduce_add_rmsnorm", "mbd_fused_allreduce_add_rmsnorm_quant_fp8",
                "mbd_fused_add_rmsnorm_quant_nvfp4", "mbd_swiglu_quant_nvfp4", "mbd_run_program",
                "mbd_program_plan_build", "mbd_program_plan_launch", "mbd_program_plan_upload",
-               "mbd_program_plan_launch_uploaded"):
+               "mbd_program_plan_launch_uploaded", "mbd_program_plan_launch_static"):
         getattr(lib, fn).restype = cint
     return lib
 
@@ -303,6 +304,11 @@ class ProgramPlan:
         _check(get_lib().mbd_program_plan_launch_uploaded(ctypes.addressof(self.buf), _ptr(schedule), _stream(stream)),
                "program_plan_launch_uploaded")
 
+    def launch_static(self, stream=None) -> None:
+        """Upload into the library's static schedule buffer and launch (allocates nothing)."""
+        _check(get_lib().mbd_program_plan_launch_static(ctypes.addressof(self.buf), _stream(stream)),
+               "program_plan_launch_static")
+
 
 def program_schedule_bytes() -> int:
     return int(get_lib().mbd_program_schedule_bytes())
@@ -314,6 +320,10 @@ def program_plan_upload(plan: ProgramPlan, schedule, stream=None) -> None:
 
 def program_plan_launch_uploaded(plan: ProgramPlan, schedule, stream=None) -> None:
     plan.launch_uploaded(schedule, stream)
+
+
+def program_plan_launch_static(plan: ProgramPlan, stream=None) -> None:
+    plan.launch_static(stream)
 
 
 def program_plan_build(ops) -> ProgramPlan:

@@ -261,6 +261,7 @@ mbd_status swiglu_common(void* out, uint8_t* out_sf, mbd::Epilogue ep, const voi
 
 static_assert(sizeof(mbd::ProgramParams) <= 32764, "program parameters exceed the kernel parameter limit");
 static_assert(mbd::kMaxProgramOps == MBD_MAX_PROGRAM_OPS, "program op limit");
+static_assert(mbd::kStaticScheduleBytes == MBD_STATIC_SCHEDULE_BYTES, "static schedule size");
 static_assert(sizeof(mbd_op) == 80 && offsetof(mbd_op, out) == 32 && offsetof(mbd_op, scale) == 72, "mbd_op layout");
 
 // A byte range an op touches: row-wise ranges (row_bytes > 0) hold `rows` rows of row_bytes each.
@@ -530,6 +531,38 @@ mbd_status launch_uploaded(const PlanImpl* plan, const void* schedule, cudaStrea
                                              plan->variant, plan->grid, stream));
 }
 
+// The library's static schedule buffer on each device: its address, looked up once per device.
+std::atomic<void*> g_static_schedule_addr[kMaxDevices];
+
+// mbd_program_plan_launch_static: the uploaded-schedule launch, with the schedule copied into the static
+// buffer instead of caller memory. Nothing is allocated: the buffer is part of the module image.
+mbd_status launch_static(const PlanImpl* plan, cudaStream_t stream) {
+    if (!plan || plan->magic != kPlanMagic) return MBD_ERR_INVALID_ARG;
+    if (plan->grid == 0) return MBD_OK;
+    const size_t used = offsetof(mbd::ProgramParams, ops) + static_cast<size_t>(plan->P.n_ops) * sizeof(mbd::ProgOp);
+    if (used > mbd::kStaticScheduleBytes || kScheduleBytes > mbd::kStaticScheduleBytes) return MBD_ERR_UNSUPPORTED;
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices) {
+        g_last_cuda_error = static_cast<int>(cudaErrorInvalidDevice);
+        (void)cudaGetLastError();
+        return MBD_ERR_CUDA;
+    }
+    if (device != plan->device) return MBD_ERR_INVALID_ARG;
+    void* addr = g_static_schedule_addr[device].load(std::memory_order_acquire);
+    if (!addr) {
+        const cudaError_t e = mbd::static_schedule_address(&addr);
+        if (e != cudaSuccess || !addr) {
+            g_last_cuda_error = static_cast<int>(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+            (void)cudaGetLastError();
+            return MBD_ERR_CUDA;
+        }
+        g_static_schedule_addr[device].store(addr, std::memory_order_release);
+    }
+    const mbd_status st = upload_plan(plan, addr, mbd::kStaticScheduleBytes, stream);
+    if (st != MBD_OK) return st;
+    return launch_uploaded(plan, addr, stream);
+}
+
 }  // namespace
 
 extern "C" {
@@ -643,6 +676,10 @@ mbd_status mbd_program_plan_launch(const mbd_program_plan* plan, mbd_stream_t st
 }
 
 size_t mbd_program_schedule_bytes(void) { return kScheduleBytes; }
+
+mbd_status mbd_program_plan_launch_static(const mbd_program_plan* plan, mbd_stream_t stream) {
+    return launch_static(reinterpret_cast<const PlanImpl*>(plan), reinterpret_cast<cudaStream_t>(stream));
+}
 
 mbd_status mbd_program_plan_upload(const mbd_program_plan* plan, void* schedule, size_t schedule_bytes,
                                    mbd_stream_t stream) {

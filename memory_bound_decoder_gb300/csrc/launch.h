@@ -104,6 +104,12 @@ constexpr int kProgramVariants = 3;
 int program_variant(int norm_mask, int swiglu_mask);
 static_assert(sizeof(ProgOp) % 8 == 0 && sizeof(ProgramParams) % 8 == 0, "schedules are copied in 8-byte words");
 
+// The library's own schedule buffer (one per device, a static array of the module image), and its address
+// on the current device.
+constexpr size_t kStaticScheduleBytes = 16384;
+static_assert(sizeof(ProgramParams) <= kStaticScheduleBytes, "a schedule fits the static buffer");
+cudaError_t static_schedule_address(void** addr);
+
 // Program kernel `variant` for `vpt` vectors per thread (1, 2 or 4) on `grid` CTAs of kProgramThreads; the
 // schedule `p` by value, or, when `dev` is not null, read from that copy of it in device memory.
 cudaError_t launch_program(const ProgramParams& p, const ProgramParams* dev, int vpt, int variant, int grid,

@@ -379,6 +379,12 @@ cudaError_t launch_program(const ProgramParams& p, const ProgramParams* dev, int
     return cudaErrorInvalidValue;
 }
 
+// Schedule storage of mbd_program_plan_launch_static: part of the module image, so nothing is allocated
+// when it is used.
+__device__ __align__(256) unsigned char g_static_schedule[kStaticScheduleBytes];
+
+cudaError_t static_schedule_address(void** addr) { return cudaGetSymbolAddress(addr, g_static_schedule); }
+
 cudaError_t device_error_flags_program(unsigned int* flags, bool clear) {
     cudaError_t e = cudaMemcpyFromSymbol(flags, g_device_error_flags, sizeof(unsigned int));
     if (e == cudaSuccess && clear) {

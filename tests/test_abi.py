@@ -34,9 +34,9 @@ def test_binding_names_match_header():
 
 
 def test_version_and_status_strings(lib):
-    assert lib.mbd_abi_version() == 5
+    assert lib.mbd_abi_version() == 6
     hdr = open(mbd.HEADER_PATH).read()
-    assert int(re.search(r"#define MBD_ABI_VERSION (\d+)", hdr).group(1)) == 5
+    assert int(re.search(r"#define MBD_ABI_VERSION (\d+)", hdr).group(1)) == 6
     for code in range(5):
         assert lib.mbd_status_string(code).decode().startswith("MBD_")
     assert lib.mbd_status_string(99) == b"unknown mbd_status"
@@ -238,3 +238,14 @@ def test_program_upload_checks(lib):
     assert lib.mbd_program_plan_upload(pp, A, n - 256, None) == mbd.ERR_INVALID_ARG
     assert lib.mbd_program_plan_launch_uploaded(pp, A + 16, None) == mbd.ERR_MISALIGNED
     assert lib.mbd_program_plan_launch_uploaded(pp, A, None) == 0                  # nothing to do: no launch
+
+
+def test_program_static_launch_checks(lib):
+    buf = (ctypes.c_uint64 * (mbd.PROGRAM_PLAN_BYTES // 8))()
+    assert lib.mbd_program_plan_launch_static(ctypes.addressof(buf), None) == mbd.ERR_INVALID_ARG   # unfilled
+    assert lib.mbd_program_plan_launch_static(None, None) == mbd.ERR_INVALID_ARG
+    n0 = mbd.kernel_launches()
+    mbd.program_plan_build([]).launch_static()                                                  # nothing to do
+    assert mbd.kernel_launches() == n0
+    hdr = open(mbd.HEADER_PATH).read()
+    assert int(re.search(r"#define MBD_STATIC_SCHEDULE_BYTES (\d+)", hdr).group(1)) >= mbd.program_schedule_bytes()
