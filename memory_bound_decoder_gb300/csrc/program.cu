@@ -266,9 +266,9 @@ __device__ __forceinline__ void program_body(const ProgramParams& P) {
 // The schedule by value in the kernel parameters (no device memory needed; a launch carries ~14 KB)...
 template <int V, int NM, int SM>
 __global__ void __launch_bounds__(kProgramThreads, min_ctas(V, NM, SM)) program_kernel(const __grid_constant__ ProgramParams P) {
-    pdl_trigger();
     pdl_wait();
     program_body<V, NM, SM>(P);
+    pdl_trigger();   // late: a dependent program waiting in SM slots would hold resources this one still uses
 }
 
 // ... or uploaded by the caller to device memory (a launch carries one pointer). Every CTA first copies the
@@ -278,7 +278,6 @@ __global__ void __launch_bounds__(kProgramThreads, min_ctas(V, NM, SM)) program_
 template <int V, int NM, int SM>
 __global__ void __launch_bounds__(kProgramThreads, min_ctas(V, NM, SM)) program_kernel_dev(const ProgramParams* __restrict__ P) {
     __shared__ __align__(16) ProgramParams S;
-    pdl_trigger();
     {
         const size_t bytes = offsetof(ProgramParams, ops) + static_cast<size_t>(P->n_ops) * sizeof(ProgOp);
         const int words = static_cast<int>(bytes / 8);
@@ -289,6 +288,7 @@ __global__ void __launch_bounds__(kProgramThreads, min_ctas(V, NM, SM)) program_
     __syncthreads();
     pdl_wait();
     program_body<V, NM, SM>(S);
+    pdl_trigger();   // late, as in program_kernel
 }
 
 template <int V, int NM, int SM>
