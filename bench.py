@@ -458,6 +458,25 @@ def run_e2e(torch, dcalls: List[DeviceCall], kstream, dev, steps: int, step_byte
                     "stream of every output; per-call events pipeline the three"}
 
 
+def resolve_tuning(arg: str, torch, dev) -> Optional[str]:
+    """The tuning file to install: an explicit path, none, or (auto) the packaged table tuned on this GPU model
+    (same name and SM count), if there is one."""
+    if arg == "none":
+        return None
+    if arg != "auto":
+        return arg
+    d = os.path.join(ROOT, "memory_bound_decoder_gb300", "tuning")
+    props = torch.cuda.get_device_properties(dev)
+    for f in sorted(os.listdir(d)) if os.path.isdir(d) else []:
+        if not f.endswith(".json"):
+            continue
+        with open(os.path.join(d, f)) as fh:
+            meta = json.load(fh)
+        if meta.get("device") == props.name and meta.get("multiprocessors") == props.multi_processor_count:
+            return os.path.join(d, f)
+    return None
+
+
 def build_device_calls(torch, mbd, work: wl.Workload, seed: int, rank: int, dev) -> List[DeviceCall]:
     """Device buffers of every launch of one step. Layers repeat the calls with fresh inputs; in a multi-layer
     step every norm of one token count updates one shared residual, as a decoder's layers do."""
@@ -603,6 +622,9 @@ def run_mine(args, work: wl.Workload, rank: int, world: int, local_rank: int) ->
         torch.distributed.barrier()
     mbd.get_lib()
     dev = torch.device("cuda", local_rank)
+    tuning = resolve_tuning(args.tuning, torch, dev)
+    if tuning:
+        mbd.tuning_load(tuning)
     torch.cuda.set_device(dev)
     props = torch.cuda.get_device_properties(dev)
     l2_bytes = int(getattr(props, "L2_cache_size", 0)) or 126 * 2 ** 20
@@ -714,7 +736,8 @@ def run_mine(args, work: wl.Workload, rank: int, world: int, local_rank: int) ->
                    "io": "bf16 inputs; bf16 or E4M3 outputs; fp32 arithmetic",
                    "l2": f"inputs larger than L2: {step_bytes / 2 ** 20:.0f} MiB of distinct buffers per step "
                          f"vs {l2_bytes / 2 ** 20:.0f} MiB L2, no flush",
-                   "parallelism": f"replicas x{world} (rows are independent; no collective)"},
+                   "parallelism": f"replicas x{world} (rows are independent; no collective)",
+                   "launch_shapes": f"tuning table {os.path.relpath(tuning, ROOT)}" if tuning else "built-in rules"},
         "tokens_per_s": round(tokens * args.steps * world / (elapsed_ms / 1e3), 1),
         "gpu_launches": int(launches),
         "roofline": {"bound": "hbm", "kernel": dcall.call.name, "achieved": round(achieved, 1),
@@ -748,6 +771,9 @@ def main():
     ap.add_argument("--decode-table", action="store_true",
                     help="time the Qwen decode sweep as per-op calls, a CUDA graph and programs (one JSON line)")
     ap.add_argument("--decode-tokens", default="", help="token counts of --decode-table (default 1,2,4,8,32,64,128,256)")
+    ap.add_argument("--tuning", default="auto",
+                    help="launch-shape table: a tuning file, 'auto' (the packaged table of this GPU model when one "
+                         "exists, else the built-in rules) or 'none' (the built-in rules)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

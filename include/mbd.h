@@ -84,7 +84,7 @@ typedef enum {
 #define MBD_MAX_REDUCED_WIDTH 262144
 
 /* ABI version of this header (bumped on any signature change or added entry point). */
-#define MBD_ABI_VERSION 6
+#define MBD_ABI_VERSION 7
 int mbd_abi_version(void);
 
 /* Static, human-readable name of a status code (never NULL). */
@@ -333,6 +333,46 @@ mbd_status mbd_program_plan_launch_uploaded(const mbd_program_plan* plan, const 
  */
 #define MBD_STATIC_SCHEDULE_BYTES 16384
 mbd_status mbd_program_plan_launch_static(const mbd_program_plan* plan, mbd_stream_t stream);
+
+/*
+ * Launch-shape tuning (shape-bucket dispatch). [TRT] "Auto-tuning, measured": TensorRT-LLM picks kernel
+ * tactics per shape bucket at startup and keeps them in a cache that can be saved to a file and reloaded.
+ * Here the knobs are the launch shape of the single-call entry points: CTAs per row (one thread-block
+ * cluster when the row is reduced), 16-byte vectors per thread and threads per CTA. Without a table the
+ * built-in rules choose (they come from sweeps on GB300). A table is a list of entries; a call takes the
+ * FIRST entry whose kind (and FP8 mode) matches and whose token and width buckets hold it, provided its
+ * shape fits the call (enough threads x vectors for a slice of the row, at most 8 CTAs when the row is
+ * reduced); otherwise the next matching entry, then the rules. The all-reduce and program entry points do
+ * not use the table. The tuner that fills it is memory_bound_decoder_gb300/tune.py.
+ */
+typedef struct {
+    int32_t kind;                 /* mbd_op_kind of the entry point */
+    int32_t mode;                 /* FP8 kinds: mbd_scale_mode; ignored otherwise */
+    int64_t tokens_min, tokens_max;  /* n_tokens bucket, inclusive */
+    int64_t width_min, width_max;    /* hidden / inter bucket, inclusive */
+    int32_t ctas_per_row;         /* >= 1 */
+    int32_t vectors_per_thread;   /* 1, 2, 4 or 8 */
+    int32_t threads;              /* 32 .. 512, a multiple of 32 */
+    int32_t reserved;             /* 0 */
+} mbd_tuning_entry;
+
+#define MBD_MAX_TUNING_ENTRIES 4096
+
+/* Replace the process-wide table with a copy of entries[0 .. n_entries) (n_entries == 0: no table, the rules
+ * alone). Thread-safe: a call in flight on another thread uses either the old or the new table. Returns
+ * MBD_ERR_INVALID_ARG (table unchanged) for a bad count, null entries, or an entry with an unknown kind or
+ * FP8 mode, an empty bucket, a non-zero reserved field or a shape outside the ranges above. */
+mbd_status mbd_tuning_set(const mbd_tuning_entry* entries, int n_entries);
+
+/* The number of entries in the table; copies the first min(that, capacity) into entries (may be NULL). */
+int mbd_tuning_get(mbd_tuning_entry* entries, int capacity);
+
+/* The launch shape (CTAs per row after rounding, vectors per thread, threads) that a call of entry point
+ * `kind` (FP8: with `mode`) on n_tokens x width would use now (table, else rules), without launching. Uses
+ * the current device's SM count. Errors: MBD_ERR_INVALID_ARG (unknown kind or mode, n_tokens or width <= 0,
+ * a null output), the width checks of the entry point (MBD_ERR_MISALIGNED, MBD_ERR_UNSUPPORTED). */
+mbd_status mbd_launch_shape(int kind, int mode, int64_t n_tokens, int64_t width, int32_t* ctas_per_row,
+                            int32_t* vectors_per_thread, int32_t* threads);
 
 #ifdef __cplusplus
 }

@@ -51,6 +51,19 @@ MAX_PROGRAM_OPS = 128
 PROGRAM_PLAN_BYTES = 16384
 
 
+class TuningEntry(ctypes.Structure):
+    """One row of the launch-shape table (the C struct mbd_tuning_entry)."""
+    _fields_ = [("kind", ctypes.c_int32), ("mode", ctypes.c_int32), ("tokens_min", ctypes.c_int64),
+                ("tokens_max", ctypes.c_int64), ("width_min", ctypes.c_int64), ("width_max", ctypes.c_int64),
+                ("ctas_per_row", ctypes.c_int32), ("vectors_per_thread", ctypes.c_int32), ("threads", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+OP_NAMES = {0: "add_rmsnorm", 1: "add_rmsnorm_quant_fp8", 2: "add_rmsnorm_quant_nvfp4", 3: "swiglu",
+            4: "swiglu_quant_fp8", 5: "swiglu_quant_nvfp4"}
+OP_KINDS = {v: k for k, v in OP_NAMES.items()}
+
+
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is missing: build it with memory_bound_decoder_gb300.build.build() "
@@ -81,6 +94,13 @@ def _load() -> ctypes.CDLL:
     lib.mbd_program_plan_upload.argtypes = [vp, vp, ctypes.c_size_t, vp]
     lib.mbd_program_plan_launch_uploaded.argtypes = [vp, vp, vp]
     lib.mbd_program_plan_launch_static.argtypes = [vp, vp]
+    lib.mbd_tuning_set.argtypes = [ctypes.POINTER(TuningEntry), cint]
+    lib.mbd_tuning_set.restype = cint
+    lib.mbd_tuning_get.argtypes = [ctypes.POINTER(TuningEntry), cint]
+    lib.mbd_tuning_get.restype = cint
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    lib.mbd_launch_shape.argtypes = [cint, cint, i64, i64, i32p, i32p, i32p]
+    lib.mbd_launch_shape.restype = cint
     for fn in ("mbd_fused_add_rmsnorm", "mbd_fused_add_rmsnorm_quant_fp8", "mbd_swiglu", "mbd_swiglu_quant_fp8",
                "mbd_fused_allreduce_add_rmsnorm", "mbd_fused_allreduce_add_rmsnorm_quant_fp8",
                "mbd_fused_add_rmsnorm_quant_nvfp4", "mbd_swiglu_quant_nvfp4", "mbd_run_program",
@@ -332,3 +352,60 @@ def program_plan_build(ops) -> ProgramPlan:
 
 def program_plan_launch(plan: ProgramPlan, stream=None) -> None:
     plan.launch(stream)
+
+
+# ------------------------------------------------------------------------------------------------ tuning
+
+def tuning_set(entries) -> None:
+    """Install a launch-shape table (a list of TuningEntry or of dicts as in tuning files); [] clears it."""
+    rows = [e if isinstance(e, TuningEntry) else _entry_from_dict(e) for e in entries]
+    arr = (TuningEntry * max(1, len(rows)))(*rows)
+    _check(get_lib().mbd_tuning_set(arr if rows else None, len(rows)), "tuning_set")
+
+
+def launch_shape(kind, mode, n_tokens: int, width: int) -> tuple:
+    """(CTAs per row, vectors per thread, threads) a call would launch with now (table, else rules)."""
+    c, v, t = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    k = OP_KINDS[kind] if isinstance(kind, str) else int(kind)
+    _check(get_lib().mbd_launch_shape(k, MODES[mode or "static"], int(n_tokens), int(width), ctypes.byref(c),
+                                      ctypes.byref(v), ctypes.byref(t)), "launch_shape")
+    return c.value, v.value, t.value
+
+
+def tuning_get() -> list:
+    lib = get_lib()
+    n = lib.mbd_tuning_get(None, 0)
+    arr = (TuningEntry * max(1, n))()
+    n = lib.mbd_tuning_get(arr, n)
+    return [_entry_to_dict(arr[i]) for i in range(n)]
+
+
+def _entry_from_dict(d) -> TuningEntry:
+    return TuningEntry(OP_KINDS[d["kind"]], MODES[d.get("mode") or "static"], int(d["tokens"][0]), int(d["tokens"][1]),
+                       int(d["width"][0]), int(d["width"][1]), int(d["ctas_per_row"]), int(d["vectors_per_thread"]),
+                       int(d["threads"]), 0)
+
+
+def _entry_to_dict(e: TuningEntry) -> dict:
+    fp8 = e.kind in (1, 4)
+    return {"kind": OP_NAMES[e.kind], "mode": ("static", "dynamic")[e.mode] if fp8 else None,
+            "tokens": [e.tokens_min, e.tokens_max], "width": [e.width_min, e.width_max],
+            "ctas_per_row": e.ctas_per_row, "vectors_per_thread": e.vectors_per_thread, "threads": e.threads}
+
+
+def tuning_save(path: str, entries, meta: Optional[dict] = None) -> None:
+    import json
+    doc = dict(meta or {})
+    doc["entries"] = [e if isinstance(e, dict) else _entry_to_dict(e) for e in entries]
+    with open(path, "w") as f:
+        json.dump(doc, f, indent=1)
+        f.write("\n")
+
+
+def tuning_load(path: str) -> dict:
+    """Read a tuning file (written by memory_bound_decoder_gb300.tune) and install its table."""
+    import json
+    with open(path) as f:
+        doc = json.load(f)
+    tuning_set(doc["entries"])
+    return doc

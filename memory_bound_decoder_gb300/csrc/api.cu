@@ -5,6 +5,8 @@
 #include <cmath>
 #include <cstddef>
 #include <cstdint>
+#include <memory>
+#include <vector>
 
 #include "mbd.h"
 #include "launch.h"
@@ -50,8 +52,9 @@ int cdiv(int a, int b) { return (a + b - 1) / b; }
 // Launch shape, chosen from a sweep of CTAs per row x vectors per thread x threads on GB300 (back-to-back
 // launches; inputs larger than L2 for the large batches):
 //  - at least one row per SM (large batches):
-//      norm: one CTA per row while the row fits 512 threads x 4 vectors (hidden <= 16384), the fewest
-//            vectors per thread (>= 2) that keep the CTA at <= 512 threads -- no cluster exchange at all;
+//      norm: one CTA per row while the row fits 512 threads x 4 vectors (hidden <= 16384), 4 vectors per
+//            thread from 512 vectors per row up (the tuner: +6 to +22% at hidden 4096 to 8192 over 2 per
+//            thread), else the fewest (>= 2) that keep the CTA at <= 512 threads -- no cluster exchange;
 //      dynamic SwiGLU: rows cut into slices of about 576 vectors over a cluster of at most 7 CTAs,
 //            2 vectors per thread (clusters of 7 beat 8 at every width measured);
 //      streams: slices of <= 1024 vectors, <= 256 threads;
@@ -59,35 +62,64 @@ int cdiv(int a, int b) { return (a + b - 1) / b; }
 //            H 8192), the SwiGLU stream ~448-vector slices at 2 vectors per thread (76.8 vs 81.5 us at
 //            T 2048, I 53248; 80.7 vs 87.3 us at T 4096, I 28672);
 //      norm over partial activations: one vector per thread, ~128-vector slices over up to 8 CTAs.
-//  - fewer rows than SMs (decode): latency-bound. Rows that reduce are cut into slices of about 256
-//    (norm) or 288 (dynamic SwiGLU) vectors -- more CTAs per row only add exchange latency; streams are
-//    split until about two CTAs per SM pull bytes at once. At most 256 threads per CTA.
+//  - one to four rows per SM: the norm stays in one CTA with the fewest vectors per thread that fit 512
+//    threads (a cluster exchange costs +50% there), the bf16 and FP8 streams take ~256-vector slices (the
+//    tuner: +26 to +57% over the large-batch shapes at 256 tokens);
+//  - fewer rows than SMs (decode): latency-bound. Norm rows are cut into slices of about 256 vectors, the
+//    dynamic SwiGLU's into up to 8 slices of up to 512 threads at one vector each (the tuner: +12 to +49%
+//    at 4 to 64 tokens); bf16 and FP8 streams are split until about six CTAs per SM pull bytes at once,
+//    in slices of at least 64 vectors (+30 to +95% at 64 tokens over two CTAs per SM), NVFP4 streams until
+//    about two. At most 256 threads per CTA except the dynamic SwiGLU.
 // `pairs` (NVFP4): slices of an even number of vectors, so that every 16-element block lies in one CTA, in
 // neighbouring lanes.
 bool plan_rows(int64_t rows, int nvec, Shape shape, int sms, bool pairs, mbd::RowPlan* plan) {
     *plan = mbd::RowPlan{};
     const bool reduces = shape != Shape::kStream;
     const bool small = rows < sms;
+    const bool mid = !small && rows < 4 * int64_t{sms};   // one to four rows per SM
     int c;
+    int min_vpt = (shape == Shape::kStream || small) ? 1 : 2;
+    int max_threads = (shape == Shape::kStream || small) ? 256 : kMaxThreads;
     if (shape == Shape::kNorm) {
-        c = cdiv(nvec, small ? 256 : 2048);
+        if (small) {
+            c = cdiv(nvec, 256);
+        } else if (mid) {        // one CTA per row (no cluster), the fewest vectors per thread for <= 512 threads
+            c = cdiv(nvec, 2048);
+            min_vpt = 1;
+        } else {
+            c = cdiv(nvec, 2048);
+            if (pairs || nvec >= 512) min_vpt = 4;
+        }
     } else if (shape == Shape::kNormPartials) {   // one vector per thread (all partials' loads in flight)
         c = cdiv(nvec, small ? 256 : 128);         // small CTAs: 8 x 256 threads beat 4 x 512 at H 16384
     } else if (shape == Shape::kRowMax) {
-        c = cdiv(nvec, small ? 288 : 576);
-        if (c > 7) c = 7;
-    } else {
-        c = cdiv(nvec, pairs ? 448 : 1024);
+        if (small) {             // up to 8 CTAs of up to 512 threads, one vector each where the row allows
+            c = cdiv(nvec, 256);
+            if (c > 8) c = 8;
+            max_threads = kMaxThreads;
+        } else {
+            c = cdiv(nvec, 576);
+            if (c > 7) c = 7;
+        }
+    } else if (pairs) {
+        c = cdiv(nvec, 448);
         if (small) {
             int want = static_cast<int>((2 * sms + rows - 1) / rows);  // about two CTAs per SM
             const int by_width = cdiv(nvec, 32);                        // at least a warp of vectors per CTA
             if (want > by_width) want = by_width;
             if (want > c) c = want;
+        } else {
+            min_vpt = 2;
+        }
+    } else {
+        c = cdiv(nvec, mid ? 256 : 1024);
+        if (small) {
+            int want = static_cast<int>((6 * sms + rows - 1) / rows);  // about six CTAs per SM
+            const int by_width = cdiv(nvec, 64);                        // slices of at least 64 vectors
+            if (want > by_width) want = by_width;
+            if (want > c) c = want;
         }
     }
-    int min_vpt = (shape == Shape::kStream || small) ? 1 : 2;
-    if (pairs && !small) min_vpt = shape == Shape::kNorm ? 4 : 2;
-    const int max_threads = (shape == Shape::kStream || small) ? 256 : kMaxThreads;
     const int widest = (shape == Shape::kNormPartials ? 1 : 8) * kMaxThreads;  // vectors one CTA can take
     if (c < cdiv(nvec, widest)) c = cdiv(nvec, widest);
     if (reduces && c > kMaxClusterCtas) c = kMaxClusterCtas;
@@ -205,6 +237,64 @@ mbd_status norm_prepare(void* out, uint8_t* out_sf, mbd::Epilogue ep, void* resi
     return MBD_OK;
 }
 
+// ------------------------------------------------------------------------------------------ tuning table
+
+// The shape-bucket dispatch table (mbd_tuning_set): an immutable vector swapped in whole, so a call reads a
+// consistent table without locking while another thread replaces it.
+std::shared_ptr<const std::vector<mbd_tuning_entry>> g_tuning;
+
+std::shared_ptr<const std::vector<mbd_tuning_entry>> tuning_table() { return std::atomic_load(&g_tuning); }
+
+bool valid_kind_mode(int kind, int mode) {
+    if (kind < MBD_OP_ADD_RMSNORM || kind > MBD_OP_SWIGLU_QUANT_NVFP4) return false;
+    const bool fp8 = kind == MBD_OP_ADD_RMSNORM_QUANT_FP8 || kind == MBD_OP_SWIGLU_QUANT_FP8;
+    return !fp8 || mode == MBD_SCALE_STATIC_PER_TENSOR || mode == MBD_SCALE_DYNAMIC_PER_TOKEN;
+}
+
+// The launch shape of an entry, made concrete for one call, or false if it does not fit the call (then the
+// built-in rules decide). The same legality as the rules' shapes: at most 8 CTAs (one cluster) when the row
+// is reduced, slices covering the row, even slices for NVFP4.
+bool entry_plan(const mbd_tuning_entry& e, int64_t rows, int nvec, bool reduces, bool pairs, int sms,
+                mbd::RowPlan* plan) {
+    const int v = e.vectors_per_thread, th = e.threads;
+    if (e.ctas_per_row < 1 || (reduces && e.ctas_per_row > 8)) return false;
+    if (!(v == 1 || v == 2 || v == 4 || v == 8) || th < 32 || th > 512 || th % 32 != 0) return false;
+    int slice = cdiv(nvec, e.ctas_per_row);
+    if (pairs && (slice & 1)) ++slice;
+    const int c = cdiv(nvec, slice);
+    if (int64_t{th} * v < slice || rows > mbd::kMaxGridYZ * mbd::kMaxGridYZ) return false;
+    *plan = mbd::RowPlan{};
+    plan->ctas_per_row = c;
+    plan->slice = slice;
+    plan->threads = th;
+    plan->vpt = v;
+    plan->prefetch = rows < sms ? 1 : 0;
+    return true;
+}
+
+// The first table entry whose buckets hold the call and whose shape fits it.
+bool tuned_plan(int kind, int mode, int64_t rows, int64_t width, int nvec, bool reduces, bool pairs, int sms,
+                mbd::RowPlan* plan) {
+    const auto table = tuning_table();
+    if (!table) return false;
+    const bool fp8 = kind == MBD_OP_ADD_RMSNORM_QUANT_FP8 || kind == MBD_OP_SWIGLU_QUANT_FP8;
+    for (const mbd_tuning_entry& e : *table) {
+        if (e.kind != kind || (fp8 && e.mode != mode)) continue;
+        if (rows < e.tokens_min || rows > e.tokens_max || width < e.width_min || width > e.width_max) continue;
+        if (entry_plan(e, rows, nvec, reduces, pairs, sms, plan)) return true;
+    }
+    return false;
+}
+
+int norm_kind(mbd::Epilogue ep) {
+    return ep == mbd::kBf16 ? MBD_OP_ADD_RMSNORM
+                            : (ep == mbd::kNvfp4 ? MBD_OP_ADD_RMSNORM_QUANT_NVFP4 : MBD_OP_ADD_RMSNORM_QUANT_FP8);
+}
+int swiglu_kind(mbd::Epilogue ep) {
+    return ep == mbd::kBf16 ? MBD_OP_SWIGLU : (ep == mbd::kNvfp4 ? MBD_OP_SWIGLU_QUANT_NVFP4 : MBD_OP_SWIGLU_QUANT_FP8);
+}
+int scale_mode(mbd::Epilogue ep) { return ep == mbd::kFp8Dynamic ? MBD_SCALE_DYNAMIC_PER_TOKEN : MBD_SCALE_STATIC_PER_TENSOR; }
+
 mbd_status norm_common(void* out, uint8_t* out_sf, mbd::Epilogue ep, void* residual, const void* x,
                        const void* weight, int64_t n_tokens, int64_t hidden, float eps, float* scale,
                        cudaStream_t stream, const void* const* partials = nullptr, int n_partials = 0) {
@@ -213,8 +303,10 @@ mbd_status norm_common(void* out, uint8_t* out_sf, mbd::Epilogue ep, void* resid
         norm_prepare(out, out_sf, ep, residual, x, weight, n_tokens, hidden, eps, scale, partials, n_partials, &p);
     if (st != MBD_OK || p.rows == 0) return st;
     mbd::RowPlan plan;
-    if (!plan_rows(p.rows, p.nvec, partials ? Shape::kNormPartials : Shape::kNorm, sm_count_of_current_device(),
-                   ep == mbd::kNvfp4, &plan))
+    const int sms = sm_count_of_current_device();
+    const bool tuned = !partials && tuned_plan(norm_kind(ep), scale_mode(ep), p.rows, hidden, p.nvec, true,
+                                                ep == mbd::kNvfp4, sms, &plan);
+    if (!tuned && !plan_rows(p.rows, p.nvec, partials ? Shape::kNormPartials : Shape::kNorm, sms, ep == mbd::kNvfp4, &plan))
         return MBD_ERR_UNSUPPORTED;
     return finish_launch(mbd::launch_add_rmsnorm(p, ep, plan, stream));
 }
@@ -251,8 +343,11 @@ mbd_status swiglu_common(void* out, uint8_t* out_sf, mbd::Epilogue ep, const voi
     const mbd_status st = swiglu_prepare(out, out_sf, ep, gate_up, n_tokens, inter, scale, &p);
     if (st != MBD_OK || p.rows == 0) return st;
     mbd::RowPlan plan;
-    if (!plan_rows(p.rows, p.nvec, ep == mbd::kFp8Dynamic ? Shape::kRowMax : Shape::kStream,
-                   sm_count_of_current_device(), ep == mbd::kNvfp4, &plan))
+    const int sms = sm_count_of_current_device();
+    const bool tuned = tuned_plan(swiglu_kind(ep), scale_mode(ep), p.rows, inter, p.nvec, ep == mbd::kFp8Dynamic,
+                                  ep == mbd::kNvfp4, sms, &plan);
+    if (!tuned && !plan_rows(p.rows, p.nvec, ep == mbd::kFp8Dynamic ? Shape::kRowMax : Shape::kStream, sms,
+                             ep == mbd::kNvfp4, &plan))
         return MBD_ERR_UNSUPPORTED;
     return finish_launch(mbd::launch_swiglu(p, ep, plan, stream));
 }
@@ -673,6 +768,50 @@ mbd_status mbd_program_plan_build(const mbd_op* ops, int n_ops, mbd_program_plan
 
 mbd_status mbd_program_plan_launch(const mbd_program_plan* plan, mbd_stream_t stream) {
     return launch_plan(reinterpret_cast<const PlanImpl*>(plan), reinterpret_cast<cudaStream_t>(stream));
+}
+
+mbd_status mbd_tuning_set(const mbd_tuning_entry* entries, int n_entries) {
+    if (n_entries < 0 || n_entries > MBD_MAX_TUNING_ENTRIES || (n_entries > 0 && !entries)) return MBD_ERR_INVALID_ARG;
+    for (int i = 0; i < n_entries; ++i) {
+        const mbd_tuning_entry& e = entries[i];
+        const int v = e.vectors_per_thread;
+        if (!valid_kind_mode(e.kind, e.mode) || e.reserved != 0 || e.tokens_min < 0 || e.tokens_max < e.tokens_min ||
+            e.width_min < 0 || e.width_max < e.width_min || e.ctas_per_row < 1 || !(v == 1 || v == 2 || v == 4 || v == 8) ||
+            e.threads < 32 || e.threads > 512 || e.threads % 32 != 0)
+            return MBD_ERR_INVALID_ARG;
+    }
+    std::shared_ptr<const std::vector<mbd_tuning_entry>> t;
+    if (n_entries > 0) t = std::make_shared<const std::vector<mbd_tuning_entry>>(entries, entries + n_entries);
+    std::atomic_store(&g_tuning, t);
+    return MBD_OK;
+}
+
+mbd_status mbd_launch_shape(int kind, int mode, int64_t n_tokens, int64_t width, int32_t* ctas_per_row,
+                            int32_t* vectors_per_thread, int32_t* threads) {
+    if (!valid_kind_mode(kind, mode) || n_tokens <= 0 || width <= 0 || !ctas_per_row || !vectors_per_thread || !threads)
+        return MBD_ERR_INVALID_ARG;
+    const bool norm = kind <= MBD_OP_ADD_RMSNORM_QUANT_NVFP4;
+    const bool fp4 = kind == MBD_OP_ADD_RMSNORM_QUANT_NVFP4 || kind == MBD_OP_SWIGLU_QUANT_NVFP4;
+    const bool dyn_swiglu = kind == MBD_OP_SWIGLU_QUANT_FP8 && mode == MBD_SCALE_DYNAMIC_PER_TOKEN;
+    if (width % (fp4 ? 16 : 8) != 0) return MBD_ERR_MISALIGNED;
+    if ((norm || dyn_swiglu) && width > MBD_MAX_REDUCED_WIDTH) return MBD_ERR_UNSUPPORTED;
+    if (width > (int64_t{1} << 28)) return MBD_ERR_UNSUPPORTED;
+    const int nvec = static_cast<int>(width / 8), sms = sm_count_of_current_device();
+    mbd::RowPlan plan;
+    if (!tuned_plan(kind, mode, n_tokens, width, nvec, norm || dyn_swiglu, fp4, sms, &plan) &&
+        !plan_rows(n_tokens, nvec, norm ? Shape::kNorm : (dyn_swiglu ? Shape::kRowMax : Shape::kStream), sms, fp4, &plan))
+        return MBD_ERR_UNSUPPORTED;
+    *ctas_per_row = plan.ctas_per_row;
+    *vectors_per_thread = plan.vpt;
+    *threads = plan.threads;
+    return MBD_OK;
+}
+
+int mbd_tuning_get(mbd_tuning_entry* entries, int capacity) {
+    const auto table = tuning_table();
+    const int n = table ? static_cast<int>(table->size()) : 0;
+    for (int i = 0; entries && i < n && i < capacity; ++i) entries[i] = (*table)[i];
+    return n;
 }
 
 size_t mbd_program_schedule_bytes(void) { return kScheduleBytes; }

@@ -34,9 +34,9 @@ def test_binding_names_match_header():
 
 
 def test_version_and_status_strings(lib):
-    assert lib.mbd_abi_version() == 6
+    assert lib.mbd_abi_version() == 7
     hdr = open(mbd.HEADER_PATH).read()
-    assert int(re.search(r"#define MBD_ABI_VERSION (\d+)", hdr).group(1)) == 6
+    assert int(re.search(r"#define MBD_ABI_VERSION (\d+)", hdr).group(1)) == 7
     for code in range(5):
         assert lib.mbd_status_string(code).decode().startswith("MBD_")
     assert lib.mbd_status_string(99) == b"unknown mbd_status"
@@ -249,3 +249,56 @@ def test_program_static_launch_checks(lib):
     assert mbd.kernel_launches() == n0
     hdr = open(mbd.HEADER_PATH).read()
     assert int(re.search(r"#define MBD_STATIC_SCHEDULE_BYTES (\d+)", hdr).group(1)) >= mbd.program_schedule_bytes()
+
+
+def test_tuning_table_roundtrip_and_checks(lib, tmp_path):
+    mbd.tuning_set([])
+    assert mbd.tuning_get() == []
+    e1 = {"kind": "swiglu_quant_fp8", "mode": "dynamic", "tokens": [1024, 4096], "width": [53248, 53248],
+          "ctas_per_row": 7, "vectors_per_thread": 2, "threads": 480}
+    e2 = {"kind": "add_rmsnorm", "mode": None, "tokens": [0, 1 << 40], "width": [1, 1 << 20],
+          "ctas_per_row": 1, "vectors_per_thread": 4, "threads": 512}
+    mbd.tuning_set([e1, e2])
+    assert mbd.tuning_get() == [e1, e2]
+    path = str(tmp_path / "t.json")
+    mbd.tuning_save(path, [e1], {"device": "test"})
+    mbd.tuning_set([])
+    doc = mbd.tuning_load(path)
+    assert doc["device"] == "test" and mbd.tuning_get() == [e1]
+    bad = [dict(e1, threads=500), dict(e1, threads=1024), dict(e1, vectors_per_thread=3), dict(e1, ctas_per_row=0),
+           dict(e1, tokens=[5, 4]), dict(e1, width=[-1, 4])]
+    for b in bad:
+        with pytest.raises(mbd.MbdError) as e:
+            mbd.tuning_set([b])
+        assert e.value.status == mbd.ERR_INVALID_ARG
+    assert mbd.tuning_get() == [e1]                     # a rejected table leaves the old one in place
+    ent = mbd.TuningEntry(9, 0, 0, 1, 0, 1, 1, 1, 32, 0)
+    assert lib.mbd_tuning_set(ctypes.byref(ent), 1) == mbd.ERR_INVALID_ARG     # unknown kind
+    ent = mbd.TuningEntry(4, 5, 0, 1, 0, 1, 1, 1, 32, 0)
+    assert lib.mbd_tuning_set(ctypes.byref(ent), 1) == mbd.ERR_INVALID_ARG     # unknown FP8 mode
+    assert lib.mbd_tuning_set(None, 1) == mbd.ERR_INVALID_ARG
+    assert lib.mbd_tuning_set(None, -1) == mbd.ERR_INVALID_ARG
+    mbd.tuning_set([])
+
+
+def test_launch_shape_follows_table_then_rules(lib):
+    mbd.tuning_set([])
+    rules = mbd.launch_shape("swiglu_quant_fp8", "dynamic", 2048, 53248)
+    rules_1000 = mbd.launch_shape("swiglu_quant_fp8", "dynamic", 1000, 53248)
+    assert rules[0] <= 8 and rules[2] % 32 == 0
+    mbd.tuning_set([{"kind": "swiglu_quant_fp8", "mode": "dynamic", "tokens": [2000, 3000], "width": [53248, 53248],
+                     "ctas_per_row": 8, "vectors_per_thread": 4, "threads": 224}])
+    assert mbd.launch_shape("swiglu_quant_fp8", "dynamic", 2048, 53248) == (8, 4, 224)
+    assert mbd.launch_shape("swiglu_quant_fp8", "dynamic", 1000, 53248) == rules_1000      # outside the bucket
+    assert mbd.launch_shape("swiglu_quant_fp8", "static", 2048, 53248) != (8, 4, 224)       # other mode
+    # a shape that cannot cover the row (8 CTAs x 4 x 32 threads < 6656 vectors) falls back to the rules
+    mbd.tuning_set([{"kind": "swiglu_quant_fp8", "mode": "dynamic", "tokens": [1, 1 << 30], "width": [1, 1 << 30],
+                     "ctas_per_row": 8, "vectors_per_thread": 4, "threads": 32}])
+    assert mbd.launch_shape("swiglu_quant_fp8", "dynamic", 2048, 53248) == rules
+    # NVFP4 slices are rounded up to an even number of vectors
+    mbd.tuning_set([{"kind": "swiglu_quant_nvfp4", "mode": None, "tokens": [1, 1 << 30], "width": [1, 1 << 30],
+                     "ctas_per_row": 3, "vectors_per_thread": 1, "threads": 64}])
+    c, v, t = mbd.launch_shape("swiglu_quant_nvfp4", None, 4, 16 * 11)   # 22 vectors: slices of 8, 3 CTAs
+    assert (c, v, t) == (3, 1, 64)
+    mbd.tuning_set([])
+    assert lib.mbd_launch_shape(9, 0, 1, 64, None, None, None) == mbd.ERR_INVALID_ARG
