@@ -19,7 +19,8 @@ namespace mbd {
 namespace {
 
 template <int VPT, int EP>
-__global__ void __launch_bounds__(512, VPT <= 2 ? 4 : 1) swiglu_kernel(const __grid_constant__ SwigluParams p, int ctas_per_row, int slice, int prefetch) {
+__global__ void __launch_bounds__(512, VPT <= 2 ? 4 : 1) swiglu_kernel(const __grid_constant__ SwigluParams p, int ctas_per_row, int slice, int prefetch,
+                                                                   int ahead) {
     __shared__ SwigluSmem sm;
     const int64_t row = launch_row();
     if (row >= p.rows) return;   // past the last row (the whole cluster shares the row)
@@ -29,6 +30,9 @@ __global__ void __launch_bounds__(512, VPT <= 2 ? 4 : 1) swiglu_kernel(const __g
     pdl_trigger();
     if (prefetch) swiglu_prefetch<VPT>(p, row, begin, end);
     pdl_wait();
+    // The row a later wave will run here is fetched into L2 now, so that its loads meet L2 instead of HBM;
+    // the bytes come from HBM once either way (the rows in flight plus those ahead fit L2 many times over).
+    if (ahead > 0 && row + ahead < p.rows) swiglu_prefetch<VPT>(p, row + ahead, begin, end);
     swiglu_row_slice<VPT, EP>(p, row, rank, ctas_per_row, begin, end, sm);
 }
 
@@ -37,7 +41,7 @@ cudaError_t launch_ep(const SwigluParams& p, const RowPlan& plan, cudaStream_t s
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
     const int cluster = EP == kFp8Dynamic ? plan.ctas_per_row : 1;
-    void (*kern)(SwigluParams, int, int, int) = nullptr;
+    void (*kern)(SwigluParams, int, int, int, int) = nullptr;
     switch (plan.vpt) {
         case 1: kern = swiglu_kernel<1, EP>; break;
         case 2: kern = swiglu_kernel<2, EP>; break;
@@ -46,7 +50,7 @@ cudaError_t launch_ep(const SwigluParams& p, const RowPlan& plan, cudaStream_t s
         default: return cudaErrorInvalidValue;
     }
     fill_launch(cfg, attr, p.rows, plan.ctas_per_row, plan.threads, cluster, s);
-    return cudaLaunchKernelEx(&cfg, kern, p, plan.ctas_per_row, plan.slice, plan.prefetch);
+    return cudaLaunchKernelEx(&cfg, kern, p, plan.ctas_per_row, plan.slice, plan.prefetch, plan.ahead);
 }
 
 }  // namespace
