@@ -43,14 +43,16 @@ DEFAULT_WORKLOAD = "llama3.1-405b_fp8_T2048+ragged"
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel, from the ncu capture
 # summarised under profiles/; valid only while the CUDA sources hash to `csrc_sha256`.
 TRAFFIC: Dict[str, Dict] = {
+    # profiles/allreduce_rmsnorm_q8_static_k8_T2048_H16384.md
+    "allreduce_rmsnorm_q8_static_k8_T2048_H16384": {"bytes": 679861248, "csrc_sha256": "80360b8eb7ee41a4379fdd0e457e9b9170c5d4e7962f76ed5c1d41b22892bd80"},
     # profiles/add_rmsnorm_nvfp4_T2048_H16384.md
-    "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 166616064, "csrc_sha256": "300ffd8e7514eafd264ff7f3e83740b746e756e7516b0fbb43c994f1cd3a598e"},
+    "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 166748416, "csrc_sha256": "80360b8eb7ee41a4379fdd0e457e9b9170c5d4e7962f76ed5c1d41b22892bd80"},
     # profiles/swiglu_nvfp4_T2048_I53248.md
-    "swiglu_nvfp4_T2048_I53248": {"bytes": 468434688, "csrc_sha256": "c0ab45a98838c8ba65209886e452fae93c9f27647759ac2613f6204cf04e51ca"},
+    "swiglu_nvfp4_T2048_I53248": {"bytes": 467989760, "csrc_sha256": "80360b8eb7ee41a4379fdd0e457e9b9170c5d4e7962f76ed5c1d41b22892bd80"},
     # profiles/swiglu_q8_dynamic_T2048_I53248.md
-    "swiglu_q8_dynamic_T2048_I53248": {"bytes": 516052736, "csrc_sha256": "300ffd8e7514eafd264ff7f3e83740b746e756e7516b0fbb43c994f1cd3a598e"},
+    "swiglu_q8_dynamic_T2048_I53248": {"bytes": 502160128, "csrc_sha256": "80360b8eb7ee41a4379fdd0e457e9b9170c5d4e7962f76ed5c1d41b22892bd80"},
     # profiles/add_rmsnorm_q8_static_T2048_H16384.md
-    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 177788416, "csrc_sha256": "300ffd8e7514eafd264ff7f3e83740b746e756e7516b0fbb43c994f1cd3a598e"},
+    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 178054656, "csrc_sha256": "80360b8eb7ee41a4379fdd0e457e9b9170c5d4e7962f76ed5c1d41b22892bd80"},
 }
 
 
