@@ -44,15 +44,15 @@ DEFAULT_WORKLOAD = "llama3.1-405b_fp8_T2048+ragged"
 # summarised under profiles/; valid only while the CUDA sources hash to `csrc_sha256`.
 TRAFFIC: Dict[str, Dict] = {
     # profiles/allreduce_rmsnorm_q8_static_k8_T2048_H16384.md
-    "allreduce_rmsnorm_q8_static_k8_T2048_H16384": {"bytes": 679861248, "csrc_sha256": "80360b8eb7ee41a4379fdd0e457e9b9170c5d4e7962f76ed5c1d41b22892bd80"},
+    "allreduce_rmsnorm_q8_static_k8_T2048_H16384": {"bytes": 679770112, "csrc_sha256": "063107bdab08091bedcadf54f0401c0e8063fca17ed752db215c66f18d945b2f"},
     # profiles/add_rmsnorm_nvfp4_T2048_H16384.md
-    "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 166748416, "csrc_sha256": "80360b8eb7ee41a4379fdd0e457e9b9170c5d4e7962f76ed5c1d41b22892bd80"},
+    "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 166345216, "csrc_sha256": "063107bdab08091bedcadf54f0401c0e8063fca17ed752db215c66f18d945b2f"},
     # profiles/swiglu_nvfp4_T2048_I53248.md
-    "swiglu_nvfp4_T2048_I53248": {"bytes": 467989760, "csrc_sha256": "80360b8eb7ee41a4379fdd0e457e9b9170c5d4e7962f76ed5c1d41b22892bd80"},
+    "swiglu_nvfp4_T2048_I53248": {"bytes": 467542528, "csrc_sha256": "063107bdab08091bedcadf54f0401c0e8063fca17ed752db215c66f18d945b2f"},
     # profiles/swiglu_q8_dynamic_T2048_I53248.md
-    "swiglu_q8_dynamic_T2048_I53248": {"bytes": 502160128, "csrc_sha256": "80360b8eb7ee41a4379fdd0e457e9b9170c5d4e7962f76ed5c1d41b22892bd80"},
+    "swiglu_q8_dynamic_T2048_I53248": {"bytes": 497629184, "csrc_sha256": "063107bdab08091bedcadf54f0401c0e8063fca17ed752db215c66f18d945b2f"},
     # profiles/add_rmsnorm_q8_static_T2048_H16384.md
-    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 178054656, "csrc_sha256": "80360b8eb7ee41a4379fdd0e457e9b9170c5d4e7962f76ed5c1d41b22892bd80"},
+    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 178528000, "csrc_sha256": "063107bdab08091bedcadf54f0401c0e8063fca17ed752db215c66f18d945b2f"},
 }
 
 

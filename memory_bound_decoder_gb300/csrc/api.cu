@@ -55,8 +55,10 @@ int cdiv(int a, int b) { return (a + b - 1) / b; }
 //      norm: one CTA per row while the row fits 512 threads x 4 vectors (hidden <= 16384), 4 vectors per
 //            thread from 512 vectors per row up (the tuner: +6 to +22% at hidden 4096 to 8192 over 2 per
 //            thread), else the fewest (>= 2) that keep the CTA at <= 512 threads -- no cluster exchange;
-//      dynamic SwiGLU: rows cut into slices of about 576 vectors over a cluster of at most 7 CTAs,
-//            2 vectors per thread (clusters of 7 beat 8 at every width measured);
+//      dynamic SwiGLU: rows cut into slices of about 576 vectors over a cluster of at most 8 CTAs,
+//            2 vectors per thread (with the wave-ahead L2 warming, 8 x 416 threads beat 7 x 480 by 4 to
+//            6% at I 53248 and 1024 to 4096 tokens; at one to four rows per SM, where no warming runs,
+//            clusters of 7 stay ahead);
 //      streams: slices of <= 1024 vectors, <= 256 threads;
 //      NVFP4 (more work per vector): the norm takes 4 vectors per thread (34.6 vs 43.0 us at T 4096,
 //            H 8192), the SwiGLU stream ~448-vector slices at 2 vectors per thread (76.8 vs 81.5 us at
@@ -97,9 +99,10 @@ bool plan_rows(int64_t rows, int nvec, Shape shape, int sms, bool pairs, mbd::Ro
             c = cdiv(nvec, 256);
             if (c > 8) c = 8;
             max_threads = kMaxThreads;
-        } else {
+        } else {                 // clusters of up to 7 CTAs, 8 where the wave-ahead warming runs (below)
             c = cdiv(nvec, 576);
-            if (c > 7) c = 7;
+            const int cap = mid ? 7 : 8;
+            if (c > cap) c = cap;
         }
     } else if (pairs) {
         c = cdiv(nvec, 448);
@@ -144,8 +147,10 @@ bool plan_rows(int64_t rows, int nvec, Shape shape, int sms, bool pairs, mbd::Ro
     plan->vpt = vpt;
     plan->prefetch = small ? 1 : 0;
     // Large dynamic-SwiGLU launches: warm L2 half a wave ahead (the rows resident at once: SMs x CTAs per SM,
-    // by threads at the <= 32 registers of 1-2 vectors per thread, over the CTAs per row). 89 vs 97 us at
-    // T 4096, I 28672; neutral at I 53248; no gain for the norms.
+    // by threads at the <= 32 registers of 1-2 vectors per thread, over the CTAs per row), one bulk prefetch
+    // per slice: 87.1 vs 99.6 us without at T 2048, I 53248 (8 x 416 threads; 91.6 with per-vector
+    // prefetches), 84.7 vs 92.6 at T 4096, I 28672; a quarter or twice the distance is no better. No gain
+    // for the norms.
     if (shape == Shape::kRowMax && !small && !mid && vpt <= 2)
         plan->ahead = static_cast<int>(int64_t{sms} * (2048 / threads) / c / 2);
     return rows <= mbd::kMaxGridYZ * mbd::kMaxGridYZ;

@@ -301,6 +301,13 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // at once and the prefetch would just double their L2 requests.
 __device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 
+// Warm L2 with `bytes` contiguous bytes through the bulk-copy engine: one instruction for a whole slice, so
+// the issuing thread is free at once and no other thread spends issue slots on it. `p` 16-byte aligned,
+// `bytes` a multiple of 16 (every row slice of 16-byte vectors is both).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ------------------------------------------------------------------------------------------ double-float
 
 // An unevaluated sum hi + lo of two fp32 values (about 48 significant bits), built with Knuth's TwoSum.

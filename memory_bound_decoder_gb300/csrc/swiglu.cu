@@ -32,7 +32,13 @@ __global__ void __launch_bounds__(512, VPT <= 2 ? 4 : 1) swiglu_kernel(const __g
     pdl_wait();
     // The row a later wave will run here is fetched into L2 now, so that its loads meet L2 instead of HBM;
     // the bytes come from HBM once either way (the rows in flight plus those ahead fit L2 many times over).
-    if (ahead > 0 && row + ahead < p.rows) swiglu_prefetch<VPT>(p, row + ahead, begin, end);
+    // Two bulk prefetches (gate and up slices) from one thread.
+    if (ahead > 0 && row + ahead < p.rows && threadIdx.x == 0) {
+        const uint4* gr = static_cast<const uint4*>(p.gate_up) + (row + ahead) * (int64_t)p.nvec * 2 + begin;
+        const uint32_t bytes = static_cast<uint32_t>(end - begin) * 16u;
+        prefetch_l2_bulk(gr, bytes);
+        prefetch_l2_bulk(gr + p.nvec, bytes);
+    }
     swiglu_row_slice<VPT, EP>(p, row, rank, ctas_per_row, begin, end, sm);
 }
 
