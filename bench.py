@@ -41,18 +41,19 @@ FALLBACK_HBM_GBS = 6800.0
 DEFAULT_WORKLOAD = "llama3.1-405b_fp8_T2048+ragged"
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel, from the ncu capture
-# summarised under profiles/; valid only while the CUDA sources hash to `csrc_sha256`.
+# summarised under profiles/; valid only while what the kernel and its launch shape are built from hashes to
+# `src_sha256` (kernel_src_hash).
 TRAFFIC: Dict[str, Dict] = {
     # profiles/allreduce_rmsnorm_q8_static_k8_T2048_H16384.md
-    "allreduce_rmsnorm_q8_static_k8_T2048_H16384": {"bytes": 679770112, "csrc_sha256": "063107bdab08091bedcadf54f0401c0e8063fca17ed752db215c66f18d945b2f"},
+    "allreduce_rmsnorm_q8_static_k8_T2048_H16384": {"bytes": 679770112, "src_sha256": "e0ea6230b4b5821fcb66b899153cbb74f4b8cb84c574cc7fe65466fa4e699636"},
     # profiles/add_rmsnorm_nvfp4_T2048_H16384.md
-    "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 166345216, "csrc_sha256": "063107bdab08091bedcadf54f0401c0e8063fca17ed752db215c66f18d945b2f"},
+    "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 166345216, "src_sha256": "e0ea6230b4b5821fcb66b899153cbb74f4b8cb84c574cc7fe65466fa4e699636"},
     # profiles/swiglu_nvfp4_T2048_I53248.md
-    "swiglu_nvfp4_T2048_I53248": {"bytes": 467542528, "csrc_sha256": "063107bdab08091bedcadf54f0401c0e8063fca17ed752db215c66f18d945b2f"},
+    "swiglu_nvfp4_T2048_I53248": {"bytes": 467542528, "src_sha256": "1e3f448bd1a38d50292063c6d1052b4436f904835087e89073259f3a23f8117c"},
     # profiles/swiglu_q8_dynamic_T2048_I53248.md
-    "swiglu_q8_dynamic_T2048_I53248": {"bytes": 497629184, "csrc_sha256": "063107bdab08091bedcadf54f0401c0e8063fca17ed752db215c66f18d945b2f"},
+    "swiglu_q8_dynamic_T2048_I53248": {"bytes": 497629184, "src_sha256": "1e3f448bd1a38d50292063c6d1052b4436f904835087e89073259f3a23f8117c"},
     # profiles/add_rmsnorm_q8_static_T2048_H16384.md
-    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 178528000, "csrc_sha256": "063107bdab08091bedcadf54f0401c0e8063fca17ed752db215c66f18d945b2f"},
+    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 178528000, "src_sha256": "e0ea6230b4b5821fcb66b899153cbb74f4b8cb84c574cc7fe65466fa4e699636"},
 }
 
 
@@ -82,6 +83,23 @@ def csrc_hash() -> str:
     for f in sorted(os.listdir(d)):
         with open(os.path.join(d, f), "rb") as fh:
             h.update(f.encode() + fh.read())
+    return h.hexdigest()
+
+
+def kernel_src_hash(call) -> str:
+    """sha256 over what one call's kernel and its launch shape are built from: the C-ABI header, the shared
+    device headers, the planner (api.cu), the kernel's translation unit and inline body, and the packaged
+    launch-shape tables. Unchanged when only other kernels' sources change."""
+    csrc = os.path.join(ROOT, "memory_bound_decoder_gb300", "csrc")
+    own = ["swiglu.cu", "swiglu_impl.cuh"] if call.kind.startswith("swiglu") else ["norm.cu", "norm_impl.cuh"]
+    paths = [os.path.join(ROOT, "include", "mbd.h")] + [os.path.join(csrc, f) for f in
+                                                         ["common.cuh", "launch.h", "api.cu"] + own]
+    tdir = os.path.join(ROOT, "memory_bound_decoder_gb300", "tuning")
+    paths += sorted(os.path.join(tdir, f) for f in os.listdir(tdir) if f.endswith(".json"))
+    h = hashlib.sha256()
+    for p in paths:
+        with open(p, "rb") as fh:
+            h.update(os.path.basename(p).encode() + fh.read())
     return h.hexdigest()
 
 
@@ -406,6 +424,97 @@ class DeviceCall:
         return sum(t.numel() * t.element_size() for t, _ in self.d2h)
 
 
+# Program variants of the library (the epilogue sets one persistent program kernel is compiled for), by call kind
+# and FP8 mode: a program holds ops of one variant only.
+PROGRAM_VARIANT = {("add_rmsnorm", None): "bf16", ("swiglu", None): "bf16",
+                   ("add_rmsnorm_q8", "static"): "fp8", ("swiglu_q8", "dynamic"): "fp8",
+                   ("add_rmsnorm_nvfp4", None): "nvfp4", ("swiglu_nvfp4", None): "nvfp4"}
+PROGRAM_MAX_NORM_WIDTH = 8192   # MBD_MAX_PROGRAM_WIDTH
+
+
+class GroupCall:
+    """The calls of one program launch, seen as one call (name, token count, algorithmic bytes)."""
+
+    def __init__(self, variant: str, calls: List[wl.Call]):
+        self.calls = calls
+        self.kind, self.mode = "program", None
+        self.name = f"program_{variant}_{len(calls)}ops_T" + "+".join(str(c.T) for c in calls)
+        self.T = sum(c.T for c in calls)
+
+    def algorithmic_bytes(self) -> int:
+        return sum(c.algorithmic_bytes() for c in self.calls)
+
+
+class ProgramGroup:
+    """Calls of one step run as ONE launch of the library's persistent program kernel: the plan is built once,
+    its schedule uploaded once to device memory, and every step launches it with one pointer
+    (mbd_program_plan_launch_uploaded). Same buffers, same outputs as the calls' own launches."""
+
+    def __init__(self, torch, mbd, variant: str, members: List[DeviceCall], dev):
+        self.members, self.mbd = members, mbd
+        self.call = GroupCall(variant, [d.call for d in members])
+        self.plan = mbd.program_plan_build([d.op() for d in members])
+        self.sched = torch.empty(mbd.program_schedule_bytes(), dtype=torch.uint8, device=dev)
+        self.h2d = [x for d in members for x in d.h2d]
+        self.d2h = [x for d in members for x in d.d2h]
+        self.handle = None
+
+    def bind(self, stream_handle: int):
+        for d in self.members:
+            d.bind(stream_handle)
+        self.handle = stream_handle
+        self.plan.upload(self.sched, stream_handle)
+
+    def launch(self):
+        lib = self.mbd.get_lib()
+        rc = lib.mbd_program_plan_launch_uploaded(ctypes.addressof(self.plan.buf), self.sched.data_ptr(), self.handle)
+        if rc != 0:
+            raise RuntimeError(f"{self.call.name}: {lib.mbd_status_string(rc).decode()}")
+
+    def bytes_in(self):
+        return sum(t.numel() * t.element_size() for t, _ in self.h2d)
+
+    def bytes_out(self):
+        return sum(t.numel() * t.element_size() for t, _ in self.d2h)
+
+
+def launch_groups(calls: List[wl.Call], layers: int, sms: int, max_ops: int = 128) -> list:
+    """Launch units of one step, in order: an int (the index of a call launched on its own) or (variant, [indices])
+    (calls run as one program launch). Calls with fewer tokens than the GPU has SMs are bound by launch latency,
+    not bandwidth; those a program takes are gathered, per program variant, into one program launch placed where
+    the first of them stood (at most max_ops per launch). Only in one-layer steps, whose calls share no buffer,
+    so that running them together computes exactly what the sequence of launches does."""
+    if layers != 1:
+        return list(range(len(calls)))
+    groups: Dict[str, List[int]] = {}
+    order: list = []
+    for i, c in enumerate(calls):
+        v = PROGRAM_VARIANT.get((c.kind, c.mode if c.kind.endswith("q8") else None))
+        small = c.T < sms and not (c.kind.startswith("add") and c.width > PROGRAM_MAX_NORM_WIDTH)
+        if v is None or not small:
+            order.append(i)
+            continue
+        if v not in groups:
+            groups[v] = []
+            order.append(v)
+        groups[v].append(i)
+    units: list = []
+    for u in order:
+        if isinstance(u, str):
+            idx = groups[u]
+            units += [(u, idx[k:k + max_ops]) for k in range(0, len(idx), max_ops)]
+        else:
+            units.append(u)
+    return units
+
+
+def group_small_calls(torch, mbd, work: wl.Workload, dcalls: List[DeviceCall], sms: int, dev) -> list:
+    """The step's launch units (launch_groups): DeviceCalls and ProgramGroups."""
+    units = launch_groups([d.call for d in dcalls], work.layers, sms, mbd.MAX_PROGRAM_OPS)
+    return [dcalls[u] if isinstance(u, int) else ProgramGroup(torch, mbd, u[0], [dcalls[i] for i in u[1]], dev)
+            for u in units]
+
+
 def run_e2e(torch, dcalls: List[DeviceCall], kstream, dev, steps: int, step_bytes: int, world: int) -> Dict:
     """Time `steps` steps from pinned host memory to pinned host memory through the same C-ABI launches:
     a three-stage pipeline (H2D copy stream -> the kernel stream -> D2H copy stream) with per-call events,
@@ -633,7 +742,11 @@ def run_mine(args, work: wl.Workload, rank: int, world: int, local_rank: int) ->
 
     t_gen = time.perf_counter()
     dcalls = build_device_calls(torch, mbd, work, args.seed, rank, dev)
-    log(f"[bench] rank {rank}: inputs for {len(dcalls)} launches ready in {time.perf_counter() - t_gen:.1f}s")
+    n_calls = len(dcalls)
+    if not args.no_programs:
+        dcalls = group_small_calls(torch, mbd, work, dcalls, props.multi_processor_count, dev)
+    log(f"[bench] rank {rank}: inputs for {n_calls} calls in {len(dcalls)} launches ready in "
+        f"{time.perf_counter() - t_gen:.1f}s")
 
     stream = torch.cuda.Stream(device=dev)
     handle = int(stream.cuda_stream)
@@ -713,7 +826,7 @@ def run_mine(args, work: wl.Workload, rank: int, world: int, local_rank: int) ->
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
     kname = f"{dcall.call.kind}{'_' + dcall.call.mode if dcall.call.mode else ''}"
     tr = TRAFFIC.get(dcall.call.name)
-    traffic = tr["bytes"] if tr and tr.get("csrc_sha256") == csrc_hash() else None
+    traffic = tr["bytes"] if tr and tr.get("src_sha256") == kernel_src_hash(dcall.call) else None
     kernels = []
     seen = set()
     for i, d in enumerate(dcalls):
@@ -739,7 +852,11 @@ def run_mine(args, work: wl.Workload, rank: int, world: int, local_rank: int) ->
                    "l2": f"inputs larger than L2: {step_bytes / 2 ** 20:.0f} MiB of distinct buffers per step "
                          f"vs {l2_bytes / 2 ** 20:.0f} MiB L2, no flush",
                    "parallelism": f"replicas x{world} (rows are independent; no collective)",
-                   "launch_shapes": f"tuning table {os.path.relpath(tuning, ROOT)}" if tuning else "built-in rules"},
+                   "launch_shapes": f"tuning table {os.path.relpath(tuning, ROOT)}" if tuning else "built-in rules",
+                   "launch_units": [d.call.name for d in dcalls],
+                   "small_calls": ("one program launch per program variant for the calls with fewer tokens than "
+                                   "SMs (--no-programs: one launch per call)"
+                                   if any(isinstance(d, ProgramGroup) for d in dcalls) else "one launch per call")},
         "tokens_per_s": round(tokens * args.steps * world / (elapsed_ms / 1e3), 1),
         "gpu_launches": int(launches),
         "roofline": {"bound": "hbm", "kernel": dcall.call.name, "achieved": round(achieved, 1),
@@ -767,6 +884,9 @@ def main():
     ap.add_argument("--calls", default="", help="comma-separated call names: run only these calls of the workload")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-programs", action="store_true",
+                    help="launch every call on its own (default: the calls with fewer tokens than SMs of a one-layer "
+                         "step run as one program launch per program variant)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=1.0, help="target wall time of the oracle sample")

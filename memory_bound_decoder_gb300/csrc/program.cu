@@ -83,7 +83,9 @@ __device__ __forceinline__ void run_swiglu_dynamic_row(const ProgOp& op, int64_t
     if constexpr ((SM & bit(kFp8Dynamic)) != 0) {
         if (op.nvec <= chunk_vecs) return run_swiglu_part<V, SM>(op, row, 0, op.nvec, sm);
         SwigluParams sp{op.in, op.out, op.scale, op.rows, op.nvec, op.out_sf};
-        swiglu_dynamic_two_pass<1>(sp, row, sm.swiglu);   // one vector per thread per step: few registers
+        // V = 4 (one CTA per SM, registers to spare): 4 vectors per thread in flight per step; else one (few
+        // registers at 2 to 4 CTAs per SM)
+        swiglu_dynamic_two_pass<(V >= 4 ? 4 : 1)>(sp, row, sm.swiglu);
     }
 }
 
@@ -234,10 +236,11 @@ __device__ void run_free_item(const ProgramParams& P, int64_t item, int& f, Prog
 }
 
 // Resident CTAs per SM each variant is compiled for (the register cap): the most that leaves it without
-// spills, from ptxas -v (40 to 128 registers; the FP8 variant at 4 vectors per thread keeps a small spill
-// at the 128-register limit).
+// large spills, from ptxas -v (40 to 255 registers; a few variants keep spills of under 200 bytes). The FP8 variant at 4 vectors per thread takes the whole
+// register file at one CTA per SM: capped at 128 registers for two it spilled 1 to 2.6 KB per thread, and
+// its programs ran 1.6x (8 layers at 64 tokens) to 3.9x (at 256 tokens) slower than at one.
 constexpr int min_ctas(int v, int nm, int sm) {
-    return sm == bit(kFp8Dynamic) ? (v == 1 ? 4 : 2)   // the dynamic SwiGLU's two-pass form adds registers
+    return sm == bit(kFp8Dynamic) ? (v == 1 ? 4 : (v == 2 ? 2 : 1))   // the dynamic SwiGLU's two-pass form adds registers
                                   : (v == 1 ? ((nm == bit(kBf16) && sm == bit(kBf16)) ? 6 : 5) : (v == 2 ? 3 : 2));
 }
 

@@ -1,0 +1,65 @@
+"""The bench's grouped step computes what its per-call step computes: the small ragged calls of the default
+step, launched one by one and as one program launch per program variant, from identical seeded inputs.
+Residuals and dynamic scales bit-identical; a norm row reduced inside one CTA (program) may sum in another
+order than one split over a cluster (single call), so bf16 outputs may differ by one ulp and static-FP8
+codes by one step, rarely."""
+import numpy as np
+import pytest
+
+import bench
+import workloads as wl
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from memory_bound_decoder_gb300 import build
+    build.build()
+    import memory_bound_decoder_gb300 as mbd
+    mbd.get_lib()
+
+
+def _run(work, grouped):
+    import memory_bound_decoder_gb300 as mbd
+    dev = torch.device("cuda", 0)
+    dcalls = bench.build_device_calls(torch, mbd, work, 0, 0, dev)
+    units = bench.group_small_calls(torch, mbd, work, dcalls, 152, dev) if grouped else list(dcalls)
+    handle = int(torch.cuda.current_stream().cuda_stream)
+    for u in units:
+        u.bind(handle)
+    mbd.device_error_flags(clear=True)
+    n0 = mbd.kernel_launches()
+    for u in units:
+        u.launch()
+    torch.cuda.synchronize()
+    assert mbd.kernel_launches() - n0 == len(units)
+    assert mbd.device_error_flags() == 0
+    outs = [(d.call, {k: getattr(d, k).cpu().numpy().copy() for k in ("out", "res", "scale") if hasattr(d, k)})
+            for d in dcalls]
+    return len(units), outs
+
+
+def test_grouped_small_calls_match_per_call_launches():
+    w = bench.workloads_by_key()[bench.DEFAULT_WORKLOAD]
+    work = wl.Workload("small", "the small calls of the default step", tuple(c for c in w.calls if c.T < 152), 1)
+    n_calls, ref = _run(work, grouped=False)
+    n_units, got = _run(work, grouped=True)
+    assert n_calls == 12 and n_units == 2
+    for (call, a), (_, b) in zip(ref, got):
+        if "res" in a:
+            np.testing.assert_array_equal(a["res"], b["res"], f"{call.name}: residual")
+        if call.mode == "dynamic":
+            np.testing.assert_array_equal(a["scale"], b["scale"], f"{call.name}: dynamic scales")
+        if call.kind in ("add_rmsnorm", "swiglu"):
+            d = np.abs(a["out"].astype(np.int32) - b["out"].astype(np.int32))
+            assert d.max() <= 1, f"{call.name}: bf16 outputs differ by more than one ulp"
+        else:
+            x, y = a["out"].astype(np.int32), b["out"].astype(np.int32)
+            diff = x != y
+            assert diff.mean() <= 1e-3, f"{call.name}: {diff.sum()} codes differ"
+            assert ((x[diff] & 0x80) == (y[diff] & 0x80)).all(), f"{call.name}: sign flipped"
+            assert (np.abs((x[diff] & 0x7F) - (y[diff] & 0x7F)) == 1).all(), f"{call.name}: more than one step"

@@ -1,0 +1,54 @@
+"""Host logic of the bench's launch units: which calls of a step run as one program launch (no GPU)."""
+import bench
+import workloads as wl
+
+
+def _names(calls, units):
+    return [calls[u].name if isinstance(u, int) else (u[0], [calls[i].name for i in u[1]]) for u in units]
+
+
+def test_default_step_groups_the_small_calls_by_variant():
+    w = bench.workloads_by_key()[bench.DEFAULT_WORKLOAD]
+    calls = list(w.calls)
+    units = bench.launch_groups(calls, w.layers, 152)
+    # the batches of at least one row per SM keep their own launches, in place
+    singles = [u for u in units if isinstance(u, int)]
+    assert all(calls[i].T >= 152 for i in singles)
+    groups = [u for u in units if not isinstance(u, int)]
+    assert [g[0] for g in groups] == ["bf16", "fp8"]
+    small = [i for i, c in enumerate(calls) if c.T < 152]
+    assert sorted(i for g in groups for i in g[1]) == small          # every small call, exactly once
+    want = {"bf16": {("add_rmsnorm", None), ("swiglu", None)},
+            "fp8": {("add_rmsnorm_q8", "static"), ("swiglu_q8", "dynamic")}}
+    for v, idx in groups:
+        assert {(calls[i].kind, calls[i].mode) for i in idx} == want[v]
+        assert idx == sorted(idx)                                     # list order kept inside a program
+    # a group sits where its first call stood
+    flat = [u if isinstance(u, int) else u[1][0] for u in units]
+    assert flat == sorted(flat)
+
+
+def test_fp8_variant_takes_static_norms_and_dynamic_swiglu_only():
+    d = wl.N01
+    calls = [wl.Call("add_rmsnorm_q8", 4, 1024, d, mode="static"), wl.Call("add_rmsnorm_q8", 4, 1024, d, mode="dynamic"),
+             wl.Call("swiglu_q8", 4, 1024, d, mode="dynamic"), wl.Call("swiglu_q8", 4, 1024, d, mode="static")]
+    units = bench.launch_groups(calls, 1, 152)
+    assert units == [("fp8", [0, 2]), 1, 3]
+
+
+def test_no_grouping_across_layers_wide_norms_or_allreduce():
+    d = wl.N01
+    calls = [wl.Call("add_rmsnorm", 1, 1536, d), wl.Call("swiglu", 1, 8960, d)]
+    assert bench.launch_groups(calls, 28, 152) == [0, 1]              # layers share a residual: keep the sequence
+    wide = [wl.Call("add_rmsnorm", 1, 16384, d), wl.Call("swiglu", 1, 53248, d)]
+    assert bench.launch_groups(wide, 1, 152) == [0, ("bf16", [1])]    # the program holds norms up to 8192 wide
+    ar = [wl.Call("allreduce_rmsnorm", 2, 4096, d, partials=2), wl.Call("add_rmsnorm", 2, 4096, d)]
+    assert bench.launch_groups(ar, 1, 152) == [0, ("bf16", [1])]
+    assert bench.launch_groups(calls, 1, 1) == [0, 1]                 # nothing below one row per SM
+
+
+def test_groups_split_at_the_op_limit():
+    d = wl.N01
+    calls = [wl.Call("swiglu", 1 + i, 256, d) for i in range(10)]
+    units = bench.launch_groups(calls, 1, 152, max_ops=4)
+    assert units == [("bf16", [0, 1, 2, 3]), ("bf16", [4, 5, 6, 7]), ("bf16", [8, 9])]
