@@ -77,15 +77,6 @@ def decode_sweep_workload() -> wl.Workload:
                        tuple(calls), layers=28)
 
 
-def csrc_hash() -> str:
-    d = os.path.join(ROOT, "memory_bound_decoder_gb300", "csrc")
-    h = hashlib.sha256()
-    for f in sorted(os.listdir(d)):
-        with open(os.path.join(d, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
-    return h.hexdigest()
-
-
 def kernel_src_hash(call) -> str:
     """sha256 over what one call's kernel and its launch shape are built from: the C-ABI header, the shared
     device headers, the planner (api.cu), the kernel's translation unit and inline body, and the packaged
