@@ -108,6 +108,12 @@ def test_decode_sizes(T):
     check_swiglu(wl.make_swiglu_inputs(T, 8960, seed=T, dist=wl.N01), 0.01)
 
 
+def test_more_rows_than_one_grid_axis():
+    """70001 rows over the grid's y and z axes (rows past 65535 in the second z plane); every row compared."""
+    check_norm(wl.make_norm_inputs(70001, 64, seed=9, dist=wl.C5_ACT, eps=1e-5), wl.NVFP4_SCALE_NORM_C5)
+    check_swiglu(wl.make_swiglu_inputs(70001, 64, seed=9, dist=wl.C5_ACT), wl.NVFP4_SCALE_SWIGLU_C5)
+
+
 def test_sign_and_zero_codes():
     """Zero rows give zero block scales and all-zero codes; negative values keep their sign bit."""
     T, H = 3, 256

@@ -195,6 +195,15 @@ def test_ragged_405b_tails(T):
 
 # ------------------------------------------------------------------------------------------------ edge cases
 
+@pytest.mark.parametrize("ep,mode", [("bf16", None), ("q8", "static"), ("q8", "dynamic")])
+def test_more_rows_than_one_grid_axis(ep, mode):
+    """70001 rows: the launch lays rows over the grid's y and z axes (at most 65535 each), so rows past 65535
+    sit in the second z plane. Every row is compared."""
+    T = 70001
+    check_norm(wl.make_norm_inputs(T, 64, seed=9, dist=wl.C5_ACT, eps=1e-5), ep, mode, static_scale=0.05)
+    check_swiglu(wl.make_swiglu_inputs(T, 64, seed=9, dist=wl.C3_GU), ep, mode, static_scale=0.05)
+
+
 def test_zero_rows_and_constant_rows():
     T, H = 4, 2048
     x = np.zeros((T, H), np.uint16)
