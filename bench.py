@@ -417,9 +417,12 @@ class DeviceCall:
 
 # Program variants of the library (the epilogue sets one persistent program kernel is compiled for), by call kind
 # and FP8 mode: a program holds ops of one variant only.
-PROGRAM_VARIANT = {("add_rmsnorm", None): "bf16", ("swiglu", None): "bf16",
-                   ("add_rmsnorm_q8", "static"): "fp8", ("swiglu_q8", "dynamic"): "fp8",
-                   ("add_rmsnorm_nvfp4", None): "nvfp4", ("swiglu_nvfp4", None): "nvfp4"}
+# Epilogue class of each call kind a program can run: "bf16" and "fp8" calls may share one launch (the
+# library's mixed bf16 + FP8 program variant; a static-FP8 SwiGLU runs only there), "nvfp4" calls have their
+# own variant. A dynamic-FP8 norm runs in no program.
+PROGRAM_CLASS = {("add_rmsnorm", None): "bf16", ("swiglu", None): "bf16",
+                 ("add_rmsnorm_q8", "static"): "fp8", ("swiglu_q8", "dynamic"): "fp8", ("swiglu_q8", "static"): "fp8",
+                 ("add_rmsnorm_nvfp4", None): "nvfp4", ("swiglu_nvfp4", None): "nvfp4"}
 PROGRAM_MAX_NORM_WIDTH = 8192   # MBD_MAX_PROGRAM_WIDTH
 
 
@@ -470,30 +473,39 @@ class ProgramGroup:
 
 
 def launch_groups(calls: List[wl.Call], layers: int, sms: int, max_ops: int = 128) -> list:
-    """Launch units of one step, in order: an int (the index of a call launched on its own) or (variant, [indices])
+    """Launch units of one step, in order: an int (the index of a call launched on its own) or (label, [indices])
     (calls run as one program launch). Calls with fewer tokens than the GPU has SMs are bound by launch latency,
-    not bandwidth; those a program takes are gathered, per program variant, into one program launch placed where
-    the first of them stood (at most max_ops per launch). Only in one-layer steps, whose calls share no buffer,
-    so that running them together computes exactly what the sequence of launches does."""
+    not bandwidth; those a program takes are gathered into one program launch placed where the first of them
+    stood (at most max_ops per launch): the bf16 and FP8 ones together when all their rows fit one row per SM
+    (one wave of the mixed variant, which runs at one CTA per SM), else one launch per class; NVFP4 ones in a
+    launch of their own. Only in one-layer steps, whose calls share no buffer, so that running them together
+    computes exactly what the sequence of launches does."""
     if layers != 1:
         return list(range(len(calls)))
+    cls: Dict[int, str] = {}
+    for i, c in enumerate(calls):
+        v = PROGRAM_CLASS.get((c.kind, c.mode if "q8" in c.kind else None))
+        small = c.T < sms and not (c.kind.startswith("add") and c.width > PROGRAM_MAX_NORM_WIDTH)
+        if v is not None and small:
+            cls[i] = v
+    mixed_rows = sum(calls[i].T for i, v in cls.items() if v in ("bf16", "fp8"))
+    key = {i: ("bf16+fp8" if v in ("bf16", "fp8") and mixed_rows <= sms else v) for i, v in cls.items()}
     groups: Dict[str, List[int]] = {}
     order: list = []
-    for i, c in enumerate(calls):
-        v = PROGRAM_VARIANT.get((c.kind, c.mode if c.kind.endswith("q8") else None))
-        small = c.T < sms and not (c.kind.startswith("add") and c.width > PROGRAM_MAX_NORM_WIDTH)
-        if v is None or not small:
+    for i in range(len(calls)):
+        if i not in key:
             order.append(i)
             continue
-        if v not in groups:
-            groups[v] = []
-            order.append(v)
-        groups[v].append(i)
+        if key[i] not in groups:
+            groups[key[i]] = []
+            order.append(key[i])
+        groups[key[i]].append(i)
     units: list = []
     for u in order:
         if isinstance(u, str):
             idx = groups[u]
-            units += [(u, idx[k:k + max_ops]) for k in range(0, len(idx), max_ops)]
+            label = "+".join(sorted({cls[i] for i in idx}))   # what the launch holds
+            units += [(label, idx[k:k + max_ops]) for k in range(0, len(idx), max_ops)]
         else:
             units.append(u)
     return units
@@ -845,8 +857,9 @@ def run_mine(args, work: wl.Workload, rank: int, world: int, local_rank: int) ->
                    "parallelism": f"replicas x{world} (rows are independent; no collective)",
                    "launch_shapes": f"tuning table {os.path.relpath(tuning, ROOT)}" if tuning else "built-in rules",
                    "launch_units": [d.call.name for d in dcalls],
-                   "small_calls": ("one program launch per program variant for the calls with fewer tokens than "
-                                   "SMs (--no-programs: one launch per call)"
+                   "small_calls": ("the calls with fewer tokens than SMs run as program launches (bf16 and FP8 "
+                                   "together while their rows fit one per SM, NVFP4 apart; --no-programs: one "
+                                   "launch per call)"
                                    if any(isinstance(d, ProgramGroup) for d in dcalls) else "one launch per call")},
         "tokens_per_s": round(tokens * args.steps * world / (elapsed_ms / 1e3), 1),
         "gpu_launches": int(launches),
@@ -877,7 +890,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-programs", action="store_true",
                     help="launch every call on its own (default: the calls with fewer tokens than SMs of a one-layer "
-                         "step run as one program launch per program variant)")
+                         "step run as program launches: bf16 and FP8 ones together while their rows fit one per SM)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=1.0, help="target wall time of the oracle sample")

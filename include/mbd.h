@@ -260,8 +260,9 @@ typedef struct {
 /* Largest number of ops in one program. */
 #define MBD_MAX_PROGRAM_OPS 128
 /* Largest hidden size of a norm in a program: one CTA of 256 threads holds the row, 4 vectors per thread.
- * SwiGLU rows of any width run in chunks (a dynamic FP8 row wider than the CTA holds takes two passes:
- * the row maximum, then the codes from the same inputs, read again from L2). */
+ * SwiGLU rows of any width run in chunks. A dynamic FP8 SwiGLU row is held whole, at up to 8 vectors per
+ * thread (16384 elements) in the programs whose epilogue sets include it; a wider one takes two passes: the
+ * row maximum, then the codes from the same inputs, read again from L2. */
 #define MBD_MAX_PROGRAM_WIDTH 8192
 
 /*
@@ -272,8 +273,11 @@ typedef struct {
  * Each op is validated exactly as its entry point validates it (and the same status is returned, nothing
  * launched). Besides: an unknown kind or a non-zero `reserved` gives MBD_ERR_INVALID_ARG; a norm wider
  * than MBD_MAX_PROGRAM_WIDTH, sharing that is not row-aligned, or epilogues outside the compiled sets
- * gives MBD_ERR_UNSUPPORTED. The compiled sets (norm epilogues / SwiGLU epilogues): bf16 / bf16, FP8
- * static / FP8 dynamic, NVFP4 / NVFP4. Ops with n_tokens == 0 are skipped; if nothing remains, nothing is launched.
+ * gives MBD_ERR_UNSUPPORTED. The compiled sets (norm epilogues / SwiGLU epilogues), of which a program
+ * takes the first that covers its ops: bf16 / bf16; FP8 static / FP8 dynamic; NVFP4 / NVFP4; bf16 and FP8
+ * static / bf16, FP8 static and FP8 dynamic (bf16 and FP8 ops mixed in one launch). A dynamic-FP8 norm
+ * therefore runs only in the single-call entry points. Ops with n_tokens == 0 are skipped; if nothing
+ * remains, nothing is launched.
  * Reductions run inside one CTA per row (no cluster), so sums may round differently from the single-call
  * entry points in their last bit; every result keeps the tolerances stated for those entry points.
  */
@@ -323,13 +327,20 @@ mbd_status mbd_program_plan_launch_uploaded(const mbd_program_plan* plan, const 
 
 /*
  * mbd_program_plan_upload + mbd_program_plan_launch_uploaded without caller memory. No counterpart on the
- * source pages. The schedule is copied (one asynchronous host-to-device copy on `stream`, as upload does)
- * into a static buffer of the library: MBD_STATIC_SCHEDULE_BYTES per device, part of the library's device
- * image, its address looked up once per device. Nothing is allocated (no cudaMalloc or other allocating
- * call). Each call copies the schedule again, so plans may alternate freely; because the buffer is shared,
- * calls must not run concurrently on different streams of one device (on one stream they are ordered).
- * A schedule larger than the buffer returns MBD_ERR_UNSUPPORTED (with this header's limits it always fits).
- * Other errors as for mbd_program_plan_launch.
+ * source pages: it exists for callers that cannot allocate device memory. Examples are serving engines that
+ * reserve nearly all of HBM for their own pool (KV cache, weights) and hand kernels only the tensors they
+ * own, plug-in interfaces that pass a kernel its inputs and outputs and nothing else, and latency-critical
+ * loops where cudaMalloc (which may synchronise the device) is not acceptable.
+ * The schedule is copied (one asynchronous host-to-device copy on `stream`, as upload does) into a static
+ * buffer of the library: MBD_STATIC_SCHEDULE_BYTES per device, part of the library's device image and held
+ * by every GPU that loads the library until the process exits. The first call on a device looks up the
+ * buffer's device address (cudaGetSymbolAddress, with that device current) and caches it; make that first
+ * call before any stream capture. Nothing is allocated (no cudaMalloc, cudaFree or other allocating call).
+ * Every call overwrites the part of the buffer its schedule uses, so plans may alternate freely; because
+ * the buffer is shared, calls that overlap on the GPU race (e.g. on different streams of one device) and
+ * must not be issued; calls on one stream are ordered. A schedule larger than the buffer returns
+ * MBD_ERR_UNSUPPORTED (with this header's limits it always fits). Other errors as for
+ * mbd_program_plan_launch.
  */
 #define MBD_STATIC_SCHEDULE_BYTES 16384
 mbd_status mbd_program_plan_launch_static(const mbd_program_plan* plan, mbd_stream_t stream);

@@ -402,11 +402,11 @@ int find_root(int* parent, int i) {
 }
 
 // Resident program CTAs per SM, queried once per device, vectors per thread and variant.
-std::atomic<int> g_prog_ctas[kMaxDevices][3][mbd::kProgramVariants];
+std::atomic<int> g_prog_ctas[kMaxDevices][4][mbd::kProgramVariants];
 
 int program_ctas_per_sm_cached(int vpt, int variant) {
     int dev = 0;
-    const int vi = vpt == 1 ? 0 : (vpt == 2 ? 1 : 2);
+    const int vi = vpt == 1 ? 0 : (vpt == 2 ? 1 : (vpt == 4 ? 2 : 3));
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         (void)cudaGetLastError();
         return mbd::program_ctas_per_sm(vpt, variant);
@@ -439,7 +439,7 @@ mbd_status build_program(const mbd_op* ops, int n_ops, PlanImpl* plan) {
     P.n_ops = n_ops;
     OpInfo info[MBD_MAX_PROGRAM_OPS];
     bool active[MBD_MAX_PROGRAM_OPS] = {};
-    int norm_mask = 0, swiglu_mask = 0, max_held_nvec = 0;
+    int norm_mask = 0, swiglu_mask = 0, max_held_nvec = 0, max_dyn_nvec = 0;
     for (int i = 0; i < n_ops; ++i) {
         const mbd_op& o = ops[i];
         if (o.reserved != 0 || o.kind < MBD_OP_ADD_RMSNORM || o.kind > MBD_OP_SWIGLU_QUANT_NVFP4) return MBD_ERR_INVALID_ARG;
@@ -474,6 +474,7 @@ mbd_status build_program(const mbd_op* ops, int n_ops, PlanImpl* plan) {
             add_region(in, o.in, sp.rows * W * 4, false, W * 4, sp.rows);
             in.holds_row = false;   // streams run in chunks; a wide dynamic row takes two passes
             swiglu_mask |= 1 << ep;
+            if (ep == mbd::kFp8Dynamic && sp.nvec > max_dyn_nvec) max_dyn_nvec = sp.nvec;
         }
         const int64_t T = po.rows;
         const size_t out_row = ep == mbd::kBf16 ? 2 * W : (ep == mbd::kNvfp4 ? W / 2 : W);
@@ -524,10 +525,19 @@ mbd_status build_program(const mbd_op* ops, int n_ops, PlanImpl* plan) {
     for (int i = 0; i < n_ops; ++i)
         if (active[i]) ++size[find_root(parent, i)];
     if (max_held_nvec > MBD_MAX_PROGRAM_WIDTH / 8) return MBD_ERR_UNSUPPORTED;
-    const int vpt = max_held_nvec <= mbd::kProgramThreads ? 1 : (max_held_nvec <= 2 * mbd::kProgramThreads ? 2 : 4);
+    int vpt = max_held_nvec <= mbd::kProgramThreads ? 1 : (max_held_nvec <= 2 * mbd::kProgramThreads ? 2 : 4);
     const int variant = mbd::program_variant(norm_mask, swiglu_mask);
     if (variant < 0) return MBD_ERR_UNSUPPORTED;
-    P.chunk_vecs = mbd::kProgramThreads * vpt;
+    // A dynamic-FP8 SwiGLU row wider than the CTA holds at this vpt runs in two passes (each a memory round
+    // trip, the products computed twice); up to 8 vectors per thread it runs in one at vpt 8. Except where
+    // the chains' norms run with the residual row in registers (vpt 1, one norm epilogue): a decode step's
+    // chained norms are its critical path, and its SwiGLU rows run beside them.
+    bool has_chain = false;
+    for (int i = 0; i < n_ops; ++i) has_chain |= active[i] && find_root(parent, i) == i && size[i] > 1;
+    if (max_dyn_nvec > mbd::kProgramThreads * vpt && max_dyn_nvec <= 8 * mbd::kProgramThreads &&
+        mbd::program_variant_has_vpt8(variant) && !(has_chain && mbd::program_norms_in_registers(vpt, variant)))
+        vpt = 8;
+    P.chunk_vecs = mbd::kProgramThreads * (vpt < 4 ? vpt : 4);
 
     // chains in the order of their first op, each op after the ops before it in the list
     int order_len = 0;

@@ -55,6 +55,9 @@ struct SwigluParams {
 
 constexpr int kMaxProgramOps = 128;     // MBD_MAX_PROGRAM_OPS
 constexpr int kProgramThreads = 256;    // CTA size of the program kernel
+// The wide form (vpt 8 on the host: a row of up to kProgramThreads * 8 vectors held by one CTA) runs
+// kProgramWideThreads threads of at most 2 vectors each.
+constexpr int kProgramWideThreads = 1024;
 constexpr int kMaxProgramGroups = kMaxProgramOps / 2;
 
 enum OpClass : int { kOpNorm = 0, kOpSwiglu = 1 };
@@ -86,7 +89,7 @@ struct ProgramParams {
     int n_ops;                                  // ops[0 .. n_ops) are filled (the kernel copies only those)
     int n_groups;
     int n_free;
-    int chunk_vecs;                             // vectors of one stream chunk (kProgramThreads * vpt)
+    int chunk_vecs;                             // vectors of one stream chunk (kProgramThreads * min(vpt, 4))
     int prefetch_chains;                        // warm each chain row's external inputs first
     int64_t n_chain_items;
     int64_t n_free_items;
@@ -100,9 +103,15 @@ struct ProgramParams {
 };
 
 // Compiled program-kernel variants, each for a set of norm and SwiGLU epilogues (bit e = Epilogue e).
-constexpr int kProgramVariants = 3;
+constexpr int kProgramVariants = 4;
 // The first variant that covers the given epilogue sets, or -1.
 int program_variant(int norm_mask, int swiglu_mask);
+// Whether `variant` is compiled in the wide form, vpt 8 (the variants with the dynamic-FP8 SwiGLU, whose rows
+// of up to kProgramThreads * 8 vectors then run in one pass).
+bool program_variant_has_vpt8(int variant);
+// Whether `variant` at `vpt` runs consecutive chained norms with the residual row in registers (vpt 1 and a
+// single norm epilogue other than dynamic FP8).
+bool program_norms_in_registers(int vpt, int variant);
 static_assert(sizeof(ProgOp) % 8 == 0 && sizeof(ProgramParams) % 8 == 0, "schedules are copied in 8-byte words");
 
 // The library's own schedule buffer (one per device, a static array of the module image), and its address
@@ -111,7 +120,8 @@ constexpr size_t kStaticScheduleBytes = 16384;
 static_assert(sizeof(ProgramParams) <= kStaticScheduleBytes, "a schedule fits the static buffer");
 cudaError_t static_schedule_address(void** addr);
 
-// Program kernel `variant` for `vpt` vectors per thread (1, 2 or 4) on `grid` CTAs of kProgramThreads; the
+// Program kernel `variant` for `vpt` vectors per thread (1, 2 or 4) on `grid` CTAs of kProgramThreads, or
+// in the wide form (vpt 8, where program_variant_has_vpt8) on `grid` CTAs of kProgramWideThreads; the
 // schedule `p` by value, or, when `dev` is not null, read from that copy of it in device memory.
 cudaError_t launch_program(const ProgramParams& p, const ProgramParams* dev, int vpt, int variant, int grid,
                            cudaStream_t s);

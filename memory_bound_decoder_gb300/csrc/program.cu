@@ -30,8 +30,29 @@ struct ProgSmem {
 // the epilogues it can meet, which keeps its registers near those of the one-launch-per-call kernels.
 constexpr int bit(int ep) { return 1 << ep; }
 
-template <int V, int NM>
+// The mixed variant's epilogues: bf16 and FP8 ops in one program. The dynamic-FP8 norm (its exact
+// double-float scaling) stays out of it.
+constexpr int kMixedNormMask = bit(kBf16) | bit(kFp8Static);
+constexpr int kMixedSwigluMask = bit(kBf16) | bit(kFp8Static) | bit(kFp8Dynamic);
+
+// Whether a variant runs each row op as a call (__noinline__) instead of inline. Inlined, every op path of
+// the mixed variant and of the 8-vectors-per-thread variants shares one register allocation, and they
+// spilled 2.5 to 5.4 KB per thread; as calls each path gets its own. The bf16, FP8 and NVFP4 decode variants
+// stay inline: a call per row op cost their chained decode programs 20 to 33%.
+constexpr bool outlined(int v, int nm, int sm) { return v == 8 || (nm == kMixedNormMask && sm == kMixedSwigluMask); }
+
+// The wide form (V = 8 in the templates: a row of up to kProgramThreads * 8 vectors in one CTA) runs
+// kProgramWideThreads threads. Its norm rows (at most kProgramThreads * 4 vectors, MBD_MAX_PROGRAM_WIDTH) and
+// stream chunks (kProgramThreads * 4 vectors) take one vector per thread, its dynamic-FP8 SwiGLU rows two.
+constexpr int threads_of(int v) { return v == 8 ? kProgramWideThreads : kProgramThreads; }
+constexpr int held_vpt(int v) { return v == 8 ? kProgramThreads * 8 / kProgramWideThreads : v; }
+constexpr int chunk_vpt(int v) { return v == 8 ? kProgramThreads * 4 / kProgramWideThreads : v; }
+static_assert(kProgramThreads * 8 % kProgramWideThreads == 0 && kProgramThreads * 4 % kProgramWideThreads == 0,
+              "the wide form holds whole vectors per thread");
+
+template <int V8, int NM>
 __device__ __forceinline__ void run_norm_row(const ProgOp& op, int64_t row, ProgSmem& sm) {
+    constexpr int V = chunk_vpt(V8);
     NormParams np;
     np.x = op.in;
     np.n_partials = 0;
@@ -58,10 +79,11 @@ __device__ __forceinline__ void run_norm_row(const ProgOp& op, int64_t row, Prog
     }
 }
 
-// Vectors [begin, end) of one SwiGLU row (end - begin <= kProgramThreads * V; the whole row for the
-// dynamic epilogue, which reduces over it, when it fits).
-template <int V, int SM>
+// Vectors [begin, end) of one SwiGLU row (a stream chunk: end - begin <= kProgramThreads * min(V8, 4); the
+// whole row for the dynamic epilogue, which reduces over it, when it fits kProgramThreads * V8).
+template <int V8, int SM>
 __device__ __forceinline__ void run_swiglu_part(const ProgOp& op, int64_t row, int begin, int end, ProgSmem& sm) {
+    constexpr int V = chunk_vpt(V8);
     SwigluParams sp{op.in, op.out, op.scale, op.rows, op.nvec, op.out_sf};
     if constexpr ((SM & bit(kBf16)) != 0) {
         if (op.ep == kBf16) return swiglu_row_slice<V, kBf16>(sp, row, 0, 1, begin, end, sm.swiglu);
@@ -70,22 +92,55 @@ __device__ __forceinline__ void run_swiglu_part(const ProgOp& op, int64_t row, i
         if (op.ep == kFp8Static) return swiglu_row_slice<V, kFp8Static>(sp, row, 0, 1, begin, end, sm.swiglu);
     }
     if constexpr ((SM & bit(kFp8Dynamic)) != 0) {
-        if (op.ep == kFp8Dynamic) return swiglu_row_slice<V, kFp8Dynamic>(sp, row, 0, 1, begin, end, sm.swiglu);
+        if (op.ep == kFp8Dynamic) return swiglu_row_slice<held_vpt(V8), kFp8Dynamic>(sp, row, 0, 1, begin, end, sm.swiglu);
     }
     if constexpr ((SM & bit(kNvfp4)) != 0) {
         if (op.ep == kNvfp4) return swiglu_row_slice<V, kNvfp4>(sp, row, 0, 1, begin, end, sm.swiglu);
     }
 }
 
-// A dynamic FP8 SwiGLU row: one pass from registers when it fits the CTA, else two passes (max, then codes).
+// A dynamic FP8 SwiGLU row: one pass from registers when it fits the CTA (kProgramThreads * V vectors),
+// else two passes (max, then codes).
 template <int V, int SM>
-__device__ __forceinline__ void run_swiglu_dynamic_row(const ProgOp& op, int64_t row, int chunk_vecs, ProgSmem& sm) {
+__device__ __forceinline__ void run_swiglu_dynamic_row(const ProgOp& op, int64_t row, ProgSmem& sm) {
     if constexpr ((SM & bit(kFp8Dynamic)) != 0) {
-        if (op.nvec <= chunk_vecs) return run_swiglu_part<V, SM>(op, row, 0, op.nvec, sm);
+        if (op.nvec <= kProgramThreads * V) return run_swiglu_part<V, SM>(op, row, 0, op.nvec, sm);
         SwigluParams sp{op.in, op.out, op.scale, op.rows, op.nvec, op.out_sf};
         // V = 4 (one CTA per SM, registers to spare): 4 vectors per thread in flight per step; else one (few
-        // registers at 2 to 4 CTAs per SM)
-        swiglu_dynamic_two_pass<(V >= 4 ? 4 : 1)>(sp, row, sm.swiglu);
+        // registers at 2 to 4 CTAs per SM, or 1024 threads in the wide form)
+        swiglu_dynamic_two_pass<(V == 4 ? 4 : 1)>(sp, row, sm.swiglu);
+    }
+}
+
+// Out-of-line forms of the row-op runners (see outlined()).
+template <int V, int NM>
+__device__ __noinline__ void run_norm_row_call(const ProgOp& op, int64_t row, ProgSmem& sm) {
+    run_norm_row<V, NM>(op, row, sm);
+}
+template <int V, int SM>
+__device__ __noinline__ void run_swiglu_part_call(const ProgOp& op, int64_t row, int begin, int end, ProgSmem& sm) {
+    run_swiglu_part<V, SM>(op, row, begin, end, sm);
+}
+template <int V, int SM>
+__device__ __noinline__ void run_swiglu_dynamic_row_call(const ProgOp& op, int64_t row, ProgSmem& sm) {
+    run_swiglu_dynamic_row<V, SM>(op, row, sm);
+}
+
+// One row op, inline or as a call: a norm or a dynamic-FP8 SwiGLU on the whole row, or a SwiGLU stream on
+// vectors [begin, end) in chunks of `chunk`.
+template <int V, int NM, int SM>
+__device__ __forceinline__ void run_row_op(const ProgOp& op, int64_t row, int begin, int end, int chunk, ProgSmem& sm) {
+    if (op.cls == kOpNorm) {
+        if constexpr (outlined(V, NM, SM)) run_norm_row_call<V, NM>(op, row, sm);
+        else run_norm_row<V, NM>(op, row, sm);
+    } else if (op.ep == kFp8Dynamic) {
+        if constexpr (outlined(V, NM, SM)) run_swiglu_dynamic_row_call<V, SM>(op, row, sm);
+        else run_swiglu_dynamic_row<V, SM>(op, row, sm);
+    } else {
+        for (int b = begin; b < end; b += chunk) {
+            if constexpr (outlined(V, NM, SM)) run_swiglu_part_call<V, SM>(op, row, b, min(b + chunk, end), sm);
+            else run_swiglu_part<V, SM>(op, row, b, min(b + chunk, end), sm);
+        }
     }
 }
 
@@ -204,13 +259,7 @@ __device__ void run_chain_item(const ProgramParams& P, int64_t item, int& g, int
                 }
             }
         }
-        if (op.cls == kOpNorm) {
-            run_norm_row<V, NM>(op, row, sm);
-        } else if (op.ep == kFp8Dynamic) {
-            run_swiglu_dynamic_row<V, SM>(op, row, P.chunk_vecs, sm);
-        } else {
-            for (int b = 0; b < op.nvec; b += P.chunk_vecs) run_swiglu_part<V, SM>(op, row, b, min(b + P.chunk_vecs, op.nvec), sm);
-        }
+        run_row_op<V, NM, SM>(op, row, 0, op.nvec, P.chunk_vecs, sm);
         __syncthreads();   // this op's stores are visible to every thread before the next op reads them
     }
 }
@@ -223,24 +272,19 @@ __device__ void run_free_item(const ProgramParams& P, int64_t item, int& f, Prog
     const int chunks = P.free_chunks[f];
     const int64_t row = local / chunks;
     const int chunk = static_cast<int>(local - row * chunks);
-    if (op.cls == kOpNorm) {
-        run_norm_row<V, NM>(op, row, sm);
-    } else if (op.ep == kFp8Dynamic) {
-        run_swiglu_dynamic_row<V, SM>(op, row, P.chunk_vecs, sm);
-    } else {
-        const int b = chunks == 1 ? 0 : chunk * P.chunk_vecs;
-        const int e = chunks == 1 ? op.nvec : min(b + P.chunk_vecs, op.nvec);
-        run_swiglu_part<V, SM>(op, row, b, e, sm);
-    }
+    const int b = chunks == 1 ? 0 : chunk * P.chunk_vecs;
+    const int e = chunks == 1 ? op.nvec : min(b + P.chunk_vecs, op.nvec);
+    run_row_op<V, NM, SM>(op, row, b, e, P.chunk_vecs, sm);
     __syncthreads();   // the next item's reduction may reuse the warp partials
 }
 
 // Resident CTAs per SM each variant is compiled for (the register cap): the most that leaves it without
 // large spills, from ptxas -v (40 to 255 registers; a few variants keep spills of under 200 bytes). The FP8 variant at 4 vectors per thread takes the whole
 // register file at one CTA per SM: capped at 128 registers for two it spilled 1 to 2.6 KB per thread, and
-// its programs ran 1.6x (8 layers at 64 tokens) to 3.9x (at 256 tokens) slower than at one.
+// its programs ran 1.6x (8 layers at 64 tokens) to 3.9x (at 256 tokens) slower than at one. The wide form
+// (1024 threads) is one CTA per SM as well.
 constexpr int min_ctas(int v, int nm, int sm) {
-    return sm == bit(kFp8Dynamic) ? (v == 1 ? 4 : (v == 2 ? 2 : 1))   // the dynamic SwiGLU's two-pass form adds registers
+    return (sm & bit(kFp8Dynamic)) != 0 ? (v == 1 ? 4 : (v == 2 ? 2 : 1))   // the dynamic SwiGLU's two-pass form adds registers
                                   : (v == 1 ? ((nm == bit(kBf16) && sm == bit(kBf16)) ? 6 : 5) : (v == 2 ? 3 : 2));
 }
 
@@ -268,7 +312,7 @@ __device__ __forceinline__ void program_body(const ProgramParams& P) {
 
 // The schedule by value in the kernel parameters (no device memory needed; a launch carries ~14 KB)...
 template <int V, int NM, int SM>
-__global__ void __launch_bounds__(kProgramThreads, min_ctas(V, NM, SM)) program_kernel(const __grid_constant__ ProgramParams P) {
+__global__ void __launch_bounds__(threads_of(V), min_ctas(V, NM, SM)) program_kernel(const __grid_constant__ ProgramParams P) {
     pdl_wait();
     program_body<V, NM, SM>(P);
     pdl_trigger();   // late: a dependent program waiting in SM slots would hold resources this one still uses
@@ -279,7 +323,7 @@ __global__ void __launch_bounds__(kProgramThreads, min_ctas(V, NM, SM)) program_
 // descriptors cost shared-memory latency rather than an L2 round trip each. The upload precedes the launch
 // in stream order and is not a kernel, so the copy may run before the grid dependency wait.
 template <int V, int NM, int SM>
-__global__ void __launch_bounds__(kProgramThreads, min_ctas(V, NM, SM)) program_kernel_dev(const ProgramParams* __restrict__ P) {
+__global__ void __launch_bounds__(threads_of(V), min_ctas(V, NM, SM)) program_kernel_dev(const ProgramParams* __restrict__ P) {
     __shared__ __align__(16) ProgramParams S;
     {
         const size_t bytes = offsetof(ProgramParams, ops) + static_cast<size_t>(P->n_ops) * sizeof(ProgOp);
@@ -297,7 +341,7 @@ __global__ void __launch_bounds__(kProgramThreads, min_ctas(V, NM, SM)) program_
 template <int V, int NM, int SM>
 int ctas_per_sm() {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, program_kernel<V, NM, SM>, kProgramThreads, 0) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, program_kernel<V, NM, SM>, threads_of(V), 0) != cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
     }
@@ -309,7 +353,7 @@ cudaError_t launch_variant(const ProgramParams& p, const ProgramParams* dev, int
     cudaLaunchConfig_t cfg = cudaLaunchConfig_t{};
     cudaLaunchAttribute attr[1];
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-    cfg.blockDim = dim3(kProgramThreads, 1, 1);
+    cfg.blockDim = dim3(threads_of(V), 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -320,12 +364,15 @@ cudaError_t launch_variant(const ProgramParams& p, const ProgramParams* dev, int
     return cudaLaunchKernelEx(&cfg, program_kernel<V, NM, SM>, p);
 }
 
-// The compiled variants: (norm epilogues, SwiGLU epilogues).
+// The compiled variants: (norm epilogues, SwiGLU epilogues). A program takes the first that covers its ops.
 constexpr int kVariantMasks[kProgramVariants][2] = {
     {bit(kBf16), bit(kBf16)},                  // bf16 layers
     {bit(kFp8Static), bit(kFp8Dynamic)},       // FP8: static-scale norm, dynamic-scale SwiGLU
     {bit(kNvfp4), bit(kNvfp4)},                // NVFP4 layers
+    {kMixedNormMask, kMixedSwigluMask},        // bf16 and FP8 ops mixed in one program
 };
+
+constexpr bool has_vpt8(int k) { return (kVariantMasks[k][1] & bit(kFp8Dynamic)) != 0; }
 
 template <int V, int K>
 int ctas_of() { return ctas_per_sm<V, kVariantMasks[K][0], kVariantMasks[K][1]>(); }
@@ -341,6 +388,7 @@ int ctas_v(int variant) {
         case 0: return ctas_of<V, 0>();
         case 1: return ctas_of<V, 1>();
         case 2: return ctas_of<V, 2>();
+        case 3: return ctas_of<V, 3>();
     }
     return 0;
 }
@@ -351,6 +399,26 @@ cudaError_t launch_v(const ProgramParams& p, const ProgramParams* dev, int varia
         case 0: return launch_of<V, 0>(p, dev, grid, s);
         case 1: return launch_of<V, 1>(p, dev, grid, s);
         case 2: return launch_of<V, 2>(p, dev, grid, s);
+        case 3: return launch_of<V, 3>(p, dev, grid, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+// 8 vectors per thread: compiled only for the variants with the dynamic-FP8 SwiGLU.
+static_assert(has_vpt8(1) && has_vpt8(3) && !has_vpt8(0) && !has_vpt8(2), "variants compiled at 8 vectors per thread");
+
+int ctas_v8(int variant) {
+    switch (variant) {
+        case 1: return ctas_of<8, 1>();
+        case 3: return ctas_of<8, 3>();
+    }
+    return 0;
+}
+
+cudaError_t launch_v8(const ProgramParams& p, const ProgramParams* dev, int variant, int grid, cudaStream_t s) {
+    switch (variant) {
+        case 1: return launch_of<8, 1>(p, dev, grid, s);
+        case 3: return launch_of<8, 3>(p, dev, grid, s);
     }
     return cudaErrorInvalidValue;
 }
@@ -363,11 +431,20 @@ int program_variant(int norm_mask, int swiglu_mask) {
     return -1;
 }
 
+bool program_variant_has_vpt8(int variant) { return variant >= 0 && variant < kProgramVariants && has_vpt8(variant); }
+
+bool program_norms_in_registers(int vpt, int variant) {
+    if (variant < 0 || variant >= kProgramVariants) return false;
+    const int ep = single_ep(kVariantMasks[variant][0]);
+    return vpt == 1 && ep >= 0 && ep != kFp8Dynamic;
+}
+
 int program_ctas_per_sm(int vpt, int variant) {
     switch (vpt) {
         case 1: return ctas_v<1>(variant);
         case 2: return ctas_v<2>(variant);
         case 4: return ctas_v<4>(variant);
+        case 8: return ctas_v8(variant);
     }
     return 0;
 }
@@ -378,13 +455,17 @@ cudaError_t launch_program(const ProgramParams& p, const ProgramParams* dev, int
         case 1: return launch_v<1>(p, dev, variant, grid, s);
         case 2: return launch_v<2>(p, dev, variant, grid, s);
         case 4: return launch_v<4>(p, dev, variant, grid, s);
+        case 8: return launch_v8(p, dev, variant, grid, s);
     }
     return cudaErrorInvalidValue;
 }
 
-// Schedule storage of mbd_program_plan_launch_static: part of the module image, so nothing is allocated
-// when it is used.
-__device__ __align__(256) unsigned char g_static_schedule[kStaticScheduleBytes];
+// Schedule storage of mbd_program_plan_launch_static, for callers that cannot allocate device memory: part
+// of the module image (every GPU that loads the library holds it until exit), so nothing is allocated when
+// it is used. In host code the name is a host-side stand-in, not a device address: the kernel gets the
+// address that cudaGetSymbolAddress returns with the device current (looked up once per device by the
+// caller of static_schedule_address).
+static __device__ __align__(256) unsigned char g_static_schedule[kStaticScheduleBytes];
 
 cudaError_t static_schedule_address(void** addr) { return cudaGetSymbolAddress(addr, g_static_schedule); }
 

@@ -194,9 +194,12 @@ def test_program_argument_checks(lib):
     assert _rc(mbd.run_program, [norm(A, 2 * A, 3 * A), w_writer]) == mbd.ERR_UNSUPPORTED
     # a row that must stay in one CTA is limited to MBD_MAX_PROGRAM_WIDTH elements
     assert _rc(mbd.run_program, [norm(A, 2 * A, 3 * A, T=1, H=8192 + 16)]) == mbd.ERR_UNSUPPORTED
-    # epilogues outside the compiled sets: a bf16 norm with an FP8 SwiGLU
-    s8 = mbd.op_swiglu_quant_fp8(10 * A, 11 * A, 4, H, "dynamic", 12 * A)
-    assert _rc(mbd.run_program, [norm(A, 2 * A, 3 * A), s8]) == mbd.ERR_UNSUPPORTED
+    # epilogues outside the compiled sets: a dynamic-FP8 norm with a bf16 SwiGLU (the mixed bf16 + FP8 variant
+    # leaves the dynamic norm out), a bf16 norm with an NVFP4 SwiGLU
+    qd = mbd.op_add_rmsnorm_quant_fp8(6 * A, 2 * A, 3 * A, 9 * A, 4, H, 1e-6, "dynamic", 7 * A)
+    assert _rc(mbd.run_program, [qd, mbd.op_swiglu(10 * A, 11 * A, 4, H)]) == mbd.ERR_UNSUPPORTED
+    s4 = mbd.op_swiglu_quant_nvfp4(10 * A, 12 * A, 11 * A, 4, H, 13 * A)
+    assert _rc(mbd.run_program, [norm(A, 2 * A, 3 * A), s4]) == mbd.ERR_UNSUPPORTED
     assert mbd.kernel_launches() == n0
 
 

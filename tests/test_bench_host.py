@@ -7,7 +7,7 @@ def _names(calls, units):
     return [calls[u].name if isinstance(u, int) else (u[0], [calls[i].name for i in u[1]]) for u in units]
 
 
-def test_default_step_groups_the_small_calls_by_variant():
+def test_default_step_groups_the_small_calls_into_one_launch():
     w = bench.workloads_by_key()[bench.DEFAULT_WORKLOAD]
     calls = list(w.calls)
     units = bench.launch_groups(calls, w.layers, 152)
@@ -15,25 +15,31 @@ def test_default_step_groups_the_small_calls_by_variant():
     singles = [u for u in units if isinstance(u, int)]
     assert all(calls[i].T >= 152 for i in singles)
     groups = [u for u in units if not isinstance(u, int)]
-    assert [g[0] for g in groups] == ["bf16", "fp8"]
+    assert [g[0] for g in groups] == ["bf16+fp8"]                    # 84 rows: one wave of the mixed variant
     small = [i for i, c in enumerate(calls) if c.T < 152]
-    assert sorted(i for g in groups for i in g[1]) == small          # every small call, exactly once
-    want = {"bf16": {("add_rmsnorm", None), ("swiglu", None)},
-            "fp8": {("add_rmsnorm_q8", "static"), ("swiglu_q8", "dynamic")}}
-    for v, idx in groups:
-        assert {(calls[i].kind, calls[i].mode) for i in idx} == want[v]
-        assert idx == sorted(idx)                                     # list order kept inside a program
+    assert groups[0][1] == small                                      # every small call once, in list order
+    assert {(calls[i].kind, calls[i].mode) for i in small} == {
+        ("add_rmsnorm", None), ("swiglu", None), ("add_rmsnorm_q8", "static"), ("swiglu_q8", "dynamic")}
     # a group sits where its first call stood
     flat = [u if isinstance(u, int) else u[1][0] for u in units]
     assert flat == sorted(flat)
 
 
-def test_fp8_variant_takes_static_norms_and_dynamic_swiglu_only():
+def test_classes_split_when_their_rows_exceed_one_per_sm():
+    d = wl.N01
+    calls = [wl.Call("add_rmsnorm", 100, 1024, d), wl.Call("swiglu_q8", 60, 1024, d, mode="dynamic"),
+             wl.Call("swiglu", 10, 1024, d)]
+    assert bench.launch_groups(calls, 1, 152) == [("bf16", [0, 2]), ("fp8", [1])]
+    assert bench.launch_groups(calls, 1, 200) == [("bf16+fp8", [0, 1, 2])]
+
+
+def test_programs_take_no_dynamic_norm():
     d = wl.N01
     calls = [wl.Call("add_rmsnorm_q8", 4, 1024, d, mode="static"), wl.Call("add_rmsnorm_q8", 4, 1024, d, mode="dynamic"),
-             wl.Call("swiglu_q8", 4, 1024, d, mode="dynamic"), wl.Call("swiglu_q8", 4, 1024, d, mode="static")]
+             wl.Call("swiglu_q8", 4, 1024, d, mode="dynamic"), wl.Call("swiglu_q8", 4, 1024, d, mode="static"),
+             wl.Call("swiglu_nvfp4", 4, 1024, d), wl.Call("add_rmsnorm", 4, 1024, d)]
     units = bench.launch_groups(calls, 1, 152)
-    assert units == [("fp8", [0, 2]), 1, 3]
+    assert units == [("bf16+fp8", [0, 2, 3, 5]), 1, ("nvfp4", [4])]
 
 
 def test_no_grouping_across_layers_wide_norms_or_allreduce():

@@ -92,9 +92,10 @@ def test_decode_step_bf16(T):
 @pytest.mark.parametrize("T,H,I", [(1, 1536, 8960), (17, 1536, 8960), (200, 1536, 8960), (9, 4096, 13824),
                                    (3, 8192, 8192)])
 def test_decode_step_fp8(T, H, I):
-    """Layers of (norm -> E4M3 static, SwiGLU -> E4M3 dynamic) sharing the residual. SwiGLU rows wider than
-    the CTA holds (8960 at 1 vector per thread, 13824 at 2) take the two-pass dynamic form; 8192 at 4 vectors
-    per thread is held in one pass."""
+    """Layers of (norm -> E4M3 static, SwiGLU -> E4M3 dynamic) sharing the residual. With 1536-wide norms the
+    chained norms keep the residual row in registers at 1 vector per thread, and the 8960-wide SwiGLU rows take
+    the two-pass dynamic form; with 4096-wide norms (2 vectors per thread) the 13824-wide rows are held whole
+    at 8 vectors per thread; 8192 at 4 vectors per thread is held in one pass."""
     mbd = _mbd()
     L, eps, S = 8, 1e-5, 0.05
     res0, layers = decode_layers(T, L, H, I, seed=T + 100, dist=wl.C5_ACT, eps=eps)
@@ -216,6 +217,101 @@ def test_independent_ops_of_mixed_shapes():
             r, _, v = orc.add_rmsnorm(inp.x, inp.residual, inp.weight, inp.eps)
             check_bf16(u16(g[0], (T, W)), v, f"norm {T}x{W}")
             np.testing.assert_array_equal(u16(g[1], (T, W)), r)
+
+
+@pytest.mark.parametrize("I", [13824, 16384, 16400])
+def test_mixed_bf16_fp8_independent_calls(I):
+    """bf16 and FP8 ops in one launch (the mixed variant), as independent calls at 1, 3 and 17 tokens: norms
+    5120 wide (bf16, static FP8) and SwiGLU (bf16, static FP8, dynamic FP8). A dynamic row of 13824 or 16384
+    elements is held whole at 8 vectors per thread; 16400 (2050 vectors) takes the two-pass form."""
+    mbd = _mbd()
+    H, eps, S = 5120, 1e-5, 0.05
+    sc = Guarded(torch, 1, torch.float32, fill=np.array([S], np.float32))
+    ops, checks, keep, guards = [], [], [sc], []
+    for k, T in enumerate([1, 3, 17]):
+        for q in (False, True):
+            n = wl.make_norm_inputs(T, H, 11, wl.C5_ACT, eps, salt=10 * k + int(q))
+            X, R, W = dev_u16(torch, n.x), dev_u16(torch, n.residual), dev_u16(torch, n.weight)
+            O = Guarded(torch, T * H, torch.uint8 if q else torch.int16)
+            ops.append(mbd.op_add_rmsnorm_quant_fp8(O.view, R.view, X.view, W.view, T, H, eps, "static", sc.view)
+                       if q else mbd.op_add_rmsnorm(O.view, R.view, X.view, W.view, T, H, eps))
+            keep += [X, W]
+            guards += [(O, "norm out"), (R, "residual")]
+            checks.append(("norm", q, n, (O, R), T))
+        for j, mode in enumerate((None, "static", "dynamic")):
+            g = wl.make_swiglu_inputs(T, I, 11, wl.C5_ACT, salt=10 * k + 2 + j)
+            GU = dev_u16(torch, g.gate_up)
+            Y = Guarded(torch, T * I, torch.int16 if mode is None else torch.uint8)
+            SY = sc if mode != "dynamic" else Guarded(torch, T, torch.float32)
+            ops.append(mbd.op_swiglu(Y.view, GU.view, T, I) if mode is None
+                       else mbd.op_swiglu_quant_fp8(Y.view, GU.view, T, I, mode, SY.view))
+            keep.append(GU)
+            guards.append((Y, "swiglu out"))
+            if mode == "dynamic":
+                guards.append((SY, "swiglu scales"))
+            checks.append(("swiglu", mode, g, (Y, SY), T))
+    run(ops, guards)
+    for kind, mode, inp, g, T in checks:
+        if kind == "norm":
+            O, R = g
+            if mode:
+                r, q_o, _, _ = orc.add_rmsnorm_quant_fp8(inp.x, inp.residual, inp.weight, eps, "static", S)
+                check_codes(O.numpy(np.uint8).reshape(T, H), q_o, f"norm e4m3 T={T}")
+            else:
+                r, _, v = orc.add_rmsnorm(inp.x, inp.residual, inp.weight, eps)
+                check_bf16(u16(O, (T, H)), v, f"norm T={T}")
+            np.testing.assert_array_equal(u16(R, (T, H)), r, f"residual T={T}")
+        elif mode is None:
+            _, h = orc.swiglu(inp.gate_up)
+            check_bf16(u16(g[0], (T, I)), h, f"swiglu T={T}")
+        else:
+            q_o, s_o, _ = orc.swiglu_quant_fp8(inp.gate_up, mode, S if mode == "static" else 0.0)
+            check_codes(g[0].numpy(np.uint8).reshape(T, I), q_o, f"swiglu e4m3 {mode} T={T}")
+            if mode == "dynamic":
+                check_scales(g[1].numpy(np.float32), s_o, f"swiglu scales T={T}")
+
+
+def test_mixed_chain_across_epilogues():
+    """One residual updated by a bf16 norm, then a static-FP8 norm, then a bf16 norm (a chain in the mixed
+    variant), beside independent SwiGLU ops: dynamic FP8 (13824 wide, held whole at 8 vectors per thread) and
+    static FP8."""
+    mbd = _mbd()
+    T, H, I, eps, S = 6, 4096, 13824, 1e-6, 0.05
+    sc = Guarded(torch, 1, torch.float32, fill=np.array([S], np.float32))
+    base = wl.make_norm_inputs(T, H, 12, wl.N01, eps, salt=0)
+    R = dev_u16(torch, base.residual)
+    xs = [wl.make_norm_inputs(T, H, 12, wl.N01, eps, salt=k + 1) for k in range(3)]
+    ops, keep, outs = [], [R, sc], []
+    for k, n in enumerate(xs):
+        X, W = dev_u16(torch, n.x), dev_u16(torch, n.weight)
+        O = Guarded(torch, T * H, torch.uint8 if k == 1 else torch.int16)
+        ops.append(mbd.op_add_rmsnorm_quant_fp8(O.view, R.view, X.view, W.view, T, H, eps, "static", sc.view)
+                   if k == 1 else mbd.op_add_rmsnorm(O.view, R.view, X.view, W.view, T, H, eps))
+        keep += [X, W]
+        outs.append(O)
+    gd = wl.make_swiglu_inputs(T, I, 12, wl.N01, salt=7)
+    gs = wl.make_swiglu_inputs(T, I, 12, wl.N01, salt=8)
+    GD, GS = dev_u16(torch, gd.gate_up), dev_u16(torch, gs.gate_up)
+    QD, SD = Guarded(torch, T * I, torch.uint8), Guarded(torch, T, torch.float32)
+    QS = Guarded(torch, T * I, torch.uint8)
+    ops += [mbd.op_swiglu_quant_fp8(QD.view, GD.view, T, I, "dynamic", SD.view),
+            mbd.op_swiglu_quant_fp8(QS.view, GS.view, T, I, "static", sc.view)]
+    keep += [GD, GS]
+    run(ops, [(R, "residual"), (QD, "q"), (SD, "s"), (QS, "q")] + [(o, "out") for o in outs])
+    r = base.residual
+    for k, (n, O) in enumerate(zip(xs, outs)):
+        if k == 1:
+            r, q_o, _, _ = orc.add_rmsnorm_quant_fp8(n.x, r, n.weight, eps, "static", S)
+            check_codes(O.numpy(np.uint8).reshape(T, H), q_o, "chained e4m3 norm")
+        else:
+            r, _, v = orc.add_rmsnorm(n.x, r, n.weight, eps)
+            check_bf16(u16(O, (T, H)), v, f"chained norm {k}")
+    np.testing.assert_array_equal(u16(R, (T, H)), r)
+    q_o, s_o, _ = orc.swiglu_quant_fp8(gd.gate_up, "dynamic")
+    check_codes(QD.numpy(np.uint8).reshape(T, I), q_o, "dynamic swiglu")
+    check_scales(SD.numpy(np.float32), s_o, "dynamic swiglu scales")
+    q_o, _, _ = orc.swiglu_quant_fp8(gs.gate_up, "static", S)
+    check_codes(QS.numpy(np.uint8).reshape(T, I), q_o, "static swiglu")
 
 
 def test_widest_held_rows_dynamic():

@@ -1,5 +1,7 @@
-"""mbd_program_plan_launch_static, the program launch that allocates nothing: its schedule goes to a static
-buffer of the library instead of caller memory. Checked against the entry point it stands in for
+"""mbd_program_plan_launch_static, the program launch that allocates nothing, for callers that cannot allocate
+device memory (engines that keep nearly all HBM in their own pool, plug-in interfaces that hand a kernel only
+its inputs and outputs, loops that cannot afford cudaMalloc's possible device synchronisation): its schedule
+goes to a static buffer of the library instead of caller memory. Checked against the entry point it stands in for
 (mbd_program_plan_upload into a caller buffer + mbd_program_plan_launch_uploaded): two consecutive calls of
 each, on identical fresh inputs, give identical bits; plans may alternate through the shared buffer; and
 the calls take no device memory. Collected last (file name), after every other GPU test.
