@@ -45,15 +45,15 @@ DEFAULT_WORKLOAD = "llama3.1-405b_fp8_T2048+ragged"
 # `src_sha256` (kernel_src_hash).
 TRAFFIC: Dict[str, Dict] = {
     # profiles/allreduce_rmsnorm_q8_static_k8_T2048_H16384.md
-    "allreduce_rmsnorm_q8_static_k8_T2048_H16384": {"bytes": 679770112, "src_sha256": "e0ea6230b4b5821fcb66b899153cbb74f4b8cb84c574cc7fe65466fa4e699636"},
+    "allreduce_rmsnorm_q8_static_k8_T2048_H16384": {"bytes": 679688960, "src_sha256": "d41fdc6df0cc2fa6fdd43372ad1a7abd1b6c17b0dc510866f42a6b2bc7df9528"},
     # profiles/add_rmsnorm_nvfp4_T2048_H16384.md
-    "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 166345216, "src_sha256": "e0ea6230b4b5821fcb66b899153cbb74f4b8cb84c574cc7fe65466fa4e699636"},
+    "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 167336960, "src_sha256": "d41fdc6df0cc2fa6fdd43372ad1a7abd1b6c17b0dc510866f42a6b2bc7df9528"},
     # profiles/swiglu_nvfp4_T2048_I53248.md
-    "swiglu_nvfp4_T2048_I53248": {"bytes": 467542528, "src_sha256": "1e3f448bd1a38d50292063c6d1052b4436f904835087e89073259f3a23f8117c"},
+    "swiglu_nvfp4_T2048_I53248": {"bytes": 467854080, "src_sha256": "f2af8b3f0704696a2ab7853fa5f3d8498737e17001fbd4c7ab308d7d25a67622"},
     # profiles/swiglu_q8_dynamic_T2048_I53248.md
-    "swiglu_q8_dynamic_T2048_I53248": {"bytes": 497629184, "src_sha256": "1e3f448bd1a38d50292063c6d1052b4436f904835087e89073259f3a23f8117c"},
+    "swiglu_q8_dynamic_T2048_I53248": {"bytes": 497590784, "src_sha256": "f2af8b3f0704696a2ab7853fa5f3d8498737e17001fbd4c7ab308d7d25a67622"},
     # profiles/add_rmsnorm_q8_static_T2048_H16384.md
-    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 178528000, "src_sha256": "e0ea6230b4b5821fcb66b899153cbb74f4b8cb84c574cc7fe65466fa4e699636"},
+    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 178110464, "src_sha256": "d41fdc6df0cc2fa6fdd43372ad1a7abd1b6c17b0dc510866f42a6b2bc7df9528"},
 }
 
 
