@@ -354,7 +354,10 @@ mbd_status mbd_program_plan_launch_static(const mbd_program_plan* plan, mbd_stre
  * FIRST entry whose kind (and FP8 mode) matches and whose token and width buckets hold it, provided its
  * shape fits the call (enough threads x vectors for a slice of the row, at most 8 CTAs when the row is
  * reduced); otherwise the next matching entry, then the rules. The all-reduce and program entry points do
- * not use the table. The tuner that fills it is memory_bound_decoder_gb300/tune.py.
+ * not use the table. One shape is fixed by the rules alone: a dynamic-FP8 SwiGLU of at least 4 rows per SM
+ * with rows of 4609 to 10240 vectors (inter 36872 to 81920) brings its row slices into shared memory by
+ * bulk copies (clusters of 7, or 8 past 8960 vectors, 4 vectors per thread), whatever the table says. The
+ * tuner that fills it is memory_bound_decoder_gb300/tune.py.
  */
 typedef struct {
     int32_t kind;                 /* mbd_op_kind of the entry point */

@@ -288,6 +288,28 @@ void set_ahead(bool dyn_swiglu, int64_t rows, int sms, mbd::RowPlan* plan) {
         plan->ahead = static_cast<int>(int64_t{sms} * (2048 / plan->threads) / plan->ctas_per_row / 2);
 }
 
+// Large batches of wide dynamic-FP8 SwiGLU rows: the slices come into shared memory by bulk copies and
+// registers hold only the products (swiglu_dyn_bulk_kernel), 5 CTAs of 256 threads per SM. Clusters of 7
+// (8 past 7 x 1280 vectors), 4 vectors per thread, L2 warmed half the resident rows ahead. Measured at
+// 4 or more rows per SM (CUDA events around back-to-back launches, inputs > L2, bit-identical outputs):
+// I 53248: 82.6 vs 87.5 us at T 2048 (clusters of 8: 88.2, of 6: 85.7), 158.5 vs 168.8 at T 4096; at
+// I 28672 the register form stays ahead (85.1 vs 87.0 us at T 4096, best bulk shape), likewise at I 13824,
+// so rows of up to 4608 vectors keep it. It supersedes table entries for the shapes it takes.
+constexpr int kBulkMinVec = 4609, kBulkMaxSlice = 1280;   // kBulkMaxSlice: 320 threads x 4 vectors
+void bulk_rule(int64_t rows, int nvec, int sms, mbd::RowPlan* plan) {
+    if (rows < 4 * int64_t{sms} || nvec < kBulkMinVec || nvec > 8 * kBulkMaxSlice) return;
+    int c = cdiv(nvec, kBulkMaxSlice);
+    if (c < 7) c = 7;
+    const int slice = cdiv(nvec, c);
+    *plan = mbd::RowPlan{};
+    plan->ctas_per_row = cdiv(nvec, slice);
+    plan->slice = slice;
+    plan->vpt = 4;
+    plan->threads = cdiv(cdiv(slice, 4), 32) * 32;
+    plan->bulk = 1;
+    plan->ahead = static_cast<int>(int64_t{sms} * 5 / plan->ctas_per_row / 2);
+}
+
 // The first table entry whose buckets hold the call and whose shape fits it.
 bool tuned_plan(int kind, int mode, int64_t rows, int64_t width, int nvec, bool reduces, bool pairs, int sms,
                 mbd::RowPlan* plan) {
@@ -366,6 +388,7 @@ mbd_status swiglu_common(void* out, uint8_t* out_sf, mbd::Epilogue ep, const voi
     if (!tuned && !plan_rows(p.rows, p.nvec, ep == mbd::kFp8Dynamic ? Shape::kRowMax : Shape::kStream, sms,
                              ep == mbd::kNvfp4, &plan))
         return MBD_ERR_UNSUPPORTED;
+    if (ep == mbd::kFp8Dynamic) bulk_rule(p.rows, p.nvec, sms, &plan);
     return finish_launch(mbd::launch_swiglu(p, ep, plan, stream));
 }
 
@@ -828,6 +851,7 @@ mbd_status mbd_launch_shape(int kind, int mode, int64_t n_tokens, int64_t width,
     if (!tuned_plan(kind, mode, n_tokens, width, nvec, norm || dyn_swiglu, fp4, sms, &plan) &&
         !plan_rows(n_tokens, nvec, norm ? Shape::kNorm : (dyn_swiglu ? Shape::kRowMax : Shape::kStream), sms, fp4, &plan))
         return MBD_ERR_UNSUPPORTED;
+    if (dyn_swiglu) bulk_rule(n_tokens, nvec, sms, &plan);
     *ctas_per_row = plan.ctas_per_row;
     *vectors_per_thread = plan.vpt;
     *threads = plan.threads;

@@ -22,6 +22,7 @@ struct RowPlan {
     int vpt;       // 1, 2, 4 or 8
     int prefetch;  // 1: single-wave launch, warm L2 with the inputs before waiting on the previous kernel
     int ahead;     // > 0: each CTA also warms L2 with the same slice of row + ahead (a later wave's row)
+    int bulk;      // dynamic-FP8 SwiGLU: 1 = the slices come into shared memory by bulk copies (vpt 4)
 };
 
 

@@ -286,18 +286,27 @@ def test_tuning_table_roundtrip_and_checks(lib, tmp_path):
 
 def test_launch_shape_follows_table_then_rules(lib):
     mbd.tuning_set([])
-    rules = mbd.launch_shape("swiglu_quant_fp8", "dynamic", 2048, 53248)
-    rules_1000 = mbd.launch_shape("swiglu_quant_fp8", "dynamic", 1000, 53248)
+    rules = mbd.launch_shape("swiglu_quant_fp8", "dynamic", 2048, 28672)
+    rules_1000 = mbd.launch_shape("swiglu_quant_fp8", "dynamic", 1000, 28672)
     assert rules[0] <= 8 and rules[2] % 32 == 0
-    mbd.tuning_set([{"kind": "swiglu_quant_fp8", "mode": "dynamic", "tokens": [2000, 3000], "width": [53248, 53248],
-                     "ctas_per_row": 8, "vectors_per_thread": 4, "threads": 224}])
-    assert mbd.launch_shape("swiglu_quant_fp8", "dynamic", 2048, 53248) == (8, 4, 224)
-    assert mbd.launch_shape("swiglu_quant_fp8", "dynamic", 1000, 53248) == rules_1000      # outside the bucket
-    assert mbd.launch_shape("swiglu_quant_fp8", "static", 2048, 53248) != (8, 4, 224)       # other mode
-    # a shape that cannot cover the row (8 CTAs x 4 x 32 threads < 6656 vectors) falls back to the rules
+    mbd.tuning_set([{"kind": "swiglu_quant_fp8", "mode": "dynamic", "tokens": [2000, 3000], "width": [28672, 28672],
+                     "ctas_per_row": 8, "vectors_per_thread": 4, "threads": 128}])
+    assert mbd.launch_shape("swiglu_quant_fp8", "dynamic", 2048, 28672) == (8, 4, 128)
+    assert mbd.launch_shape("swiglu_quant_fp8", "dynamic", 1000, 28672) == rules_1000      # outside the bucket
+    assert mbd.launch_shape("swiglu_quant_fp8", "static", 2048, 28672) != (8, 4, 128)       # other mode
+    # a shape that cannot cover the row (8 CTAs x 4 x 32 threads < 3584 vectors) falls back to the rules
     mbd.tuning_set([{"kind": "swiglu_quant_fp8", "mode": "dynamic", "tokens": [1, 1 << 30], "width": [1, 1 << 30],
                      "ctas_per_row": 8, "vectors_per_thread": 4, "threads": 32}])
-    assert mbd.launch_shape("swiglu_quant_fp8", "dynamic", 2048, 53248) == rules
+    assert mbd.launch_shape("swiglu_quant_fp8", "dynamic", 2048, 28672) == rules
+    # wide dynamic rows at >= 4 rows per SM take the bulk-copy form whatever the table says: 6656 vectors in
+    # clusters of 7 (slices of 951: 256 threads x 4), 10240 in clusters of 8 (320 threads); rows of 4608
+    # vectors, and fewer rows, follow the table
+    mbd.tuning_set([{"kind": "swiglu_quant_fp8", "mode": "dynamic", "tokens": [1, 1 << 30], "width": [1, 1 << 30],
+                     "ctas_per_row": 8, "vectors_per_thread": 2, "threads": 512}])
+    assert mbd.launch_shape("swiglu_quant_fp8", "dynamic", 2048, 53248) == (7, 4, 256)
+    assert mbd.launch_shape("swiglu_quant_fp8", "dynamic", 2048, 81920) == (8, 4, 320)
+    assert mbd.launch_shape("swiglu_quant_fp8", "dynamic", 2048, 36864) == (8, 2, 512)
+    assert mbd.launch_shape("swiglu_quant_fp8", "dynamic", 100, 53248) == (8, 2, 512)
     # NVFP4 slices are rounded up to an even number of vectors
     mbd.tuning_set([{"kind": "swiglu_quant_nvfp4", "mode": None, "tokens": [1, 1 << 30], "width": [1, 1 << 30],
                      "ctas_per_row": 3, "vectors_per_thread": 1, "threads": 64}])

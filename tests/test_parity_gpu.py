@@ -193,6 +193,19 @@ def test_ragged_405b_tails(T):
     check_swiglu(gu, "q8", "dynamic")
 
 
+@pytest.mark.parametrize("I,shape", [(36872, (7, 4, 192)), (81920, (8, 4, 320))])
+def test_dynamic_swiglu_bulk_form(I, shape):
+    """Wide dynamic-FP8 SwiGLU rows at four or more rows per SM take the bulk-copy form (slices brought into
+    shared memory): 4609 vectors (the narrowest such row; clusters of 7, a ragged last slice) and 10240
+    (the widest; clusters of 8, 320 threads). Sampled rows, including the first and the last."""
+    mbd = _mbd()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    T = 4 * sms + 3
+    assert mbd.launch_shape("swiglu_quant_fp8", "dynamic", T, I) == shape
+    inp = wl.make_swiglu_inputs(T, I, seed=4, dist=wl.C5_ACT)
+    check_swiglu(inp, "q8", "dynamic", rows=sample_rows(T, 16, seed=5))
+
+
 # ------------------------------------------------------------------------------------------------ edge cases
 
 @pytest.mark.parametrize("ep,mode", [("bf16", None), ("q8", "static"), ("q8", "dynamic")])
