@@ -46,15 +46,15 @@ DEFAULT_WORKLOAD = "llama3.1-405b_fp8_T2048+ragged"
 # `src_sha256` (kernel_src_hash).
 TRAFFIC: Dict[str, Dict] = {
     # profiles/allreduce_rmsnorm_q8_static_k8_T2048_H16384.md
-    "allreduce_rmsnorm_q8_static_k8_T2048_H16384": {"bytes": 679688960, "src_sha256": "d41fdc6df0cc2fa6fdd43372ad1a7abd1b6c17b0dc510866f42a6b2bc7df9528"},
+    "allreduce_rmsnorm_q8_static_k8_T2048_H16384": {"bytes": 679976192, "src_sha256": "bb374cac90de044f5c76e94f206b04788d44fe00f69c1b2c2d1d25737dc6be96"},
     # profiles/add_rmsnorm_nvfp4_T2048_H16384.md
-    "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 167336960, "src_sha256": "d41fdc6df0cc2fa6fdd43372ad1a7abd1b6c17b0dc510866f42a6b2bc7df9528"},
+    "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 167424768, "src_sha256": "bb374cac90de044f5c76e94f206b04788d44fe00f69c1b2c2d1d25737dc6be96"},
     # profiles/swiglu_nvfp4_T2048_I53248.md
-    "swiglu_nvfp4_T2048_I53248": {"bytes": 467854080, "src_sha256": "f2af8b3f0704696a2ab7853fa5f3d8498737e17001fbd4c7ab308d7d25a67622"},
+    "swiglu_nvfp4_T2048_I53248": {"bytes": 467893504, "src_sha256": "7cf61b954f5554ad43ecb5dc50698cfcb0193ade854613c00aaf1345eabbbe38"},
     # profiles/swiglu_q8_dynamic_T2048_I53248.md
-    "swiglu_q8_dynamic_T2048_I53248": {"bytes": 526635008, "src_sha256": "7cf61b954f5554ad43ecb5dc50698cfcb0193ade854613c00aaf1345eabbbe38"},
+    "swiglu_q8_dynamic_T2048_I53248": {"bytes": 526622720, "src_sha256": "7cf61b954f5554ad43ecb5dc50698cfcb0193ade854613c00aaf1345eabbbe38"},
     # profiles/add_rmsnorm_q8_static_T2048_H16384.md
-    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 178110464, "src_sha256": "d41fdc6df0cc2fa6fdd43372ad1a7abd1b6c17b0dc510866f42a6b2bc7df9528"},
+    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 178219264, "src_sha256": "bb374cac90de044f5c76e94f206b04788d44fe00f69c1b2c2d1d25737dc6be96"},
 }
 
 
