@@ -45,6 +45,8 @@ DEFAULT_WORKLOAD = "llama3.1-405b_fp8_T2048+ragged"
 # summarised under profiles/; valid only while what the kernel and its launch shape are built from hashes to
 # `src_sha256` (kernel_src_hash).
 TRAFFIC: Dict[str, Dict] = {
+    # profiles/swiglu_q8_dynamic_T4096_I28672.md
+    "swiglu_q8_dynamic_T4096_I28672": {"bytes": 539390720, "src_sha256": "7cf61b954f5554ad43ecb5dc50698cfcb0193ade854613c00aaf1345eabbbe38"},
     # profiles/allreduce_rmsnorm_q8_static_k8_T2048_H16384.md
     "allreduce_rmsnorm_q8_static_k8_T2048_H16384": {"bytes": 679976192, "src_sha256": "bb374cac90de044f5c76e94f206b04788d44fe00f69c1b2c2d1d25737dc6be96"},
     # profiles/add_rmsnorm_nvfp4_T2048_H16384.md
