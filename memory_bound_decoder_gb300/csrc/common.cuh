@@ -269,20 +269,38 @@ __device__ __forceinline__ bool row_reduce(P mine, P* warp_part, Exchange& ex, i
     return *ok_flag != 0;
 }
 
+// Four warp partials read as one 16-byte vector, slots from `first` on past the last warp counting as zero,
+// combined as a pairwise tree.
+template <class P>
+__device__ __forceinline__ P combine4(float4 f, int first, int nwarps) {
+    const P a = first < nwarps ? P{f.x} : P::zero(), b = first + 1 < nwarps ? P{f.y} : P::zero();
+    const P c = first + 2 < nwarps ? P{f.z} : P::zero(), d = first + 3 < nwarps ? P{f.w} : P::zero();
+    return P::combine(P::combine(a, b), P::combine(c, d));
+}
+
 // Total over a row held by ONE CTA, returned to every thread: the warps reduce their lanes, then every
-// thread combines the warp partials in warp order (the same order everywhere, so all threads get identical
-// bits). One CTA barrier. warp_part must not be written again before the CTA has passed another barrier
-// (the callers' next barrier, or the end of the CTA).
+// thread reads all warp partials at once (16 bytes at a time) and combines them in a fixed pairwise tree
+// (the same order everywhere, so all threads get identical bits; a loop over the warps would be a chain of
+// dependent shared-memory loads). One CTA barrier. warp_part (one float per partial, 32 slots, 16-byte
+// aligned) must not be written again before the CTA has passed another barrier (the callers' next barrier,
+// or the end of the CTA).
 template <class P>
 __device__ __forceinline__ P block_total(P mine, P* warp_part) {
+    static_assert(sizeof(P) == sizeof(float), "one-float partials");
     mine = warp_allreduce_p(mine);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (lane == 0) warp_part[warp] = mine;
     __syncthreads();
     const int nwarps = (blockDim.x + 31) >> 5;
-    P t = warp_part[0];
-    for (int w = 1; w < nwarps; ++w) t = P::combine(t, warp_part[w]);
-    return t;
+    const float4* q = reinterpret_cast<const float4*>(warp_part);
+    if (nwarps <= 4) return combine4<P>(q[0], 0, nwarps);
+    if (nwarps <= 8) return P::combine(combine4<P>(q[0], 0, nwarps), combine4<P>(q[1], 4, nwarps));
+    const P lo = P::combine(P::combine(combine4<P>(q[0], 0, nwarps), combine4<P>(q[1], 4, nwarps)),
+                            P::combine(combine4<P>(q[2], 8, nwarps), combine4<P>(q[3], 12, nwarps)));
+    if (nwarps <= 16) return lo;
+    const P hi = P::combine(P::combine(combine4<P>(q[4], 16, nwarps), combine4<P>(q[5], 20, nwarps)),
+                            P::combine(combine4<P>(q[6], 24, nwarps), combine4<P>(q[7], 28, nwarps)));
+    return P::combine(lo, hi);
 }
 
 // ------------------------------------------------------------------------------------------ PDL
