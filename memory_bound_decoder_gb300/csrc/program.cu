@@ -24,6 +24,7 @@ namespace {
 struct ProgSmem {
     NormSmem norm;
     SwigluSmem swiglu;
+    alignas(16) PSum run_part[2][32];   // norm_run's warp partials, alternating between consecutive ops
 };
 
 // Epilogue sets of a program kernel variant: bit e set = epilogue e compiled in. Each variant carries only
@@ -193,8 +194,13 @@ __device__ void norm_run(const ProgOp* ops, int n, int64_t row, ProgSmem& sm) {
             xv = load_stream(static_cast<const uint4*>(ops[k + 1].in) + row * nvec + c);
             wn = load_cached(static_cast<const uint4*>(ops[k + 1].weight) + c);
         }
-        const PSum t = block_total(PSum{ss2.x + ss2.y}, sm.norm.part_sum);
-        const float inv = 1.0f / sqrtf(t.v / static_cast<float>(op.hidden) + op.eps);
+        // Partials alternate between two buffers: when a thread writes op k + 2's partials into this one,
+        // every thread has passed op k + 1's barrier and so has read op k's, so no barrier closes the op.
+        const PSum t = block_total(PSum{ss2.x + ss2.y}, sm.run_part[k & 1]);
+        // the hardware reciprocal square root and a multiply by 1 / hidden instead of a correctly rounded
+        // square root and two divisions: a few ulps, against a bf16 tolerance of 2^-7, and a shorter
+        // dependent chain on the decode step's critical path
+        const float inv = rsqrtf(t.v * (1.0f / static_cast<float>(op.hidden)) + op.eps);
         NormParams np;
         np.x = op.in;
         np.n_partials = 0;
@@ -209,7 +215,6 @@ __device__ void norm_run(const ProgOp* ops, int n, int64_t row, ProgSmem& sm) {
         np.eps = op.eps;
         norm_store<1, EP>(np, row, 0, sv, wv, live, inv);
         if (k + 1 < n) wv[0] = wn;
-        __syncthreads();   // the warp partials are read by every thread before the next op writes them
     }
     if (live[0]) store_stream(rr, sv[0]);
 }
