@@ -46,17 +46,17 @@ DEFAULT_WORKLOAD = "llama3.1-405b_fp8_T2048+ragged"
 # `src_sha256` (kernel_src_hash).
 TRAFFIC: Dict[str, Dict] = {
     # profiles/swiglu_q8_dynamic_T4096_I28672.md
-    "swiglu_q8_dynamic_T4096_I28672": {"bytes": 539390720, "src_sha256": "7cf61b954f5554ad43ecb5dc50698cfcb0193ade854613c00aaf1345eabbbe38"},
+    "swiglu_q8_dynamic_T4096_I28672": {"bytes": 539429376, "src_sha256": "2e7fbf83b82af3737a8890baa1897c6e023aab80a0234018d740dc6823cd72b7"},
     # profiles/allreduce_rmsnorm_q8_static_k8_T2048_H16384.md
-    "allreduce_rmsnorm_q8_static_k8_T2048_H16384": {"bytes": 679976192, "src_sha256": "bb374cac90de044f5c76e94f206b04788d44fe00f69c1b2c2d1d25737dc6be96"},
+    "allreduce_rmsnorm_q8_static_k8_T2048_H16384": {"bytes": 680005632, "src_sha256": "5d2b89e30af90271a65dde2cb235194e756f7108b8438840a606d8fc83833cdf"},
     # profiles/add_rmsnorm_nvfp4_T2048_H16384.md
-    "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 167424768, "src_sha256": "bb374cac90de044f5c76e94f206b04788d44fe00f69c1b2c2d1d25737dc6be96"},
+    "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 166785024, "src_sha256": "5d2b89e30af90271a65dde2cb235194e756f7108b8438840a606d8fc83833cdf"},
     # profiles/swiglu_nvfp4_T2048_I53248.md
-    "swiglu_nvfp4_T2048_I53248": {"bytes": 467893504, "src_sha256": "7cf61b954f5554ad43ecb5dc50698cfcb0193ade854613c00aaf1345eabbbe38"},
+    "swiglu_nvfp4_T2048_I53248": {"bytes": 468088320, "src_sha256": "2e7fbf83b82af3737a8890baa1897c6e023aab80a0234018d740dc6823cd72b7"},
     # profiles/swiglu_q8_dynamic_T2048_I53248.md
-    "swiglu_q8_dynamic_T2048_I53248": {"bytes": 526622720, "src_sha256": "7cf61b954f5554ad43ecb5dc50698cfcb0193ade854613c00aaf1345eabbbe38"},
+    "swiglu_q8_dynamic_T2048_I53248": {"bytes": 526432256, "src_sha256": "2e7fbf83b82af3737a8890baa1897c6e023aab80a0234018d740dc6823cd72b7"},
     # profiles/add_rmsnorm_q8_static_T2048_H16384.md
-    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 178219264, "src_sha256": "bb374cac90de044f5c76e94f206b04788d44fe00f69c1b2c2d1d25737dc6be96"},
+    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 178139136, "src_sha256": "5d2b89e30af90271a65dde2cb235194e756f7108b8438840a606d8fc83833cdf"},
 }
 
 

@@ -269,6 +269,22 @@ __device__ __forceinline__ bool row_reduce(P mine, P* warp_part, Exchange& ex, i
     return *ok_flag != 0;
 }
 
+// Total over a row held by ONE CTA, returned to every thread: the warps reduce their lanes, then every
+// thread combines the warp partials in warp order (the same order everywhere, so all threads get identical
+// bits). One CTA barrier. warp_part must not be written again before the CTA has passed another barrier
+// (the callers' next barrier, or the end of the CTA).
+template <class P>
+__device__ __forceinline__ P block_total(P mine, P* warp_part) {
+    mine = warp_allreduce_p(mine);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) warp_part[warp] = mine;
+    __syncthreads();
+    const int nwarps = (blockDim.x + 31) >> 5;
+    P t = warp_part[0];
+    for (int w = 1; w < nwarps; ++w) t = P::combine(t, warp_part[w]);
+    return t;
+}
+
 // Four warp partials read as one 16-byte vector, slots from `first` on past the last warp counting as zero,
 // combined as a pairwise tree.
 template <class P>
@@ -278,14 +294,14 @@ __device__ __forceinline__ P combine4(float4 f, int first, int nwarps) {
     return P::combine(P::combine(a, b), P::combine(c, d));
 }
 
-// Total over a row held by ONE CTA, returned to every thread: the warps reduce their lanes, then every
+// block_total for a chain of reductions on the critical path (the decode programs' chained norms): every
 // thread reads all warp partials at once (16 bytes at a time) and combines them in a fixed pairwise tree
-// (the same order everywhere, so all threads get identical bits; a loop over the warps would be a chain of
-// dependent shared-memory loads). One CTA barrier. warp_part (one float per partial, 32 slots, 16-byte
-// aligned) must not be written again before the CTA has passed another barrier (the callers' next barrier,
-// or the end of the CTA).
+// (the same order everywhere, so all threads get identical bits) instead of a chain of dependent
+// shared-memory loads and adds. warp_part: one float per partial, 32 slots, 16-byte aligned. (Compiled into
+// the single-call kernels, even in a branch they do not take, it cost them about 1% in their other paths, so
+// they keep block_total.)
 template <class P>
-__device__ __forceinline__ P block_total(P mine, P* warp_part) {
+__device__ __forceinline__ P block_total_tree(P mine, P* warp_part) {
     static_assert(sizeof(P) == sizeof(float), "one-float partials");
     mine = warp_allreduce_p(mine);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

@@ -196,7 +196,7 @@ __device__ void norm_run(const ProgOp* ops, int n, int64_t row, ProgSmem& sm) {
         }
         // Partials alternate between two buffers: when a thread writes op k + 2's partials into this one,
         // every thread has passed op k + 1's barrier and so has read op k's, so no barrier closes the op.
-        const PSum t = block_total(PSum{ss2.x + ss2.y}, sm.run_part[k & 1]);
+        const PSum t = block_total_tree(PSum{ss2.x + ss2.y}, sm.run_part[k & 1]);
         // the hardware reciprocal square root and a multiply by 1 / hidden instead of a correctly rounded
         // square root and two divisions: a few ulps, against a bf16 tolerance of 2^-7, and a shorter
         // dependent chain on the decode step's critical path

@@ -49,7 +49,8 @@ __global__ void __launch_bounds__(512, VPT <= 2 ? 4 : 1) swiglu_kernel(const __g
 // Dynamic FP8 SwiGLU with the CTA's gate and up slices brought into shared memory by two bulk copies
 // (cp.async.bulk, completion counted on an mbarrier) instead of per-thread loads into registers: registers
 // then hold only the fp32 products, so more CTAs (and more bytes in flight) fit on an SM while others sit in
-// their row reduction. Same arithmetic, reduction and stores as swiglu_row_slice.
+// their row reduction. Same arithmetic, reduction and stores as swiglu_row_slice. Rows always span a cluster
+// (ctas_per_row >= 2; the planner uses 7 or 8).
 struct BulkSmem {
     unsigned long long load_bar;
 };
@@ -87,7 +88,7 @@ __global__ void __launch_bounds__(320, 4) swiglu_dyn_bulk_kernel(const __grid_co
             prefetch_l2_bulk(gr + ahead * (int64_t)p.nvec * 2 + p.nvec, bytes);
         }
     }
-    if (ctas_per_row > 1) exchange_init(sm.ex, ctas_per_row);   // its cluster barrier overlaps the copies
+    exchange_init(sm.ex, ctas_per_row);   // its cluster barrier overlaps the copies
     // every thread waits for both slices (bounded; on expiry: error flag, and the copies are waited for once
     // more before the CTA may leave, since they write into its shared memory)
     bool landed = false;
@@ -123,20 +124,13 @@ __global__ void __launch_bounds__(320, 4) swiglu_dyn_bulk_kernel(const __grid_co
             amax = fmaxf(amax, fmaxf(fabsf(h[i][k].x), fabsf(h[i][k].y)));
         }
     }
-    float qmul;
-    if (ctas_per_row == 1) {
-        const float sc = block_total(PMax{amax}, sm.part_max).v / 448.0f;
-        qmul = sc > 0.0f ? 1.0f / sc : 0.0f;
-        if (threadIdx.x == 0 && landed) p.scale[row] = sc;
-    } else {
-        if (!row_reduce(PMax{amax}, sm.part_max, sm.ex, rank, ctas_per_row, &sm.ok_flag, [&](PMax t) {
-                const float sc = t.v / 448.0f;
-                sm.row_qmul = sc > 0.0f ? 1.0f / sc : 0.0f;
-                if (rank == 0) p.scale[row] = sc;
-            }))
-            return;
-        qmul = sm.row_qmul;
-    }
+    if (!row_reduce(PMax{amax}, sm.part_max, sm.ex, rank, ctas_per_row, &sm.ok_flag, [&](PMax t) {
+            const float sc = t.v / 448.0f;
+            sm.row_qmul = sc > 0.0f ? 1.0f / sc : 0.0f;
+            if (rank == 0) p.scale[row] = sc;
+        }))
+        return;
+    const float qmul = sm.row_qmul;
     if (!landed) return;
     uint2* outr = reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + row * (int64_t)p.nvec * 8) + begin;
     const float2 q2 = f2(qmul);
@@ -156,7 +150,7 @@ __global__ void __launch_bounds__(320, 4) swiglu_dyn_bulk_kernel(const __grid_co
 std::atomic<int> g_bulk_carveout_set[64];
 
 cudaError_t launch_dyn_bulk(const SwigluParams& p, const RowPlan& plan, cudaStream_t s) {
-    if (plan.vpt != 4) return cudaErrorInvalidValue;
+    if (plan.vpt != 4 || plan.ctas_per_row < 2 || plan.ctas_per_row > kMaxClusterCtas) return cudaErrorInvalidValue;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
