@@ -149,6 +149,10 @@ constexpr long long kWaitLimitCycles = 2LL << 30;
 // seen every peer's bytes, so no write can target a CTA that has exited.
 constexpr int kMaxClusterCtas = 8;   // portable cluster size
 
+// Where a row reduction runs, as a compile-time choice of the row-slice bodies: the row in one CTA, the row
+// over a cluster, or either (decided by the CTA count at run time).
+constexpr int kRowAny = 0, kRowInCta = 1, kRowInCluster = 2;
+
 struct alignas(16) Exchange {
     float4 slot[kMaxClusterCtas];
     unsigned long long mbar;

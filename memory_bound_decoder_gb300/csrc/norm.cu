@@ -23,7 +23,7 @@ namespace {
 
 // The partial-sum form asks for two 512-thread CTAs per SM (<= 64 registers): its eight loads in flight
 // per vector would otherwise leave one CTA, a quarter of the SM's warps.
-template <int VPT, int EP, bool ALLRED>
+template <int VPT, int EP, bool ALLRED, int CL>
 __global__ void __launch_bounds__(512, ALLRED ? 2 : 1) add_rmsnorm_kernel(const __grid_constant__ NormParams p, int ctas_per_row, int slice,
                                                                         int prefetch) {
     __shared__ NormSmem sm;
@@ -35,7 +35,7 @@ __global__ void __launch_bounds__(512, ALLRED ? 2 : 1) add_rmsnorm_kernel(const 
     pdl_trigger();
     if (prefetch) norm_prefetch<VPT, ALLRED>(p, row, begin, end);
     pdl_wait();
-    norm_row_slice<VPT, EP, ALLRED>(p, row, rank, ctas_per_row, begin, end, sm);
+    norm_row_slice<VPT, EP, ALLRED, CL>(p, row, rank, ctas_per_row, begin, end, sm);
 }
 
 template <int EP>
@@ -43,15 +43,16 @@ cudaError_t launch_ep(const NormParams& p, const RowPlan& plan, cudaStream_t s) 
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
     void (*kern)(NormParams, int, int, int) = nullptr;
+    const bool cl = plan.ctas_per_row > 1;
     if (p.n_partials > 0) {
         if (plan.vpt != 1) return cudaErrorInvalidValue;
-        kern = add_rmsnorm_kernel<1, EP, true>;
+        kern = cl ? add_rmsnorm_kernel<1, EP, true, kRowInCluster> : add_rmsnorm_kernel<1, EP, true, kRowInCta>;
     } else {
         switch (plan.vpt) {
-            case 1: kern = add_rmsnorm_kernel<1, EP, false>; break;
-            case 2: kern = add_rmsnorm_kernel<2, EP, false>; break;
-            case 4: kern = add_rmsnorm_kernel<4, EP, false>; break;
-            case 8: kern = add_rmsnorm_kernel<8, EP, false>; break;
+            case 1: kern = cl ? add_rmsnorm_kernel<1, EP, false, kRowInCluster> : add_rmsnorm_kernel<1, EP, false, kRowInCta>; break;
+            case 2: kern = cl ? add_rmsnorm_kernel<2, EP, false, kRowInCluster> : add_rmsnorm_kernel<2, EP, false, kRowInCta>; break;
+            case 4: kern = cl ? add_rmsnorm_kernel<4, EP, false, kRowInCluster> : add_rmsnorm_kernel<4, EP, false, kRowInCta>; break;
+            case 8: kern = cl ? add_rmsnorm_kernel<8, EP, false, kRowInCluster> : add_rmsnorm_kernel<8, EP, false, kRowInCta>; break;
             default: return cudaErrorInvalidValue;
         }
     }

@@ -143,8 +143,10 @@ __device__ __forceinline__ void norm_store(const NormParams& p, int64_t row, int
 
 // One CTA's share of one row: vectors [begin, end) of `row` (at most VPT per thread), the CTA being `rank`
 // of the `nctas` CTAs of the row (one thread-block cluster when nctas > 1). Every thread of the CTA calls
-// it. On a cluster-exchange timeout the CTA returns without writing its outputs.
-template <int VPT, int EP, bool ALLRED>
+// it. On a cluster-exchange timeout the CTA returns without writing its outputs. CL: kRowInCta (nctas is 1)
+// or kRowInCluster (nctas > 1) compile only the reduction that runs (code for the other, even untaken, has
+// cost the kernels about 1%); kRowAny decides at run time.
+template <int VPT, int EP, bool ALLRED, int CL = kRowAny>
 __device__ __forceinline__ void norm_row_slice(const NormParams& p, int64_t row, int rank, int nctas, int begin,
                                                int end, NormSmem& sm) {
     PSum* part_sum = sm.part_sum;
@@ -154,7 +156,8 @@ __device__ __forceinline__ void norm_row_slice(const NormParams& p, int64_t row,
     // The weight is an L2 hit; load it up front when registers allow (small rows, latency-bound), else
     // after the reduction. The dynamic variant needs it before the reduction anyway.
     constexpr bool kEarlyWeight = EP == kFp8Dynamic || VPT <= 2;
-    const int ctas_per_row = nctas;
+    const int ctas_per_row = CL == kRowInCta ? 1 : nctas;
+    const bool single = CL == kRowInCta || (CL == kRowAny && nctas == 1);
 
     const uint4* xr = static_cast<const uint4*>(p.x) + row * p.nvec;
     uint4* rr = static_cast<uint4*>(p.residual) + row * p.nvec;
@@ -180,7 +183,7 @@ __device__ __forceinline__ void norm_row_slice(const NormParams& p, int64_t row,
             for (int i = 0; i < VPT; ++i)
                 if (live[i]) xv[i] = reduce_partials(p, row, begin + threadIdx.x + i * blockDim.x);
         }
-        if (ctas_per_row > 1) exchange_init(ex, ctas_per_row);   // overlaps the loads in flight
+        if (!single) exchange_init(ex, ctas_per_row);   // overlaps the loads in flight
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
             if (!live[i]) continue;
@@ -206,7 +209,7 @@ __device__ __forceinline__ void norm_row_slice(const NormParams& p, int64_t row,
             }
         }
         float inv;
-        if (ctas_per_row == 1) {   // the whole row in this CTA: one barrier, every thread forms inv
+        if (single) {   // the whole row in this CTA: one barrier, every thread forms inv
             const PSum t = block_total(PSum{ss2.x + ss2.y}, part_sum);
             inv = 1.0f / sqrtf(t.v / static_cast<float>(p.hidden) + p.eps);
         } else {

@@ -67,16 +67,16 @@ __device__ __forceinline__ void run_norm_row(const ProgOp& op, int64_t row, Prog
     np.hidden = op.hidden;
     np.eps = op.eps;
     if constexpr ((NM & bit(kBf16)) != 0) {
-        if (op.ep == kBf16) return norm_row_slice<V, kBf16, false>(np, row, 0, 1, 0, op.nvec, sm.norm);
+        if (op.ep == kBf16) return norm_row_slice<V, kBf16, false, kRowInCta>(np, row, 0, 1, 0, op.nvec, sm.norm);
     }
     if constexpr ((NM & bit(kFp8Static)) != 0) {
-        if (op.ep == kFp8Static) return norm_row_slice<V, kFp8Static, false>(np, row, 0, 1, 0, op.nvec, sm.norm);
+        if (op.ep == kFp8Static) return norm_row_slice<V, kFp8Static, false, kRowInCta>(np, row, 0, 1, 0, op.nvec, sm.norm);
     }
     if constexpr ((NM & bit(kFp8Dynamic)) != 0) {
-        if (op.ep == kFp8Dynamic) return norm_row_slice<V, kFp8Dynamic, false>(np, row, 0, 1, 0, op.nvec, sm.norm);
+        if (op.ep == kFp8Dynamic) return norm_row_slice<V, kFp8Dynamic, false, kRowInCta>(np, row, 0, 1, 0, op.nvec, sm.norm);
     }
     if constexpr ((NM & bit(kNvfp4)) != 0) {
-        if (op.ep == kNvfp4) return norm_row_slice<V, kNvfp4, false>(np, row, 0, 1, 0, op.nvec, sm.norm);
+        if (op.ep == kNvfp4) return norm_row_slice<V, kNvfp4, false, kRowInCta>(np, row, 0, 1, 0, op.nvec, sm.norm);
     }
 }
 
@@ -87,16 +87,16 @@ __device__ __forceinline__ void run_swiglu_part(const ProgOp& op, int64_t row, i
     constexpr int V = chunk_vpt(V8);
     SwigluParams sp{op.in, op.out, op.scale, op.rows, op.nvec, op.out_sf};
     if constexpr ((SM & bit(kBf16)) != 0) {
-        if (op.ep == kBf16) return swiglu_row_slice<V, kBf16>(sp, row, 0, 1, begin, end, sm.swiglu);
+        if (op.ep == kBf16) return swiglu_row_slice<V, kBf16, kRowInCta>(sp, row, 0, 1, begin, end, sm.swiglu);
     }
     if constexpr ((SM & bit(kFp8Static)) != 0) {
-        if (op.ep == kFp8Static) return swiglu_row_slice<V, kFp8Static>(sp, row, 0, 1, begin, end, sm.swiglu);
+        if (op.ep == kFp8Static) return swiglu_row_slice<V, kFp8Static, kRowInCta>(sp, row, 0, 1, begin, end, sm.swiglu);
     }
     if constexpr ((SM & bit(kFp8Dynamic)) != 0) {
-        if (op.ep == kFp8Dynamic) return swiglu_row_slice<held_vpt(V8), kFp8Dynamic>(sp, row, 0, 1, begin, end, sm.swiglu);
+        if (op.ep == kFp8Dynamic) return swiglu_row_slice<held_vpt(V8), kFp8Dynamic, kRowInCta>(sp, row, 0, 1, begin, end, sm.swiglu);
     }
     if constexpr ((SM & bit(kNvfp4)) != 0) {
-        if (op.ep == kNvfp4) return swiglu_row_slice<V, kNvfp4>(sp, row, 0, 1, begin, end, sm.swiglu);
+        if (op.ep == kNvfp4) return swiglu_row_slice<V, kNvfp4, kRowInCta>(sp, row, 0, 1, begin, end, sm.swiglu);
     }
 }
 

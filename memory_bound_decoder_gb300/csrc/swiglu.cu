@@ -22,7 +22,7 @@ namespace mbd {
 
 namespace {
 
-template <int VPT, int EP>
+template <int VPT, int EP, int CL>
 __global__ void __launch_bounds__(512, VPT <= 2 ? 4 : 1) swiglu_kernel(const __grid_constant__ SwigluParams p, int ctas_per_row, int slice, int prefetch,
                                                                    int ahead) {
     __shared__ SwigluSmem sm;
@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(512, VPT <= 2 ? 4 : 1) swiglu_kernel(const __g
         prefetch_l2_bulk(gr, bytes);
         prefetch_l2_bulk(gr + p.nvec, bytes);
     }
-    swiglu_row_slice<VPT, EP>(p, row, rank, ctas_per_row, begin, end, sm);
+    swiglu_row_slice<VPT, EP, CL>(p, row, rank, ctas_per_row, begin, end, sm);
 }
 
 // Dynamic FP8 SwiGLU with the CTA's gate and up slices brought into shared memory by two bulk copies
@@ -173,11 +173,14 @@ cudaError_t launch_ep(const SwigluParams& p, const RowPlan& plan, cudaStream_t s
     cudaLaunchAttribute attr[2];
     const int cluster = EP == kFp8Dynamic ? plan.ctas_per_row : 1;
     void (*kern)(SwigluParams, int, int, int, int) = nullptr;
+    // only the dynamic epilogue reduces over the row; the streams compile no reduction either way
+    constexpr int kMulti = EP == kFp8Dynamic ? kRowInCluster : kRowInCta;
+    const bool cl = cluster > 1;
     switch (plan.vpt) {
-        case 1: kern = swiglu_kernel<1, EP>; break;
-        case 2: kern = swiglu_kernel<2, EP>; break;
-        case 4: kern = swiglu_kernel<4, EP>; break;
-        case 8: kern = swiglu_kernel<8, EP>; break;
+        case 1: kern = cl ? swiglu_kernel<1, EP, kMulti> : swiglu_kernel<1, EP, kRowInCta>; break;
+        case 2: kern = cl ? swiglu_kernel<2, EP, kMulti> : swiglu_kernel<2, EP, kRowInCta>; break;
+        case 4: kern = cl ? swiglu_kernel<4, EP, kMulti> : swiglu_kernel<4, EP, kRowInCta>; break;
+        case 8: kern = cl ? swiglu_kernel<8, EP, kMulti> : swiglu_kernel<8, EP, kRowInCta>; break;
         default: return cudaErrorInvalidValue;
     }
     if (EP == kFp8Dynamic && plan.bulk) return launch_dyn_bulk(p, plan, s);

@@ -61,13 +61,15 @@ __device__ __forceinline__ void swiglu_prefetch(const SwigluParams p, int64_t ro
 
 // One CTA's share of one row: vectors [begin, end) of `row` (at most VPT per thread; begin even for
 // NVFP4), the CTA being `rank` of the `nctas` CTAs of the row (a cluster when nctas > 1; only the dynamic
-// FP8 epilogue reduces over the row). Every thread of the CTA calls it.
-template <int VPT, int EP>
+// FP8 epilogue reduces over the row). Every thread of the CTA calls it. CL as for norm_row_slice (it
+// matters only to the dynamic epilogue).
+template <int VPT, int EP, int CL = kRowAny>
 __device__ __forceinline__ void swiglu_row_slice(const SwigluParams p, int64_t row, int rank, int nctas, int begin,
                                                  int end, SwigluSmem& sm) {
     PMax* part_max = sm.part_max;
     Exchange& ex = sm.ex;
-    const int ctas_per_row = nctas;
+    const int ctas_per_row = CL == kRowInCta ? 1 : nctas;
+    const bool single = CL == kRowInCta || (CL == kRowAny && nctas == 1);
     const uint4* gr = static_cast<const uint4*>(p.gate_up) + row * (int64_t)p.nvec * 2;
     const uint4* ur = gr + p.nvec;
 
@@ -83,7 +85,7 @@ __device__ __forceinline__ void swiglu_row_slice(const SwigluParams p, int64_t r
         }
     }
     if constexpr (EP == kFp8Dynamic) {
-        if (ctas_per_row > 1) exchange_init(ex, ctas_per_row);   // overlaps the loads in flight
+        if (!single) exchange_init(ex, ctas_per_row);   // overlaps the loads in flight
     }
 
     if constexpr (EP == kBf16) {
@@ -140,7 +142,7 @@ __device__ __forceinline__ void swiglu_row_slice(const SwigluParams p, int64_t r
             }
         }
         if constexpr (EP == kFp8Dynamic) {
-            if (ctas_per_row == 1) {   // the whole row in this CTA: one barrier, every thread forms the scale
+            if (single) {   // the whole row in this CTA: one barrier, every thread forms the scale
                 const float sc = block_total(PMax{amax}, part_max).v / 448.0f;
                 qmul = sc > 0.0f ? 1.0f / sc : 0.0f;
                 if (threadIdx.x == 0) p.scale[row] = sc;
