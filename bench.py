@@ -46,17 +46,17 @@ DEFAULT_WORKLOAD = "llama3.1-405b_fp8_T2048+ragged"
 # `src_sha256` (kernel_src_hash).
 TRAFFIC: Dict[str, Dict] = {
     # profiles/swiglu_q8_dynamic_T4096_I28672.md
-    "swiglu_q8_dynamic_T4096_I28672": {"bytes": 539429376, "src_sha256": "2e7fbf83b82af3737a8890baa1897c6e023aab80a0234018d740dc6823cd72b7"},
+    "swiglu_q8_dynamic_T4096_I28672": {"bytes": 539456256, "src_sha256": "49260d006bde0def11f8aa4a1f56077217f24815dfce4c534a11e2439189ec34"},
     # profiles/allreduce_rmsnorm_q8_static_k8_T2048_H16384.md
-    "allreduce_rmsnorm_q8_static_k8_T2048_H16384": {"bytes": 680005632, "src_sha256": "5d2b89e30af90271a65dde2cb235194e756f7108b8438840a606d8fc83833cdf"},
+    "allreduce_rmsnorm_q8_static_k8_T2048_H16384": {"bytes": 680083712, "src_sha256": "69d14552657702ffe7eae79b2440600db263b29684eec120b4756ac1845077a0"},
     # profiles/add_rmsnorm_nvfp4_T2048_H16384.md
-    "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 166785024, "src_sha256": "5d2b89e30af90271a65dde2cb235194e756f7108b8438840a606d8fc83833cdf"},
+    "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 167228416, "src_sha256": "69d14552657702ffe7eae79b2440600db263b29684eec120b4756ac1845077a0"},
     # profiles/swiglu_nvfp4_T2048_I53248.md
-    "swiglu_nvfp4_T2048_I53248": {"bytes": 468088320, "src_sha256": "2e7fbf83b82af3737a8890baa1897c6e023aab80a0234018d740dc6823cd72b7"},
+    "swiglu_nvfp4_T2048_I53248": {"bytes": 467772160, "src_sha256": "49260d006bde0def11f8aa4a1f56077217f24815dfce4c534a11e2439189ec34"},
     # profiles/swiglu_q8_dynamic_T2048_I53248.md
-    "swiglu_q8_dynamic_T2048_I53248": {"bytes": 526432256, "src_sha256": "2e7fbf83b82af3737a8890baa1897c6e023aab80a0234018d740dc6823cd72b7"},
+    "swiglu_q8_dynamic_T2048_I53248": {"bytes": 527144960, "src_sha256": "49260d006bde0def11f8aa4a1f56077217f24815dfce4c534a11e2439189ec34"},
     # profiles/add_rmsnorm_q8_static_T2048_H16384.md
-    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 178139136, "src_sha256": "5d2b89e30af90271a65dde2cb235194e756f7108b8438840a606d8fc83833cdf"},
+    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 177783808, "src_sha256": "69d14552657702ffe7eae79b2440600db263b29684eec120b4756ac1845077a0"},
 }
 
 
