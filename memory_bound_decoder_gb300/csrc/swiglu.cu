@@ -145,8 +145,9 @@ __global__ void __launch_bounds__(320, 4) swiglu_dyn_bulk_kernel(const __grid_co
     }
 }
 
-// Shared memory of the bulk kernel: the two slices. Set once per device: the largest shared-memory carveout,
-// so that the SM's shared memory, not its L1 share, bounds the resident CTAs.
+// Per device (up to 64): whether the bulk kernel's preferred carveout, the largest shared-memory share, has
+// been requested, so that the SM's shared memory rather than its L1 share bounds the resident CTAs (each
+// holds two row slices, up to 40 KB).
 std::atomic<int> g_bulk_carveout_set[64];
 
 cudaError_t launch_dyn_bulk(const SwigluParams& p, const RowPlan& plan, cudaStream_t s) {
