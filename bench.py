@@ -46,17 +46,17 @@ DEFAULT_WORKLOAD = "llama3.1-405b_fp8_T2048+ragged"
 # `src_sha256` (kernel_src_hash).
 TRAFFIC: Dict[str, Dict] = {
     # profiles/swiglu_q8_dynamic_T4096_I28672.md
-    "swiglu_q8_dynamic_T4096_I28672": {"bytes": 539456256, "src_sha256": "49260d006bde0def11f8aa4a1f56077217f24815dfce4c534a11e2439189ec34"},
+    "swiglu_q8_dynamic_T4096_I28672": {"bytes": 539456256, "src_sha256": "849582ef35a93e1ad365304d71de45e588c31f4ec0445b995fcc2045cf6bfdfe"},
     # profiles/allreduce_rmsnorm_q8_static_k8_T2048_H16384.md
-    "allreduce_rmsnorm_q8_static_k8_T2048_H16384": {"bytes": 680083712, "src_sha256": "69d14552657702ffe7eae79b2440600db263b29684eec120b4756ac1845077a0"},
+    "allreduce_rmsnorm_q8_static_k8_T2048_H16384": {"bytes": 680083712, "src_sha256": "13f15eb1dca99e9c05a95cef2020adc193334f695d1c618baf7bcc7711dfc44a"},
     # profiles/add_rmsnorm_nvfp4_T2048_H16384.md
-    "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 167228416, "src_sha256": "69d14552657702ffe7eae79b2440600db263b29684eec120b4756ac1845077a0"},
+    "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 167228416, "src_sha256": "13f15eb1dca99e9c05a95cef2020adc193334f695d1c618baf7bcc7711dfc44a"},
     # profiles/swiglu_nvfp4_T2048_I53248.md
-    "swiglu_nvfp4_T2048_I53248": {"bytes": 467772160, "src_sha256": "49260d006bde0def11f8aa4a1f56077217f24815dfce4c534a11e2439189ec34"},
+    "swiglu_nvfp4_T2048_I53248": {"bytes": 467772160, "src_sha256": "849582ef35a93e1ad365304d71de45e588c31f4ec0445b995fcc2045cf6bfdfe"},
     # profiles/swiglu_q8_dynamic_T2048_I53248.md
-    "swiglu_q8_dynamic_T2048_I53248": {"bytes": 527144960, "src_sha256": "49260d006bde0def11f8aa4a1f56077217f24815dfce4c534a11e2439189ec34"},
+    "swiglu_q8_dynamic_T2048_I53248": {"bytes": 527144960, "src_sha256": "849582ef35a93e1ad365304d71de45e588c31f4ec0445b995fcc2045cf6bfdfe"},
     # profiles/add_rmsnorm_q8_static_T2048_H16384.md
-    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 177783808, "src_sha256": "69d14552657702ffe7eae79b2440600db263b29684eec120b4756ac1845077a0"},
+    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 177783808, "src_sha256": "13f15eb1dca99e9c05a95cef2020adc193334f695d1c618baf7bcc7711dfc44a"},
 }
 
 
@@ -82,8 +82,9 @@ def decode_sweep_workload() -> wl.Workload:
 
 def kernel_src_hash(call) -> str:
     """sha256 over what one call's kernel and its launch shape are built from: the C-ABI header, the shared
-    device headers, the planner (api.cu), the kernel's translation unit and inline body (comments removed), and
-    the packaged launch-shape tables. Unchanged when only other kernels' sources or comments change."""
+    device headers, the planner (api.cu), the kernel's translation unit and inline body (comments and whitespace
+    removed), and the packaged launch-shape tables. Unchanged when only other kernels' sources, comments or
+    layout change."""
     csrc = os.path.join(ROOT, "memory_bound_decoder_gb300", "csrc")
     own = ["swiglu.cu", "swiglu_impl.cuh"] if call.kind.startswith("swiglu") else ["norm.cu", "norm_impl.cuh"]
     paths = [os.path.join(ROOT, "include", "mbd.h")] + [os.path.join(csrc, f) for f in
@@ -94,8 +95,8 @@ def kernel_src_hash(call) -> str:
     for p in paths:
         with open(p, "rb") as fh:
             text = fh.read()
-        if not p.endswith(".json"):   # comments do not change what is built
-            text = re.sub(rb"/\*.*?\*/|//[^\n]*", b"", text, flags=re.S)
+        if not p.endswith(".json"):   # comments and layout do not change what is built
+            text = re.sub(rb"\s+", b"", re.sub(rb"/\*.*?\*/|//[^\n]*", b"", text, flags=re.S))
         h.update(os.path.basename(p).encode() + text)
     return h.hexdigest()
 
