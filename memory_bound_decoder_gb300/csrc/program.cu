@@ -179,6 +179,13 @@ __device__ void norm_run(const ProgOp* ops, int n, int64_t row, ProgSmem& sm) {
         xv = load_stream(static_cast<const uint4*>(ops[0].in) + row * nvec + c);
         wv[0] = load_cached(static_cast<const uint4*>(ops[0].weight) + c);
     }
+    // static FP8: the op's code multiplier 1 / scale, its scale loaded one op ahead (a global load and a
+    // division per op would otherwise sit on the chain)
+    float qmul = 0.0f, sc_next = 0.0f;
+    if constexpr (EP == kFp8Static) {
+        const float sc = __ldg(ops[0].scale);
+        qmul = sc > 0.0f ? 1.0f / sc : 0.0f;
+    }
     for (int k = 0; k < n; ++k) {
         const ProgOp& op = ops[k];
         float2 ss2 = f2(0.0f);
@@ -197,6 +204,9 @@ __device__ void norm_run(const ProgOp* ops, int n, int64_t row, ProgSmem& sm) {
             xv = load_stream(static_cast<const uint4*>(ops[k + 1].in) + row * nvec + c);
             wn = load_cached(static_cast<const uint4*>(ops[k + 1].weight) + c);
         }
+        if constexpr (EP == kFp8Static) {
+            if (k + 1 < n) sc_next = __ldg(ops[k + 1].scale);
+        }
         // Partials alternate between two buffers: when a thread writes op k + 2's partials into this one,
         // every thread has passed op k + 1's barrier and so has read op k's, so no barrier closes the op.
         const PSum t = block_total_tree(PSum{ss2.x + ss2.y}, sm.run_part[k & 1]);
@@ -204,19 +214,34 @@ __device__ void norm_run(const ProgOp* ops, int n, int64_t row, ProgSmem& sm) {
         // square root and two divisions: a few ulps, against a bf16 tolerance of 2^-7, and a shorter
         // dependent chain on the decode step's critical path
         const float inv = rsqrtf(t.v * inv_h + op.eps);
-        NormParams np;
-        np.x = op.in;
-        np.n_partials = 0;
-        np.residual = op.residual;
-        np.weight = op.weight;
-        np.out = op.out;
-        np.out_sf = op.out_sf;
-        np.scale = op.scale;
-        np.rows = op.rows;
-        np.nvec = op.nvec;
-        np.hidden = op.hidden;
-        np.eps = op.eps;
-        norm_store<1, EP>(np, row, 0, sv, wv, live, inv);
+        if constexpr (EP == kFp8Static) {   // the codes of v / scale, as norm_store forms them
+            if (live[0]) {
+                const float cm = inv * qmul;
+                const uint32_t* sw = reinterpret_cast<const uint32_t*>(&sv[0]);
+                const uint32_t* ww = reinterpret_cast<const uint32_t*>(&wv[0]);
+                float2 y[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    y[q] = __fmul2_rn(__fmul2_rn(bf16x2_to_float2(sw[q]), bf16x2_to_float2(ww[q])), f2(cm));
+                store_stream(reinterpret_cast<uint2*>(static_cast<uint8_t*>(op.out) + row * (int64_t)nvec * 8) + c,
+                             make_uint2(pack_e4m3x4(y[0], y[1]), pack_e4m3x4(y[2], y[3])));
+            }
+            if (k + 1 < n) qmul = sc_next > 0.0f ? 1.0f / sc_next : 0.0f;
+        } else {
+            NormParams np;
+            np.x = op.in;
+            np.n_partials = 0;
+            np.residual = op.residual;
+            np.weight = op.weight;
+            np.out = op.out;
+            np.out_sf = op.out_sf;
+            np.scale = op.scale;
+            np.rows = op.rows;
+            np.nvec = op.nvec;
+            np.hidden = op.hidden;
+            np.eps = op.eps;
+            norm_store<1, EP>(np, row, 0, sv, wv, live, inv);
+        }
         if (k + 1 < n) wv[0] = wn;
     }
     if (live[0]) store_stream(rr, sv[0]);
