@@ -1,4 +1,6 @@
 """Host logic of the bench's launch units: which calls of a step run as one program launch (no GPU)."""
+import os
+
 import bench
 import workloads as wl
 
@@ -58,3 +60,25 @@ def test_groups_split_at_the_op_limit():
     calls = [wl.Call("swiglu", 1 + i, 256, d) for i in range(10)]
     units = bench.launch_groups(calls, 1, 152, max_ops=4)
     assert units == [("bf16", [0, 1, 2, 3]), ("bf16", [4, 5, 6, 7]), ("bf16", [8, 9])]
+
+
+def test_traffic_hash_ignores_comments_and_layout_but_not_code(tmp_path, monkeypatch):
+    """A recorded DRAM traffic figure stays valid while the kernel's sources change only in comments or layout,
+    and is dropped (hash mismatch) when code changes."""
+    import shutil
+    root = tmp_path / "repo"
+    for sub in ("include", "memory_bound_decoder_gb300/csrc", "memory_bound_decoder_gb300/tuning"):
+        shutil.copytree(os.path.join(bench.ROOT, sub), root / sub)
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    call = next(c for w in bench.workloads_by_key().values() for c in w.calls if c.kind == "swiglu_q8")
+    base = bench.kernel_src_hash(call)
+    src = root / "memory_bound_decoder_gb300/csrc/swiglu.cu"
+    text = src.read_text()
+    src.write_text(text.replace("namespace mbd {", "// a new comment\n/* and a block\n   comment */\n\n  namespace mbd {", 1))
+    assert bench.kernel_src_hash(call) == base
+    src.write_text(text.replace("namespace mbd {", "namespace mbd { constexpr int kUnused = 1;", 1))
+    assert bench.kernel_src_hash(call) != base
+    src.write_text(text)
+    norm = root / "memory_bound_decoder_gb300/csrc/norm.cu"   # another kernel's source: no effect
+    norm.write_text(norm.read_text() + "\nstatic int unused_norm_symbol;\n")
+    assert bench.kernel_src_hash(call) == base
