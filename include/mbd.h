@@ -260,9 +260,11 @@ typedef struct {
 /* Largest number of ops in one program. */
 #define MBD_MAX_PROGRAM_OPS 128
 /* Largest hidden size of a norm in a program: one CTA of 256 threads holds the row, 4 vectors per thread.
- * SwiGLU rows of any width run in chunks. A dynamic FP8 SwiGLU row is held whole, at up to 8 vectors per
- * thread (16384 elements) in the programs whose epilogue sets include it; a wider one takes two passes: the
- * row maximum, then the codes from the same inputs, read again from L2. */
+ * SwiGLU rows of any width run in chunks. A dynamic FP8 SwiGLU row of up to 16384 elements is held whole by
+ * one CTA (1024 threads, 2 vectors each) in the programs whose epilogue sets include it, except where the
+ * program's chained norms run at one vector per thread (rows of up to 2048 elements), which keeps 256-thread
+ * CTAs; a row wider than its CTA holds takes two passes: the row maximum, then the codes from the same
+ * inputs, read again from L2. */
 #define MBD_MAX_PROGRAM_WIDTH 8192
 
 /*
@@ -279,7 +281,9 @@ typedef struct {
  * therefore runs only in the single-call entry points. Ops with n_tokens == 0 are skipped; if nothing
  * remains, nothing is launched.
  * Reductions run inside one CTA per row (no cluster), so sums may round differently from the single-call
- * entry points in their last bit; every result keeps the tolerances stated for those entry points.
+ * entry points in their last bit, and consecutive norms on one residual row form 1/sqrt(mean + eps) with the
+ * hardware reciprocal square root (a few ulps); every result keeps the tolerances stated for those entry
+ * points.
  */
 mbd_status mbd_run_program(const mbd_op* ops, int n_ops, mbd_stream_t stream);
 
