@@ -338,13 +338,16 @@ mbd_status mbd_program_plan_launch_uploaded(const mbd_program_plan* plan, const 
  * The schedule is copied (one asynchronous host-to-device copy on `stream`, as upload does) into a static
  * buffer of the library: MBD_STATIC_SCHEDULE_BYTES per device, part of the library's device image and held
  * by every GPU that loads the library until the process exits. The first call on a device looks up the
- * buffer's device address (cudaGetSymbolAddress, with that device current) and caches it; make that first
- * call before any stream capture. Nothing is allocated (no cudaMalloc, cudaFree or other allocating call).
- * Every call overwrites the part of the buffer its schedule uses, so plans may alternate freely; because
- * the buffer is shared, calls that overlap on the GPU race (e.g. on different streams of one device) and
- * must not be issued; calls on one stream are ordered. A schedule larger than the buffer returns
- * MBD_ERR_UNSUPPORTED (with this header's limits it always fits). Other errors as for
- * mbd_program_plan_launch.
+ * buffer's device address (cudaGetSymbolAddress, with that device current) and caches it together with the
+ * id of the current CUDA context; a call made in another context of that device (for instance after
+ * cudaDeviceReset has re-created the primary context, whose module image may sit elsewhere) looks it up
+ * again. Make the first call on a device, and the first after a reset, before any stream capture. Nothing is
+ * allocated (no cudaMalloc, cudaFree or other allocating call). Every call overwrites the buffer's whole
+ * schedule record with its own plan's, so plans may alternate freely; because the buffer is shared, calls
+ * that overlap on the GPU race (e.g. on different streams of one device) and must not be issued; calls on
+ * one stream are ordered. Every schedule the build accepts fits the buffer (a compile-time check of the
+ * library), so no plan is refused for its size. Errors as for mbd_program_plan_launch; MBD_ERR_CUDA also
+ * when the current device cannot be read or the address lookup fails (mbd_last_cuda_error has the cause).
  */
 #define MBD_STATIC_SCHEDULE_BYTES 16384
 mbd_status mbd_program_plan_launch_static(const mbd_program_plan* plan, mbd_stream_t stream);

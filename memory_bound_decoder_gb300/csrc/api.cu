@@ -8,8 +8,45 @@
 #include <memory>
 #include <vector>
 
+#include <cuda.h>
+
 #include "mbd.h"
 #include "launch.h"
+
+namespace mbd {
+
+unsigned long long current_context_id() {
+    using GetCurrent = CUresult (*)(CUcontext*);
+    using GetId = CUresult (*)(CUcontext, unsigned long long*);
+    struct Entry {
+        GetCurrent get_current = nullptr;
+        GetId get_id = nullptr;
+    };
+    // Driver entry points through the runtime, so the library links no driver library at build time.
+    static const Entry entry = [] {
+        Entry f;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            f.get_current = reinterpret_cast<GetCurrent>(p);
+        p = nullptr;
+        q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            f.get_id = reinterpret_cast<GetId>(p);
+        (void)cudaGetLastError();
+        return f;
+    }();
+    if (!entry.get_current || !entry.get_id) return 0;
+    CUcontext ctx = nullptr;
+    if (entry.get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    unsigned long long id = 0;
+    if (entry.get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+}  // namespace mbd
 
 namespace {
 
@@ -676,32 +713,27 @@ mbd_status launch_uploaded(const PlanImpl* plan, const void* schedule, cudaStrea
                                              plan->variant, plan->grid, stream));
 }
 
-// The library's static schedule buffer on each device: its address, looked up once per device.
-std::atomic<void*> g_static_schedule_addr[kMaxDevices];
+static_assert(kScheduleBytes <= mbd::kStaticScheduleBytes, "every schedule record fits the static buffer");
 
 // mbd_program_plan_launch_static: the uploaded-schedule launch, with the schedule copied into the static
 // buffer instead of caller memory. Nothing is allocated: the buffer is part of the module image.
 mbd_status launch_static(const PlanImpl* plan, cudaStream_t stream) {
     if (!plan || plan->magic != kPlanMagic) return MBD_ERR_INVALID_ARG;
     if (plan->grid == 0) return MBD_OK;
-    const size_t used = offsetof(mbd::ProgramParams, ops) + static_cast<size_t>(plan->P.n_ops) * sizeof(mbd::ProgOp);
-    if (used > mbd::kStaticScheduleBytes || kScheduleBytes > mbd::kStaticScheduleBytes) return MBD_ERR_UNSUPPORTED;
     int device = 0;
-    if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices) {
-        g_last_cuda_error = static_cast<int>(cudaErrorInvalidDevice);
+    const cudaError_t de = cudaGetDevice(&device);
+    if (de != cudaSuccess || device < 0 || device >= mbd::kMaxCachedDevices) {
+        g_last_cuda_error = static_cast<int>(de != cudaSuccess ? de : cudaErrorInvalidDevice);
         (void)cudaGetLastError();
         return MBD_ERR_CUDA;
     }
     if (device != plan->device) return MBD_ERR_INVALID_ARG;
-    void* addr = g_static_schedule_addr[device].load(std::memory_order_acquire);
-    if (!addr) {
-        const cudaError_t e = mbd::static_schedule_address(&addr);
-        if (e != cudaSuccess || !addr) {
-            g_last_cuda_error = static_cast<int>(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
-            (void)cudaGetLastError();
-            return MBD_ERR_CUDA;
-        }
-        g_static_schedule_addr[device].store(addr, std::memory_order_release);
+    void* addr = nullptr;
+    const cudaError_t e = mbd::static_schedule_address(device, &addr);
+    if (e != cudaSuccess) {
+        g_last_cuda_error = static_cast<int>(e);
+        (void)cudaGetLastError();
+        return MBD_ERR_CUDA;
     }
     const mbd_status st = upload_plan(plan, addr, mbd::kStaticScheduleBytes, stream);
     if (st != MBD_OK) return st;

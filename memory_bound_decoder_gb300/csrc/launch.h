@@ -116,10 +116,16 @@ bool program_norms_in_registers(int vpt, int variant);
 static_assert(sizeof(ProgOp) % 8 == 0 && sizeof(ProgramParams) % 8 == 0, "schedules are copied in 8-byte words");
 
 // The library's own schedule buffer (one per device, a static array of the module image), and its address
-// on the current device.
+// on `device`, which must be the current device (0 <= device < kMaxCachedDevices). The address is looked up
+// once per device and context: a context re-created on that device (cudaDeviceReset) is looked up again.
 constexpr size_t kStaticScheduleBytes = 16384;
 static_assert(sizeof(ProgramParams) <= kStaticScheduleBytes, "a schedule fits the static buffer");
-cudaError_t static_schedule_address(void** addr);
+constexpr int kMaxCachedDevices = 64;
+cudaError_t static_schedule_address(int device, void** addr);
+
+// The unique id (cuCtxGetId) of the calling thread's current CUDA context, or 0 when no context is current or
+// the driver does not report one. Host-side caches of per-context state key on it.
+unsigned long long current_context_id();
 
 // Program kernel `variant` for `vpt` vectors per thread (1, 2 or 4) on `grid` CTAs of kProgramThreads, or
 // in the wide form (vpt 8, where program_variant_has_vpt8) on `grid` CTAs of kProgramWideThreads; the

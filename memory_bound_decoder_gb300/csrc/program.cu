@@ -13,6 +13,7 @@
 // more than running them, hence CUDA graphs for decoding; "Introduction to torch.compile and How It Works
 // with vLLM", section 5: one kernel for a whole forward pass).
 #include <cstddef>
+#include <mutex>
 
 #include "norm_impl.cuh"
 #include "swiglu_impl.cuh"
@@ -496,11 +497,41 @@ cudaError_t launch_program(const ProgramParams& p, const ProgramParams* dev, int
 // Schedule storage of mbd_program_plan_launch_static, for callers that cannot allocate device memory: part
 // of the module image (every GPU that loads the library holds it until exit), so nothing is allocated when
 // it is used. In host code the name is a host-side stand-in, not a device address: the kernel gets the
-// address that cudaGetSymbolAddress returns with the device current (looked up once per device by the
-// caller of static_schedule_address).
+// address that cudaGetSymbolAddress returns with the device current.
 static __device__ __align__(256) unsigned char g_static_schedule[kStaticScheduleBytes];
 
-cudaError_t static_schedule_address(void** addr) { return cudaGetSymbolAddress(addr, g_static_schedule); }
+namespace {
+// Per device: the buffer's address and the id of the context it was looked up in. The module's globals live
+// in a context; cudaDeviceReset destroys the device's primary context, and the one that replaces it may load
+// the module at another address, so an address is reused only while the same context is current.
+struct StaticScheduleSlot {
+    unsigned long long context = 0;
+    void* addr = nullptr;
+};
+std::mutex g_static_schedule_mu;
+StaticScheduleSlot g_static_schedule_slot[kMaxCachedDevices];
+}  // namespace
+
+cudaError_t static_schedule_address(int device, void** addr) {
+    if (device < 0 || device >= kMaxCachedDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_static_schedule_mu);
+    StaticScheduleSlot& slot = g_static_schedule_slot[device];
+    const unsigned long long ctx = current_context_id();
+    if (ctx != 0 && slot.context == ctx && slot.addr) {
+        *addr = slot.addr;
+        return cudaSuccess;
+    }
+    void* a = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&a, g_static_schedule);
+    if (e != cudaSuccess) return e;
+    if (!a) return cudaErrorInvalidSymbol;
+    // The lookup makes the device's primary context current if none was, so its id is read afterwards; with
+    // no id (0) the slot never matches and every call looks the address up.
+    slot.context = current_context_id();
+    slot.addr = a;
+    *addr = a;
+    return cudaSuccess;
+}
 
 cudaError_t device_error_flags_program(unsigned int* flags, bool clear) {
     cudaError_t e = cudaMemcpyFromSymbol(flags, g_device_error_flags, sizeof(unsigned int));

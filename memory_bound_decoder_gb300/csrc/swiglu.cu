@@ -145,21 +145,25 @@ __global__ void __launch_bounds__(320, 4) swiglu_dyn_bulk_kernel(const __grid_co
     }
 }
 
-// Per device (up to 64): whether the bulk kernel's preferred carveout, the largest shared-memory share, has
-// been requested, so that the SM's shared memory rather than its L1 share bounds the resident CTAs (each
-// holds two row slices, up to 40 KB).
-std::atomic<int> g_bulk_carveout_set[64];
+// Per device (up to 64): the id of the context in which the bulk kernel's preferred carveout, the largest
+// shared-memory share, was last requested, so that the SM's shared memory rather than its L1 share bounds
+// the resident CTAs (each holds two row slices, up to 40 KB). A kernel attribute belongs to a context: a
+// context re-created on the device (cudaDeviceReset) gets the request again; with no context id (0) every
+// launch requests it.
+std::atomic<unsigned long long> g_bulk_carveout_ctx[kMaxCachedDevices];
 
 cudaError_t launch_dyn_bulk(const SwigluParams& p, const RowPlan& plan, cudaStream_t s) {
     if (plan.vpt != 4 || plan.ctas_per_row < 2 || plan.ctas_per_row > kMaxClusterCtas) return cudaErrorInvalidValue;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64 && !g_bulk_carveout_set[dev].load(std::memory_order_acquire)) {
+    const unsigned long long ctx = current_context_id();
+    if (dev < 0 || dev >= kMaxCachedDevices || ctx == 0 ||
+        g_bulk_carveout_ctx[dev].load(std::memory_order_acquire) != ctx) {
         e = cudaFuncSetAttribute(swiglu_dyn_bulk_kernel<4>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  static_cast<int>(cudaSharedmemCarveoutMaxShared));
         if (e != cudaSuccess) return e;
-        g_bulk_carveout_set[dev].store(1, std::memory_order_release);
+        if (dev >= 0 && dev < kMaxCachedDevices) g_bulk_carveout_ctx[dev].store(ctx, std::memory_order_release);
     }
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];

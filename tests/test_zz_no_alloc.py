@@ -3,14 +3,16 @@ device memory (engines that keep nearly all HBM in their own pool, plug-in inter
 its inputs and outputs, loops that cannot afford cudaMalloc's possible device synchronisation): its schedule
 goes to a static buffer of the library instead of caller memory. Checked against the entry point it stands in for
 (mbd_program_plan_upload into a caller buffer + mbd_program_plan_launch_uploaded): two consecutive calls of
-each, on identical fresh inputs, give identical bits; plans may alternate through the shared buffer; and
-the calls take no device memory. Collected last (file name), after every other GPU test.
+each, on identical fresh inputs, give identical bits; plans may alternate through the shared buffer; the
+calls take no device memory. Also checked directly against the oracle: two static launches in a row of a
+decode step, the second on the residual the first left, with bf16 outputs within tolerance and the final
+residual bit-exact. Collected last (file name), after every other GPU test.
 """
 import numpy as np
 import pytest
 
 import workloads as wl
-from tests.parity import dev_u16
+from tests.parity import check_bf16, dev_u16
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -111,3 +113,28 @@ def test_static_launches_take_no_device_memory():
     torch.cuda.synchronize()
     free1, _ = torch.cuda.mem_get_info()
     assert free1 == free0 and torch.cuda.memory_allocated() == alloc0
+
+
+def test_two_static_launches_match_the_oracle(orc):
+    """A 28-layer decode step (norm, norm, SwiGLU per layer, one residual) launched twice in a row through the
+    static buffer: each launch's outputs against the oracle run op by op, and the residual bit-exact."""
+    T, L, H, I, eps, seed = 3, 28, 1536, 8960, 1e-6, 51
+    plan, state = make_program(T=T, L=L, seed=seed, H=H, I=I, eps=eps)
+    R, outs, _ = state
+    r = wl.make_norm_inputs(T, H, seed, wl.N01, eps, salt=999).residual
+    for call in range(2):
+        plan.launch_static()
+        torch.cuda.synchronize()
+        for l in range(L):
+            n1 = wl.make_norm_inputs(T, H, seed, wl.N01, eps, salt=3 * l)
+            n2 = wl.make_norm_inputs(T, H, seed, wl.N01, eps, salt=3 * l + 1)
+            gu = wl.make_swiglu_inputs(T, I, seed, wl.N01, salt=3 * l + 2)
+            O1, O2, Y = (t.cpu().numpy().view(np.uint16) for t in outs[3 * l:3 * l + 3])
+            r, _, v1 = orc.add_rmsnorm(n1.x, r, n1.weight, eps)
+            check_bf16(O1.reshape(T, H), v1, f"call {call} layer {l} norm 1")
+            r, _, v2 = orc.add_rmsnorm(n2.x, r, n2.weight, eps)
+            check_bf16(O2.reshape(T, H), v2, f"call {call} layer {l} norm 2")
+            _, h = orc.swiglu(gu.gate_up)
+            check_bf16(Y.reshape(T, I), h, f"call {call} layer {l} swiglu")
+        np.testing.assert_array_equal(R.numpy(np.uint16).reshape(T, H), r,
+                                      f"call {call}: the residual must be bit-exact")
