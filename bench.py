@@ -479,22 +479,81 @@ class ProgramGroup:
         return sum(t.numel() * t.element_size() for t, _ in self.d2h)
 
 
-def launch_groups(calls: List[wl.Call], layers: int, sms: int, max_ops: int = 128) -> list:
+class BatchCall:
+    """The calls of one batch, seen as one call (name, token count, algorithmic bytes)."""
+
+    def __init__(self, calls: List[wl.Call]):
+        self.calls = calls
+        self.kind, self.mode = "batch", None
+        self.name = f"batch_{len(calls)}ops_" + "+".join(c.name for c in calls)
+        self.T = sum(c.T for c in calls)
+
+    def algorithmic_bytes(self) -> int:
+        return sum(c.algorithmic_bytes() for c in self.calls)
+
+
+class BatchGroup:
+    """Independent calls of one step run as ONE call of mbd_run_independent: each op keeps its own single-call
+    kernel and launch shape, and each launch after the first overlaps the one before it. Same buffers, same
+    outputs (bit for bit) as the calls' own launches."""
+
+    def __init__(self, mbd, members: List[DeviceCall]):
+        self.members, self.mbd = members, mbd
+        self.call = BatchCall([d.call for d in members])
+        self.arr, self.n = mbd.program_array([d.op() for d in members])
+        self.h2d = [x for d in members for x in d.h2d]
+        self.d2h = [x for d in members for x in d.d2h]
+        self.handle = None
+
+    def bind(self, stream_handle: int):
+        for d in self.members:
+            d.bind(stream_handle)
+        self.handle = stream_handle
+
+    def launch(self):
+        lib = self.mbd.get_lib()
+        rc = lib.mbd_run_independent(self.arr, self.n, self.handle)
+        if rc != 0:
+            raise RuntimeError(f"{self.call.name}: {lib.mbd_status_string(rc).decode()}")
+
+    def bytes_in(self):
+        return sum(t.numel() * t.element_size() for t, _ in self.h2d)
+
+    def bytes_out(self):
+        return sum(t.numel() * t.element_size() for t, _ in self.d2h)
+
+
+def launch_groups(calls: List[wl.Call], layers: int, sms: int, max_ops: int = 128, max_batch: int = 64,
+                  programs: bool = True, batches: bool = True) -> list:
     """Launch units of one step, in order: an int (the index of a call launched on its own) or (label, [indices])
-    (calls run as one program launch). Calls with fewer tokens than the GPU has SMs are bound by launch latency,
-    not bandwidth; those a program takes are gathered into one program launch placed where the first of them
-    stood (at most max_ops per launch): the bf16 and FP8 ones together when all their rows fit one row per SM
-    (one wave of the mixed variant, which runs at one CTA per SM), else one launch per class; NVFP4 ones in a
-    launch of their own. Only in one-layer steps, whose calls share no buffer, so that running them together
-    computes exactly what the sequence of launches does."""
+    (calls run together). Only in one-layer steps, whose calls share no buffer, so that running them together,
+    in any order, computes exactly what the sequence of launches does.
+    - Calls with fewer tokens than the GPU has SMs are bound by launch latency, not bandwidth; those a program
+      takes are gathered into program launches (at most max_ops each): the bf16 and FP8 ones together when all
+      their rows fit one row per SM (one wave of the mixed variant, which runs at one CTA per SM), else one
+      launch per class; NVFP4 ones in a launch of their own.
+    - The call with the most algorithmic bytes keeps a launch of its own (the bench times it with CUDA events,
+      which would split a batch). The other calls of at least one row per SM, if there are two or more, run as
+      one batch of their own single-call launches, each overlapping the one before (label "batch",
+      mbd_run_independent, at most max_batch per batch): a call of a thousand rows streams its bytes in a few
+      microseconds, about as long as a launch takes to ramp up and drain.
+    - Order: the largest call, then the batches, then the programs, then any other call in list order (with
+      batches, the tails of the large launches overlap the next; the latency-bound programs come last).
+    Without batches the units keep list order, each group where its first call stood."""
     if layers != 1:
         return list(range(len(calls)))
     cls: Dict[int, str] = {}
     for i, c in enumerate(calls):
         v = PROGRAM_CLASS.get((c.kind, c.mode if "q8" in c.kind else None))
         small = c.T < sms and not (c.kind.startswith("add") and c.width > PROGRAM_MAX_NORM_WIDTH)
-        if v is not None and small:
+        if programs and v is not None and small:
             cls[i] = v
+    largest = max(range(len(calls)), key=lambda i: calls[i].algorithmic_bytes()) if calls else -1
+    batch = [i for i, c in enumerate(calls) if batches and i != largest and c.T >= sms
+             and not c.kind.startswith("allreduce")]
+    if len(batch) >= 2:
+        for i in batch:
+            cls[i] = "batch"
     mixed_rows = sum(calls[i].T for i, v in cls.items() if v in ("bf16", "fp8"))
     key = {i: ("bf16+fp8" if v in ("bf16", "fp8") and mixed_rows <= sms else v) for i, v in cls.items()}
     groups: Dict[str, List[int]] = {}
@@ -512,17 +571,30 @@ def launch_groups(calls: List[wl.Call], layers: int, sms: int, max_ops: int = 12
         if isinstance(u, str):
             idx = groups[u]
             label = "+".join(sorted({cls[i] for i in idx}))   # what the launch holds
-            units += [(label, idx[k:k + max_ops]) for k in range(0, len(idx), max_ops)]
+            step = max_batch if u == "batch" else max_ops
+            units += [(label, idx[k:k + step]) for k in range(0, len(idx), step)]
         else:
             units.append(u)
+    if "batch" in groups:
+        rank = lambda u: (0 if u == largest else 3) if isinstance(u, int) else (1 if u[0] == "batch" else 2)
+        units.sort(key=rank)   # stable: list order within each rank
     return units
 
 
-def group_small_calls(torch, mbd, work: wl.Workload, dcalls: List[DeviceCall], sms: int, dev) -> list:
-    """The step's launch units (launch_groups): DeviceCalls and ProgramGroups."""
-    units = launch_groups([d.call for d in dcalls], work.layers, sms, mbd.MAX_PROGRAM_OPS)
-    return [dcalls[u] if isinstance(u, int) else ProgramGroup(torch, mbd, u[0], [dcalls[i] for i in u[1]], dev)
-            for u in units]
+def group_small_calls(torch, mbd, work: wl.Workload, dcalls: List[DeviceCall], sms: int, dev,
+                      programs: bool = True, batches: bool = True) -> list:
+    """The step's launch units (launch_groups): DeviceCalls, ProgramGroups and BatchGroups."""
+    units = launch_groups([d.call for d in dcalls], work.layers, sms, mbd.MAX_PROGRAM_OPS, mbd.MAX_INDEPENDENT_OPS,
+                          programs, batches)
+    out = []
+    for u in units:
+        if isinstance(u, int):
+            out.append(dcalls[u])
+        elif u[0] == "batch":
+            out.append(BatchGroup(mbd, [dcalls[i] for i in u[1]]))
+        else:
+            out.append(ProgramGroup(torch, mbd, u[0], [dcalls[i] for i in u[1]], dev))
+    return out
 
 
 def run_e2e(torch, dcalls: List[DeviceCall], kstream, dev, steps: int, step_bytes: int, world: int) -> Dict:
@@ -733,6 +805,227 @@ def run_decode_table(args) -> Dict:
             "table": table}
 
 
+def prepare_step(torch, mbd, args, work: wl.Workload, rank: int, dev, props):
+    """Device buffers and launch units of one step of `work`, bound to a fresh stream."""
+    t_gen = time.perf_counter()
+    dcalls = build_device_calls(torch, mbd, work, args.seed, rank, dev)
+    n_calls = len(dcalls)
+    if not (args.no_programs and args.no_batches):
+        dcalls = group_small_calls(torch, mbd, work, dcalls, props.multi_processor_count, dev,
+                                   programs=not args.no_programs, batches=not args.no_batches)
+    log(f"[bench] rank {rank}: {work.key}: inputs for {n_calls} calls in {len(dcalls)} launch units ready in "
+        f"{time.perf_counter() - t_gen:.1f}s")
+    stream = torch.cuda.Stream(device=dev)
+    handle = int(stream.cuda_stream)
+    for d in dcalls:
+        d.bind(handle)
+    return dcalls, stream
+
+
+def time_step(torch, mbd, dcalls, stream, steps: int, warmup: int, dev, props, rank: int, world: int) -> Dict:
+    """W untimed steps, a per-unit breakdown pass (CUDA events around every launch unit, untimed), then exactly
+    `steps` timed steps between events on the launch stream (barrier and synchronise on both sides), with events
+    around the roofline kernel's launch in every step and the clocks sampled meanwhile."""
+    def step():
+        for d in dcalls:
+            d.launch()
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+    torch.cuda.synchronize(dev)
+
+    nb = max(3, min(20, steps))
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in dcalls]
+           for _ in range(nb)]
+    with torch.cuda.stream(stream):
+        for k in range(nb):
+            for d, (a, b) in zip(dcalls, evs[k]):
+                a.record(stream)
+                d.launch()
+                b.record(stream)
+    torch.cuda.synchronize(dev)
+    per_call_ms = [statistics.median(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(nb))
+                   for i in range(len(dcalls))]
+    # the roofline kernel: the slowest launch of a single call (batches and programs hold several kernels)
+    singles = [i for i, d in enumerate(dcalls) if isinstance(d, DeviceCall)] or list(range(len(dcalls)))
+    dom = max(singles, key=lambda i: per_call_ms[i])
+
+    clock = ClockSampler(str(getattr(props, "uuid", ""))) if rank == 0 else None
+    dom_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if clock:
+        clock.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = mbd.kernel_launches()
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for k in range(steps):
+            for i, d in enumerate(dcalls):
+                if i == dom:
+                    dom_ev[k][0].record(stream)
+                    d.launch()
+                    dom_ev[k][1].record(stream)
+                else:
+                    d.launch()
+        ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    launches = mbd.kernel_launches() - launches0
+    clocks = clock.stop(t0, t1) if clock else None
+    return {"elapsed_ms": max_over_ranks(ev0.elapsed_time(ev1), dev), "per_call_ms": per_call_ms, "dom": dom,
+            "dom_ms": statistics.mean(a.elapsed_time(b) for a, b in dom_ev), "clocks": clocks, "launches": launches}
+
+
+def step_summary(work: wl.Workload, dcalls, t: Dict, steps: int, world: int) -> Dict:
+    """value (GB/s), tokens/s, the roofline of the dominant kernel and the per-unit breakdown of a timed step."""
+    peak, peak_kind = measured_peak()
+    step_bytes = work.algorithmic_bytes()
+    dcall = dcalls[t["dom"]]
+    dom_bytes = dcall.call.algorithmic_bytes()
+    achieved = dom_bytes / (t["dom_ms"] / 1e3) / 1e9
+    tr = TRAFFIC.get(dcall.call.name)
+    traffic = tr["bytes"] if tr and tr.get("src_sha256") == kernel_src_hash(dcall.call) else None
+    kernels, seen = [], set()
+    for d in dcalls:
+        if d.call.name in seen:
+            continue
+        seen.add(d.call.name)
+        idx = [j for j, e in enumerate(dcalls) if e.call.name == d.call.name]
+        ms = statistics.mean(t["per_call_ms"][j] for j in idx)
+        b = d.call.algorithmic_bytes()
+        kernels.append({"call": d.call.name, "us": round(ms * 1e3, 2), "GBps": round(b / (ms / 1e3) / 1e9, 1),
+                        "frac_of_measured_peak": round(b / (ms / 1e3) / 1e9 / peak, 4),
+                        "tokens_per_s": round(d.call.T / (ms / 1e3), 1), "bytes": b, "launches_per_step": len(idx)})
+    value = aggregate_rate(step_bytes, steps, world, t["elapsed_ms"])
+    return {
+        "value": round(value, 3), "ms_per_step": round(t["elapsed_ms"] / steps, 5),
+        "frac_of_measured_peak": round(value / world / peak, 4),
+        "tokens_per_s": round(work.tokens() * steps * world / (t["elapsed_ms"] / 1e3), 1),
+        "gpu_launches": int(t["launches"]),
+        "roofline": {"bound": "hbm", "kernel": dcall.call.name, "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes": dom_bytes, "us_per_launch": round(t["dom_ms"] * 1e3, 2),
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                     else "fallback 6.8 TB/s", "frac_of_nominal_8TBps": round(achieved / 8000.0, 4)},
+        "kernels": kernels,
+        "clocks": t["clocks"],
+    }
+
+
+def measure_configs(torch, mbd, args, dev, props, headline: Dict, head_work: wl.Workload) -> Dict:
+    """One entry per named workload configuration, each with its own CUDA-event timing and clock samples:
+    the Qwen2.5-1.5B 16-token layer (latency, L2 flushed before every step, and back to back), the
+    Qwen2.5-1.5B decode sweep (28 layers per step as one program launch: us per layer, GB/s, tokens/s), the
+    Llama-3-8B prefill and Llama-3-70B FP8 steps (GB/s, fraction of the measured copy, the dominant kernel's
+    roofline, tokens/s) and the headline step."""
+    peak, _ = measured_peak()
+    lib = mbd.get_lib()
+    l2 = int(getattr(props, "L2_cache_size", 0)) or 126 * 2 ** 20
+    flush = torch.empty(4 * l2, dtype=torch.uint8, device=dev)
+    out: Dict[str, Dict] = {}
+    steps = args.config_steps
+
+    # Qwen2.5-1.5B, 16 tokens: latency-bound (the step's 1 MB stays in L2 when repeated)
+    work = wl.qwen_t16()
+    dcalls, stream = prepare_step(torch, mbd, args, work, 0, dev, props)
+    warm = time_step(torch, mbd, dcalls, stream, steps, args.warmup, dev, props, 0, 1)
+    cold = []
+    clock = ClockSampler(str(getattr(props, "uuid", "")))
+    clock.start()
+    t0 = time.time()
+    for _ in range(steps):
+        with torch.cuda.stream(stream):
+            flush.fill_(1)                     # evicts the step's buffers from L2 (outside the events)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for d in dcalls:
+                d.launch()
+            b.record(stream)
+        cold.append((a, b))
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    cold_us = statistics.median(a.elapsed_time(b) for a, b in cold) * 1e3
+    B = work.algorithmic_bytes()
+    warm_us = warm["elapsed_ms"] / steps * 1e3
+    out["qwen2.5-1.5b_t16"] = {
+        "calls": [c.name for c in work.calls], "launch_units": [d.call.name for d in dcalls],
+        "bytes_per_step": B, "us_per_step_l2_flushed": round(cold_us, 2), "us_per_step_back_to_back": round(warm_us, 2),
+        "GBps_l2_flushed": round(B / cold_us / 1e3, 1), "tokens_per_s_l2_flushed": round(16 / cold_us * 1e6, 1),
+        "basis": f"median of {steps} steps, each between CUDA events after an L2 flush; and {steps} steps back to back",
+        "clocks": clock.stop(t0, t1)}
+    del dcalls
+    torch.cuda.empty_cache()
+
+    # Qwen2.5-1.5B decode sweep: 28 layers of (add+RMSNorm, add+RMSNorm, SwiGLU), one program launch per step
+    rows = {}
+    clock = ClockSampler(str(getattr(props, "uuid", "")))
+    clock.start()
+    t0 = time.time()
+    for w in wl.qwen_decode_sweep():
+        T = w.calls[0].T
+        dc = build_device_calls(torch, mbd, w, args.seed, 0, dev)
+        st = torch.cuda.Stream(device=dev)
+        h = int(st.cuda_stream)
+        plans = [mbd.program_plan_build([d.op() for d in dc][i:i + mbd.MAX_PROGRAM_OPS])
+                 for i in range(0, len(dc), mbd.MAX_PROGRAM_OPS)]
+        scheds = [torch.empty(mbd.program_schedule_bytes(), dtype=torch.uint8, device=dev) for _ in plans]
+        for p_, sc in zip(plans, scheds):
+            p_.upload(sc, h)
+        pairs = [(ctypes.addressof(p_.buf), sc.data_ptr()) for p_, sc in zip(plans, scheds)]
+
+        def launch():
+            for pp, sp in pairs:
+                rc = lib.mbd_program_plan_launch_uploaded(pp, sp, h)
+                if rc != 0:
+                    raise RuntimeError(lib.mbd_status_string(rc).decode())
+
+        with torch.cuda.stream(st):
+            for _ in range(args.warmup):
+                launch()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(st):
+            e0.record(st)
+            for _ in range(steps):
+                launch()
+            e1.record(st)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / steps
+        Bw = w.algorithmic_bytes()
+        rows[str(T)] = {"us_per_layer": round(ms * 1e3 / w.layers, 3), "us_per_step": round(ms * 1e3, 2),
+                        "GBps": round(Bw / (ms / 1e3) / 1e9, 1), "frac_of_measured_peak": round(Bw / (ms / 1e3) / 1e9 / peak, 4),
+                        "tokens_per_s": round(T / (ms / 1e3), 1), "bytes_per_step": Bw, "launches_per_step": len(plans)}
+        del dc, plans, scheds
+        torch.cuda.empty_cache()
+    t1 = time.time()
+    out["qwen2.5-1.5b_decode_sweep"] = {
+        "per_tokens": rows, "layers": 28, "launch": "one program launch per step (plan built once, schedule uploaded once)",
+        "basis": f"{steps} steps back to back between CUDA events per token count; below ~64 tokens the step's "
+                 "buffers stay in L2 between steps, so these are latencies", "clocks": clock.stop(t0, t1)}
+
+    # bandwidth-bound configurations
+    for work in (wl.llama3_8b_prefill(), wl.llama3_70b_fp8()):
+        dcalls, stream = prepare_step(torch, mbd, args, work, 0, dev, props)
+        t = time_step(torch, mbd, dcalls, stream, steps, args.warmup, dev, props, 0, 1)
+        e = step_summary(work, dcalls, t, steps, 1)
+        e.update({"calls": [c.name for c in work.calls], "bytes_per_step": work.algorithmic_bytes(),
+                  "l2": "inputs larger than L2, no flush"})
+        out[work.key] = e
+        del dcalls
+        torch.cuda.empty_cache()
+
+    out[head_work.key] = {"see": "the line's headline (value, roofline, kernels, clocks)",
+                          "value": headline["value"], "frac_of_measured_peak": headline["frac_of_measured_peak"],
+                          "roofline_frac": headline["roofline"]["frac"], "tokens_per_s": headline["tokens_per_s"]}
+    return out
+
+
 def run_mine(args, work: wl.Workload, rank: int, world: int, local_rank: int) -> Optional[Dict]:
     import torch
     import memory_bound_decoder_gb300 as mbd
@@ -750,77 +1043,9 @@ def run_mine(args, work: wl.Workload, rank: int, world: int, local_rank: int) ->
     props = torch.cuda.get_device_properties(dev)
     l2_bytes = int(getattr(props, "L2_cache_size", 0)) or 126 * 2 ** 20
 
-    t_gen = time.perf_counter()
-    dcalls = build_device_calls(torch, mbd, work, args.seed, rank, dev)
-    n_calls = len(dcalls)
-    if not args.no_programs:
-        dcalls = group_small_calls(torch, mbd, work, dcalls, props.multi_processor_count, dev)
-    log(f"[bench] rank {rank}: inputs for {n_calls} calls in {len(dcalls)} launches ready in "
-        f"{time.perf_counter() - t_gen:.1f}s")
-
-    stream = torch.cuda.Stream(device=dev)
-    handle = int(stream.cuda_stream)
-    for d in dcalls:
-        d.bind(handle)
+    dcalls, stream = prepare_step(torch, mbd, args, work, rank, dev, props)
     step_bytes = work.algorithmic_bytes()
-
-    def step():
-        for d in dcalls:
-            d.launch()
-
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            step()
-    torch.cuda.synchronize(dev)
-
-    # per-launch breakdown (untimed pass): CUDA events around every launch on the launch stream
-    nb = max(3, min(20, args.steps))
-    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in dcalls]
-           for _ in range(nb)]
-    with torch.cuda.stream(stream):
-        for k in range(nb):
-            for d, (a, b) in zip(dcalls, evs[k]):
-                a.record(stream)
-                d.launch()
-                b.record(stream)
-    torch.cuda.synchronize(dev)
-    per_call_ms = [statistics.median(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(nb))
-                   for i in range(len(dcalls))]
-    dom = int(np.argmax(per_call_ms))
-
-    # timed region: exactly K steps; events around the dominant launch in every step
-    clock = ClockSampler(str(getattr(props, "uuid", ""))) if rank == 0 else None
-    dom_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if clock:
-        clock.start()
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(dev)
-    launches0 = mbd.kernel_launches()
-    t0 = time.time()
-    with torch.cuda.stream(stream):
-        ev0.record(stream)
-        for k in range(args.steps):
-            for i, d in enumerate(dcalls):
-                if i == dom:
-                    dom_ev[k][0].record(stream)
-                    d.launch()
-                    dom_ev[k][1].record(stream)
-                else:
-                    d.launch()
-        ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    t1 = time.time()
-    if world > 1:
-        torch.distributed.barrier()
-    launches = mbd.kernel_launches() - launches0
-    elapsed_ms = ev0.elapsed_time(ev1)
-    clocks = clock.stop(t0, t1) if clock else None
-    dom_ms = statistics.mean(a.elapsed_time(b) for a, b in dom_ev)
-
-    elapsed_ms = max_over_ranks(elapsed_ms, dev)
+    t = time_step(torch, mbd, dcalls, stream, args.steps, args.warmup, dev, props, rank, world)
 
     # end-to-end leg through the same public entry points: host buffers, copies inside the timed region
     e2e = None
@@ -829,56 +1054,44 @@ def run_mine(args, work: wl.Workload, rank: int, world: int, local_rank: int) ->
 
     if rank != 0:
         return None
-
-    peak, peak_kind = measured_peak()
-    dcall = dcalls[dom]
-    dom_bytes = dcall.call.algorithmic_bytes()
-    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
-    kname = f"{dcall.call.kind}{'_' + dcall.call.mode if dcall.call.mode else ''}"
-    tr = TRAFFIC.get(dcall.call.name)
-    traffic = tr["bytes"] if tr and tr.get("src_sha256") == kernel_src_hash(dcall.call) else None
-    kernels = []
-    seen = set()
-    for i, d in enumerate(dcalls):
-        if d.call.name in seen:
-            continue
-        seen.add(d.call.name)
-        idx = [j for j, e in enumerate(dcalls) if e.call.name == d.call.name]
-        ms = statistics.mean(per_call_ms[j] for j in idx)
-        b = d.call.algorithmic_bytes()
-        kernels.append({"call": d.call.name, "us": round(ms * 1e3, 2), "GBps": round(b / (ms / 1e3) / 1e9, 1),
-                        "frac_of_measured_peak": round(b / (ms / 1e3) / 1e9 / peak, 4),
-                        "tokens_per_s": round(d.call.T / (ms / 1e3), 1), "bytes": b, "launches_per_step": len(idx)})
-    tokens = work.tokens()
+    summ = step_summary(work, dcalls, t, args.steps, world)
+    tuning_desc = f"tuning table {os.path.relpath(tuning, ROOT)}" if tuning else "built-in rules"
     result = {
-        "metric": METRIC, "value": round(aggregate_rate(step_bytes, args.steps, world, elapsed_ms), 3),
+        "metric": METRIC, "value": summ["value"],
         "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(elapsed_ms / args.steps, 5), "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": summ["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": work.key, "description": work.description,
                    "calls": [c.name for c in work.calls], "layers": work.layers, "seed": args.seed,
-                   "bytes_per_step": step_bytes, "tokens_per_step": tokens,
+                   "bytes_per_step": step_bytes, "tokens_per_step": work.tokens(),
                    "io": "bf16 inputs; bf16 or E4M3 outputs; fp32 arithmetic",
                    "l2": f"inputs larger than L2: {step_bytes / 2 ** 20:.0f} MiB of distinct buffers per step "
                          f"vs {l2_bytes / 2 ** 20:.0f} MiB L2, no flush",
                    "parallelism": f"replicas x{world} (rows are independent; no collective)",
-                   "launch_shapes": f"tuning table {os.path.relpath(tuning, ROOT)}" if tuning else "built-in rules",
+                   "launch_shapes": tuning_desc,
                    "launch_units": [d.call.name for d in dcalls],
                    "small_calls": ("the calls with fewer tokens than SMs run as program launches (bf16 and FP8 "
                                    "together while their rows fit one per SM, NVFP4 apart; --no-programs: one "
                                    "launch per call)"
-                                   if any(isinstance(d, ProgramGroup) for d in dcalls) else "one launch per call")},
-        "tokens_per_s": round(tokens * args.steps * world / (elapsed_ms / 1e3), 1),
-        "gpu_launches": int(launches),
-        "roofline": {"bound": "hbm", "kernel": dcall.call.name, "achieved": round(achieved, 1),
-                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "algorithmic_bytes": dom_bytes, "us_per_launch": round(dom_ms * 1e3, 2),
-                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-                     else "fallback 6.8 TB/s", "frac_of_nominal_8TBps": round(achieved / 8000.0, 4)},
-        "kernels": kernels,
-        "clocks": clocks,
+                                   if any(isinstance(d, ProgramGroup) for d in dcalls) else "one launch per call"),
+                   "batches": ("the calls of at least one row per SM other than the largest run as one batch "
+                               "of overlapping single-call launches (mbd_run_independent; --no-batches: one launch "
+                               "unit per call)"
+                               if any(isinstance(d, BatchGroup) for d in dcalls) else "none"),
+                   "roofline_events": "CUDA events around the roofline kernel's launch in every timed step (they "
+                                      "break its overlap with the launches beside it)"},
+        "frac_of_measured_peak": summ["frac_of_measured_peak"],
+        "tokens_per_s": summ["tokens_per_s"],
+        "gpu_launches": summ["gpu_launches"],
+        "roofline": summ["roofline"],
+        "kernels": summ["kernels"],
+        "clocks": summ["clocks"],
         "e2e": e2e,
     }
+    if world == 1 and not args.no_configs and work.key == DEFAULT_WORKLOAD:
+        del dcalls
+        torch.cuda.empty_cache()
+        result["configs"] = measure_configs(torch, mbd, args, dev, props, result, work)
     return result
 
 
@@ -895,6 +1108,14 @@ def main():
     ap.add_argument("--calls", default="", help="comma-separated call names: run only these calls of the workload")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration block (default workload only: the Qwen2.5-1.5B 16-token layer and "
+                         "decode sweep, Llama-3-8B prefill and Llama-3-70B FP8 steps, each timed on its own)")
+    ap.add_argument("--config-steps", type=int, default=200, help="timed steps per configuration of that block")
+    ap.add_argument("--no-batches", action="store_true",
+                    help="no batches: every call of at least one row per SM of a one-layer step gets a launch unit of "
+                         "its own (default: all but the largest run as one mbd_run_independent batch of overlapping "
+                         "launches)")
     ap.add_argument("--no-programs", action="store_true",
                     help="launch every call on its own (default: the calls with fewer tokens than SMs of a one-layer "
                          "step run as program launches: bf16 and FP8 ones together while their rows fit one per SM)")

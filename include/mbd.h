@@ -84,7 +84,7 @@ typedef enum {
 #define MBD_MAX_REDUCED_WIDTH 262144
 
 /* ABI version of this header (bumped on any signature change or added entry point). */
-#define MBD_ABI_VERSION 7
+#define MBD_ABI_VERSION 8
 int mbd_abi_version(void);
 
 /* Static, human-readable name of a status code (never NULL). */
@@ -286,6 +286,28 @@ typedef struct {
  * points.
  */
 mbd_status mbd_run_program(const mbd_op* ops, int n_ops, mbd_stream_t stream);
+
+/*
+ * A batch of independent ops, each run by its own single-call kernel with the launch shape its entry point
+ * would use, the launches overlapping one another. No counterpart on the source pages as an API; it answers
+ * [TRT] "Fusing operations, measured" on the cost of many short launches for batches too large for a
+ * program: a call of about a thousand rows streams its bytes in a few microseconds, about as long as a
+ * launch takes to ramp up and drain, and here each launch after the first starts while the one before it
+ * still runs.
+ *   ops    : HOST array of n_ops descriptors (mbd_op, as in programs), read during the call only.
+ *   n_ops  : 0 (no-op) .. MBD_MAX_INDEPENDENT_OPS.
+ * The ops must be independent: no op may read or write memory that another op of the batch writes (its
+ * output, residual, block scales or dynamic scales); sharing read-only memory (a weight, a static scale) is
+ * allowed. Results are bit-identical to calling the entry points one after another on `stream`, in any
+ * order. Stream order holds for the batch as a whole: the first launch waits for the work enqueued before
+ * the call, and work enqueued after the call starts only once every op of the batch has completed.
+ * Each op is validated exactly as its entry point validates it (same status, nothing launched); besides,
+ * an unknown kind or a non-zero `reserved` gives MBD_ERR_INVALID_ARG, and so does a pair of ops that are not
+ * independent. All checks run before the first launch; a launch failure returns MBD_ERR_CUDA with the ops
+ * before it enqueued. Ops with n_tokens == 0 are skipped. One launch per remaining op.
+ */
+#define MBD_MAX_INDEPENDENT_OPS 64
+mbd_status mbd_run_independent(const mbd_op* ops, int n_ops, mbd_stream_t stream);
 
 /*
  * The same in two steps, for a program that runs many times (every decode step): build validates and

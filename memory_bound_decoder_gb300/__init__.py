@@ -48,6 +48,7 @@ OP_SWIGLU = 3
 OP_SWIGLU_QUANT_FP8 = 4
 OP_SWIGLU_QUANT_NVFP4 = 5
 MAX_PROGRAM_OPS = 128
+MAX_INDEPENDENT_OPS = 64
 PROGRAM_PLAN_BYTES = 16384
 
 
@@ -88,6 +89,7 @@ def _load() -> ctypes.CDLL:
     lib.mbd_fused_add_rmsnorm_quant_nvfp4.argtypes = [vp, vp, vp, vp, vp, i64, i64, f32, vp, vp]
     lib.mbd_swiglu_quant_nvfp4.argtypes = [vp, vp, vp, i64, i64, vp, vp]
     lib.mbd_run_program.argtypes = [ctypes.POINTER(Op), cint, vp]
+    lib.mbd_run_independent.argtypes = [ctypes.POINTER(Op), cint, vp]
     lib.mbd_program_plan_build.argtypes = [ctypes.POINTER(Op), cint, vp]
     lib.mbd_program_plan_launch.argtypes = [vp, vp]
     lib.mbd_program_schedule_bytes.restype = ctypes.c_size_t
@@ -104,7 +106,7 @@ def _load() -> ctypes.CDLL:
     for fn in ("mbd_fused_add_rmsnorm", "mbd_fused_add_rmsnorm_quant_fp8", "mbd_swiglu", "mbd_swiglu_quant_fp8",
                "mbd_fused_allreduce_add_rmsnorm", "mbd_fused_allreduce_add_rmsnorm_quant_fp8",
                "mbd_fused_add_rmsnorm_quant_nvfp4", "mbd_swiglu_quant_nvfp4", "mbd_run_program",
-               "mbd_program_plan_build", "mbd_program_plan_launch", "mbd_program_plan_upload",
+               "mbd_run_independent", "mbd_program_plan_build", "mbd_program_plan_launch", "mbd_program_plan_upload",
                "mbd_program_plan_launch_uploaded", "mbd_program_plan_launch_static"):
         getattr(lib, fn).restype = cint
     return lib
@@ -299,6 +301,13 @@ def run_program(ops, stream=None) -> None:
     """Run a list of Op (or a program_array result) as one persistent kernel launch."""
     arr, n = ops if isinstance(ops, tuple) else program_array(ops)
     _check(get_lib().mbd_run_program(arr if n else None, n, _stream(stream)), "run_program")
+
+
+def run_independent(ops, stream=None) -> None:
+    """Run a list of Op (or a program_array result) that share no written memory as their own single-call
+    launches, each overlapping the one before it (mbd_run_independent)."""
+    arr, n = ops if isinstance(ops, tuple) else program_array(ops)
+    _check(get_lib().mbd_run_independent(arr if n else None, n, _stream(stream)), "run_independent")
 
 
 class ProgramPlan:

@@ -370,6 +370,15 @@ int swiglu_kind(mbd::Epilogue ep) {
 }
 int scale_mode(mbd::Epilogue ep) { return ep == mbd::kFp8Dynamic ? MBD_SCALE_DYNAMIC_PER_TOKEN : MBD_SCALE_STATIC_PER_TENSOR; }
 
+// The launch shape of a prepared norm call (the table, else the rules); false if none fits.
+bool norm_plan(const mbd::NormParams& p, mbd::Epilogue ep, int sms, mbd::RowPlan* plan) {
+    const bool partials = p.n_partials > 0;
+    const bool tuned = !partials && tuned_plan(norm_kind(ep), scale_mode(ep), p.rows, p.hidden, p.nvec, true,
+                                                ep == mbd::kNvfp4, sms, plan);
+    return tuned ||
+           plan_rows(p.rows, p.nvec, partials ? Shape::kNormPartials : Shape::kNorm, sms, ep == mbd::kNvfp4, plan);
+}
+
 mbd_status norm_common(void* out, uint8_t* out_sf, mbd::Epilogue ep, void* residual, const void* x,
                        const void* weight, int64_t n_tokens, int64_t hidden, float eps, float* scale,
                        cudaStream_t stream, const void* const* partials = nullptr, int n_partials = 0) {
@@ -378,11 +387,7 @@ mbd_status norm_common(void* out, uint8_t* out_sf, mbd::Epilogue ep, void* resid
         norm_prepare(out, out_sf, ep, residual, x, weight, n_tokens, hidden, eps, scale, partials, n_partials, &p);
     if (st != MBD_OK || p.rows == 0) return st;
     mbd::RowPlan plan;
-    const int sms = sm_count_of_current_device();
-    const bool tuned = !partials && tuned_plan(norm_kind(ep), scale_mode(ep), p.rows, hidden, p.nvec, true,
-                                                ep == mbd::kNvfp4, sms, &plan);
-    if (!tuned && !plan_rows(p.rows, p.nvec, partials ? Shape::kNormPartials : Shape::kNorm, sms, ep == mbd::kNvfp4, &plan))
-        return MBD_ERR_UNSUPPORTED;
+    if (!norm_plan(p, ep, sm_count_of_current_device(), &plan)) return MBD_ERR_UNSUPPORTED;
     return finish_launch(mbd::launch_add_rmsnorm(p, ep, plan, stream));
 }
 
@@ -412,20 +417,27 @@ mbd_status swiglu_prepare(void* out, uint8_t* out_sf, mbd::Epilogue ep, const vo
     return MBD_OK;
 }
 
+// The launch shape of a prepared SwiGLU call (the table, else the rules; the bulk-copy rule last); false if
+// none fits.
+bool swiglu_plan(const mbd::SwigluParams& p, mbd::Epilogue ep, int sms, mbd::RowPlan* plan) {
+    const int64_t inter = int64_t{p.nvec} * 8;
+    const bool tuned = tuned_plan(swiglu_kind(ep), scale_mode(ep), p.rows, inter, p.nvec, ep == mbd::kFp8Dynamic,
+                                  ep == mbd::kNvfp4, sms, plan);
+    if (tuned) set_ahead(ep == mbd::kFp8Dynamic, p.rows, sms, plan);
+    if (!tuned && !plan_rows(p.rows, p.nvec, ep == mbd::kFp8Dynamic ? Shape::kRowMax : Shape::kStream, sms,
+                             ep == mbd::kNvfp4, plan))
+        return false;
+    if (ep == mbd::kFp8Dynamic) bulk_rule(p.rows, p.nvec, sms, plan);
+    return true;
+}
+
 mbd_status swiglu_common(void* out, uint8_t* out_sf, mbd::Epilogue ep, const void* gate_up, int64_t n_tokens,
                          int64_t inter, float* scale, cudaStream_t stream) {
     mbd::SwigluParams p;
     const mbd_status st = swiglu_prepare(out, out_sf, ep, gate_up, n_tokens, inter, scale, &p);
     if (st != MBD_OK || p.rows == 0) return st;
     mbd::RowPlan plan;
-    const int sms = sm_count_of_current_device();
-    const bool tuned = tuned_plan(swiglu_kind(ep), scale_mode(ep), p.rows, inter, p.nvec, ep == mbd::kFp8Dynamic,
-                                  ep == mbd::kNvfp4, sms, &plan);
-    if (tuned) set_ahead(ep == mbd::kFp8Dynamic, p.rows, sms, &plan);
-    if (!tuned && !plan_rows(p.rows, p.nvec, ep == mbd::kFp8Dynamic ? Shape::kRowMax : Shape::kStream, sms,
-                             ep == mbd::kNvfp4, &plan))
-        return MBD_ERR_UNSUPPORTED;
-    if (ep == mbd::kFp8Dynamic) bulk_rule(p.rows, p.nvec, sms, &plan);
+    if (!swiglu_plan(p, ep, sm_count_of_current_device(), &plan)) return MBD_ERR_UNSUPPORTED;
     return finish_launch(mbd::launch_swiglu(p, ep, plan, stream));
 }
 
@@ -740,6 +752,83 @@ mbd_status launch_static(const PlanImpl* plan, cudaStream_t stream) {
     return launch_uploaded(plan, addr, stream);
 }
 
+// ------------------------------------------------------------------------------------------ batches
+
+// mbd_run_independent: ops that share no written memory, each launched as its single call, the first in
+// PdlOrder kPdlHead and the rest kPdlOverlap. Every op is checked, and then planned, before the first launch.
+mbd_status run_independent(const mbd_op* ops, int n_ops, cudaStream_t stream) {
+    if (n_ops < 0 || n_ops > MBD_MAX_INDEPENDENT_OPS || (n_ops > 0 && !ops)) return MBD_ERR_INVALID_ARG;
+    struct Prepared {
+        bool norm;
+        mbd::Epilogue ep;
+        mbd::NormParams np;
+        mbd::SwigluParams sp;
+        OpInfo info;
+    };
+    Prepared prep[MBD_MAX_INDEPENDENT_OPS];
+    int active[MBD_MAX_INDEPENDENT_OPS];
+    int n_active = 0;
+    for (int i = 0; i < n_ops; ++i) {
+        const mbd_op& o = ops[i];
+        if (o.reserved != 0 || o.kind < MBD_OP_ADD_RMSNORM || o.kind > MBD_OP_SWIGLU_QUANT_NVFP4) return MBD_ERR_INVALID_ARG;
+        Prepared& q = prep[i];
+        q.norm = o.kind <= MBD_OP_ADD_RMSNORM_QUANT_NVFP4;
+        const int sub = q.norm ? o.kind : o.kind - MBD_OP_SWIGLU;   // 0 bf16, 1 FP8, 2 NVFP4
+        q.ep = sub == 0 ? mbd::kBf16 : mbd::kNvfp4;
+        if (sub == 1 && !fp8_epilogue(o.mode, &q.ep)) return MBD_ERR_INVALID_ARG;
+        q.info.nreg = 0;
+        const size_t W = static_cast<size_t>(o.width);
+        int64_t T = 0;
+        if (q.norm) {
+            const mbd_status st = norm_prepare(o.out, o.out_sf, q.ep, o.residual, o.in, o.weight, o.n_tokens, o.width,
+                                               o.eps, o.scale, nullptr, 0, &q.np);
+            if (st != MBD_OK) return st;
+            T = q.np.rows;
+            add_region(q.info, o.in, T * W * 2, false, 0, 0);
+            add_region(q.info, o.residual, T * W * 2, true, 0, 0);
+            add_region(q.info, o.weight, W * 2, false, 0, 0);
+        } else {
+            const mbd_status st = swiglu_prepare(o.out, o.out_sf, q.ep, o.in, o.n_tokens, o.width, o.scale, &q.sp);
+            if (st != MBD_OK) return st;
+            T = q.sp.rows;
+            add_region(q.info, o.in, T * W * 4, false, 0, 0);
+        }
+        if (T == 0) continue;   // nothing to do, nothing touched
+        add_region(q.info, o.out, out_bytes(q.ep, T, o.width), true, 0, 0);
+        if (q.ep == mbd::kNvfp4) add_region(q.info, o.out_sf, T * (W / 16), true, 0, 0);
+        if (q.ep == mbd::kFp8Dynamic) add_region(q.info, o.scale, T * 4, true, 0, 0);
+        else if (q.ep != mbd::kBf16) add_region(q.info, o.scale, 4, false, 0, 0);
+        active[n_active++] = i;
+    }
+    // independence: what one op writes, no other op may read or write
+    for (int a = 0; a < n_active; ++a)
+        for (int b = a + 1; b < n_active; ++b) {
+            const OpInfo& x = prep[active[a]].info;
+            const OpInfo& y = prep[active[b]].info;
+            for (int u = 0; u < x.nreg; ++u)
+                for (int v = 0; v < y.nreg; ++v)
+                    if ((x.reg[u].write || y.reg[v].write) &&
+                        overlap(x.reg[u].ptr, x.reg[u].bytes, y.reg[v].ptr, y.reg[v].bytes))
+                        return MBD_ERR_INVALID_ARG;
+        }
+    if (n_active == 0) return MBD_OK;
+    const int sms = sm_count_of_current_device();
+    mbd::RowPlan plans[MBD_MAX_INDEPENDENT_OPS];
+    for (int a = 0; a < n_active; ++a) {
+        const Prepared& q = prep[active[a]];
+        if (!(q.norm ? norm_plan(q.np, q.ep, sms, &plans[a]) : swiglu_plan(q.sp, q.ep, sms, &plans[a])))
+            return MBD_ERR_UNSUPPORTED;
+        plans[a].order = a == 0 ? mbd::kPdlHead : mbd::kPdlOverlap;
+    }
+    for (int a = 0; a < n_active; ++a) {
+        const Prepared& q = prep[active[a]];
+        const mbd_status st = finish_launch(q.norm ? mbd::launch_add_rmsnorm(q.np, q.ep, plans[a], stream)
+                                                   : mbd::launch_swiglu(q.sp, q.ep, plans[a], stream));
+        if (st != MBD_OK) return st;
+    }
+    return MBD_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -911,6 +1000,10 @@ mbd_status mbd_program_plan_upload(const mbd_program_plan* plan, void* schedule,
 
 mbd_status mbd_program_plan_launch_uploaded(const mbd_program_plan* plan, const void* schedule, mbd_stream_t stream) {
     return launch_uploaded(reinterpret_cast<const PlanImpl*>(plan), schedule, reinterpret_cast<cudaStream_t>(stream));
+}
+
+mbd_status mbd_run_independent(const mbd_op* ops, int n_ops, mbd_stream_t stream) {
+    return run_independent(ops, n_ops, reinterpret_cast<cudaStream_t>(stream));
 }
 
 mbd_status mbd_run_program(const mbd_op* ops, int n_ops, mbd_stream_t stream) {

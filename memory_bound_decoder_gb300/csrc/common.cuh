@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "launch.h"
+
 namespace mbd {
 
 namespace cg = cooperative_groups;
@@ -331,6 +333,25 @@ __device__ __forceinline__ P block_total_tree(P mine, P* warp_part) {
 // programmatic stream serialization.
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// The single-call kernels order themselves against the previous kernel by RowPlan::order (PdlOrder, launch.h):
+// pdl_enter before the first global access (anything before it may only warm L2), pdl_leave after the last.
+//   kPdlWaitFirst: trigger, wait                 (every single call)
+//   kPdlHead:      wait, trigger                 (first launch of a batch of independent ops: no later launch
+//                                                 of the batch starts before the work ahead of it is done)
+//   kPdlOverlap:   trigger, ..., wait at exit    (later launches of the batch: they run beside the previous
+//                                                 launch, and none completes before its predecessor, so the
+//                                                 batch still completes in stream order)
+__device__ __forceinline__ void pdl_enter_trigger(int order) {
+    if (order != kPdlHead) pdl_trigger();
+}
+__device__ __forceinline__ void pdl_enter_wait(int order) {
+    if (order != kPdlOverlap) pdl_wait();
+    if (order == kPdlHead) pdl_trigger();
+}
+__device__ __forceinline__ void pdl_leave(int order) {
+    if (order == kPdlOverlap) pdl_wait();
+}
 
 // Warm L2 with a 16-byte vector this thread will load after pdl_wait. A prefetch returns no data, and L2 is
 // the point of coherence for global memory, so the load that follows the wait still observes every write

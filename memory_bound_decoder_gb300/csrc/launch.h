@@ -23,7 +23,14 @@ struct RowPlan {
     int prefetch;  // 1: single-wave launch, warm L2 with the inputs before waiting on the previous kernel
     int ahead;     // > 0: each CTA also warms L2 with the same slice of row + ahead (a later wave's row)
     int bulk;      // dynamic-FP8 SwiGLU: 1 = the slices come into shared memory by bulk copies (vpt 4)
+    int order;     // PdlOrder: how the launch orders itself against the previous kernel on the stream
 };
+
+// Programmatic dependent launch order of a single-call kernel (RowPlan::order). kPdlWaitFirst for every
+// call on its own; a batch of independent ops (mbd_run_independent) launches its first op kPdlHead and the
+// rest kPdlOverlap (a later op's CTAs run while the previous op's still do, and wait for it only before they
+// exit). Legal only where no op of the batch touches memory that another op of the batch writes.
+enum PdlOrder : int { kPdlWaitFirst = 0, kPdlHead = 1, kPdlOverlap = 2 };
 
 
 constexpr int kMaxPartials = 8;

@@ -25,24 +25,25 @@ namespace {
 // per vector would otherwise leave one CTA, a quarter of the SM's warps.
 template <int VPT, int EP, bool ALLRED, int CL>
 __global__ void __launch_bounds__(512, ALLRED ? 2 : 1) add_rmsnorm_kernel(const __grid_constant__ NormParams p, int ctas_per_row, int slice,
-                                                                        int prefetch) {
+                                                                        int prefetch, int order) {
     __shared__ NormSmem sm;
     const int64_t row = launch_row();
     if (row >= p.rows) return;   // past the last row (the whole cluster shares the row)
     const int rank = static_cast<int>(blockIdx.x);
     const int begin = rank * slice;
     const int end = min(begin + slice, p.nvec);
-    pdl_trigger();
+    pdl_enter_trigger(order);
     if (prefetch) norm_prefetch<VPT, ALLRED>(p, row, begin, end);
-    pdl_wait();
+    pdl_enter_wait(order);
     norm_row_slice<VPT, EP, ALLRED, CL>(p, row, rank, ctas_per_row, begin, end, sm);
+    pdl_leave(order);
 }
 
 template <int EP>
 cudaError_t launch_ep(const NormParams& p, const RowPlan& plan, cudaStream_t s) {
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
-    void (*kern)(NormParams, int, int, int) = nullptr;
+    void (*kern)(NormParams, int, int, int, int) = nullptr;
     const bool cl = plan.ctas_per_row > 1;
     if (p.n_partials > 0) {
         if (plan.vpt != 1) return cudaErrorInvalidValue;
@@ -57,7 +58,7 @@ cudaError_t launch_ep(const NormParams& p, const RowPlan& plan, cudaStream_t s) 
         }
     }
     fill_launch(cfg, attr, p.rows, plan.ctas_per_row, plan.threads, plan.ctas_per_row, s);
-    return cudaLaunchKernelEx(&cfg, kern, p, plan.ctas_per_row, plan.slice, plan.prefetch);
+    return cudaLaunchKernelEx(&cfg, kern, p, plan.ctas_per_row, plan.slice, plan.prefetch, plan.order);
 }
 
 }  // namespace

@@ -24,16 +24,16 @@ namespace {
 
 template <int VPT, int EP, int CL>
 __global__ void __launch_bounds__(512, VPT <= 2 ? 4 : 1) swiglu_kernel(const __grid_constant__ SwigluParams p, int ctas_per_row, int slice, int prefetch,
-                                                                   int ahead) {
+                                                                   int ahead, int order) {
     __shared__ SwigluSmem sm;
     const int64_t row = launch_row();
     if (row >= p.rows) return;   // past the last row (the whole cluster shares the row)
     const int rank = static_cast<int>(blockIdx.x);
     const int begin = rank * slice;
     const int end = min(begin + slice, p.nvec);
-    pdl_trigger();
+    pdl_enter_trigger(order);
     if (prefetch) swiglu_prefetch<VPT>(p, row, begin, end);
-    pdl_wait();
+    pdl_enter_wait(order);
     // The row a later wave will run here is fetched into L2 now, so that its loads meet L2 instead of HBM;
     // the bytes come from HBM once either way (the rows in flight plus those ahead fit L2 many times over).
     // Two bulk prefetches (gate and up slices) from one thread.
@@ -44,6 +44,7 @@ __global__ void __launch_bounds__(512, VPT <= 2 ? 4 : 1) swiglu_kernel(const __g
         prefetch_l2_bulk(gr + p.nvec, bytes);
     }
     swiglu_row_slice<VPT, EP, CL>(p, row, rank, ctas_per_row, begin, end, sm);
+    pdl_leave(order);
 }
 
 // Dynamic FP8 SwiGLU with the CTA's gate and up slices brought into shared memory by two bulk copies
@@ -56,25 +57,21 @@ struct BulkSmem {
 };
 
 template <int VPT>
-__global__ void __launch_bounds__(320, 4) swiglu_dyn_bulk_kernel(const __grid_constant__ SwigluParams p, int ctas_per_row,
-                                                                 int slice, int ahead) {
-    extern __shared__ __align__(16) uint4 slices[];   // gate slice [0, slice), up slice [slice, 2 slice)
-    __shared__ SwigluSmem sm;
-    __shared__ BulkSmem bs;
-    const int64_t row = launch_row();
-    if (row >= p.rows) return;   // past the last row (the whole cluster shares the row)
+__device__ __forceinline__ void swiglu_dyn_bulk_row(const SwigluParams& p, int64_t row, int ctas_per_row, int slice,
+                                                    int ahead, int order, uint4* slices, SwigluSmem& sm,
+                                                    BulkSmem& bs) {
     const int rank = static_cast<int>(blockIdx.x);
     const int begin = rank * slice;
     const int end = min(begin + slice, p.nvec);
     const int n = end - begin;
     const uint32_t bar = smem_addr(&bs.load_bar);
-    pdl_trigger();
+    pdl_enter_trigger(order);
     if (threadIdx.x == 0) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
-    pdl_wait();
+    pdl_enter_wait(order);
     if (threadIdx.x == 0) {
         const uint4* gr = static_cast<const uint4*>(p.gate_up) + row * (int64_t)p.nvec * 2 + begin;
         const uint32_t bytes = static_cast<uint32_t>(n) * 16u;
@@ -145,6 +142,18 @@ __global__ void __launch_bounds__(320, 4) swiglu_dyn_bulk_kernel(const __grid_co
     }
 }
 
+template <int VPT>
+__global__ void __launch_bounds__(320, 4) swiglu_dyn_bulk_kernel(const __grid_constant__ SwigluParams p, int ctas_per_row,
+                                                                 int slice, int ahead, int order) {
+    extern __shared__ __align__(16) uint4 slices[];   // gate slice [0, slice), up slice [slice, 2 slice)
+    __shared__ SwigluSmem sm;
+    __shared__ BulkSmem bs;
+    const int64_t row = launch_row();
+    if (row >= p.rows) return;   // past the last row (the whole cluster shares the row)
+    swiglu_dyn_bulk_row<VPT>(p, row, ctas_per_row, slice, ahead, order, slices, sm, bs);
+    pdl_leave(order);
+}
+
 // Per device (up to 64): the id of the context in which the bulk kernel's preferred carveout, the largest
 // shared-memory share, was last requested, so that the SM's shared memory rather than its L1 share bounds
 // the resident CTAs (each holds two row slices, up to 40 KB). A kernel attribute belongs to a context: a
@@ -169,7 +178,7 @@ cudaError_t launch_dyn_bulk(const SwigluParams& p, const RowPlan& plan, cudaStre
     cudaLaunchAttribute attr[2];
     fill_launch(cfg, attr, p.rows, plan.ctas_per_row, plan.threads, plan.ctas_per_row, s);
     cfg.dynamicSmemBytes = static_cast<size_t>(plan.slice) * 32;
-    return cudaLaunchKernelEx(&cfg, swiglu_dyn_bulk_kernel<4>, p, plan.ctas_per_row, plan.slice, plan.ahead);
+    return cudaLaunchKernelEx(&cfg, swiglu_dyn_bulk_kernel<4>, p, plan.ctas_per_row, plan.slice, plan.ahead, plan.order);
 }
 
 template <int EP>
@@ -177,7 +186,7 @@ cudaError_t launch_ep(const SwigluParams& p, const RowPlan& plan, cudaStream_t s
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
     const int cluster = EP == kFp8Dynamic ? plan.ctas_per_row : 1;
-    void (*kern)(SwigluParams, int, int, int, int) = nullptr;
+    void (*kern)(SwigluParams, int, int, int, int, int) = nullptr;
     // only the dynamic epilogue reduces over the row; the streams compile no reduction either way
     constexpr int kMulti = EP == kFp8Dynamic ? kRowInCluster : kRowInCta;
     const bool cl = cluster > 1;
@@ -190,7 +199,7 @@ cudaError_t launch_ep(const SwigluParams& p, const RowPlan& plan, cudaStream_t s
     }
     if (EP == kFp8Dynamic && plan.bulk) return launch_dyn_bulk(p, plan, s);
     fill_launch(cfg, attr, p.rows, plan.ctas_per_row, plan.threads, cluster, s);
-    return cudaLaunchKernelEx(&cfg, kern, p, plan.ctas_per_row, plan.slice, plan.prefetch, plan.ahead);
+    return cudaLaunchKernelEx(&cfg, kern, p, plan.ctas_per_row, plan.slice, plan.prefetch, plan.ahead, plan.order);
 }
 
 }  // namespace

@@ -34,9 +34,9 @@ def test_binding_names_match_header():
 
 
 def test_version_and_status_strings(lib):
-    assert lib.mbd_abi_version() == 7
+    assert lib.mbd_abi_version() == 8
     hdr = open(mbd.HEADER_PATH).read()
-    assert int(re.search(r"#define MBD_ABI_VERSION (\d+)", hdr).group(1)) == 7
+    assert int(re.search(r"#define MBD_ABI_VERSION (\d+)", hdr).group(1)) == 8
     for code in range(5):
         assert lib.mbd_status_string(code).decode().startswith("MBD_")
     assert lib.mbd_status_string(99) == b"unknown mbd_status"
@@ -314,3 +314,39 @@ def test_launch_shape_follows_table_then_rules(lib):
     assert (c, v, t) == (3, 1, 64)
     mbd.tuning_set([])
     assert lib.mbd_launch_shape(9, 0, 1, 64, None, None, None) == mbd.ERR_INVALID_ARG
+
+
+def test_independent_batch_checks(lib):
+    """mbd_run_independent checks every op as its entry point does, and that no op touches what another
+    writes, before any launch."""
+    H = 64
+    n0 = mbd.kernel_launches()
+    a = mbd.op_add_rmsnorm(A, 2 * A, 3 * A, 9 * A, 4, H, 1e-6)
+    # two norms updating one residual are not independent (the second reads what the first writes)
+    b = mbd.op_add_rmsnorm(4 * A, 2 * A, 5 * A, 9 * A, 4, H, 1e-6)
+    assert _rc(mbd.run_independent, [a, b]) == mbd.ERR_INVALID_ARG
+    # a SwiGLU whose input is another op's output, and one whose output lands inside another op's input
+    s_in = mbd.op_swiglu(6 * A, A, 4, H // 2)
+    assert _rc(mbd.run_independent, [a, s_in]) == mbd.ERR_INVALID_ARG
+    s_out = mbd.op_swiglu(3 * A + 64, 7 * A, 1, 8)
+    assert _rc(mbd.run_independent, [a, s_out]) == mbd.ERR_INVALID_ARG
+    # a dynamic scale written by one op and read as a static scale by another
+    qd = mbd.op_swiglu_quant_fp8(8 * A, 7 * A, 4, H, "dynamic", 10 * A)
+    qs = mbd.op_add_rmsnorm_quant_fp8(11 * A, 12 * A, 13 * A, 9 * A, 4, H, 1e-6, "static", 10 * A + 8)
+    assert _rc(mbd.run_independent, [qd, qs]) == mbd.ERR_INVALID_ARG
+    # each op's own checks, with its entry point's status
+    assert _rc(mbd.run_independent, [a, mbd.op_add_rmsnorm(A + 2 * 4 * H * 8, 14 * A, 15 * A + 2, 9 * A, 4, H,
+                                                            1e-6)]) == mbd.ERR_MISALIGNED
+    assert _rc(mbd.run_independent, [a, mbd.op_swiglu(16 * A, 17 * A, -1, H)]) == mbd.ERR_INVALID_ARG
+    bad = mbd.op_swiglu(16 * A, 17 * A, 4, H)
+    bad.reserved = 1
+    assert _rc(mbd.run_independent, [bad]) == mbd.ERR_INVALID_ARG
+    bad = mbd.op_swiglu(16 * A, 17 * A, 4, H)
+    bad.kind = 9
+    assert _rc(mbd.run_independent, [bad]) == mbd.ERR_INVALID_ARG
+    assert _rc(mbd.run_independent, [mbd.op_swiglu(16 * A, 17 * A, 4, H)] * (mbd.MAX_INDEPENDENT_OPS + 1)) \
+        == mbd.ERR_INVALID_ARG
+    # ops with no tokens are skipped, and touch nothing: an empty batch launches nothing
+    mbd.run_independent([])
+    mbd.run_independent([mbd.op_swiglu(None, None, 0, H), mbd.op_add_rmsnorm(None, None, None, None, 0, H, 1e-6)])
+    assert mbd.kernel_launches() == n0

@@ -1,5 +1,6 @@
 """The bench's grouped step computes what its per-call step computes: the small ragged calls of the default
-step, launched one by one and as one program launch (bf16 and FP8 ops together), from identical seeded inputs.
+step, launched one by one and as one program launch (bf16 and FP8 ops together), from identical seeded inputs;
+and its 1000-token calls, one by one and as one batch of overlapping launches (bit for bit).
 Residuals and dynamic scales bit-identical; a norm row reduced inside one CTA (program) may sum in another
 order than one split over a cluster (single call), so bf16 outputs may differ by one ulp and static-FP8
 codes by one step, rarely."""
@@ -36,7 +37,8 @@ def _run(work, grouped):
     for u in units:
         u.launch()
     torch.cuda.synchronize()
-    assert mbd.kernel_launches() - n0 == len(units)
+    launches = sum(len(u.members) if isinstance(u, bench.BatchGroup) else 1 for u in units)
+    assert mbd.kernel_launches() - n0 == launches
     assert mbd.device_error_flags() == 0
     outs = [(d.call, {k: getattr(d, k).cpu().numpy().copy() for k in ("out", "res", "scale") if hasattr(d, k)})
             for d in dcalls]
@@ -63,3 +65,14 @@ def test_grouped_small_calls_match_per_call_launches():
             assert diff.mean() <= 1e-3, f"{call.name}: {diff.sum()} codes differ"
             assert ((x[diff] & 0x80) == (y[diff] & 0x80)).all(), f"{call.name}: sign flipped"
             assert (np.abs((x[diff] & 0x7F) - (y[diff] & 0x7F)) == 1).all(), f"{call.name}: more than one step"
+
+
+def test_batched_1000_token_calls_match_per_call_launches():
+    w = bench.workloads_by_key()[bench.DEFAULT_WORKLOAD]
+    work = wl.Workload("t1000", "the 1000-token calls of the default step", tuple(c for c in w.calls if c.T == 1000), 1)
+    n_calls, ref = _run(work, grouped=False)
+    n_units, got = _run(work, grouped=True)
+    assert n_calls == 4 and n_units == 2                # the largest call alone, the other three as one batch
+    for (call, a), (_, b) in zip(ref, got):
+        for k in a:
+            np.testing.assert_array_equal(a[k], b[k], f"{call.name}: {k}")

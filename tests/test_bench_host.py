@@ -13,18 +13,19 @@ def test_default_step_groups_the_small_calls_into_one_launch():
     w = bench.workloads_by_key()[bench.DEFAULT_WORKLOAD]
     calls = list(w.calls)
     units = bench.launch_groups(calls, w.layers, 152)
-    # the batches of at least one row per SM keep their own launches, in place
-    singles = [u for u in units if isinstance(u, int)]
-    assert all(calls[i].T >= 152 for i in singles)
-    groups = [u for u in units if not isinstance(u, int)]
-    assert [g[0] for g in groups] == ["bf16+fp8"]                    # 84 rows: one wave of the mixed variant
+    # the largest call keeps its own launch, first; then one batch of the other calls of at least one row per SM;
+    # then one program launch of the small calls (84 rows: one wave of the mixed variant)
+    assert units[0] == 1 and calls[1].name == "swiglu_q8_dynamic_T2048_I53248"
+    assert [u[0] for u in units[1:]] == ["batch", "bf16+fp8"]
+    assert units[1][1] == [0] + [i for i, c in enumerate(calls) if c.T == 1000]
     small = [i for i, c in enumerate(calls) if c.T < 152]
-    assert groups[0][1] == small                                      # every small call once, in list order
+    assert units[2][1] == small                                       # every small call once, in list order
     assert {(calls[i].kind, calls[i].mode) for i in small} == {
         ("add_rmsnorm", None), ("swiglu", None), ("add_rmsnorm_q8", "static"), ("swiglu_q8", "dynamic")}
-    # a group sits where its first call stood
+    # without batches, every unit sits where its first call stood
+    units = bench.launch_groups(calls, w.layers, 152, batches=False)
     flat = [u if isinstance(u, int) else u[1][0] for u in units]
-    assert flat == sorted(flat)
+    assert flat == sorted(flat) and [u[0] for u in units if not isinstance(u, int)] == ["bf16+fp8"]
 
 
 def test_classes_split_when_their_rows_exceed_one_per_sm():
@@ -52,7 +53,23 @@ def test_no_grouping_across_layers_wide_norms_or_allreduce():
     assert bench.launch_groups(wide, 1, 152) == [0, ("bf16", [1])]    # the program holds norms up to 8192 wide
     ar = [wl.Call("allreduce_rmsnorm", 2, 4096, d, partials=2), wl.Call("add_rmsnorm", 2, 4096, d)]
     assert bench.launch_groups(ar, 1, 152) == [0, ("bf16", [1])]
-    assert bench.launch_groups(calls, 1, 1) == [0, 1]                 # nothing below one row per SM
+    assert bench.launch_groups(calls, 1, 1, batches=False) == [0, 1]  # nothing below one row per SM
+
+
+def test_batches_take_every_call_of_one_row_per_sm_but_the_largest():
+    d = wl.N01
+    calls = [wl.Call("add_rmsnorm", 152, 1024, d), wl.Call("swiglu", 1215, 1024, d), wl.Call("swiglu", 4000, 1024, d),
+             wl.Call("swiglu_q8", 500, 1024, d, mode="dynamic"), wl.Call("add_rmsnorm_nvfp4", 300, 1024, d),
+             wl.Call("swiglu", 5, 1024, d)]
+    assert bench.launch_groups(calls, 1, 152) == [2, ("batch", [0, 1, 3, 4]), ("bf16", [5])]
+    assert bench.launch_groups(calls, 1, 152, max_batch=3) == [2, ("batch", [0, 1, 3]), ("batch", [4]), ("bf16", [5])]
+    assert bench.launch_groups(calls[:3], 1, 152) == [2, ("batch", [0, 1])]
+    assert bench.launch_groups(calls[1:3], 1, 152) == [0, 1]           # one call besides the largest: no batch
+    assert bench.launch_groups(calls[:5], 28, 152) == [0, 1, 2, 3, 4]  # layers share buffers: no batch
+    assert bench.launch_groups(calls, 1, 152, batches=False) == [0, 1, 2, 3, 4, ("bf16", [5])]
+    ar = [wl.Call("add_rmsnorm", 2000, 4096, d), wl.Call("allreduce_rmsnorm", 400, 4096, d, partials=2),
+          wl.Call("add_rmsnorm", 300, 4096, d)]
+    assert bench.launch_groups(ar, 1, 152) == [0, 1, 2]               # the all-reduce norm is no batch op
 
 
 def test_groups_split_at_the_op_limit():
