@@ -50,6 +50,7 @@ def _load():
         i64, f32, cint = ctypes.c_int64, ctypes.c_float, ctypes.c_int
         lib.orc_bf16_to_double.argtypes, lib.orc_bf16_to_double.restype = [ctypes.c_uint16], ctypes.c_double
         lib.orc_bf16_round.argtypes, lib.orc_bf16_round.restype = [ctypes.c_double], ctypes.c_uint16
+        lib.orc_bf16_sum.argtypes, lib.orc_bf16_sum.restype = [ctypes.POINTER(ctypes.c_uint16), ctypes.c_int], ctypes.c_uint16
         lib.orc_e4m3_decode.argtypes, lib.orc_e4m3_decode.restype = [ctypes.c_uint8], ctypes.c_double
         lib.orc_e4m3_encode.argtypes, lib.orc_e4m3_encode.restype = [ctypes.c_double], ctypes.c_uint8
         lib.orc_silu.argtypes, lib.orc_silu.restype = [ctypes.c_double], ctypes.c_double
@@ -94,6 +95,14 @@ def bf16_to_double(b: int) -> float:
 
 def bf16_round(v: float) -> int:
     return int(_load().orc_bf16_round(float(v)))
+
+
+def bf16_sum(bits) -> int:
+    """bf16 bits of the exact sum of up to 8 bf16 values (given as bits), rounded once; a zero sum is +0."""
+    a = np.ascontiguousarray(np.asarray(bits, np.uint16).reshape(-1))
+    if not 1 <= a.size <= 8:
+        raise ValueError("1 to 8 addends")
+    return int(_load().orc_bf16_sum(a.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)), int(a.size)))
 
 
 def e4m3_decode(code: int) -> float:

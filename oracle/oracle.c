@@ -234,12 +234,94 @@ int orc_add_rmsnorm_quant_nvfp4(const uint16_t* x, const uint16_t* r, const uint
 
 /* ---------------------------------------------------------------- AllReduce half + add + RMSNorm */
 
+/* Exact sum of bf16 values, rounded once to bf16.
+ * Every finite bf16 value is an integer multiple of 2^-133 (the subnormal step): with exponent field e and
+ * mantissa m, v = +-M * 2^sh * 2^-133 where M = m, sh = 0 for e == 0 and M = 128 + m, sh = e - 1 otherwise.
+ * A double does not hold such a sum exactly when the addends' exponents span more than about 42 bits (a
+ * subnormal beside a value near 1), so the sum is kept as an integer: the positive and the negative addends
+ * accumulate separately in 320-bit unsigned integers (five 64-bit limbs; 8 addends below 2^(8 + 253) fit),
+ * the smaller total is subtracted from the larger, and the difference N (sum = +-N * 2^-133) is rounded to 8
+ * significant bits, ties to even. A zero sum is +0 (an empty sum plus zero terms). */
+#define ORC_LIMBS 5
+typedef struct {
+    uint64_t w[ORC_LIMBS]; /* little-endian limbs */
+} orc_u320;
+
+static void u320_add_shifted(orc_u320* a, uint64_t m, int sh) { /* a += m * 2^sh, m < 2^8, 0 <= sh < 255 */
+    int limb = sh / 64, off = sh % 64;
+    uint64_t lo = m << off;
+    uint64_t hi = off ? (m >> (64 - off)) : 0;
+    uint64_t carry = 0;
+    for (int i = limb; i < ORC_LIMBS; ++i) {
+        uint64_t add = (i == limb) ? lo : ((i == limb + 1) ? hi : 0);
+        uint64_t s1 = a->w[i] + add;
+        uint64_t c1 = s1 < add ? 1 : 0;
+        uint64_t s2 = s1 + carry;
+        uint64_t c2 = s2 < carry ? 1 : 0;
+        a->w[i] = s2;
+        carry = c1 | c2;
+    }
+}
+
+static int u320_cmp(const orc_u320* a, const orc_u320* b) {
+    for (int i = ORC_LIMBS - 1; i >= 0; --i)
+        if (a->w[i] != b->w[i]) return a->w[i] < b->w[i] ? -1 : 1;
+    return 0;
+}
+
+static orc_u320 u320_sub(const orc_u320* a, const orc_u320* b) { /* a - b, a >= b */
+    orc_u320 r;
+    uint64_t borrow = 0;
+    for (int i = 0; i < ORC_LIMBS; ++i) {
+        uint64_t d1 = a->w[i] - b->w[i];
+        uint64_t b1 = a->w[i] < b->w[i] ? 1 : 0;
+        uint64_t d2 = d1 - borrow;
+        uint64_t b2 = d1 < borrow ? 1 : 0;
+        r.w[i] = d2;
+        borrow = b1 | b2;
+    }
+    return r;
+}
+
+static int u320_bit(const orc_u320* a, int i) { return (int)((a->w[i / 64] >> (i % 64)) & 1u); }
+
+uint16_t orc_bf16_sum(const uint16_t* v, int n) {
+    orc_u320 pos, neg;
+    memset(&pos, 0, sizeof pos);
+    memset(&neg, 0, sizeof neg);
+    for (int k = 0; k < n; ++k) {
+        int e = (v[k] >> 7) & 0xFF, m = v[k] & 0x7F;
+        uint64_t M = (uint64_t)(e == 0 ? m : 128 + m);
+        int sh = e == 0 ? 0 : e - 1;
+        u320_add_shifted((v[k] & 0x8000) ? &neg : &pos, M, sh);
+    }
+    int c = u320_cmp(&pos, &neg);
+    if (c == 0) return 0; /* +0 */
+    uint16_t sign = c < 0 ? (uint16_t)0x8000 : (uint16_t)0;
+    orc_u320 N = c < 0 ? u320_sub(&neg, &pos) : u320_sub(&pos, &neg);
+    int p = ORC_LIMBS * 64 - 1;
+    while (!u320_bit(&N, p)) --p; /* highest set bit */
+    if (p < 8) return (uint16_t)(sign | (uint16_t)N.w[0]); /* N < 256: exactly a bf16 (subnormal or field 1) */
+    uint32_t q = 0;
+    for (int i = p; i > p - 8; --i) q = (q << 1) | (uint32_t)u320_bit(&N, i);   /* 8 significant bits */
+    int round = u320_bit(&N, p - 8), sticky = 0;
+    for (int i = p - 9; i >= 0 && !sticky; --i) sticky = u320_bit(&N, i);
+    if (round && (sticky || (q & 1u))) ++q;
+    if (q == 256) {
+        q = 128;
+        ++p;
+    }
+    int field = p - 6; /* value = q / 128 * 2^(p - 133) */
+    if (field >= 255) return (uint16_t)(sign | 0x7F80);
+    return (uint16_t)(sign | (uint16_t)(field << 7) | (uint16_t)(q - 128));
+}
+
 /* x row t = bf16 of the exact sum of the partials' row t. */
 static void reduce_partials(const uint16_t* const* partials, int n, int64_t t, int64_t H, uint16_t* x_row) {
+    uint16_t v[8];
     for (int64_t j = 0; j < H; ++j) {
-        double sum = 0.0;
-        for (int k = 0; k < n; ++k) sum += orc_bf16_to_double(partials[k][t * H + j]);
-        x_row[j] = orc_bf16_round(sum);
+        for (int k = 0; k < n; ++k) v[k] = partials[k][t * H + j];
+        x_row[j] = orc_bf16_sum(v, n);
     }
 }
 

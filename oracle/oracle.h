@@ -35,6 +35,8 @@ extern "C" {
 double orc_bf16_to_double(uint16_t b);
 /* double -> nearest bf16 pattern, ties to even (8 significant bits, subnormals, overflow to inf). */
 uint16_t orc_bf16_round(double v);
+/* The exact sum of n finite bf16 values (n <= 8), rounded once to bf16, ties to even; a zero sum is +0. */
+uint16_t orc_bf16_sum(const uint16_t* v, int n);
 
 /* OCP E4M3FN: bias 7, 3 mantissa bits, max finite 448 (0x7E), no infinities, NaN 0x7F / 0xFF.
  * encode: nearest code by exhaustive search over the 127 non-negative finite magnitudes, ties to the

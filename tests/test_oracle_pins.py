@@ -464,3 +464,60 @@ def test_nvfp4_codes_vs_exact_rational(orc):
                     want = best
                 assert code & 7 == want
                 assert (code >> 3) == (1 if x < 0 else 0)   # the sign is kept, also on a rounded zero
+
+
+def test_bf16_sum_golden(orc):
+    """Hand-derived exact sums (tests/golden/bf16_sums.txt): ties to even, carries into the exponent, zero sums,
+    subnormals, overflow, and tiny terms that decide a tie, which a float64 accumulation loses."""
+    rows = _golden("bf16_sums.txt")
+    assert len(rows) >= 12
+    for *addends, want in rows:
+        bits = [int(a, 16) for a in addends]
+        assert orc.bf16_sum(bits) == int(want, 16), addends
+
+
+def _wide_bf16_sets(rng, n_sets, k):
+    """bf16 addend sets with exponents spread over the whole range (normal values near 1 beside subnormals,
+    huge and tiny values) and exact midpoint constructions tipped by tiny terms."""
+    sets = []
+    for i in range(n_sets):
+        kind = i % 3 if k >= 2 else 0
+        if kind == 0:      # any finite exponent field, random mantissas and signs
+            e = rng.integers(0, 250, k)
+            m = rng.integers(0, 128, k)
+            s = rng.integers(0, 2, k)
+            sets.append((s << 15) | (e << 7) | m)
+        elif kind == 1:    # a value, half its bf16 ulp, and tiny terms of random sign
+            e0 = int(rng.integers(40, 200))
+            base = (int(rng.integers(0, 2)) << 15) | (e0 << 7) | int(rng.integers(0, 128))
+            half = (base & 0x8000) | ((e0 - 8) << 7)
+            tiny = [(int(rng.integers(0, 2)) << 15) | (int(rng.integers(0, max(1, e0 - 9))) << 7) | int(rng.integers(0, 128))
+                    for _ in range(k - 2)]
+            sets.append(np.array([base, half] + tiny))
+        else:              # cancellation: x, -x and small terms
+            x = int(rng.integers(0x0080, 0x7F00))
+            rest = rng.integers(0, 0x7F00, k - 2) | (rng.integers(0, 2, k - 2) << 15)
+            sets.append(np.array([x, x | 0x8000] + list(rest)))
+    return [np.asarray(s, np.uint16) for s in sets]
+
+
+def test_bf16_sum_is_the_exact_sum_rounded_once(orc):
+    """Against rational arithmetic (Fractions, test-side rounding) on addend sets whose exponents span far more
+    than a float64 holds."""
+    rng = np.random.default_rng(2024)
+    for k in (1, 2, 3, 8):
+        for bits in _wide_bf16_sets(rng, 600, k):
+            exact = sum((Fraction(float(v)) for v in bf16_vals(bits)), Fraction(0))
+            assert orc.bf16_sum(bits) == _exact_bf16_round(exact), [hex(int(b)) for b in bits]
+
+
+def test_allreduce_reduces_with_the_exact_sum(orc):
+    """The all-reduce half's x is bf16_sum of the partials, element by element (wide-span partials)."""
+    rng = np.random.default_rng(7)
+    sets = _wide_bf16_sets(rng, 3 * 64, 8)
+    ps = [np.array([s[j] for s in sets], np.uint16).reshape(3, 64) for j in range(8)]
+    r = np.zeros((3, 64), np.uint16)                      # x + (+0) = x
+    w = wl.weight_bf16(64, 1)
+    res, _, _ = orc.allreduce_add_rmsnorm(ps, r, w, 1e-5)
+    want = np.array([orc.bf16_sum(s) for s in sets], np.uint16).reshape(3, 64)
+    np.testing.assert_array_equal(res, np.where(want == 0x8000, 0, want))
