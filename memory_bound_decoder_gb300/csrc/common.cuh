@@ -26,6 +26,18 @@ __device__ __forceinline__ uint4 load_cached(const uint4* p) { return __ldg(p); 
 
 // ------------------------------------------------------------------------------------------ bf16 / e4m3
 
+// Lane-wise bf16 maximum and minimum of two pairs given as bits (for non-negative values: magnitudes).
+__device__ __forceinline__ uint32_t max_bf16x2_bits(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t min_bf16x2_bits(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("min.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 // A 32-bit word holds two bf16 values: element 2k in the low half, element 2k+1 in the high half.
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }

@@ -35,29 +35,83 @@ __device__ __forceinline__ float2 exact_side(float2 p, float c_hi, float c_lo) {
     return make_float2(nudge(y_hi.x, y_lo.x), nudge(y_hi.y, y_lo.y));
 }
 
-// Sum the partial activations of this thread's vector exactly (packed double-float accumulation) and round
-// once to bf16: the reduced activation x of the all-reduce half. All the partials' loads are issued before
-// the first is used, so the vector costs one memory round trip.
+// Sum the partial activations of this thread's vector and round once to bf16, as the exact sum rounds: the
+// reduced activation x of the all-reduce half. All the partials' loads are issued before the first is used,
+// so the vector costs one memory round trip.
+//
+// Fast path: the plain fp32 sum s (from +0, packed fp32x2) is exact when the addends' exponents span little.
+// Every addend is a multiple of 2^(emin - 134) (emin, emax: the smallest and largest bf16 exponent field
+// among the element's addends, read off the smallest and largest magnitude; a field of 0, a zero or a
+// subnormal, is the conservative case) and every partial sum is below k 2^(emax - 126) <= 2^(emax - 126 + L),
+// L = ceil(log2 k); fp32 holds every multiple of that step below 2^24 times it, so each addition is exact when
+// emax - emin <= 16 - L, and s is then the exact sum. The span is checked first (a pass over the partials'
+// registers), then s is formed. Elements with a wider span are summed again exactly from the same registers (a
+// double-float sum, Knuth's TwoSum, rounded by dd_nudge_bf16), element slot by element slot, so a warp runs a
+// slot's exact sum only when one of its lanes needs it (about 1 element in 1000 of N(0,1) partials, k = 8).
 __device__ __forceinline__ uint4 reduce_partials(const NormParams& p, int64_t row, int c) {
+    const int n = p.n_partials;
     uint4 pv[kMaxPartials];
 #pragma unroll
     for (int k = 0; k < kMaxPartials; ++k)
-        if (k < p.n_partials) pv[k] = load_stream(static_cast<const uint4*>(p.partials[k]) + row * p.nvec + c);
-    DD2 acc[4];
+        if (k < n) pv[k] = load_stream(static_cast<const uint4*>(p.partials[k]) + row * p.nvec + c);
+    // largest exact span, in exponent-field units at bit 7: 16 - ceil(log2 n)
+    const uint32_t span_max = static_cast<uint32_t>(n <= 1 ? 16 : (n <= 2 ? 15 : (n <= 4 ? 14 : 13))) << 7;
+    unsigned int redo = 0;   // bit e: element e must be summed exactly
+    {
+        uint32_t emax[4], emin[4];   // largest and smallest addend magnitude, lane by lane (bf16 bits)
 #pragma unroll
-    for (int q = 0; q < 4; ++q) acc[q] = DD2{f2(0.0f), f2(0.0f)};
+        for (int q = 0; q < 4; ++q) emax[q] = emin[q] = reinterpret_cast<const uint32_t*>(&pv[0])[q] & 0x7FFF7FFFu;
 #pragma unroll
-    for (int k = 0; k < kMaxPartials; ++k) {
-        if (k >= p.n_partials) break;
+        for (int k = 1; k < kMaxPartials; ++k) {
+            if (k >= n) break;
+            const uint32_t* w = reinterpret_cast<const uint32_t*>(&pv[k]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t e = w[q] & 0x7FFF7FFFu;
+                emax[q] = max_bf16x2_bits(emax[q], e);
+                emin[q] = min_bf16x2_bits(emin[q], e);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t span = (emax[q] & 0x7F807F80u) - (emin[q] & 0x7F807F80u);   // lane-wise: no borrow
+            if ((span & 0xFFFFu) > span_max) redo |= 1u << (2 * q);
+            if ((span >> 16) > span_max) redo |= 2u << (2 * q);
+        }
+    }
+    float2 s[4];
+    {
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(&pv[0]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) s[q] = __fadd2_rn(f2(0.0f), bf16x2_to_float2(w[q]));   // from +0, as the exact sum
+    }
+#pragma unroll
+    for (int k = 1; k < kMaxPartials; ++k) {
+        if (k >= n) break;
         const uint32_t* w = reinterpret_cast<const uint32_t*>(&pv[k]);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) dd_accumulate(acc[q], bf16x2_to_float2(w[q]));
+        for (int q = 0; q < 4; ++q) s[q] = __fadd2_rn(s[q], bf16x2_to_float2(w[q]));
     }
     uint4 x;
     uint32_t* xw = reinterpret_cast<uint32_t*>(&x);
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-        xw[q] = pack_bf16x2(dd_nudge_bf16(acc[q].hi.x, acc[q].lo.x), dd_nudge_bf16(acc[q].hi.y, acc[q].lo.y));
+    for (int q = 0; q < 4; ++q) xw[q] = pack_bf16x2(s[q]);
+    if (redo) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            if (!(redo & (1u << e))) continue;
+            DD acc{0.0f, 0.0f};
+#pragma unroll
+            for (int k = 0; k < kMaxPartials; ++k) {
+                if (k >= n) break;
+                const uint32_t w = reinterpret_cast<const uint32_t*>(&pv[k])[e >> 1];
+                dd_accumulate(acc, (e & 1) ? bf16_hi(w) : bf16_lo(w));
+            }
+            const float v = dd_nudge_bf16(acc.hi, acc.lo);
+            const uint32_t b16 = pack_bf16x2(v, 0.0f) & 0xFFFFu;
+            xw[e >> 1] = (e & 1) ? ((xw[e >> 1] & 0x0000FFFFu) | (b16 << 16)) : ((xw[e >> 1] & 0xFFFF0000u) | b16);
+        }
+    }
     return x;
 }
 
@@ -175,13 +229,19 @@ __device__ __forceinline__ void norm_row_slice(const NormParams& p, int64_t row,
             if (live[i]) {
                 if constexpr (!ALLRED) xv[i] = load_stream(xr + c);
                 sv[i] = load_stream(rr + c);
-                if constexpr (kEarlyWeight) wv[i] = load_cached(wr + c);
+                if constexpr (kEarlyWeight && !ALLRED) wv[i] = load_cached(wr + c);
             }
         }
         if constexpr (ALLRED) {
 #pragma unroll
             for (int i = 0; i < VPT; ++i)
                 if (live[i]) xv[i] = reduce_partials(p, row, begin + threadIdx.x + i * blockDim.x);
+            // the weight (an L2 hit) after the partials, whose registers it would otherwise hold during the sum
+            if constexpr (kEarlyWeight) {
+#pragma unroll
+                for (int i = 0; i < VPT; ++i)
+                    if (live[i]) wv[i] = load_cached(wr + (begin + threadIdx.x + i * blockDim.x));
+            }
         }
         if (!single) exchange_init(ex, ctas_per_row);   // overlaps the loads in flight
 #pragma unroll

@@ -104,3 +104,71 @@ def test_inplace_out_is_first_partial():
     res_o, _, v = orc.allreduce_add_rmsnorm(ps, r, w, 1e-6)
     np.testing.assert_array_equal(res_g, res_o)
     check_bf16(o_g, v, "in place")
+
+
+def _bf16(x):
+    return wl.f32_to_bf16_bits(np.asarray(x, np.float32))
+
+
+def _adversarial_partials(k, T, H, seed):
+    """Partials whose sums stress the exactness test of the partial sum: every row mixes four constructions,
+    column by column (each appears in every 32-lane warp's vectors).
+      - wide spans: partial 0 scaled by 2^20, partial 1 by 2^-10 (the fp32 sum is inexact);
+      - near ties tipped by tiny terms: partial 0 a bf16 value, partial 1 half its bf16 ulp (the two sum exactly
+        to a rounding midpoint), the rest +-2^-(9..40) of it, so the exact sum lies just off the midpoint;
+      - cancellation: partial 1 = -partial 0, the rest small;
+      - zeros of either sign and bf16 subnormals."""
+    rng = np.random.default_rng(seed)
+    p = rng.standard_normal((k, T, H))
+    kind = rng.integers(0, 4, (T, H))
+    wide = kind == 0
+    if k >= 2:
+        p[0][wide] *= 2.0 ** 20
+        p[1][wide] *= 2.0 ** -10
+    tie = kind == 1
+    base = wl.bf16_bits_to_f32(_bf16(p[0] * 4)).astype(np.float64)
+    e = np.floor(np.log2(np.maximum(np.abs(base), 1e-30)))
+    if k >= 2:
+        p[0][tie] = base[tie]
+        p[1][tie] = (np.sign(base) * 2.0 ** (e - 8))[tie]
+        for j in range(2, k):
+            p[j][tie] = (rng.choice([-1.0, 1.0], (T, H)) * 2.0 ** (e - 8 - rng.integers(1, 33, (T, H))))[tie]
+    canc = kind == 2
+    if k >= 2:
+        p[0][canc] = wl.bf16_bits_to_f32(_bf16(p[0]))[canc]
+        p[1][canc] = -p[0][canc]
+        for j in range(2, k):
+            p[j][canc] *= 1e-3
+    odd = kind == 3
+    z = rng.integers(0, 4, (k, T, H))
+    for j in range(k):
+        p[j][odd & (z[j] == 0)] = 0.0
+        p[j][odd & (z[j] == 1)] = -0.0
+        p[j][odd & (z[j] == 2)] *= 2.0 ** -130          # bf16 subnormals
+    return [_bf16(p[j]) for j in range(k)]
+
+
+@pytest.mark.parametrize("k,T,H", [(8, 64, 4096), (2, 33, 1536), (3, 300, 8192), (4, 5, 16384), (8, 2048, 1024)])
+def test_allreduce_exactness_edges(k, T, H):
+    """The reduced activation equals the bf16 rounding of the exact sum where the fp32 sum is inexact, lands on
+    a rounding midpoint, cancels, or meets zeros and subnormals: the residual is compared bit for bit."""
+    ps = _adversarial_partials(k, T, H, seed=k * 7 + T)
+    r = wl.normal_bf16((T, H), T, "residual")
+    w = wl.weight_bf16(H, k)
+    res_g, o_g, _ = run(ps, r, w, 1e-5, "bf16")
+    res_o, _, v = orc.allreduce_add_rmsnorm(ps, r, w, 1e-5)
+    np.testing.assert_array_equal(res_g, res_o, "residual must be bit-exact")
+    check_bf16(o_g, v, "allreduce_add_rmsnorm")
+
+
+def test_allreduce_all_zero_partials_keep_the_sign_of_the_exact_sum():
+    """Every partial -0: the exact sum is +0 (an empty sum plus -0 terms), so x = +0 and the residual keeps its
+    own bits (r + 0 = r, including r = -0)."""
+    T, H, k = 4, 1024, 8
+    ps = [np.full((T, H), 0x8000, np.uint16) for _ in range(k)]
+    r = wl.normal_bf16((T, H), 3, "residual")
+    r[:, ::3] = 0x8000                                     # -0 residuals: -0 + x must give what +0 + -0 gives
+    w = wl.weight_bf16(H, 1)
+    res_g, _, _ = run(ps, r, w, 1e-5, "bf16")
+    res_o, _, _ = orc.allreduce_add_rmsnorm(ps, r, w, 1e-5)
+    np.testing.assert_array_equal(res_g, res_o)
