@@ -823,9 +823,10 @@ def prepare_step(torch, mbd, args, work: wl.Workload, rank: int, dev, props):
 
 
 def time_step(torch, mbd, dcalls, stream, steps: int, warmup: int, dev, props, rank: int, world: int) -> Dict:
-    """W untimed steps, a per-unit breakdown pass (CUDA events around every launch unit, untimed), then exactly
-    `steps` timed steps between events on the launch stream (barrier and synchronise on both sides), with events
-    around the roofline kernel's launch in every step and the clocks sampled meanwhile."""
+    """W untimed steps, a per-unit breakdown pass (CUDA events around every launch unit, each after a read of
+    twice the L2 size; untimed), then exactly `steps` timed steps between events on the launch stream (barrier
+    and synchronise on both sides), with events around the roofline kernel's launch in every step and the clocks
+    sampled meanwhile."""
     def step():
         for d in dcalls:
             d.launch()
@@ -835,16 +836,22 @@ def time_step(torch, mbd, dcalls, stream, steps: int, warmup: int, dev, props, r
             step()
     torch.cuda.synchronize(dev)
 
+    # per-unit breakdown: each unit between CUDA events after a read of twice the L2 size, so that L2 holds no
+    # dirty lines of an earlier kernel whose write-back the unit would pay for (as under ncu's cache control)
+    l2 = int(getattr(props, "L2_cache_size", 0)) or 126 * 2 ** 20
+    flush = torch.ones(2 * l2 // 4, dtype=torch.int32, device=dev)
     nb = max(3, min(20, steps))
     evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in dcalls]
            for _ in range(nb)]
     with torch.cuda.stream(stream):
         for k in range(nb):
             for d, (a, b) in zip(dcalls, evs[k]):
+                flush.max()
                 a.record(stream)
                 d.launch()
                 b.record(stream)
     torch.cuda.synchronize(dev)
+    del flush
     per_call_ms = [statistics.median(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(nb))
                    for i in range(len(dcalls))]
     # the roofline kernel: the slowest launch of a single call (batches and programs hold several kernels)
@@ -1079,7 +1086,10 @@ def run_mine(args, work: wl.Workload, rank: int, world: int, local_rank: int) ->
                                "unit per call)"
                                if any(isinstance(d, BatchGroup) for d in dcalls) else "none"),
                    "roofline_events": "CUDA events around the roofline kernel's launch in every timed step (they "
-                                      "break its overlap with the launches beside it)"},
+                                      "break its overlap with the launches beside it)",
+                   "kernels_breakdown": "each launch unit alone between CUDA events after a read of twice the L2 "
+                                        "size (no dirty lines of an earlier kernel left in L2 for it to write back), "
+                                        "untimed pass before the timed region"},
         "frac_of_measured_peak": summ["frac_of_measured_peak"],
         "tokens_per_s": summ["tokens_per_s"],
         "gpu_launches": summ["gpu_launches"],
