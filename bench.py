@@ -45,18 +45,24 @@ DEFAULT_WORKLOAD = "llama3.1-405b_fp8_T2048+ragged"
 # summarised under profiles/; valid only while what the kernel and its launch shape are built from hashes to
 # `src_sha256` (kernel_src_hash).
 TRAFFIC: Dict[str, Dict] = {
-    # profiles/swiglu_q8_dynamic_T4096_I28672.md
-    "swiglu_q8_dynamic_T4096_I28672": {"bytes": 539456256, "src_sha256": "849582ef35a93e1ad365304d71de45e588c31f4ec0445b995fcc2045cf6bfdfe"},
-    # profiles/allreduce_rmsnorm_q8_static_k8_T2048_H16384.md
-    "allreduce_rmsnorm_q8_static_k8_T2048_H16384": {"bytes": 680083712, "src_sha256": "13f15eb1dca99e9c05a95cef2020adc193334f695d1c618baf7bcc7711dfc44a"},
-    # profiles/add_rmsnorm_nvfp4_T2048_H16384.md
-    "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 167228416, "src_sha256": "13f15eb1dca99e9c05a95cef2020adc193334f695d1c618baf7bcc7711dfc44a"},
-    # profiles/swiglu_nvfp4_T2048_I53248.md
-    "swiglu_nvfp4_T2048_I53248": {"bytes": 467772160, "src_sha256": "849582ef35a93e1ad365304d71de45e588c31f4ec0445b995fcc2045cf6bfdfe"},
     # profiles/swiglu_q8_dynamic_T2048_I53248.md
-    "swiglu_q8_dynamic_T2048_I53248": {"bytes": 527144960, "src_sha256": "849582ef35a93e1ad365304d71de45e588c31f4ec0445b995fcc2045cf6bfdfe"},
+    "swiglu_q8_dynamic_T2048_I53248": {"bytes": 526824960, "src_sha256": "0e2de2bb58c5dcdcf65bb816ea289940c4d65d7e9088fb66751d9cbdddf2f649"},
+    # profiles/add_rmsnorm_q8_static_T1000_H5120.md
+    "add_rmsnorm_q8_static_T1000_H5120": {"bytes": 20503296, "src_sha256": "1097adc14743143331e9e95ac9f51c465c3db07934c921e1050caaebf1094439"},
     # profiles/add_rmsnorm_q8_static_T2048_H16384.md
-    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 177783808, "src_sha256": "13f15eb1dca99e9c05a95cef2020adc193334f695d1c618baf7bcc7711dfc44a"},
+    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 177612032, "src_sha256": "1097adc14743143331e9e95ac9f51c465c3db07934c921e1050caaebf1094439"},
+    # profiles/add_rmsnorm_T8192_H4096.md
+    "add_rmsnorm_T8192_H4096": {"bytes": 209935360, "src_sha256": "1097adc14743143331e9e95ac9f51c465c3db07934c921e1050caaebf1094439"},
+    # profiles/swiglu_T8192_I14336.md
+    "swiglu_T8192_I14336": {"bytes": 658269696, "src_sha256": "0e2de2bb58c5dcdcf65bb816ea289940c4d65d7e9088fb66751d9cbdddf2f649"},
+    # profiles/swiglu_q8_dynamic_T4096_I28672.md
+    "swiglu_q8_dynamic_T4096_I28672": {"bytes": 539296512, "src_sha256": "0e2de2bb58c5dcdcf65bb816ea289940c4d65d7e9088fb66751d9cbdddf2f649"},
+    # profiles/swiglu_nvfp4_T2048_I53248.md
+    "swiglu_nvfp4_T2048_I53248": {"bytes": 467791104, "src_sha256": "0e2de2bb58c5dcdcf65bb816ea289940c4d65d7e9088fb66751d9cbdddf2f649"},
+    # profiles/add_rmsnorm_nvfp4_T2048_H16384.md
+    "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 166748416, "src_sha256": "1097adc14743143331e9e95ac9f51c465c3db07934c921e1050caaebf1094439"},
+    # profiles/allreduce_rmsnorm_q8_static_k8_T2048_H16384.md
+    "allreduce_rmsnorm_q8_static_k8_T2048_H16384": {"bytes": 679209728, "src_sha256": "1097adc14743143331e9e95ac9f51c465c3db07934c921e1050caaebf1094439"},
 }
 
 
