@@ -15,28 +15,66 @@
 // walkthrough, Part V, quantization co-designed with the hardware). The dynamic per-token variant
 // reduces the sum of squares and max |w * s| together (the scale is max |w * s| * inv / 448), then stores
 // the codes from registers.
+#include <atomic>
+
 #include "norm_impl.cuh"
 
 namespace mbd {
 
 namespace {
 
-// The partial-sum form asks for two 512-thread CTAs per SM (<= 64 registers): its eight loads in flight
-// per vector would otherwise leave one CTA, a quarter of the SM's warps.
+// The partial-sum form brings the CTA's slices of the partials into shared memory with bulk copies (one thread
+// issues them; dynamic shared memory, n_partials x slice vectors) and asks for three 512-thread CTAs' worth of
+// registers per SM: registers hold one partial vector at a time, not all of them.
 template <int VPT, int EP, bool ALLRED, int CL>
-__global__ void __launch_bounds__(512, ALLRED ? 2 : 1) add_rmsnorm_kernel(const __grid_constant__ NormParams p, int ctas_per_row, int slice,
+__global__ void __launch_bounds__(512, ALLRED ? 3 : 1) add_rmsnorm_kernel(const __grid_constant__ NormParams p, int ctas_per_row, int slice,
                                                                         int prefetch, int order) {
+    extern __shared__ __align__(16) uint4 pslices[];   // all-reduce half: partial k's slice at [k * slice, ...)
     __shared__ NormSmem sm;
+    __shared__ unsigned long long pbar;
     const int64_t row = launch_row();
     if (row >= p.rows) return;   // past the last row (the whole cluster shares the row)
     const int rank = static_cast<int>(blockIdx.x);
     const int begin = rank * slice;
     const int end = min(begin + slice, p.nvec);
     pdl_enter_trigger(order);
+    if constexpr (ALLRED) {
+        if (threadIdx.x == 0) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&pbar)) : "memory");
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+    }
     if (prefetch) norm_prefetch<VPT, ALLRED>(p, row, begin, end);
     pdl_enter_wait(order);
-    norm_row_slice<VPT, EP, ALLRED, CL>(p, row, rank, ctas_per_row, begin, end, sm);
+    if constexpr (ALLRED) {
+        if (threadIdx.x == 0) load_partials_bulk(p, row, begin, end - begin, slice, pslices, smem_addr(&pbar));
+        norm_row_slice<VPT, EP, ALLRED, CL>(p, row, rank, ctas_per_row, begin, end, sm, pslices, slice, smem_addr(&pbar));
+    } else {
+        norm_row_slice<VPT, EP, ALLRED, CL>(p, row, rank, ctas_per_row, begin, end, sm);
+    }
     pdl_leave(order);
+}
+
+// Per device and partial-sum kernel variant (epilogue x row in one CTA or a cluster): the id of the context in
+// which its preferred carveout, the largest shared-memory share, was last requested, so that shared memory
+// (n_partials x slice vectors per CTA) rather than the L1 share bounds the resident CTAs. A kernel attribute
+// belongs to a context; with no context id (0) every launch requests it.
+std::atomic<unsigned long long> g_partials_carveout_ctx[kMaxCachedDevices][8];
+
+cudaError_t prefer_shared_carveout(const void* kern, int variant) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long ctx = current_context_id();
+    if (dev < 0 || dev >= kMaxCachedDevices || ctx == 0 ||
+        g_partials_carveout_ctx[dev][variant].load(std::memory_order_acquire) != ctx) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 static_cast<int>(cudaSharedmemCarveoutMaxShared));
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < kMaxCachedDevices) g_partials_carveout_ctx[dev][variant].store(ctx, std::memory_order_release);
+    }
+    return cudaSuccess;
 }
 
 template <int EP>
@@ -58,6 +96,17 @@ cudaError_t launch_ep(const NormParams& p, const RowPlan& plan, cudaStream_t s) 
         }
     }
     fill_launch(cfg, attr, p.rows, plan.ctas_per_row, plan.threads, plan.ctas_per_row, s);
+    if (p.n_partials > 0) {
+        const cudaError_t ce = prefer_shared_carveout(reinterpret_cast<const void*>(kern), EP * 2 + (cl ? 1 : 0));
+        if (ce != cudaSuccess) return ce;
+        const size_t smem = static_cast<size_t>(p.n_partials) * static_cast<size_t>(plan.slice) * 16;
+        if (smem > 48 * 1024) {   // above the default dynamic shared-memory limit: opt in (a kernel attribute)
+            const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       static_cast<int>(smem));
+            if (e != cudaSuccess) return e;
+        }
+        cfg.dynamicSmemBytes = smem;
+    }
     return cudaLaunchKernelEx(&cfg, kern, p, plan.ctas_per_row, plan.slice, plan.prefetch, plan.order);
 }
 

@@ -35,84 +35,103 @@ __device__ __forceinline__ float2 exact_side(float2 p, float c_hi, float c_lo) {
     return make_float2(nudge(y_hi.x, y_lo.x), nudge(y_hi.y, y_lo.y));
 }
 
-// Sum the partial activations of this thread's vector and round once to bf16, as the exact sum rounds: the
-// reduced activation x of the all-reduce half. All the partials' loads are issued before the first is used,
-// so the vector costs one memory round trip.
+// Sum the partial activations of one vector and round once to bf16, as the exact sum rounds: the reduced
+// activation x of the all-reduce half. The CTA's slices of the n partials sit in shared memory (brought in by
+// bulk copies, `slice` vectors each, this thread's vector at index c of every slice).
 //
 // Fast path: the plain fp32 sum s (from +0, packed fp32x2) is exact when the addends' exponents span little.
 // Every addend is a multiple of 2^(emin - 134) (emin, emax: the smallest and largest bf16 exponent field
 // among the element's addends, read off the smallest and largest magnitude; a field of 0, a zero or a
 // subnormal, is the conservative case) and every partial sum is below k 2^(emax - 126) <= 2^(emax - 126 + L),
 // L = ceil(log2 k); fp32 holds every multiple of that step below 2^24 times it, so each addition is exact when
-// emax - emin <= 16 - L, and s is then the exact sum. The span is checked first (a pass over the partials'
-// registers), then s is formed. Elements with a wider span are summed again exactly from the same registers (a
-// double-float sum, Knuth's TwoSum, rounded by dd_nudge_bf16), element slot by element slot, so a warp runs a
-// slot's exact sum only when one of its lanes needs it (about 1 element in 1000 of N(0,1) partials, k = 8).
-__device__ __forceinline__ uint4 reduce_partials(const NormParams& p, int64_t row, int c) {
-    const int n = p.n_partials;
-    uint4 pv[kMaxPartials];
-#pragma unroll
-    for (int k = 0; k < kMaxPartials; ++k)
-        if (k < n) pv[k] = load_stream(static_cast<const uint4*>(p.partials[k]) + row * p.nvec + c);
-    // largest exact span, in exponent-field units at bit 7: 16 - ceil(log2 n)
-    const uint32_t span_max = static_cast<uint32_t>(n <= 1 ? 16 : (n <= 2 ? 15 : (n <= 4 ? 14 : 13))) << 7;
-    unsigned int redo = 0;   // bit e: element e must be summed exactly
+// emax - emin <= 16 - L, and s is then the exact sum. Elements with a wider span are summed again exactly from
+// shared memory (a double-float sum, Knuth's TwoSum, rounded by dd_nudge_bf16), element slot by element slot,
+// so a warp runs a slot's exact sum only when one of its lanes needs it (about 1 element in 1000 of N(0,1)
+// partials, k = 8).
+__device__ __forceinline__ uint4 reduce_partials_smem(const uint4* slices, int slice, int n, int c) {
+    float2 s[4];
+    uint32_t emax[4], emin[4];   // largest and smallest addend magnitude, lane by lane (bf16 bits)
     {
-        uint32_t emax[4], emin[4];   // largest and smallest addend magnitude, lane by lane (bf16 bits)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) emax[q] = emin[q] = reinterpret_cast<const uint32_t*>(&pv[0])[q] & 0x7FFF7FFFu;
-#pragma unroll
-        for (int k = 1; k < kMaxPartials; ++k) {
-            if (k >= n) break;
-            const uint32_t* w = reinterpret_cast<const uint32_t*>(&pv[k]);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint32_t e = w[q] & 0x7FFF7FFFu;
-                emax[q] = max_bf16x2_bits(emax[q], e);
-                emin[q] = min_bf16x2_bits(emin[q], e);
-            }
-        }
+        const uint4 v = slices[c];
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(&v);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const uint32_t span = (emax[q] & 0x7F807F80u) - (emin[q] & 0x7F807F80u);   // lane-wise: no borrow
-            if ((span & 0xFFFFu) > span_max) redo |= 1u << (2 * q);
-            if ((span >> 16) > span_max) redo |= 2u << (2 * q);
+            s[q] = __fadd2_rn(f2(0.0f), bf16x2_to_float2(w[q]));   // from +0, as the exact sum: -0 + -0 is +0
+            emax[q] = emin[q] = w[q] & 0x7FFF7FFFu;
         }
-    }
-    float2 s[4];
-    {
-        const uint32_t* w = reinterpret_cast<const uint32_t*>(&pv[0]);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) s[q] = __fadd2_rn(f2(0.0f), bf16x2_to_float2(w[q]));   // from +0, as the exact sum
     }
 #pragma unroll
     for (int k = 1; k < kMaxPartials; ++k) {
         if (k >= n) break;
-        const uint32_t* w = reinterpret_cast<const uint32_t*>(&pv[k]);
+        const uint4 v = slices[k * slice + c];
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(&v);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) s[q] = __fadd2_rn(s[q], bf16x2_to_float2(w[q]));
+        for (int q = 0; q < 4; ++q) {
+            s[q] = __fadd2_rn(s[q], bf16x2_to_float2(w[q]));
+            const uint32_t m = w[q] & 0x7FFF7FFFu;
+            emax[q] = max_bf16x2_bits(emax[q], m);
+            emin[q] = min_bf16x2_bits(emin[q], m);
+        }
     }
+    // largest exact span, in exponent-field units at bit 7: 16 - ceil(log2 n)
+    const uint32_t span_max = static_cast<uint32_t>(n <= 1 ? 16 : (n <= 2 ? 15 : (n <= 4 ? 14 : 13))) << 7;
+    unsigned int redo = 0;   // bit e: element e must be summed exactly
     uint4 x;
     uint32_t* xw = reinterpret_cast<uint32_t*>(&x);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) xw[q] = pack_bf16x2(s[q]);
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t span = (emax[q] & 0x7F807F80u) - (emin[q] & 0x7F807F80u);   // lane-wise: no borrow
+        if ((span & 0xFFFFu) > span_max) redo |= 1u << (2 * q);
+        if ((span >> 16) > span_max) redo |= 2u << (2 * q);
+        xw[q] = pack_bf16x2(s[q]);
+    }
     if (redo) {
+        const uint16_t* e16 = reinterpret_cast<const uint16_t*>(slices);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             if (!(redo & (1u << e))) continue;
             DD acc{0.0f, 0.0f};
-#pragma unroll
-            for (int k = 0; k < kMaxPartials; ++k) {
-                if (k >= n) break;
-                const uint32_t w = reinterpret_cast<const uint32_t*>(&pv[k])[e >> 1];
-                dd_accumulate(acc, (e & 1) ? bf16_hi(w) : bf16_lo(w));
-            }
+            for (int k = 0; k < n; ++k)
+                dd_accumulate(acc, __uint_as_float(static_cast<uint32_t>(e16[(k * slice + c) * 8 + e]) << 16));
             const float v = dd_nudge_bf16(acc.hi, acc.lo);
             const uint32_t b16 = pack_bf16x2(v, 0.0f) & 0xFFFFu;
             xw[e >> 1] = (e & 1) ? ((xw[e >> 1] & 0x0000FFFFu) | (b16 << 16)) : ((xw[e >> 1] & 0xFFFF0000u) | b16);
         }
     }
     return x;
+}
+
+// Thread 0: the CTA's slices of the n partials, `slice` vectors each from vector `begin` of `row` (`count` of them
+// are real), into shared memory by bulk copies counted on the mbarrier `bar` (initialised beforehand).
+__device__ __forceinline__ void load_partials_bulk(const NormParams& p, int64_t row, int begin, int count, int slice,
+                                                   uint4* slices, uint32_t bar) {
+    const uint32_t bytes = static_cast<uint32_t>(count) * 16u;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes * p.n_partials)
+                 : "memory");
+    for (int k = 0; k < p.n_partials; ++k) {
+        const uint4* src = static_cast<const uint4*>(p.partials[k]) + row * p.nvec + begin;
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                     ::"r"(smem_addr(slices + k * slice)), "l"(src), "r"(bytes), "r"(bar) : "memory");
+    }
+}
+
+// Every thread: wait (bounded) for the bulk copies counted on `bar` (phase 0). On expiry: an error bit, and a
+// second bounded wait for the copies, which write into this CTA's shared memory, before it may leave.
+__device__ __forceinline__ bool wait_partials(uint32_t bar) {
+    const long long t0 = clock64();
+    uint32_t done = 0;
+    while (true) {
+        asm volatile("{\n .reg .pred q;\n mbarrier.try_wait.parity.shared::cta.b64 q, [%1], 0;\n selp.u32 %0, 1, 0, q;\n}"
+                     : "=r"(done) : "r"(bar) : "memory");
+        if (done || clock64() - t0 > kWaitLimitCycles) break;
+    }
+    if (done) return true;
+    if (threadIdx.x == 0) atomicOr(&g_device_error_flags, kDevErrExchangeTimeout);
+    const long long t1 = clock64();
+    while (!done && clock64() - t1 < kWaitLimitCycles)
+        asm volatile("{\n .reg .pred q;\n mbarrier.try_wait.parity.shared::cta.b64 q, [%1], 0;\n selp.u32 %0, 1, 0, q;\n}"
+                     : "=r"(done) : "r"(bar) : "memory");
+    return false;
 }
 
 }  // namespace
@@ -127,11 +146,7 @@ __device__ __forceinline__ void norm_prefetch(const NormParams& p, int64_t row, 
         const int c = begin + threadIdx.x + i * blockDim.x;
         if (c >= end) continue;
         prefetch_l2(rr + c);
-        if constexpr (ALLRED) {
-            for (int k = 0; k < p.n_partials; ++k) prefetch_l2(static_cast<const uint4*>(p.partials[k]) + row * p.nvec + c);
-        } else {
-            prefetch_l2(xr + c);
-        }
+        if constexpr (!ALLRED) prefetch_l2(xr + c);   // the partials come by bulk copies after the wait
     }
 }
 
@@ -202,7 +217,8 @@ __device__ __forceinline__ void norm_store(const NormParams& p, int64_t row, int
 // cost the kernels about 1%); kRowAny decides at run time.
 template <int VPT, int EP, bool ALLRED, int CL = kRowAny>
 __device__ __forceinline__ void norm_row_slice(const NormParams& p, int64_t row, int rank, int nctas, int begin,
-                                               int end, NormSmem& sm) {
+                                               int end, NormSmem& sm, const uint4* pslices = nullptr,
+                                               int pslice = 0, uint32_t pbar = 0) {
     PSum* part_sum = sm.part_sum;
     RowStats* part_stats = sm.part_stats;
     Exchange& ex = sm.ex;
@@ -220,6 +236,7 @@ __device__ __forceinline__ void norm_row_slice(const NormParams& p, int64_t row,
     // 1. one pass over HBM: x and residual in, s = bf16(x + r) kept packed in registers and written back
     uint4 sv[VPT], wv[VPT];
     bool live[VPT];
+    bool landed = true;   // all-reduce half: the partials' bulk copies completed (false: a bounded wait expired)
     {
         uint4 xv[VPT];
 #pragma unroll
@@ -233,20 +250,24 @@ __device__ __forceinline__ void norm_row_slice(const NormParams& p, int64_t row,
             }
         }
         if constexpr (ALLRED) {
+            // the partials' slices are in flight into shared memory (bulk copies issued at kernel start); the
+            // barrier that follows makes the copies' mbarrier initialisation visible to every thread
+            if (single) __syncthreads(); else exchange_init(ex, ctas_per_row);
+            landed = wait_partials(pbar);
 #pragma unroll
             for (int i = 0; i < VPT; ++i)
-                if (live[i]) xv[i] = reduce_partials(p, row, begin + threadIdx.x + i * blockDim.x);
-            // the weight (an L2 hit) after the partials, whose registers it would otherwise hold during the sum
+                if (live[i]) xv[i] = reduce_partials_smem(pslices, pslice, p.n_partials, threadIdx.x + i * blockDim.x);
             if constexpr (kEarlyWeight) {
 #pragma unroll
                 for (int i = 0; i < VPT; ++i)
                     if (live[i]) wv[i] = load_cached(wr + (begin + threadIdx.x + i * blockDim.x));
             }
+        } else {
+            if (!single) exchange_init(ex, ctas_per_row);   // overlaps the loads in flight
         }
-        if (!single) exchange_init(ex, ctas_per_row);   // overlaps the loads in flight
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
-            if (!live[i]) continue;
+            if (!live[i] || !landed) continue;
             const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv[i]);
             uint32_t* sw = reinterpret_cast<uint32_t*>(&sv[i]);
 #pragma unroll
@@ -285,6 +306,7 @@ __device__ __forceinline__ void norm_row_slice(const NormParams& p, int64_t row,
             for (int i = 0; i < VPT; ++i)
                 if (live[i]) wv[i] = load_cached(wr + (begin + threadIdx.x + i * blockDim.x));
         }
+        if (!landed) return;   // the error bit is set; nothing is written
 
         norm_store<VPT, EP>(p, row, begin, sv, wv, live, inv);
     } else {
@@ -318,9 +340,10 @@ __device__ __forceinline__ void norm_row_slice(const NormParams& p, int64_t row,
                 const float c_hi = static_cast<float>(c);
                 row_const[0] = c_hi;
                 row_const[1] = static_cast<float>(c - static_cast<double>(c_hi));
-                if (rank == 0) p.scale[row] = sc;
+                if (rank == 0 && landed) p.scale[row] = sc;
             }))
             return;
+        if (!landed) return;   // the error bit is set; nothing is written
         const float c_hi = row_const[0], c_lo = row_const[1];
         uint2* outr = reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + row * (int64_t)p.nvec * 8);
 #pragma unroll
