@@ -100,7 +100,8 @@ int cdiv(int a, int b) { return (a + b - 1) / b; }
 //      NVFP4 (more work per vector): the norm takes 4 vectors per thread (34.6 vs 43.0 us at T 4096,
 //            H 8192), the SwiGLU stream ~448-vector slices at 2 vectors per thread (76.8 vs 81.5 us at
 //            T 2048, I 53248; 80.7 vs 87.3 us at T 4096, I 28672);
-//      norm over partial activations: one vector per thread, ~128-vector slices over up to 8 CTAs.
+//      norm over partial activations: one vector per thread, ~256-vector slices over up to 8 CTAs (the
+//            slices of the partials come into shared memory by bulk copies).
 //  - one to four rows per SM: the norm stays in one CTA with the fewest vectors per thread that fit 512
 //    threads (a cluster exchange costs +50% there), the bf16 and FP8 streams take ~256-vector slices (the
 //    tuner: +26 to +57% over the large-batch shapes at 256 tokens);
@@ -130,7 +131,8 @@ bool plan_rows(int64_t rows, int nvec, Shape shape, int sms, bool pairs, mbd::Ro
             if (pairs || nvec >= 512) min_vpt = 4;
         }
     } else if (shape == Shape::kNormPartials) {   // one vector per thread (all partials' loads in flight)
-        c = cdiv(nvec, small ? 256 : 128);         // small CTAs: 8 x 256 threads beat 4 x 512 at H 16384
+        c = cdiv(nvec, 256);   // slices of ~256 vectors (8 x 256 threads at H 16384): at H 5120 and 8192 they
+                               // beat ~128 by 8 to 26%, at H 16384 rows over 4 x 512 lose 3%
     } else if (shape == Shape::kRowMax) {
         if (small) {             // up to 8 CTAs of up to 512 threads, one vector each where the row allows
             c = cdiv(nvec, 256);
