@@ -46,23 +46,23 @@ DEFAULT_WORKLOAD = "llama3.1-405b_fp8_T2048+ragged"
 # `src_sha256` (kernel_src_hash).
 TRAFFIC: Dict[str, Dict] = {
     # profiles/swiglu_q8_dynamic_T2048_I53248.md
-    "swiglu_q8_dynamic_T2048_I53248": {"bytes": 526824960, "src_sha256": "0e2de2bb58c5dcdcf65bb816ea289940c4d65d7e9088fb66751d9cbdddf2f649"},
+    "swiglu_q8_dynamic_T2048_I53248": {"bytes": 526723328, "src_sha256": "26e1097a2a1e98e5997676367e17d4d485b541db6dcf82f681c0813bcb64aede"},
     # profiles/add_rmsnorm_q8_static_T1000_H5120.md
-    "add_rmsnorm_q8_static_T1000_H5120": {"bytes": 20503296, "src_sha256": "1097adc14743143331e9e95ac9f51c465c3db07934c921e1050caaebf1094439"},
+    "add_rmsnorm_q8_static_T1000_H5120": {"bytes": 20503808, "src_sha256": "23d30dc5eae61bc04ae393cf5bc05553cdd9ce0d252cc43004be88db361148bd"},
     # profiles/add_rmsnorm_q8_static_T2048_H16384.md
-    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 177612032, "src_sha256": "1097adc14743143331e9e95ac9f51c465c3db07934c921e1050caaebf1094439"},
+    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 178109184, "src_sha256": "23d30dc5eae61bc04ae393cf5bc05553cdd9ce0d252cc43004be88db361148bd"},
     # profiles/add_rmsnorm_T8192_H4096.md
-    "add_rmsnorm_T8192_H4096": {"bytes": 209935360, "src_sha256": "1097adc14743143331e9e95ac9f51c465c3db07934c921e1050caaebf1094439"},
+    "add_rmsnorm_T8192_H4096": {"bytes": 210001664, "src_sha256": "23d30dc5eae61bc04ae393cf5bc05553cdd9ce0d252cc43004be88db361148bd"},
     # profiles/swiglu_T8192_I14336.md
-    "swiglu_T8192_I14336": {"bytes": 658269696, "src_sha256": "0e2de2bb58c5dcdcf65bb816ea289940c4d65d7e9088fb66751d9cbdddf2f649"},
+    "swiglu_T8192_I14336": {"bytes": 658686208, "src_sha256": "26e1097a2a1e98e5997676367e17d4d485b541db6dcf82f681c0813bcb64aede"},
     # profiles/swiglu_q8_dynamic_T4096_I28672.md
-    "swiglu_q8_dynamic_T4096_I28672": {"bytes": 539296512, "src_sha256": "0e2de2bb58c5dcdcf65bb816ea289940c4d65d7e9088fb66751d9cbdddf2f649"},
+    "swiglu_q8_dynamic_T4096_I28672": {"bytes": 539926272, "src_sha256": "26e1097a2a1e98e5997676367e17d4d485b541db6dcf82f681c0813bcb64aede"},
     # profiles/swiglu_nvfp4_T2048_I53248.md
-    "swiglu_nvfp4_T2048_I53248": {"bytes": 467791104, "src_sha256": "0e2de2bb58c5dcdcf65bb816ea289940c4d65d7e9088fb66751d9cbdddf2f649"},
+    "swiglu_nvfp4_T2048_I53248": {"bytes": 467696640, "src_sha256": "26e1097a2a1e98e5997676367e17d4d485b541db6dcf82f681c0813bcb64aede"},
     # profiles/add_rmsnorm_nvfp4_T2048_H16384.md
-    "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 166748416, "src_sha256": "1097adc14743143331e9e95ac9f51c465c3db07934c921e1050caaebf1094439"},
+    "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 166826240, "src_sha256": "23d30dc5eae61bc04ae393cf5bc05553cdd9ce0d252cc43004be88db361148bd"},
     # profiles/allreduce_rmsnorm_q8_static_k8_T2048_H16384.md
-    "allreduce_rmsnorm_q8_static_k8_T2048_H16384": {"bytes": 679209728, "src_sha256": "1097adc14743143331e9e95ac9f51c465c3db07934c921e1050caaebf1094439"},
+    "allreduce_rmsnorm_q8_static_k8_T2048_H16384": {"bytes": 689894144, "src_sha256": "23d30dc5eae61bc04ae393cf5bc05553cdd9ce0d252cc43004be88db361148bd"},
 }
 
 
