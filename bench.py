@@ -46,23 +46,23 @@ DEFAULT_WORKLOAD = "llama3.1-405b_fp8_T2048+ragged"
 # `src_sha256` (kernel_src_hash).
 TRAFFIC: Dict[str, Dict] = {
     # profiles/swiglu_q8_dynamic_T2048_I53248.md
-    "swiglu_q8_dynamic_T2048_I53248": {"bytes": 526723328, "src_sha256": "26e1097a2a1e98e5997676367e17d4d485b541db6dcf82f681c0813bcb64aede"},
+    "swiglu_q8_dynamic_T2048_I53248": {"bytes": 526931200, "src_sha256": "35b3b830f6b2604e9101f507e895278e5fe67df3bc9bab458c61c04674f127ad"},
     # profiles/add_rmsnorm_q8_static_T1000_H5120.md
-    "add_rmsnorm_q8_static_T1000_H5120": {"bytes": 20503808, "src_sha256": "23d30dc5eae61bc04ae393cf5bc05553cdd9ce0d252cc43004be88db361148bd"},
+    "add_rmsnorm_q8_static_T1000_H5120": {"bytes": 20503296, "src_sha256": "ceb7187f682340517820309fff4792c19e20c3f01c204d0fe3c2506cdf778831"},
     # profiles/add_rmsnorm_q8_static_T2048_H16384.md
-    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 178109184, "src_sha256": "23d30dc5eae61bc04ae393cf5bc05553cdd9ce0d252cc43004be88db361148bd"},
+    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 177857024, "src_sha256": "ceb7187f682340517820309fff4792c19e20c3f01c204d0fe3c2506cdf778831"},
     # profiles/add_rmsnorm_T8192_H4096.md
-    "add_rmsnorm_T8192_H4096": {"bytes": 210001664, "src_sha256": "23d30dc5eae61bc04ae393cf5bc05553cdd9ce0d252cc43004be88db361148bd"},
+    "add_rmsnorm_T8192_H4096": {"bytes": 210126848, "src_sha256": "ceb7187f682340517820309fff4792c19e20c3f01c204d0fe3c2506cdf778831"},
     # profiles/swiglu_T8192_I14336.md
-    "swiglu_T8192_I14336": {"bytes": 658686208, "src_sha256": "26e1097a2a1e98e5997676367e17d4d485b541db6dcf82f681c0813bcb64aede"},
+    "swiglu_T8192_I14336": {"bytes": 657681920, "src_sha256": "35b3b830f6b2604e9101f507e895278e5fe67df3bc9bab458c61c04674f127ad"},
     # profiles/swiglu_q8_dynamic_T4096_I28672.md
-    "swiglu_q8_dynamic_T4096_I28672": {"bytes": 539926272, "src_sha256": "26e1097a2a1e98e5997676367e17d4d485b541db6dcf82f681c0813bcb64aede"},
+    "swiglu_q8_dynamic_T4096_I28672": {"bytes": 539317248, "src_sha256": "35b3b830f6b2604e9101f507e895278e5fe67df3bc9bab458c61c04674f127ad"},
     # profiles/swiglu_nvfp4_T2048_I53248.md
-    "swiglu_nvfp4_T2048_I53248": {"bytes": 467696640, "src_sha256": "26e1097a2a1e98e5997676367e17d4d485b541db6dcf82f681c0813bcb64aede"},
+    "swiglu_nvfp4_T2048_I53248": {"bytes": 467557376, "src_sha256": "35b3b830f6b2604e9101f507e895278e5fe67df3bc9bab458c61c04674f127ad"},
     # profiles/add_rmsnorm_nvfp4_T2048_H16384.md
-    "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 166826240, "src_sha256": "23d30dc5eae61bc04ae393cf5bc05553cdd9ce0d252cc43004be88db361148bd"},
+    "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 166977792, "src_sha256": "ceb7187f682340517820309fff4792c19e20c3f01c204d0fe3c2506cdf778831"},
     # profiles/allreduce_rmsnorm_q8_static_k8_T2048_H16384.md
-    "allreduce_rmsnorm_q8_static_k8_T2048_H16384": {"bytes": 689894144, "src_sha256": "23d30dc5eae61bc04ae393cf5bc05553cdd9ce0d252cc43004be88db361148bd"},
+    "allreduce_rmsnorm_q8_static_k8_T2048_H16384": {"bytes": 689718784, "src_sha256": "ceb7187f682340517820309fff4792c19e20c3f01c204d0fe3c2506cdf778831"},
 }
 
 
@@ -529,6 +529,39 @@ class BatchGroup:
         return sum(t.numel() * t.element_size() for t, _ in self.d2h)
 
 
+class ProgramBatchGroup:
+    """A program launch and a batch as ONE call of mbd_run_independent_with_program: the program (the small,
+    latency-bound calls) launches first and the batch's single calls start beside it, each overlapping the one
+    before. Same buffers and outputs as the program launch followed by the calls."""
+
+    def __init__(self, mbd, program: "ProgramGroup", batch: "BatchGroup"):
+        self.mbd, self.program, self.batch = mbd, program, batch
+        self.members = program.members + batch.members
+        self.call = BatchCall(program.call.calls + batch.call.calls)
+        self.call.name = f"{program.call.name}+{batch.call.name}"
+        self.h2d = program.h2d + batch.h2d
+        self.d2h = program.d2h + batch.d2h
+        self.handle = None
+
+    def bind(self, stream_handle: int):
+        self.program.bind(stream_handle)
+        self.batch.bind(stream_handle)
+        self.handle = stream_handle
+
+    def launch(self):
+        lib = self.mbd.get_lib()
+        rc = lib.mbd_run_independent_with_program(ctypes.addressof(self.program.plan.buf), self.program.sched.data_ptr(),
+                                                  self.batch.arr, self.batch.n, self.handle)
+        if rc != 0:
+            raise RuntimeError(f"{self.call.name}: {lib.mbd_status_string(rc).decode()}")
+
+    def bytes_in(self):
+        return sum(t.numel() * t.element_size() for t, _ in self.h2d)
+
+    def bytes_out(self):
+        return sum(t.numel() * t.element_size() for t, _ in self.d2h)
+
+
 def launch_groups(calls: List[wl.Call], layers: int, sms: int, max_ops: int = 128, max_batch: int = 64,
                   programs: bool = True, batches: bool = True) -> list:
     """Launch units of one step, in order: an int (the index of a call launched on its own) or (label, [indices])
@@ -600,6 +633,13 @@ def group_small_calls(torch, mbd, work: wl.Workload, dcalls: List[DeviceCall], s
             out.append(BatchGroup(mbd, [dcalls[i] for i in u[1]]))
         else:
             out.append(ProgramGroup(torch, mbd, u[0], [dcalls[i] for i in u[1]], dev))
+    # one program launch and one batch: the program opens the batch (mbd_run_independent_with_program), so
+    # its latency-bound rows run beside the batch's bandwidth-bound ones
+    progs = [u for u in out if isinstance(u, ProgramGroup)]
+    batches = [u for u in out if isinstance(u, BatchGroup)]
+    if len(progs) == 1 and len(batches) == 1:
+        fused = ProgramBatchGroup(mbd, progs[0], batches[0])
+        out = [fused if u is batches[0] else u for u in out if u is not progs[0]]
     return out
 
 
@@ -1086,11 +1126,14 @@ def run_mine(args, work: wl.Workload, rank: int, world: int, local_rank: int) ->
                    "small_calls": ("the calls with fewer tokens than SMs run as program launches (bf16 and FP8 "
                                    "together while their rows fit one per SM, NVFP4 apart; --no-programs: one "
                                    "launch per call)"
-                                   if any(isinstance(d, ProgramGroup) for d in dcalls) else "one launch per call"),
+                                   if any(isinstance(d, (ProgramGroup, ProgramBatchGroup)) for d in dcalls)
+                                   else "one launch per call"),
                    "batches": ("the calls of at least one row per SM other than the largest run as one batch "
                                "of overlapping single-call launches (mbd_run_independent; --no-batches: one launch "
-                               "unit per call)"
-                               if any(isinstance(d, BatchGroup) for d in dcalls) else "none"),
+                               "unit per call)" + ("; the program launch of the small calls opens that batch "
+                                                   "(mbd_run_independent_with_program)"
+                                                   if any(isinstance(d, ProgramBatchGroup) for d in dcalls) else "")
+                               if any(isinstance(d, (BatchGroup, ProgramBatchGroup)) for d in dcalls) else "none"),
                    "roofline_events": "CUDA events around the roofline kernel's launch in every timed step (they "
                                       "break its overlap with the launches beside it)",
                    "kernels_breakdown": "each launch unit alone between CUDA events after a read of twice the L2 "

@@ -84,7 +84,7 @@ typedef enum {
 #define MBD_MAX_REDUCED_WIDTH 262144
 
 /* ABI version of this header (bumped on any signature change or added entry point). */
-#define MBD_ABI_VERSION 8
+#define MBD_ABI_VERSION 9
 int mbd_abi_version(void);
 
 /* Static, human-readable name of a status code (never NULL). */
@@ -309,6 +309,7 @@ mbd_status mbd_run_program(const mbd_op* ops, int n_ops, mbd_stream_t stream);
 #define MBD_MAX_INDEPENDENT_OPS 64
 mbd_status mbd_run_independent(const mbd_op* ops, int n_ops, mbd_stream_t stream);
 
+
 /*
  * The same in two steps, for a program that runs many times (every decode step): build validates and
  * schedules once on the host; launch enqueues the kernel with no further host work beyond the launch
@@ -350,6 +351,22 @@ size_t mbd_program_schedule_bytes(void);
 mbd_status mbd_program_plan_upload(const mbd_program_plan* plan, void* schedule, size_t schedule_bytes,
                                    mbd_stream_t stream);
 mbd_status mbd_program_plan_launch_uploaded(const mbd_program_plan* plan, const void* schedule, mbd_stream_t stream);
+
+/*
+ * A batch of independent ops (mbd_run_independent) with a program in front of it: the program (`plan` with its schedule uploaded to `schedule`,
+ * as for mbd_program_plan_launch_uploaded) launches first and lets the ops' launches start once the work
+ * before the call is complete, so small, latency-bound rows (the program) run beside large, bandwidth-bound
+ * ones (the ops). No op may read or write memory that the program writes, nor the reverse (checked for every
+ * pair of a program op and a batch op, so the host checks grow with their product); within the program the
+ * program's own rules apply. Stream order holds for the whole: the program waits for the work enqueued
+ * before the call, and work enqueued after it starts once the program and every op have completed. Results
+ * are bit-identical to launching the program, then calling the ops, one after another.
+ * Errors: those of mbd_program_plan_launch_uploaded (a null, unfilled or other-device plan, a null or
+ * misaligned schedule) and of mbd_run_independent; MBD_ERR_INVALID_ARG also when an op and the program are not
+ * independent. A plan with nothing to do launches only the ops, as mbd_run_independent does.
+ */
+mbd_status mbd_run_independent_with_program(const mbd_program_plan* plan, const void* schedule, const mbd_op* ops,
+                                            int n_ops, mbd_stream_t stream);
 
 /*
  * mbd_program_plan_upload + mbd_program_plan_launch_uploaded without caller memory. No counterpart on the

@@ -90,6 +90,7 @@ def _load() -> ctypes.CDLL:
     lib.mbd_swiglu_quant_nvfp4.argtypes = [vp, vp, vp, i64, i64, vp, vp]
     lib.mbd_run_program.argtypes = [ctypes.POINTER(Op), cint, vp]
     lib.mbd_run_independent.argtypes = [ctypes.POINTER(Op), cint, vp]
+    lib.mbd_run_independent_with_program.argtypes = [vp, vp, ctypes.POINTER(Op), cint, vp]
     lib.mbd_program_plan_build.argtypes = [ctypes.POINTER(Op), cint, vp]
     lib.mbd_program_plan_launch.argtypes = [vp, vp]
     lib.mbd_program_schedule_bytes.restype = ctypes.c_size_t
@@ -106,7 +107,7 @@ def _load() -> ctypes.CDLL:
     for fn in ("mbd_fused_add_rmsnorm", "mbd_fused_add_rmsnorm_quant_fp8", "mbd_swiglu", "mbd_swiglu_quant_fp8",
                "mbd_fused_allreduce_add_rmsnorm", "mbd_fused_allreduce_add_rmsnorm_quant_fp8",
                "mbd_fused_add_rmsnorm_quant_nvfp4", "mbd_swiglu_quant_nvfp4", "mbd_run_program",
-               "mbd_run_independent", "mbd_program_plan_build", "mbd_program_plan_launch", "mbd_program_plan_upload",
+               "mbd_run_independent", "mbd_run_independent_with_program", "mbd_program_plan_build", "mbd_program_plan_launch", "mbd_program_plan_upload",
                "mbd_program_plan_launch_uploaded", "mbd_program_plan_launch_static"):
         getattr(lib, fn).restype = cint
     return lib
@@ -308,6 +309,14 @@ def run_independent(ops, stream=None) -> None:
     launches, each overlapping the one before it (mbd_run_independent)."""
     arr, n = ops if isinstance(ops, tuple) else program_array(ops)
     _check(get_lib().mbd_run_independent(arr if n else None, n, _stream(stream)), "run_independent")
+
+
+def run_independent_with_program(plan, schedule, ops, stream=None) -> None:
+    """A program (a built plan whose schedule was uploaded to `schedule`) launched first, then the independent ops
+    of a batch, every launch after the program overlapping the one before (mbd_run_independent_with_program)."""
+    arr, n = ops if isinstance(ops, tuple) else program_array(ops)
+    _check(get_lib().mbd_run_independent_with_program(ctypes.addressof(plan.buf), _ptr(schedule), arr if n else None,
+                                                      n, _stream(stream)), "run_independent_with_program")
 
 
 class ProgramPlan:

@@ -756,10 +756,47 @@ mbd_status launch_static(const PlanImpl* plan, cudaStream_t stream) {
 
 // ------------------------------------------------------------------------------------------ batches
 
-// mbd_run_independent: ops that share no written memory, each launched as its single call, the first in
-// PdlOrder kPdlHead and the rest kPdlOverlap. Every op is checked, and then planned, before the first launch.
-mbd_status run_independent(const mbd_op* ops, int n_ops, cudaStream_t stream) {
+// The byte ranges one op of a program touches (for the independence check of a batch it opens).
+OpInfo prog_op_regions(const mbd::ProgOp& op) {
+    OpInfo in;
+    in.nreg = 0;
+    in.holds_row = false;
+    if (op.rows <= 0) return in;
+    const size_t T = static_cast<size_t>(op.rows), V = static_cast<size_t>(op.nvec);
+    if (op.cls == mbd::kOpNorm) {
+        add_region(in, op.in, T * V * 16, false, 0, 0);
+        add_region(in, op.residual, T * V * 16, true, 0, 0);
+        add_region(in, op.weight, V * 16, false, 0, 0);
+    } else {
+        add_region(in, op.in, T * V * 32, false, 0, 0);
+    }
+    const size_t out_row = op.ep == mbd::kBf16 ? V * 16 : (op.ep == mbd::kNvfp4 ? V * 4 : V * 8);
+    add_region(in, op.out, T * out_row, true, 0, 0);
+    if (op.ep == mbd::kNvfp4) add_region(in, op.out_sf, T * (V / 2), true, 0, 0);
+    if (op.ep == mbd::kFp8Dynamic) add_region(in, op.scale, T * 4, true, 0, 0);
+    else if (op.ep != mbd::kBf16) add_region(in, op.scale, 4, false, 0, 0);
+    return in;
+}
+
+bool conflict(const OpInfo& x, const OpInfo& y) {   // one writes what the other reads or writes
+    for (int u = 0; u < x.nreg; ++u)
+        for (int v = 0; v < y.nreg; ++v)
+            if ((x.reg[u].write || y.reg[v].write) && overlap(x.reg[u].ptr, x.reg[u].bytes, y.reg[v].ptr, y.reg[v].bytes))
+                return true;
+    return false;
+}
+
+// mbd_run_independent[_with_program]: ops that share no written memory, each launched as its single call, and
+// optionally a program (uploaded schedule) in front of them. The first launch takes PdlOrder kPdlHead (the
+// program: its early trigger), the rest kPdlOverlap. Every op is checked, and then planned, before the first
+// launch.
+mbd_status run_independent(const PlanImpl* plan, const void* schedule, const mbd_op* ops, int n_ops,
+                           cudaStream_t stream) {
     if (n_ops < 0 || n_ops > MBD_MAX_INDEPENDENT_OPS || (n_ops > 0 && !ops)) return MBD_ERR_INVALID_ARG;
+    if (plan) {
+        if (plan->magic != kPlanMagic || !schedule) return MBD_ERR_INVALID_ARG;
+        if (!aligned(schedule, 256)) return MBD_ERR_MISALIGNED;
+    }
     struct Prepared {
         bool norm;
         mbd::Epilogue ep;
@@ -802,25 +839,44 @@ mbd_status run_independent(const mbd_op* ops, int n_ops, cudaStream_t stream) {
         else if (q.ep != mbd::kBf16) add_region(q.info, o.scale, 4, false, 0, 0);
         active[n_active++] = i;
     }
-    // independence: what one op writes, no other op may read or write
+    // independence: what one op writes, no other op may read or write (the program's ops among themselves are
+    // the program's business)
     for (int a = 0; a < n_active; ++a)
-        for (int b = a + 1; b < n_active; ++b) {
-            const OpInfo& x = prep[active[a]].info;
-            const OpInfo& y = prep[active[b]].info;
-            for (int u = 0; u < x.nreg; ++u)
-                for (int v = 0; v < y.nreg; ++v)
-                    if ((x.reg[u].write || y.reg[v].write) &&
-                        overlap(x.reg[u].ptr, x.reg[u].bytes, y.reg[v].ptr, y.reg[v].bytes))
-                        return MBD_ERR_INVALID_ARG;
+        for (int b = a + 1; b < n_active; ++b)
+            if (conflict(prep[active[a]].info, prep[active[b]].info)) return MBD_ERR_INVALID_ARG;
+    const bool with_program = plan && plan->grid > 0;
+    if (with_program) {
+        for (int k = 0; k < plan->P.n_ops; ++k) {
+            const OpInfo pi = prog_op_regions(plan->P.ops[k]);
+            if (pi.nreg == 0) continue;
+            for (int a = 0; a < n_active; ++a)
+                if (conflict(pi, prep[active[a]].info)) return MBD_ERR_INVALID_ARG;
         }
-    if (n_active == 0) return MBD_OK;
+        int device = 0;
+        const cudaError_t de = cudaGetDevice(&device);
+        if (de != cudaSuccess) {
+            g_last_cuda_error = static_cast<int>(de);
+            (void)cudaGetLastError();
+            return MBD_ERR_CUDA;
+        }
+        if (device != plan->device) return MBD_ERR_INVALID_ARG;
+    }
+    if (n_active == 0 && !with_program) return MBD_OK;
     const int sms = sm_count_of_current_device();
     mbd::RowPlan plans[MBD_MAX_INDEPENDENT_OPS];
     for (int a = 0; a < n_active; ++a) {
         const Prepared& q = prep[active[a]];
         if (!(q.norm ? norm_plan(q.np, q.ep, sms, &plans[a]) : swiglu_plan(q.sp, q.ep, sms, &plans[a])))
             return MBD_ERR_UNSUPPORTED;
-        plans[a].order = a == 0 ? mbd::kPdlHead : mbd::kPdlOverlap;
+        plans[a].order = (a == 0 && !with_program) ? mbd::kPdlHead : mbd::kPdlOverlap;
+    }
+    // The program first (measured on the 405B step's twelve small calls beside five large ones: 169.4 us per
+    // step with the program first, 170.1 with it last, where its CTAs wait for SMs the ops' last wave frees)
+    if (with_program) {
+        const mbd_status st = finish_launch(mbd::launch_program(plan->P, static_cast<const mbd::ProgramParams*>(schedule),
+                                                                plan->vpt, plan->variant, plan->grid, stream,
+                                                                mbd::kPdlHead));
+        if (st != MBD_OK) return st;
     }
     for (int a = 0; a < n_active; ++a) {
         const Prepared& q = prep[active[a]];
@@ -1005,7 +1061,14 @@ mbd_status mbd_program_plan_launch_uploaded(const mbd_program_plan* plan, const 
 }
 
 mbd_status mbd_run_independent(const mbd_op* ops, int n_ops, mbd_stream_t stream) {
-    return run_independent(ops, n_ops, reinterpret_cast<cudaStream_t>(stream));
+    return run_independent(nullptr, nullptr, ops, n_ops, reinterpret_cast<cudaStream_t>(stream));
+}
+
+mbd_status mbd_run_independent_with_program(const mbd_program_plan* plan, const void* schedule, const mbd_op* ops,
+                                            int n_ops, mbd_stream_t stream) {
+    if (!plan) return MBD_ERR_INVALID_ARG;
+    return run_independent(reinterpret_cast<const PlanImpl*>(plan), schedule, ops, n_ops,
+                           reinterpret_cast<cudaStream_t>(stream));
 }
 
 mbd_status mbd_run_program(const mbd_op* ops, int n_ops, mbd_stream_t stream) {

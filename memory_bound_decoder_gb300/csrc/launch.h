@@ -136,9 +136,11 @@ unsigned long long current_context_id();
 
 // Program kernel `variant` for `vpt` vectors per thread (1, 2 or 4) on `grid` CTAs of kProgramThreads, or
 // in the wide form (vpt 8, where program_variant_has_vpt8) on `grid` CTAs of kProgramWideThreads; the
-// schedule `p` by value, or, when `dev` is not null, read from that copy of it in device memory.
+// schedule `p` by value, or, when `dev` is not null, read from that copy of it in device memory. `order`
+// (PdlOrder; other than kPdlWaitFirst with an uploaded schedule only): its place in a batch of independent
+// launches; on its own a program waits first and lets the next kernel start at its end.
 cudaError_t launch_program(const ProgramParams& p, const ProgramParams* dev, int vpt, int variant, int grid,
-                           cudaStream_t s);
+                           cudaStream_t s, int order = 0);
 // Resident program CTAs per SM (occupancy query; 0 on error).
 int program_ctas_per_sm(int vpt, int variant);
 cudaError_t device_error_flags_program(unsigned int* flags, bool clear);

@@ -356,8 +356,13 @@ __global__ void __launch_bounds__(threads_of(V), min_ctas(V, NM, SM)) program_ke
 // used part of it into shared memory with coalesced loads (one L2 round trip), so that the item lookups and
 // descriptors cost shared-memory latency rather than an L2 round trip each. The upload precedes the launch
 // in stream order and is not a kernel, so the copy may run before the grid dependency wait.
+// `order` (PdlOrder): kPdlWaitFirst for a program on its own (wait, run, then let the next kernel start: a
+// dependent program waiting in SM slots would hold resources this one still uses); in a batch of independent
+// launches (mbd_run_independent_with_program), kPdlHead (wait, let the next launch start, run) or kPdlOverlap
+// (let the next launch start, run without waiting, wait for the previous launch before exiting).
 template <int V, int NM, int SM>
-__global__ void __launch_bounds__(threads_of(V), min_ctas(V, NM, SM)) program_kernel_dev(const ProgramParams* __restrict__ P) {
+__global__ void __launch_bounds__(threads_of(V), min_ctas(V, NM, SM)) program_kernel_dev(const ProgramParams* __restrict__ P,
+                                                                                        int order) {
     __shared__ __align__(16) ProgramParams S;
     {
         const size_t bytes = offsetof(ProgramParams, ops) + static_cast<size_t>(P->n_ops) * sizeof(ProgOp);
@@ -367,9 +372,11 @@ __global__ void __launch_bounds__(threads_of(V), min_ctas(V, NM, SM)) program_ke
         for (int i = threadIdx.x; i < words; i += blockDim.x) dst[i] = src[i];
     }
     __syncthreads();
-    pdl_wait();
+    if (order != kPdlOverlap) pdl_wait();
+    if (order != kPdlWaitFirst) pdl_trigger();
     program_body<V, NM, SM>(S);
-    pdl_trigger();   // late, as in program_kernel
+    if (order == kPdlOverlap) pdl_wait();
+    pdl_trigger();   // late, as in program_kernel (a no-op after an early one)
 }
 
 template <int V, int NM, int SM>
@@ -383,7 +390,7 @@ int ctas_per_sm() {
 }
 
 template <int V, int NM, int SM>
-cudaError_t launch_variant(const ProgramParams& p, const ProgramParams* dev, int grid, cudaStream_t s) {
+cudaError_t launch_variant(const ProgramParams& p, const ProgramParams* dev, int grid, cudaStream_t s, int order) {
     cudaLaunchConfig_t cfg = cudaLaunchConfig_t{};
     cudaLaunchAttribute attr[1];
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
@@ -394,7 +401,7 @@ cudaError_t launch_variant(const ProgramParams& p, const ProgramParams* dev, int
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (dev) return cudaLaunchKernelEx(&cfg, program_kernel_dev<V, NM, SM>, dev);
+    if (dev) return cudaLaunchKernelEx(&cfg, program_kernel_dev<V, NM, SM>, dev, order);
     return cudaLaunchKernelEx(&cfg, program_kernel<V, NM, SM>, p);
 }
 
@@ -412,8 +419,8 @@ template <int V, int K>
 int ctas_of() { return ctas_per_sm<V, kVariantMasks[K][0], kVariantMasks[K][1]>(); }
 
 template <int V, int K>
-cudaError_t launch_of(const ProgramParams& p, const ProgramParams* dev, int grid, cudaStream_t s) {
-    return launch_variant<V, kVariantMasks[K][0], kVariantMasks[K][1]>(p, dev, grid, s);
+cudaError_t launch_of(const ProgramParams& p, const ProgramParams* dev, int grid, cudaStream_t s, int head) {
+    return launch_variant<V, kVariantMasks[K][0], kVariantMasks[K][1]>(p, dev, grid, s, head);
 }
 
 template <int V>
@@ -428,12 +435,12 @@ int ctas_v(int variant) {
 }
 
 template <int V>
-cudaError_t launch_v(const ProgramParams& p, const ProgramParams* dev, int variant, int grid, cudaStream_t s) {
+cudaError_t launch_v(const ProgramParams& p, const ProgramParams* dev, int variant, int grid, cudaStream_t s, int head) {
     switch (variant) {
-        case 0: return launch_of<V, 0>(p, dev, grid, s);
-        case 1: return launch_of<V, 1>(p, dev, grid, s);
-        case 2: return launch_of<V, 2>(p, dev, grid, s);
-        case 3: return launch_of<V, 3>(p, dev, grid, s);
+        case 0: return launch_of<V, 0>(p, dev, grid, s, head);
+        case 1: return launch_of<V, 1>(p, dev, grid, s, head);
+        case 2: return launch_of<V, 2>(p, dev, grid, s, head);
+        case 3: return launch_of<V, 3>(p, dev, grid, s, head);
     }
     return cudaErrorInvalidValue;
 }
@@ -449,10 +456,10 @@ int ctas_v8(int variant) {
     return 0;
 }
 
-cudaError_t launch_v8(const ProgramParams& p, const ProgramParams* dev, int variant, int grid, cudaStream_t s) {
+cudaError_t launch_v8(const ProgramParams& p, const ProgramParams* dev, int variant, int grid, cudaStream_t s, int head) {
     switch (variant) {
-        case 1: return launch_of<8, 1>(p, dev, grid, s);
-        case 3: return launch_of<8, 3>(p, dev, grid, s);
+        case 1: return launch_of<8, 1>(p, dev, grid, s, head);
+        case 3: return launch_of<8, 3>(p, dev, grid, s, head);
     }
     return cudaErrorInvalidValue;
 }
@@ -484,12 +491,14 @@ int program_ctas_per_sm(int vpt, int variant) {
 }
 
 cudaError_t launch_program(const ProgramParams& p, const ProgramParams* dev, int vpt, int variant, int grid,
-                           cudaStream_t s) {
+                           cudaStream_t s, int order) {
+    if (order != kPdlWaitFirst && !dev) return cudaErrorInvalidValue;   // only the uploaded form joins a batch
+    const int h = order;
     switch (vpt) {
-        case 1: return launch_v<1>(p, dev, variant, grid, s);
-        case 2: return launch_v<2>(p, dev, variant, grid, s);
-        case 4: return launch_v<4>(p, dev, variant, grid, s);
-        case 8: return launch_v8(p, dev, variant, grid, s);
+        case 1: return launch_v<1>(p, dev, variant, grid, s, h);
+        case 2: return launch_v<2>(p, dev, variant, grid, s, h);
+        case 4: return launch_v<4>(p, dev, variant, grid, s, h);
+        case 8: return launch_v8(p, dev, variant, grid, s, h);
     }
     return cudaErrorInvalidValue;
 }

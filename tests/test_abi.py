@@ -34,9 +34,9 @@ def test_binding_names_match_header():
 
 
 def test_version_and_status_strings(lib):
-    assert lib.mbd_abi_version() == 8
+    assert lib.mbd_abi_version() == 9
     hdr = open(mbd.HEADER_PATH).read()
-    assert int(re.search(r"#define MBD_ABI_VERSION (\d+)", hdr).group(1)) == 8
+    assert int(re.search(r"#define MBD_ABI_VERSION (\d+)", hdr).group(1)) == 9
     for code in range(5):
         assert lib.mbd_status_string(code).decode().startswith("MBD_")
     assert lib.mbd_status_string(99) == b"unknown mbd_status"
@@ -349,4 +349,25 @@ def test_independent_batch_checks(lib):
     # ops with no tokens are skipped, and touch nothing: an empty batch launches nothing
     mbd.run_independent([])
     mbd.run_independent([mbd.op_swiglu(None, None, 0, H), mbd.op_add_rmsnorm(None, None, None, None, 0, H, 1e-6)])
+    assert mbd.kernel_launches() == n0
+
+
+def test_batch_with_program_checks(lib):
+    """mbd_run_independent_with_program rejects a null or unfilled plan and a misaligned schedule before any
+    launch; a plan with nothing to do leaves the ops' own checks."""
+    H = 64
+    buf = (ctypes.c_uint64 * (mbd.PROGRAM_PLAN_BYTES // 8))()
+    a = mbd.op_add_rmsnorm(A, 2 * A, 3 * A, 9 * A, 4, H, 1e-6)
+    arr, n = mbd.program_array([a])
+    n0 = mbd.kernel_launches()
+    assert lib.mbd_run_independent_with_program(None, A, arr, n, None) == mbd.ERR_INVALID_ARG
+    assert lib.mbd_run_independent_with_program(ctypes.addressof(buf), A, arr, n, None) == mbd.ERR_INVALID_ARG
+    empty = mbd.program_plan_build([])
+    pp = ctypes.addressof(empty.buf)
+    assert lib.mbd_run_independent_with_program(pp, None, arr, n, None) == mbd.ERR_INVALID_ARG
+    assert lib.mbd_run_independent_with_program(pp, A + 16, arr, n, None) == mbd.ERR_MISALIGNED
+    b = mbd.op_add_rmsnorm(4 * A, 2 * A, 5 * A, 9 * A, 4, H, 1e-6)   # shares the residual with a
+    arr2, n2 = mbd.program_array([a, b])
+    assert lib.mbd_run_independent_with_program(pp, A, arr2, n2, None) == mbd.ERR_INVALID_ARG
+    assert lib.mbd_run_independent_with_program(pp, A, None, 0, None) == 0     # nothing to do at all
     assert mbd.kernel_launches() == n0

@@ -37,7 +37,8 @@ def _run(work, grouped):
     for u in units:
         u.launch()
     torch.cuda.synchronize()
-    launches = sum(len(u.members) if isinstance(u, bench.BatchGroup) else 1 for u in units)
+    launches = sum(len(u.members) if isinstance(u, bench.BatchGroup) else
+                   (1 + len(u.batch.members) if isinstance(u, bench.ProgramBatchGroup) else 1) for u in units)
     assert mbd.kernel_launches() - n0 == launches
     assert mbd.device_error_flags() == 0
     outs = [(d.call, {k: getattr(d, k).cpu().numpy().copy() for k in ("out", "res", "scale") if hasattr(d, k)})
@@ -65,6 +66,37 @@ def test_grouped_small_calls_match_per_call_launches():
             assert diff.mean() <= 1e-3, f"{call.name}: {diff.sum()} codes differ"
             assert ((x[diff] & 0x80) == (y[diff] & 0x80)).all(), f"{call.name}: sign flipped"
             assert (np.abs((x[diff] & 0x7F) - (y[diff] & 0x7F)) == 1).all(), f"{call.name}: more than one step"
+
+
+def _compare(ref, got):
+    """Large calls (the same single-call kernels) bit for bit; program rows within the program's rounding."""
+    for (call, a), (_, b) in zip(ref, got):
+        if call.T >= 152 or "res" in a:
+            if call.T >= 152:
+                for k in a:
+                    np.testing.assert_array_equal(a[k], b[k], f"{call.name}: {k}")
+                continue
+            np.testing.assert_array_equal(a["res"], b["res"], f"{call.name}: residual")
+        if call.mode == "dynamic":
+            np.testing.assert_array_equal(a["scale"], b["scale"], f"{call.name}: dynamic scales")
+        if call.kind in ("add_rmsnorm", "swiglu"):
+            d = np.abs(a["out"].astype(np.int32) - b["out"].astype(np.int32))
+            assert d.max() <= 1, f"{call.name}: bf16 outputs differ by more than one ulp"
+        else:
+            x, y = a["out"].astype(np.int32), b["out"].astype(np.int32)
+            diff = x != y
+            assert diff.sum() <= diff.size // 1000, f"{call.name}: {diff.sum()} codes differ"
+            assert (np.abs((x[diff] & 0x7F) - (y[diff] & 0x7F)) == 1).all(), f"{call.name}: more than one step"
+
+
+def test_default_step_units_match_per_call_launches():
+    """The whole default step: the largest call alone, the program of the small calls opening the batch of the
+    others (one mbd_run_independent_with_program call), against every call launched on its own."""
+    w = bench.workloads_by_key()[bench.DEFAULT_WORKLOAD]
+    n_calls, ref = _run(w, grouped=False)
+    n_units, got = _run(w, grouped=True)
+    assert n_calls == 18 and n_units == 2
+    _compare(ref, got)
 
 
 def test_batched_1000_token_calls_match_per_call_launches():

@@ -224,3 +224,105 @@ def test_stream_order_around_the_batch(reader_first):
         got = sequence(True)
         for a, b in zip(want, got):
             np.testing.assert_array_equal(a, b)
+
+
+def _program_cases():
+    """Small calls for the program (1, 3 and 17 tokens; bf16, static-FP8 and dynamic-FP8 ops) and large ones for
+    the batch after it."""
+    small = [OpCase("add_rmsnorm", 1, 5120, 51), OpCase("add_rmsnorm_quant_fp8", 3, 5120, 52, "static"),
+             OpCase("swiglu", 17, 13824, 53), OpCase("swiglu_quant_fp8", 17, 13824, 54, "dynamic"),
+             OpCase("swiglu_quant_fp8", 1, 13824, 55, "dynamic"), OpCase("add_rmsnorm", 17, 5120, 56)]
+    large = [OpCase("add_rmsnorm_quant_fp8", 2048, 16384, 57, "static"), OpCase("swiglu", 1000, 13824, 58),
+             OpCase("swiglu_quant_fp8", 1000, 13824, 59, "dynamic")]
+    return small, large
+
+
+def test_batch_with_program_matches_the_sequence():
+    """The program in front of the batch, against the program launched alone and then the ops' single calls."""
+    mbd = _mbd()
+    small, large = _program_cases()
+    results = []
+    for mode in ("sequence", "batch"):
+        for c in small + large:
+            c.alloc()
+        plan = mbd.program_plan_build([c.op() for c in small])
+        sched = torch.empty(mbd.program_schedule_bytes(), dtype=torch.uint8, device="cuda")
+        plan.upload(sched)
+        mbd.device_error_flags(clear=True)
+        n0 = mbd.kernel_launches()
+        if mode == "sequence":
+            plan.launch_uploaded(sched)
+            for c in large:
+                c.call()
+        else:
+            mbd.run_independent_with_program(plan, sched, [c.op() for c in large])
+        torch.cuda.synchronize()
+        assert mbd.kernel_launches() - n0 == 1 + len(large)
+        assert mbd.device_error_flags() == 0
+        results.append([c.snapshot() for c in small + large])
+    assert_same(*results)
+
+
+def test_batch_with_program_rejects_shared_memory():
+    """An op that writes what the program reads (or reads what it writes) is refused before any launch."""
+    mbd = _mbd()
+    small, large = _program_cases()
+    for c in small + large:
+        c.alloc()
+    plan = mbd.program_plan_build([c.op() for c in small])
+    sched = torch.empty(mbd.program_schedule_bytes(), dtype=torch.uint8, device="cuda")
+    plan.upload(sched)
+    T, H = small[0].T, small[0].W
+    clash = OpCase("add_rmsnorm", T, H, 60).alloc()
+    clash.d["residual"] = small[0].d["residual"]        # the program's norm updates this residual
+    n0 = mbd.kernel_launches()
+    with pytest.raises(mbd.MbdError) as e:
+        mbd.run_independent_with_program(plan, sched, [large[0].op(), clash.op()])
+    assert e.value.status == mbd.ERR_INVALID_ARG
+    assert mbd.kernel_launches() == n0
+
+
+@pytest.mark.parametrize("reader_in_program", [False, True])
+def test_stream_order_around_a_batch_with_program(reader_in_program):
+    """A SwiGLU writes t; t feeds a norm in the program or in the batch beside a long op; a norm after the batch
+    reads that norm's output. Five runs, each equal to the one-launch-at-a-time sequence."""
+    mbd = _mbd()
+    W, eps = 8192, 1e-5
+    Tn = 17 if reader_in_program else 1000
+    gu = wl.make_swiglu_inputs(Tn, W, 61, wl.N01).gate_up
+    long_op = OpCase("swiglu_quant_fp8", 2048, 53248, 62, "dynamic")
+    other_small = OpCase("swiglu", 3, 13824, 63)
+    r1 = wl.make_norm_inputs(Tn, W, 64, wl.N01, eps)
+    r2 = wl.make_norm_inputs(Tn, W, 65, wl.N01, eps)
+
+    def sequence(batched):
+        G = dev_u16(torch, gu)
+        t = Guarded(torch, Tn * W, torch.int16)
+        R1, W1, R2, W2 = (dev_u16(torch, a) for a in (r1.residual, r1.weight, r2.residual, r2.weight))
+        o1, o2 = Guarded(torch, Tn * W, torch.int16), Guarded(torch, Tn * W, torch.int16)
+        long_op.alloc()
+        other_small.alloc()
+        n1 = mbd.op_add_rmsnorm(o1.view, R1.view, t.view, W1.view, Tn, W, eps)   # reads t
+        prog_ops = [other_small.op()] + ([n1] if reader_in_program else [])
+        batch_ops = [long_op.op()] + ([] if reader_in_program else [n1])
+        plan = mbd.program_plan_build(prog_ops)
+        sched = torch.empty(mbd.program_schedule_bytes(), dtype=torch.uint8, device="cuda")
+        plan.upload(sched)
+        mbd.swiglu(t.view, G.view, Tn, W)                                             # writes t
+        if batched:
+            mbd.run_independent_with_program(plan, sched, batch_ops)
+        else:
+            plan.launch_uploaded(sched)
+            mbd.run_independent(batch_ops[:1])
+            for op in batch_ops[1:]:
+                mbd.run_independent([op])
+        mbd.fused_add_rmsnorm(o2.view, R2.view, o1.view, W2.view, Tn, W, eps)         # reads o1
+        torch.cuda.synchronize()
+        return ([g.raw.cpu().numpy().copy() for g in (t, R1, o1, R2, o2)] + list(long_op.snapshot().values())
+                + list(other_small.snapshot().values()))
+
+    want = sequence(False)
+    for _ in range(5):
+        got = sequence(True)
+        for a, b in zip(want, got):
+            np.testing.assert_array_equal(a, b)
