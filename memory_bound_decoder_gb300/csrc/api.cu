@@ -130,7 +130,7 @@ bool plan_rows(int64_t rows, int nvec, Shape shape, int sms, bool pairs, mbd::Ro
             c = cdiv(nvec, 2048);
             if (pairs || nvec >= 512) min_vpt = 4;
         }
-    } else if (shape == Shape::kNormPartials) {   // one vector per thread (all partials' loads in flight)
+    } else if (shape == Shape::kNormPartials) {   // one vector per thread (the partials' slices in shared memory)
         c = cdiv(nvec, 256);   // slices of ~256 vectors (8 x 256 threads at H 16384): at H 5120 and 8192 they
                                // beat ~128 by 8 to 26%, at H 16384 rows over 4 x 512 lose 3%
     } else if (shape == Shape::kRowMax) {

@@ -347,7 +347,8 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // The single-call kernels order themselves against the previous kernel by RowPlan::order (PdlOrder, launch.h):
-// pdl_enter before the first global access (anything before it may only warm L2), pdl_leave after the last.
+// pdl_enter_trigger first, pdl_enter_wait before the first global load or store (what comes between may only
+// warm L2), pdl_leave after the last store.
 //   kPdlWaitFirst: trigger, wait                 (every single call)
 //   kPdlHead:      wait, trigger                 (first launch of a batch of independent ops: no later launch
 //                                                 of the batch starts before the work ahead of it is done)
