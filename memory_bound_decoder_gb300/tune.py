@@ -173,6 +173,23 @@ def measured_hbm_gbs() -> float:
         return FALLBACK_HBM_GBS
 
 
+def rank(rules_shape, rules_us, timed, gbps, bound, full_rotation):
+    """The best shape of one point: the rules' shape unless a candidate is faster. `timed`: (shape, us) of the
+    candidates that fit the call; `gbps(us)` the algorithmic rate of a timing. A timing above `bound` counts as
+    L2-served, and is kept out of the ranking, where the rotation is short (below ROTATE_L2 x L2); with the full
+    rotation it is kept. Returns (best shape, best us, shapes timed above the bound)."""
+    best_shape, best_us = rules_shape, rules_us
+    above = [list(rules_shape)] if gbps(rules_us) > bound else []
+    for shape, us in timed:
+        if gbps(us) > bound:
+            above.append(list(shape))
+            if not full_rotation:
+                continue
+        if us < best_us:
+            best_shape, best_us = shape, us
+    return best_shape, best_us, above
+
+
 def tune(shapes, tokens, hbm_gbs, log=print):
     import torch
     l2 = int(getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 0)) or 126 * 2 ** 20
@@ -191,23 +208,15 @@ def tune(shapes, tokens, hbm_gbs, log=print):
             base = time_call(torch, call, 5)
             reps = max(5, min(MAX_SETS, int(2000 / max(base, 0.5))))   # about 2 ms of launches per timing
             rules_us = time_call(torch, call, reps)
-            # the rules' shape stands unless a candidate is measurably faster from HBM (if the rules' own timing
-            # is L2-served, no candidate measured below the bound can beat it)
-            best_us, best = rules_us, rules_shape
-            above = [] if gbps(rules_us) <= bound else [list(rules_shape)]   # timings above the copy-rate bound
+            timed = []
             for cand in candidates(kind, mode, width):
                 mbd.tuning_set([entry(kind, mode, T, T, width, cand)])
                 got = mbd.launch_shape(kind, mode, T, width)
                 if got[1:] != cand[1:]:
                     continue   # the shape does not fit this call: the rules would run instead
-                us = time_call(torch, call, reps)
-                if gbps(us) > bound:
-                    above.append(list(got))
-                    if not full_rotation:
-                        continue              # L2-served: not a valid measurement of this shape
-                if us < best_us:
-                    best_us, best = us, got
+                timed.append((got, time_call(torch, call, reps)))
             mbd.tuning_set([])
+            best, best_us, above = rank(rules_shape, rules_us, timed, gbps, bound, full_rotation)
             rotation_mb = call.nsets * call.bytes / 2 ** 20
             rows.append((T, best, best_us, rules_shape, rules_us, rotation_mb, above, full_rotation))
             log(f"[tune] {kind} {mode or ''} W={width} T={T}: rules {rules_shape} {rules_us:.2f} us "

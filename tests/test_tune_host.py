@@ -37,3 +37,20 @@ def test_rotation_covers_three_l2_sizes_where_the_launch_count_allows():
         b = tune.algorithmic_bytes("swiglu", None, T, W)
         n = max(1, min(tune.MAX_SETS, -(-tune.ROTATE_L2 * l2 // b)))
         assert n * b >= tune.ROTATE_L2 * l2 or n == tune.MAX_SETS
+
+
+def test_ranking_keeps_l2_served_timings_out_only_under_a_short_rotation():
+    gbps = lambda us: 1000.0 / us          # a point of 1000 "bytes" per microsecond unit
+    bound = 1.05 * 100.0                   # 1.05 x a copy rate of 100
+    rules = (1, 2, 256)
+    # a faster candidate above the bound: excluded when the rotation is short, kept when it is full
+    timed = [((2, 2, 128), 9.0), ((4, 1, 128), 9.8)]          # 111 and 102 GB/s
+    best, us, above = tune.rank(rules, 10.5, timed, gbps, bound, full_rotation=False)
+    assert best == (4, 1, 128) and us == 9.8 and above == [[2, 2, 128]]
+    best, us, above = tune.rank(rules, 10.5, timed, gbps, bound, full_rotation=True)
+    assert best == (2, 2, 128) and us == 9.0 and above == [[2, 2, 128]]
+    # the rules stand unless a candidate is faster, even when their own timing is above the bound
+    best, us, above = tune.rank(rules, 9.0, [((4, 1, 128), 9.8)], gbps, bound, full_rotation=False)
+    assert best == rules and us == 9.0 and above == [[1, 2, 256]]
+    best, us, above = tune.rank(rules, 10.0, [], gbps, bound, full_rotation=False)
+    assert best == rules and us == 10.0 and above == []
