@@ -16,6 +16,8 @@
 // reduces the sum of squares and max |w * s| together (the scale is max |w * s| * inv / 448), then stores
 // the codes from registers.
 #include <atomic>
+#include <mutex>
+#include <vector>
 
 #include "norm_impl.cuh"
 
@@ -26,9 +28,12 @@ namespace {
 // The partial-sum form brings the CTA's slices of the partials into shared memory with bulk copies (one thread
 // issues them; dynamic shared memory, n_partials x slice vectors) and asks for three 512-thread CTAs' worth of
 // registers per SM: registers hold one partial vector at a time, not all of them.
+// ahead > 0: thread 0 also warms L2 with the CTA's input slices of row + ahead (bulk prefetches of the residual
+// and x, or of the residual and every partial), the row a later wave runs on this slot, so that its loads meet L2
+// while this wave sits in its reduction and epilogue.
 template <int VPT, int EP, bool ALLRED, int CL>
 __global__ void __launch_bounds__(512, ALLRED ? 3 : 1) add_rmsnorm_kernel(const __grid_constant__ NormParams p, int ctas_per_row, int slice,
-                                                                        int prefetch, int order) {
+                                                                        int prefetch, int ahead, int order) {
     extern __shared__ __align__(16) uint4 pslices[];   // all-reduce half: partial k's slice at [k * slice, ...)
     __shared__ NormSmem sm;
     __shared__ unsigned long long pbar;
@@ -47,6 +52,16 @@ __global__ void __launch_bounds__(512, ALLRED ? 3 : 1) add_rmsnorm_kernel(const 
     }
     if (prefetch) norm_prefetch<VPT, ALLRED>(p, row, begin, end);
     pdl_enter_wait(order);
+    if (ahead > 0 && row + ahead < p.rows && threadIdx.x == 0) {
+        const uint32_t bytes = static_cast<uint32_t>(end - begin) * 16u;
+        const int64_t at = (row + ahead) * static_cast<int64_t>(p.nvec) + begin;
+        prefetch_l2_bulk(static_cast<const uint4*>(p.residual) + at, bytes);
+        if constexpr (ALLRED) {
+            for (int k = 0; k < p.n_partials; ++k) prefetch_l2_bulk(static_cast<const uint4*>(p.partials[k]) + at, bytes);
+        } else {
+            prefetch_l2_bulk(static_cast<const uint4*>(p.x) + at, bytes);
+        }
+    }
     if constexpr (ALLRED) {
         if (threadIdx.x == 0) load_partials_bulk(p, row, begin, end - begin, slice, pslices, smem_addr(&pbar));
         norm_row_slice<VPT, EP, ALLRED, CL>(p, row, rank, ctas_per_row, begin, end, sm, pslices, slice, smem_addr(&pbar));
@@ -77,11 +92,66 @@ cudaError_t prefer_shared_carveout(const void* kern, int variant) {
     return cudaSuccess;
 }
 
+// Resident CTAs per SM of a kernel at a block size and dynamic shared-memory size (the occupancy calculator,
+// which also sees the kernel's carveout preference), cached per device, context, kernel and launch shape. 0 when
+// the calculator fails (no warming then; its error is cleared).
+struct ResidentKey {
+    int dev;
+    unsigned long long ctx;
+    const void* kern;
+    int threads;
+    size_t smem;
+};
+std::mutex g_resident_mu;
+std::vector<std::pair<ResidentKey, int>> g_resident;
+constexpr size_t kMaxResidentEntries = 256;
+
+int resident_ctas_per_sm(int dev, const void* kern, int threads, size_t smem) {
+    const unsigned long long ctx = current_context_id();
+    {
+        std::lock_guard<std::mutex> lock(g_resident_mu);
+        for (const auto& e : g_resident)
+            if (e.first.dev == dev && e.first.ctx == ctx && e.first.kern == kern && e.first.threads == threads &&
+                e.first.smem == smem)
+                return e.second;
+    }
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    if (ctx != 0) {
+        std::lock_guard<std::mutex> lock(g_resident_mu);
+        if (g_resident.size() >= kMaxResidentEntries) g_resident.clear();
+        g_resident.push_back({ResidentKey{dev, ctx, kern, threads, smem}, n});
+    }
+    return n;
+}
+
+// Wave-ahead distance of a launch of more rows than fit on the GPU at once (R = SMs x resident CTAs per SM /
+// CTAs per row): R / 2 rows for the plain norm, R / 8 for the all-reduce half, whose bulk copies of the partials
+// already keep many bytes in flight and whose rows are nine or more row-sized reads (a longer distance evicts
+// rows before they are used). Measured on GB300 over 0 to R (CUDA events around back-to-back launches, inputs
+// above 3x L2): the plain norm peaks between 3R/8 and 3R/4 (NVFP4 T 2048, H 16384: 36.65 -> 35.65 us; static
+// FP8 T 1000, H 16384: 20.10 -> 19.28; bf16 T 2048, H 4096: 12.32 -> 11.56), the all-reduce half at R / 8 (k 8,
+// T 2048, H 16384, static FP8: 124.0 -> 119.6 us) and falls below no warming past R / 2.
+int wave_ahead(const NormParams& p, const RowPlan& plan, const void* kern, size_t smem) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    const int64_t resident = int64_t{sms} * resident_ctas_per_sm(dev, kern, plan.threads, smem) / plan.ctas_per_row;
+    if (resident <= 0 || p.rows <= resident) return 0;
+    return static_cast<int>(p.n_partials > 0 ? resident / 8 : resident / 2);
+}
+
 template <int EP>
 cudaError_t launch_ep(const NormParams& p, const RowPlan& plan, cudaStream_t s) {
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
-    void (*kern)(NormParams, int, int, int, int) = nullptr;
+    void (*kern)(NormParams, int, int, int, int, int) = nullptr;
     const bool cl = plan.ctas_per_row > 1;
     if (p.n_partials > 0) {
         if (plan.vpt != 1) return cudaErrorInvalidValue;
@@ -107,7 +177,8 @@ cudaError_t launch_ep(const NormParams& p, const RowPlan& plan, cudaStream_t s) 
         }
         cfg.dynamicSmemBytes = smem;
     }
-    return cudaLaunchKernelEx(&cfg, kern, p, plan.ctas_per_row, plan.slice, plan.prefetch, plan.order);
+    const int ahead = wave_ahead(p, plan, reinterpret_cast<const void*>(kern), cfg.dynamicSmemBytes);
+    return cudaLaunchKernelEx(&cfg, kern, p, plan.ctas_per_row, plan.slice, plan.prefetch, ahead, plan.order);
 }
 
 }  // namespace
