@@ -28,10 +28,11 @@ namespace {
 // The partial-sum form brings the CTA's slices of the partials into shared memory with bulk copies (one thread
 // issues them; dynamic shared memory, n_partials x slice vectors) and asks for three 512-thread CTAs' worth of
 // registers per SM: registers hold one partial vector at a time, not all of them.
-// ahead > 0: thread 0 also warms L2 with the CTA's input slices of row + ahead (bulk prefetches of the residual
-// and x, or of the residual and every partial), the row a later wave runs on this slot, so that its loads meet L2
-// while this wave sits in its reduction and epilogue.
-template <int VPT, int EP, bool ALLRED, int CL>
+// AHEAD: thread 0 also warms L2 with the CTA's input slices of row + ahead (bulk prefetches of the residual and
+// x, or of the residual and every partial), the row a later wave runs on this slot, so that its loads meet L2
+// while this wave sits in its reduction and epilogue. A compile-time choice: the branch alone, never taken, cost
+// single-wave launches 0.1 to 0.4 us (static FP8, H 16384, T 16: 2.52 -> 2.90 us).
+template <int VPT, int EP, bool ALLRED, int CL, bool AHEAD>
 __global__ void __launch_bounds__(512, ALLRED ? 3 : 1) add_rmsnorm_kernel(const __grid_constant__ NormParams p, int ctas_per_row, int slice,
                                                                         int prefetch, int ahead, int order) {
     extern __shared__ __align__(16) uint4 pslices[];   // all-reduce half: partial k's slice at [k * slice, ...)
@@ -52,7 +53,7 @@ __global__ void __launch_bounds__(512, ALLRED ? 3 : 1) add_rmsnorm_kernel(const 
     }
     if (prefetch) norm_prefetch<VPT, ALLRED>(p, row, begin, end);
     pdl_enter_wait(order);
-    if (ahead > 0 && row + ahead < p.rows && threadIdx.x == 0) {
+    if (AHEAD && row + ahead < p.rows && threadIdx.x == 0) {
         const uint32_t bytes = static_cast<uint32_t>(end - begin) * 16u;
         const int64_t at = (row + ahead) * static_cast<int64_t>(p.nvec) + begin;
         prefetch_l2_bulk(static_cast<const uint4*>(p.residual) + at, bytes);
@@ -71,11 +72,11 @@ __global__ void __launch_bounds__(512, ALLRED ? 3 : 1) add_rmsnorm_kernel(const 
     pdl_leave(order);
 }
 
-// Per device and partial-sum kernel variant (epilogue x row in one CTA or a cluster): the id of the context in
-// which its preferred carveout, the largest shared-memory share, was last requested, so that shared memory
-// (n_partials x slice vectors per CTA) rather than the L1 share bounds the resident CTAs. A kernel attribute
+// Per device and partial-sum kernel variant (epilogue x row in one CTA or a cluster x warming): the id of the
+// context in which its preferred carveout, the largest shared-memory share, was last requested, so that shared
+// memory (n_partials x slice vectors per CTA) rather than the L1 share bounds the resident CTAs. A kernel attribute
 // belongs to a context; with no context id (0) every launch requests it.
-std::atomic<unsigned long long> g_partials_carveout_ctx[kMaxCachedDevices][8];
+std::atomic<unsigned long long> g_partials_carveout_ctx[kMaxCachedDevices][16];
 
 cudaError_t prefer_shared_carveout(const void* kern, int variant) {
     int dev = 0;
@@ -128,14 +129,17 @@ int resident_ctas_per_sm(int dev, const void* kern, int threads, size_t smem) {
     return n;
 }
 
-// Wave-ahead distance of a launch of more rows than fit on the GPU at once (R = SMs x resident CTAs per SM /
-// CTAs per row): R / 2 rows for the plain norm, R / 8 for the all-reduce half, whose bulk copies of the partials
-// already keep many bytes in flight and whose rows are nine or more row-sized reads (a longer distance evicts
-// rows before they are used). Measured on GB300 over 0 to R (CUDA events around back-to-back launches, inputs
-// above 3x L2): the plain norm peaks between 3R/8 and 3R/4 (NVFP4 T 2048, H 16384: 36.65 -> 35.65 us; static
-// FP8 T 1000, H 16384: 20.10 -> 19.28; bf16 T 2048, H 4096: 12.32 -> 11.56), the all-reduce half at R / 8 (k 8,
-// T 2048, H 16384, static FP8: 124.0 -> 119.6 us) and falls below no warming past R / 2.
-int wave_ahead(const NormParams& p, const RowPlan& plan, const void* kern, size_t smem) {
+// Wave-ahead distance of a launch (R = SMs x resident CTAs per SM / CTAs per row, the rows that fit on the GPU at
+// once): R / 2 rows for the plain norm from 2R rows on with the bf16 epilogue and from 4R rows on with the FP8 and
+// NVFP4 ones; R / 8 for the all-reduce half from R rows on, whose bulk copies of the partials already keep many
+// bytes in flight and whose rows are nine or more row-sized reads (a longer distance evicts rows before they are
+// used). Measured on GB300 (CUDA-graph replay, inputs above 3x L2, each shape with and without): the distance is
+// best between 3R/8 and 3R/4 for the plain norm, at R / 8 for the all-reduce half, and costs time past R; the
+// warming pays from about 4R rows with the quantising epilogues (static FP8, H 16384: T 1000 +0.3%, T 3000 -6%,
+// T 8192 -9%; NVFP4, H 16384: T 1000 +3.5%, T 2048 -1.6%, T 8192 -11%) and from about 2R with bf16 (H 4096:
+// T 3000 -3%, T 4096 -2.5%; H 5120: T 2048 -2%); the all-reduce half, k 8, T 2048, H 16384, static FP8: 127.5 ->
+// 123.6 us (the bench's per-unit breakdown).
+int wave_ahead(const NormParams& p, const RowPlan& plan, const void* kern, size_t smem, int min_waves) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
@@ -143,41 +147,64 @@ int wave_ahead(const NormParams& p, const RowPlan& plan, const void* kern, size_
         return 0;
     }
     const int64_t resident = int64_t{sms} * resident_ctas_per_sm(dev, kern, plan.threads, smem) / plan.ctas_per_row;
-    if (resident <= 0 || p.rows <= resident) return 0;
+    if (resident <= 0 || p.rows < resident * min_waves || p.rows <= resident) return 0;
     return static_cast<int>(p.n_partials > 0 ? resident / 8 : resident / 2);
+}
+
+using NormKernel = void (*)(NormParams, int, int, int, int, int);
+
+// The kernel of a plan: the partial-sum form (one vector per thread) or the plain one, with or without warming.
+template <int EP, bool AHEAD>
+NormKernel norm_kernel(const NormParams& p, const RowPlan& plan) {
+    const bool cl = plan.ctas_per_row > 1;
+    if (p.n_partials > 0) {
+        if (plan.vpt != 1) return nullptr;
+        return cl ? add_rmsnorm_kernel<1, EP, true, kRowInCluster, AHEAD> : add_rmsnorm_kernel<1, EP, true, kRowInCta, AHEAD>;
+    }
+    switch (plan.vpt) {
+        case 1: return cl ? add_rmsnorm_kernel<1, EP, false, kRowInCluster, AHEAD> : add_rmsnorm_kernel<1, EP, false, kRowInCta, AHEAD>;
+        case 2: return cl ? add_rmsnorm_kernel<2, EP, false, kRowInCluster, AHEAD> : add_rmsnorm_kernel<2, EP, false, kRowInCta, AHEAD>;
+        case 4: return cl ? add_rmsnorm_kernel<4, EP, false, kRowInCluster, AHEAD> : add_rmsnorm_kernel<4, EP, false, kRowInCta, AHEAD>;
+        case 8: return cl ? add_rmsnorm_kernel<8, EP, false, kRowInCluster, AHEAD> : add_rmsnorm_kernel<8, EP, false, kRowInCta, AHEAD>;
+        default: return nullptr;
+    }
+}
+
+// The partial-sum kernels' attributes: the carveout (above) and, above the default 48 KB, the opt-in to the
+// CTA's dynamic shared memory (n_partials x slice vectors).
+cudaError_t prepare_partials_kernel(NormKernel kern, int variant, size_t smem) {
+    const cudaError_t ce = prefer_shared_carveout(reinterpret_cast<const void*>(kern), variant);
+    if (ce != cudaSuccess) return ce;
+    if (smem > 48 * 1024)
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    return cudaSuccess;
 }
 
 template <int EP>
 cudaError_t launch_ep(const NormParams& p, const RowPlan& plan, cudaStream_t s) {
-    cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[2];
-    void (*kern)(NormParams, int, int, int, int, int) = nullptr;
-    const bool cl = plan.ctas_per_row > 1;
-    if (p.n_partials > 0) {
-        if (plan.vpt != 1) return cudaErrorInvalidValue;
-        kern = cl ? add_rmsnorm_kernel<1, EP, true, kRowInCluster> : add_rmsnorm_kernel<1, EP, true, kRowInCta>;
-    } else {
-        switch (plan.vpt) {
-            case 1: kern = cl ? add_rmsnorm_kernel<1, EP, false, kRowInCluster> : add_rmsnorm_kernel<1, EP, false, kRowInCta>; break;
-            case 2: kern = cl ? add_rmsnorm_kernel<2, EP, false, kRowInCluster> : add_rmsnorm_kernel<2, EP, false, kRowInCta>; break;
-            case 4: kern = cl ? add_rmsnorm_kernel<4, EP, false, kRowInCluster> : add_rmsnorm_kernel<4, EP, false, kRowInCta>; break;
-            case 8: kern = cl ? add_rmsnorm_kernel<8, EP, false, kRowInCluster> : add_rmsnorm_kernel<8, EP, false, kRowInCta>; break;
-            default: return cudaErrorInvalidValue;
-        }
+    const bool partials = p.n_partials > 0;
+    const int variant = EP * 2 + (plan.ctas_per_row > 1 ? 1 : 0);
+    const size_t smem = partials ? static_cast<size_t>(p.n_partials) * static_cast<size_t>(plan.slice) * 16 : 0;
+    // the warming form where the launch has more rows than fit at once (its residency decides), else the plain one
+    NormKernel kern = norm_kernel<EP, true>(p, plan);
+    if (kern == nullptr) return cudaErrorInvalidValue;
+    if (partials) {
+        const cudaError_t e = prepare_partials_kernel(kern, variant + 8, smem);
+        if (e != cudaSuccess) return e;
     }
-    fill_launch(cfg, attr, p.rows, plan.ctas_per_row, plan.threads, plan.ctas_per_row, s);
-    if (p.n_partials > 0) {
-        const cudaError_t ce = prefer_shared_carveout(reinterpret_cast<const void*>(kern), EP * 2 + (cl ? 1 : 0));
-        if (ce != cudaSuccess) return ce;
-        const size_t smem = static_cast<size_t>(p.n_partials) * static_cast<size_t>(plan.slice) * 16;
-        if (smem > 48 * 1024) {   // above the default dynamic shared-memory limit: opt in (a kernel attribute)
-            const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                       static_cast<int>(smem));
+    const int min_waves = partials ? 1 : (EP == kBf16 ? 2 : 4);
+    const int ahead = wave_ahead(p, plan, reinterpret_cast<const void*>(kern), smem, min_waves);
+    if (ahead == 0) {
+        kern = norm_kernel<EP, false>(p, plan);
+        if (partials) {
+            const cudaError_t e = prepare_partials_kernel(kern, variant, smem);
             if (e != cudaSuccess) return e;
         }
-        cfg.dynamicSmemBytes = smem;
     }
-    const int ahead = wave_ahead(p, plan, reinterpret_cast<const void*>(kern), cfg.dynamicSmemBytes);
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    fill_launch(cfg, attr, p.rows, plan.ctas_per_row, plan.threads, plan.ctas_per_row, s);
+    cfg.dynamicSmemBytes = smem;
     return cudaLaunchKernelEx(&cfg, kern, p, plan.ctas_per_row, plan.slice, plan.prefetch, ahead, plan.order);
 }
 
