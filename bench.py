@@ -48,11 +48,11 @@ TRAFFIC: Dict[str, Dict] = {
     # profiles/swiglu_q8_dynamic_T2048_I53248.md
     "swiglu_q8_dynamic_T2048_I53248": {"bytes": 526931200, "src_sha256": "35b3b830f6b2604e9101f507e895278e5fe67df3bc9bab458c61c04674f127ad"},
     # profiles/add_rmsnorm_q8_static_T1000_H5120.md
-    "add_rmsnorm_q8_static_T1000_H5120": {"bytes": 20503296, "src_sha256": "ceb7187f682340517820309fff4792c19e20c3f01c204d0fe3c2506cdf778831"},
+    "add_rmsnorm_q8_static_T1000_H5120": {"bytes": 20503552, "src_sha256": "0b212fdaac0d7f660892aee3a251bff462bd38471fb316e31f7f62f4b91a713f"},
     # profiles/add_rmsnorm_q8_static_T2048_H16384.md
-    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 177857024, "src_sha256": "ceb7187f682340517820309fff4792c19e20c3f01c204d0fe3c2506cdf778831"},
+    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 175203840, "src_sha256": "0b212fdaac0d7f660892aee3a251bff462bd38471fb316e31f7f62f4b91a713f"},
     # profiles/add_rmsnorm_T8192_H4096.md
-    "add_rmsnorm_T8192_H4096": {"bytes": 210126848, "src_sha256": "ceb7187f682340517820309fff4792c19e20c3f01c204d0fe3c2506cdf778831"},
+    "add_rmsnorm_T8192_H4096": {"bytes": 208334592, "src_sha256": "0b212fdaac0d7f660892aee3a251bff462bd38471fb316e31f7f62f4b91a713f"},
     # profiles/swiglu_T8192_I14336.md
     "swiglu_T8192_I14336": {"bytes": 657681920, "src_sha256": "35b3b830f6b2604e9101f507e895278e5fe67df3bc9bab458c61c04674f127ad"},
     # profiles/swiglu_q8_dynamic_T4096_I28672.md
@@ -60,9 +60,9 @@ TRAFFIC: Dict[str, Dict] = {
     # profiles/swiglu_nvfp4_T2048_I53248.md
     "swiglu_nvfp4_T2048_I53248": {"bytes": 467557376, "src_sha256": "35b3b830f6b2604e9101f507e895278e5fe67df3bc9bab458c61c04674f127ad"},
     # profiles/add_rmsnorm_nvfp4_T2048_H16384.md
-    "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 166977792, "src_sha256": "ceb7187f682340517820309fff4792c19e20c3f01c204d0fe3c2506cdf778831"},
+    "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 161293056, "src_sha256": "0b212fdaac0d7f660892aee3a251bff462bd38471fb316e31f7f62f4b91a713f"},
     # profiles/allreduce_rmsnorm_q8_static_k8_T2048_H16384.md
-    "allreduce_rmsnorm_q8_static_k8_T2048_H16384": {"bytes": 689718784, "src_sha256": "ceb7187f682340517820309fff4792c19e20c3f01c204d0fe3c2506cdf778831"},
+    "allreduce_rmsnorm_q8_static_k8_T2048_H16384": {"bytes": 690913280, "src_sha256": "0b212fdaac0d7f660892aee3a251bff462bd38471fb316e31f7f62f4b91a713f"},
 }
 
 
