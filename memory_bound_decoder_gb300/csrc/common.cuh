@@ -104,10 +104,8 @@ __device__ __forceinline__ float rcp_approx_ftz(float x) {
 
 // The per-tensor fp32 scale S of an NVFP4 output, read once per thread. S outside [2^-64, 2^64] (or not a
 // number) counts as unusable and gives zero block scales and zero codes everywhere.
-__device__ __forceinline__ float nvfp4_tensor_scale(const float* scale) {
-    const float s = __ldg(scale);
-    return (s >= 0x1p-64f && s <= 0x1p64f) ? s : 0.0f;
-}
+__device__ __forceinline__ float nvfp4_tensor_scale_of(float s) { return (s >= 0x1p-64f && s <= 0x1p64f) ? s : 0.0f; }
+__device__ __forceinline__ float nvfp4_tensor_scale(const float* scale) { return nvfp4_tensor_scale_of(__ldg(scale)); }
 
 // Row constants of the NVFP4 epilogue for row values v = y * vmul under the tensor scale S (0 when
 // unusable): k = vmul / (6 S) turns a block maximum of |y| into the block scale's argument, and

@@ -65,9 +65,10 @@ __global__ void __launch_bounds__(512, ALLRED ? 3 : 1) add_rmsnorm_kernel(const 
     }
     if constexpr (ALLRED) {
         if (threadIdx.x == 0) load_partials_bulk(p, row, begin, end - begin, slice, pslices, smem_addr(&pbar));
-        norm_row_slice<VPT, EP, ALLRED, CL>(p, row, rank, ctas_per_row, begin, end, sm, pslices, slice, smem_addr(&pbar));
+        norm_row_slice<VPT, EP, ALLRED, CL, true>(p, row, rank, ctas_per_row, begin, end, sm, pslices, slice,
+                                                 smem_addr(&pbar));
     } else {
-        norm_row_slice<VPT, EP, ALLRED, CL>(p, row, rank, ctas_per_row, begin, end, sm);
+        norm_row_slice<VPT, EP, ALLRED, CL, true>(p, row, rank, ctas_per_row, begin, end, sm);
     }
     pdl_leave(order);
 }

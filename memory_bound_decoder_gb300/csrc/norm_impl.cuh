@@ -152,9 +152,11 @@ __device__ __forceinline__ void norm_prefetch(const NormParams& p, int64_t row, 
 
 // Step 3 of the norm for the bf16, static-FP8 and NVFP4 epilogues: v = (w * s) * inv (w * s of two bf16
 // values is exact in fp32) and its store, for this thread's vectors of one row slice starting at `begin`.
-template <int VPT, int EP>
+// SCALE_IN: the static or tensor scale was loaded earlier (`scale_in`), else it is loaded here.
+template <int VPT, int EP, bool SCALE_IN = false>
 __device__ __forceinline__ void norm_store(const NormParams& p, int64_t row, int begin, const uint4 (&sv)[VPT],
-                                           const uint4 (&wv)[VPT], const bool (&live)[VPT], float inv) {
+                                           const uint4 (&wv)[VPT], const bool (&live)[VPT], float inv,
+                                           float scale_in = 0.0f) {
     if constexpr (EP == kBf16) {
         uint4* outr = static_cast<uint4*>(p.out) + row * p.nvec;
 #pragma unroll
@@ -172,7 +174,7 @@ __device__ __forceinline__ void norm_store(const NormParams& p, int64_t row, int
     } else if constexpr (EP == kNvfp4) {
         // NVFP4: block scales over 16 elements (this vector and the neighbouring lane's), E2M1 codes of
         // v = (w * s) * inv scaled by the block's decoded scale times the tensor scale.
-        const Nvfp4Row nr = nvfp4_row(inv, nvfp4_tensor_scale(p.scale));
+        const Nvfp4Row nr = nvfp4_row(inv, SCALE_IN ? nvfp4_tensor_scale_of(scale_in) : nvfp4_tensor_scale(p.scale));
         unsigned int* qr = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(p.out) + row * (int64_t)p.nvec * 4);
         uint8_t* sfr = p.out_sf + row * (int64_t)(p.nvec / 2);
 #pragma unroll
@@ -192,7 +194,7 @@ __device__ __forceinline__ void norm_store(const NormParams& p, int64_t row, int
         }
     } else {
         // static per-tensor scale: codes of v / scale
-        const float sc = __ldg(p.scale);
+        const float sc = SCALE_IN ? scale_in : __ldg(p.scale);
         const float c = sc > 0.0f ? inv * (1.0f / sc) : 0.0f;
         uint2* outr = reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + row * (int64_t)p.nvec * 8);
 #pragma unroll
@@ -215,7 +217,10 @@ __device__ __forceinline__ void norm_store(const NormParams& p, int64_t row, int
 // it. On a cluster-exchange timeout the CTA returns without writing its outputs. CL: kRowInCta (nctas is 1)
 // or kRowInCluster (nctas > 1) compile only the reduction that runs (code for the other, even untaken, has
 // cost the kernels about 1%); kRowAny decides at run time.
-template <int VPT, int EP, bool ALLRED, int CL = kRowAny>
+//
+// EARLY_SCALE: where the weight is loaded up front, load the static or tensor scale with it (the single-call
+// kernels; the persistent program keeps its register budget for its own prefetches and loads it late).
+template <int VPT, int EP, bool ALLRED, int CL = kRowAny, bool EARLY_SCALE = false>
 __device__ __forceinline__ void norm_row_slice(const NormParams& p, int64_t row, int rank, int nctas, int begin,
                                                int end, NormSmem& sm, const uint4* pslices = nullptr,
                                                int pslice = 0, uint32_t pbar = 0) {
@@ -224,8 +229,10 @@ __device__ __forceinline__ void norm_row_slice(const NormParams& p, int64_t row,
     Exchange& ex = sm.ex;
     float* row_const = sm.row_const;
     // The weight is an L2 hit; load it up front when registers allow (small rows, latency-bound), else
-    // after the reduction. The dynamic variant needs it before the reduction anyway.
+    // after the reduction. The dynamic variant needs it before the reduction anyway. With it (EARLY_SCALE), the
+    // static or tensor scale: otherwise its L2 round trip sits alone between the reduction and the stores.
     constexpr bool kEarlyWeight = EP == kFp8Dynamic || VPT <= 2;
+    constexpr bool kEarlyScale = EARLY_SCALE && kEarlyWeight && (EP == kFp8Static || EP == kNvfp4);
     const int ctas_per_row = CL == kRowInCta ? 1 : nctas;
     const bool single = CL == kRowInCta || (CL == kRowAny && nctas == 1);
 
@@ -235,6 +242,7 @@ __device__ __forceinline__ void norm_row_slice(const NormParams& p, int64_t row,
 
     // 1. one pass over HBM: x and residual in, s = bf16(x + r) kept packed in registers and written back
     uint4 sv[VPT], wv[VPT];
+    float qscale = 0.0f;   // kEarlyScale: the static or tensor scale
     bool live[VPT];
     bool landed = true;   // all-reduce half: the partials' bulk copies completed (false: a bounded wait expired)
     {
@@ -249,6 +257,7 @@ __device__ __forceinline__ void norm_row_slice(const NormParams& p, int64_t row,
                 if constexpr (kEarlyWeight && !ALLRED) wv[i] = load_cached(wr + c);
             }
         }
+        if constexpr (kEarlyScale) qscale = __ldg(p.scale);
         if constexpr (ALLRED) {
             // the partials' slices are in flight into shared memory (bulk copies issued at kernel start); the
             // barrier that follows makes the copies' mbarrier initialisation visible to every thread
@@ -257,6 +266,8 @@ __device__ __forceinline__ void norm_row_slice(const NormParams& p, int64_t row,
 #pragma unroll
             for (int i = 0; i < VPT; ++i)
                 if (live[i]) xv[i] = reduce_partials_smem(pslices, pslice, p.n_partials, threadIdx.x + i * blockDim.x);
+            // the weight only now: issued with the residual loads it would share the small L1 share of this form
+            // (the largest shared-memory carveout) with them (measured 2.6% slower at k 8, T 2048, H 16384)
             if constexpr (kEarlyWeight) {
 #pragma unroll
                 for (int i = 0; i < VPT; ++i)
@@ -308,7 +319,7 @@ __device__ __forceinline__ void norm_row_slice(const NormParams& p, int64_t row,
         }
         if (!landed) return;   // the error bit is set; nothing is written
 
-        norm_store<VPT, EP>(p, row, begin, sv, wv, live, inv);
+        norm_store<VPT, EP, kEarlyScale>(p, row, begin, sv, wv, live, inv, qscale);
     } else {
         // Dynamic per-token scale. The codes are ratios of exact bf16 products, 448 * (w_j s_j) / (w_k s_k),
         // rescaled by the fp32 rounding of the scale, so exact E4M3 ties are common; resolving them as the
