@@ -46,23 +46,23 @@ DEFAULT_WORKLOAD = "llama3.1-405b_fp8_T2048+ragged"
 # `src_sha256` (kernel_src_hash).
 TRAFFIC: Dict[str, Dict] = {
     # profiles/swiglu_q8_dynamic_T2048_I53248.md
-    "swiglu_q8_dynamic_T2048_I53248": {"bytes": 526931200, "src_sha256": "35b3b830f6b2604e9101f507e895278e5fe67df3bc9bab458c61c04674f127ad"},
+    "swiglu_q8_dynamic_T2048_I53248": {"bytes": 526700032, "src_sha256": "74cab478785cc9571472d05ce066d28edc4885cf97aa580d142a4528fab2d0f8"},
     # profiles/add_rmsnorm_q8_static_T1000_H5120.md
-    "add_rmsnorm_q8_static_T1000_H5120": {"bytes": 20503552, "src_sha256": "0b212fdaac0d7f660892aee3a251bff462bd38471fb316e31f7f62f4b91a713f"},
+    "add_rmsnorm_q8_static_T1000_H5120": {"bytes": 20503552, "src_sha256": "d0c4050f54f92f814b324993372a64616aa6f31961dac075118254988cffee00"},
     # profiles/add_rmsnorm_q8_static_T2048_H16384.md
-    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 175203840, "src_sha256": "0b212fdaac0d7f660892aee3a251bff462bd38471fb316e31f7f62f4b91a713f"},
+    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 174811648, "src_sha256": "d0c4050f54f92f814b324993372a64616aa6f31961dac075118254988cffee00"},
     # profiles/add_rmsnorm_T8192_H4096.md
-    "add_rmsnorm_T8192_H4096": {"bytes": 208334592, "src_sha256": "0b212fdaac0d7f660892aee3a251bff462bd38471fb316e31f7f62f4b91a713f"},
+    "add_rmsnorm_T8192_H4096": {"bytes": 208051456, "src_sha256": "d0c4050f54f92f814b324993372a64616aa6f31961dac075118254988cffee00"},
     # profiles/swiglu_T8192_I14336.md
-    "swiglu_T8192_I14336": {"bytes": 657681920, "src_sha256": "35b3b830f6b2604e9101f507e895278e5fe67df3bc9bab458c61c04674f127ad"},
+    "swiglu_T8192_I14336": {"bytes": 657848064, "src_sha256": "74cab478785cc9571472d05ce066d28edc4885cf97aa580d142a4528fab2d0f8"},
     # profiles/swiglu_q8_dynamic_T4096_I28672.md
-    "swiglu_q8_dynamic_T4096_I28672": {"bytes": 539317248, "src_sha256": "35b3b830f6b2604e9101f507e895278e5fe67df3bc9bab458c61c04674f127ad"},
+    "swiglu_q8_dynamic_T4096_I28672": {"bytes": 539429632, "src_sha256": "74cab478785cc9571472d05ce066d28edc4885cf97aa580d142a4528fab2d0f8"},
     # profiles/swiglu_nvfp4_T2048_I53248.md
-    "swiglu_nvfp4_T2048_I53248": {"bytes": 467557376, "src_sha256": "35b3b830f6b2604e9101f507e895278e5fe67df3bc9bab458c61c04674f127ad"},
+    "swiglu_nvfp4_T2048_I53248": {"bytes": 467830272, "src_sha256": "74cab478785cc9571472d05ce066d28edc4885cf97aa580d142a4528fab2d0f8"},
     # profiles/add_rmsnorm_nvfp4_T2048_H16384.md
-    "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 161293056, "src_sha256": "0b212fdaac0d7f660892aee3a251bff462bd38471fb316e31f7f62f4b91a713f"},
+    "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 161476352, "src_sha256": "d0c4050f54f92f814b324993372a64616aa6f31961dac075118254988cffee00"},
     # profiles/allreduce_rmsnorm_q8_static_k8_T2048_H16384.md
-    "allreduce_rmsnorm_q8_static_k8_T2048_H16384": {"bytes": 690913280, "src_sha256": "0b212fdaac0d7f660892aee3a251bff462bd38471fb316e31f7f62f4b91a713f"},
+    "allreduce_rmsnorm_q8_static_k8_T2048_H16384": {"bytes": 691024896, "src_sha256": "d0c4050f54f92f814b324993372a64616aa6f31961dac075118254988cffee00"},
 }
 
 
