@@ -32,8 +32,9 @@
  *   - All tensor pointers are DEVICE pointers (or managed memory visible to the device), row-major and
  *     contiguous. bf16 tensors are passed as void* and hold IEEE bfloat16 bit patterns. The caller owns all
  *     memory: the library allocates nothing, never synchronises, keeps no state between calls (apart from
- *     per-device caches of device attributes and kernel attributes, and the static schedule buffer's address)
- *     and is safe to call from several host threads.
+ *     per-device caches of device attributes, kernel attributes and kernel occupancies, keyed by the current
+ *     context where they belong to one, and the static schedule buffer's address) and is safe to call from
+ *     several host threads.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default stream) and runs in stream
  *     order. Each successful call of an entry point launches exactly one kernel (a batch: one per op).
  *   - Arithmetic is fp32 in registers; every intermediate stays unrounded until the single final rounding
