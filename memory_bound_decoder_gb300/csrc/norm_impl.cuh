@@ -18,6 +18,26 @@ struct NormSmem {
 
 namespace {
 
+// Exact fp32 products of the bf16 halves of two packed words by the mixed-precision fma (bf16 operands, fp32
+// addend and result): a product of two bf16 values is exact in fp32 and the -0 addend keeps the sign of a zero
+// product, so these are the values of unpacking both words and multiplying in fp32, without the unpacking.
+__device__ __forceinline__ float2 mul_bf16x2(uint32_t a, uint32_t b) {
+    float lo, hi;
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, 0f80000000;\n\tfma.rn.f32.bf16 %1, ah, bh, 0f80000000;\n\t}"
+        : "=f"(lo), "=f"(hi) : "r"(a), "r"(b));
+    return make_float2(lo, hi);
+}
+
+// acc + a * a for both bf16 halves of a, one rounding each: the fp32 fma of the unpacked values.
+__device__ __forceinline__ float2 fma_sq_bf16x2(uint32_t a, float2 acc) {
+    float lo, hi;
+    asm("{\n\t.reg .b16 al, ah;\n\tmov.b32 {al, ah}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, al, al, %3;\n\tfma.rn.f32.bf16 %1, ah, ah, %4;\n\t}"
+        : "=f"(lo), "=f"(hi) : "r"(a), "f"(acc.x), "f"(acc.y));
+    return make_float2(lo, hi);
+}
+
 // Quantise y = p * (c_hi + c_lo) to E4M3, rounding the double-float product as if it were exact.
 // p * c_hi is split exactly into y_hi + err (FMA); y_lo = err + p * c_lo. Rounding y_hi alone is correct
 // unless y_hi lands exactly on a rounding boundary of the E4M3 grid; every such boundary (and every code
@@ -168,7 +188,7 @@ __device__ __forceinline__ void norm_store(const NormParams& p, int64_t row, int
             uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                ow[k] = pack_bf16x2(__fmul2_rn(__fmul2_rn(bf16x2_to_float2(sw[k]), bf16x2_to_float2(ww[k])), f2(inv)));
+                ow[k] = pack_bf16x2(__fmul2_rn(mul_bf16x2(sw[k], ww[k]), f2(inv)));
             store_stream(outr + (begin + threadIdx.x + i * blockDim.x), o);
         }
     } else if constexpr (EP == kNvfp4) {
@@ -184,7 +204,7 @@ __device__ __forceinline__ void norm_store(const NormParams& p, int64_t row, int
             const uint32_t* ww = reinterpret_cast<const uint32_t*>(&wv[i]);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                y[k] = live[i] ? __fmul2_rn(bf16x2_to_float2(sw[k]), bf16x2_to_float2(ww[k])) : f2(0.0f);
+                y[k] = live[i] ? mul_bf16x2(sw[k], ww[k]) : f2(0.0f);
             uint32_t sf;
             const uint32_t q = nvfp4_encode(y, nr, &sf);   // whole warp (block max by shuffle)
             if (!live[i]) continue;
@@ -205,7 +225,7 @@ __device__ __forceinline__ void norm_store(const NormParams& p, int64_t row, int
             float2 y[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                y[k] = __fmul2_rn(__fmul2_rn(bf16x2_to_float2(sw[k]), bf16x2_to_float2(ww[k])), f2(c));
+                y[k] = __fmul2_rn(mul_bf16x2(sw[k], ww[k]), f2(c));
             store_stream(outr + (begin + threadIdx.x + i * blockDim.x),
                          make_uint2(pack_e4m3x4(y[0], y[1]), pack_e4m3x4(y[2], y[3])));
         }
@@ -295,10 +315,7 @@ __device__ __forceinline__ void norm_row_slice(const NormParams& p, int64_t row,
             if (!live[i]) continue;
             const uint32_t* sw = reinterpret_cast<const uint32_t*>(&sv[i]);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float2 s2 = bf16x2_to_float2(sw[k]);
-                ss2 = __ffma2_rn(s2, s2, ss2);
-            }
+            for (int k = 0; k < 4; ++k) ss2 = fma_sq_bf16x2(sw[k], ss2);
         }
         float inv;
         if (single) {   // the whole row in this CTA: one barrier, every thread forms inv
@@ -335,9 +352,8 @@ __device__ __forceinline__ void norm_row_slice(const NormParams& p, int64_t row,
             const uint32_t* ww = reinterpret_cast<const uint32_t*>(&wv[i]);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const float2 s2 = bf16x2_to_float2(sw[k]);
-                dd_accumulate(acc, __fmul2_rn(s2, s2));   // exact squares of bf16 values
-                const float2 p2 = __fmul2_rn(s2, bf16x2_to_float2(ww[k]));
+                dd_accumulate(acc, mul_bf16x2(sw[k], sw[k]));   // exact squares of bf16 values
+                const float2 p2 = mul_bf16x2(sw[k], ww[k]);
                 pmax = fmaxf(pmax, fmaxf(fabsf(p2.x), fabsf(p2.y)));
             }
         }
@@ -365,7 +381,7 @@ __device__ __forceinline__ void norm_row_slice(const NormParams& p, int64_t row,
             float2 y[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                y[k] = exact_side(__fmul2_rn(bf16x2_to_float2(sw[k]), bf16x2_to_float2(ww[k])), c_hi, c_lo);
+                y[k] = exact_side(mul_bf16x2(sw[k], ww[k]), c_hi, c_lo);
             store_stream(outr + (begin + threadIdx.x + i * blockDim.x),
                          make_uint2(pack_e4m3x4(y[0], y[1]), pack_e4m3x4(y[2], y[3])));
         }

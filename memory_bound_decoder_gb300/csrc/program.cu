@@ -196,8 +196,7 @@ __device__ void norm_run(const ProgOp* ops, int n, int64_t row, ProgSmem& sm) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 sw[q] = pack_bf16x2(__fadd2_rn(bf16x2_to_float2(xw[q]), bf16x2_to_float2(sw[q])));
-                const float2 s2 = bf16x2_to_float2(sw[q]);
-                ss2 = __ffma2_rn(s2, s2, ss2);
+                ss2 = fma_sq_bf16x2(sw[q], ss2);
             }
         }
         uint4 wn;
@@ -223,7 +222,7 @@ __device__ void norm_run(const ProgOp* ops, int n, int64_t row, ProgSmem& sm) {
                 float2 y[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
-                    y[q] = __fmul2_rn(__fmul2_rn(bf16x2_to_float2(sw[q]), bf16x2_to_float2(ww[q])), f2(cm));
+                    y[q] = __fmul2_rn(mul_bf16x2(sw[q], ww[q]), f2(cm));
                 store_stream(reinterpret_cast<uint2*>(static_cast<uint8_t*>(op.out) + row * (int64_t)nvec * 8) + c,
                              make_uint2(pack_e4m3x4(y[0], y[1]), pack_e4m3x4(y[2], y[3])));
             }
