@@ -29,6 +29,15 @@ __device__ __forceinline__ float2 mul_bf16x2(uint32_t a, uint32_t b) {
     return make_float2(lo, hi);
 }
 
+// bf16(a + b) for both halves by the packed bf16 add, which rounds the exact sum once. Rounding the fp32 sum gives
+// the same bits: that sum is exact unless the addends' exponents differ by 16 or more, and then the smaller one is
+// below 2^-15 of the larger, far inside half a bf16 step of it, so both roundings return the larger.
+__device__ __forceinline__ uint32_t add_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 // acc + a * a for both bf16 halves of a, one rounding each: the fp32 fma of the unpacked values.
 __device__ __forceinline__ float2 fma_sq_bf16x2(uint32_t a, float2 acc) {
     float lo, hi;
@@ -302,7 +311,12 @@ __device__ __forceinline__ void norm_row_slice(const NormParams& p, int64_t row,
             const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv[i]);
             uint32_t* sw = reinterpret_cast<uint32_t*>(&sv[i]);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) sw[k] = pack_bf16x2(__fadd2_rn(bf16x2_to_float2(xw[k]), bf16x2_to_float2(sw[k])));
+            for (int k = 0; k < 4; ++k) {
+                // the same bits either way; the packed add measured faster in the all-reduce half (1 to 3%) and
+                // slower in some decode-size single calls (static FP8, H 16384, T 16: 2.29 -> 2.54 us)
+                if constexpr (ALLRED) sw[k] = add_bf16x2(xw[k], sw[k]);
+                else sw[k] = pack_bf16x2(__fadd2_rn(bf16x2_to_float2(xw[k]), bf16x2_to_float2(sw[k])));
+            }
             store_stream(rr + (begin + threadIdx.x + i * blockDim.x), sv[i]);
         }
     }

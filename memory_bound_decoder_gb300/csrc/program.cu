@@ -195,7 +195,7 @@ __device__ void norm_run(const ProgOp* ops, int n, int64_t row, ProgSmem& sm) {
             uint32_t* sw = reinterpret_cast<uint32_t*>(&sv[0]);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                sw[q] = pack_bf16x2(__fadd2_rn(bf16x2_to_float2(xw[q]), bf16x2_to_float2(sw[q])));
+                sw[q] = add_bf16x2(xw[q], sw[q]);
                 ss2 = fma_sq_bf16x2(sw[q], ss2);
             }
         }

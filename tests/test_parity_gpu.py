@@ -237,6 +237,43 @@ def test_zero_rows_and_constant_rows():
     assert (q[1] == 0xFE).all()          # every element is the row's amax -> -448
 
 
+def _residual_edge_rows(T, H, seed):
+    """x and residual whose sums stress bf16(x + r): exponent spans of 0 to 40 between the addends (the fp32 sum
+    is inexact beyond 15), exact midpoints of the bf16 rounding (ties to even), cancellation to zero, bf16
+    subnormals (with each other and with normal values) and signed zeros, every kind in every row."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((T, H))
+    r = rng.standard_normal((T, H))
+    kind = rng.integers(0, 5, (T, H))
+    xb = wl.bf16_bits_to_f32(wl.f32_to_bf16_bits(x.astype(np.float32))).astype(np.float64)
+    wide = kind == 0
+    r[wide] = (xb * 2.0 ** -rng.integers(0, 41, (T, H)) * rng.choice([-1.0, 1.0], (T, H)))[wide]
+    tie = kind == 1
+    e = np.floor(np.log2(np.maximum(np.abs(xb), 1e-30)))
+    r[tie] = (np.sign(xb) * rng.choice([-1.0, 1.0], (T, H)) * 2.0 ** (e - 8))[tie]
+    canc = kind == 2
+    r[canc] = -xb[canc]
+    sub = kind == 3
+    x[sub] *= 2.0 ** -130
+    r[sub] *= 2.0 ** rng.choice([-131.0, -120.0, 0.0], (T, H))[sub]
+    zero = kind == 4
+    x[zero] = rng.choice([0.0, -0.0], (T, H))[zero] * 1.0
+    x[zero & (rng.random((T, H)) < 0.5)] = -0.0
+    r[zero & (rng.random((T, H)) < 0.5)] = -0.0
+    return wl.f32_to_bf16_bits(x.astype(np.float32)), wl.f32_to_bf16_bits(r.astype(np.float32))
+
+
+@pytest.mark.parametrize("T,H", [(8, 5120), (6, 16384), (300, 4096)])
+def test_residual_add_edges(T, H):
+    """The residual s = bf16(x + r) bit-exact where the fp32 sum is inexact, lands on a rounding midpoint,
+    cancels, or meets subnormals and signed zeros; the outputs within the usual tolerances."""
+    xb, rb = _residual_edge_rows(T, H, seed=T + H)
+    inp = wl.NormInputs(xb, rb, wl.weight_bf16(H, 3), 1e-5)
+    check_norm(inp, "bf16")
+    check_norm(inp, "q8", "static")
+    check_norm(inp, "q8", "dynamic")
+
+
 def test_static_saturation():
     inp = wl.make_norm_inputs(8, 4096, seed=2, dist=wl.C5_ACT, eps=1e-5)
     check_norm(inp, "q8", "static", static_scale=1e-3)
