@@ -38,6 +38,14 @@ __device__ __forceinline__ uint32_t add_bf16x2(uint32_t a, uint32_t b) {
     return d;
 }
 
+// acc + a for both bf16 halves of a, one rounding each: the fp32 add of the unpacked values (mixed-precision add).
+__device__ __forceinline__ float2 add_f32_bf16x2(float2 acc, uint32_t a) {
+    asm("{\n\t.reg .b16 al, ah;\n\tmov.b32 {al, ah}, %2;\n\t"
+        "add.rn.f32.bf16 %0, al, %0;\n\tadd.rn.f32.bf16 %1, ah, %1;\n\t}"
+        : "+f"(acc.x), "+f"(acc.y) : "r"(a));
+    return acc;
+}
+
 // acc + a * a for both bf16 halves of a, one rounding each: the fp32 fma of the unpacked values.
 __device__ __forceinline__ float2 fma_sq_bf16x2(uint32_t a, float2 acc) {
     float lo, hi;
@@ -85,7 +93,7 @@ __device__ __forceinline__ uint4 reduce_partials_smem(const uint4* slices, int s
         const uint32_t* w = reinterpret_cast<const uint32_t*>(&v);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            s[q] = __fadd2_rn(f2(0.0f), bf16x2_to_float2(w[q]));   // from +0, as the exact sum: -0 + -0 is +0
+            s[q] = add_f32_bf16x2(f2(0.0f), w[q]);   // from +0, as the exact sum: -0 + -0 is +0
             emax[q] = emin[q] = w[q] & 0x7FFF7FFFu;
         }
     }
@@ -96,7 +104,7 @@ __device__ __forceinline__ uint4 reduce_partials_smem(const uint4* slices, int s
         const uint32_t* w = reinterpret_cast<const uint32_t*>(&v);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            s[q] = __fadd2_rn(s[q], bf16x2_to_float2(w[q]));
+            s[q] = add_f32_bf16x2(s[q], w[q]);
             const uint32_t m = w[q] & 0x7FFF7FFFu;
             emax[q] = max_bf16x2_bits(emax[q], m);
             emin[q] = min_bf16x2_bits(emin[q], m);
