@@ -48,11 +48,11 @@ TRAFFIC: Dict[str, Dict] = {
     # profiles/swiglu_q8_dynamic_T2048_I53248.md
     "swiglu_q8_dynamic_T2048_I53248": {"bytes": 526700032, "src_sha256": "74cab478785cc9571472d05ce066d28edc4885cf97aa580d142a4528fab2d0f8"},
     # profiles/add_rmsnorm_q8_static_T1000_H5120.md
-    "add_rmsnorm_q8_static_T1000_H5120": {"bytes": 20502784, "src_sha256": "cddc06d8288450006b0f762dceb2d669b7afc52b278271335d0de623849aceb7"},
+    "add_rmsnorm_q8_static_T1000_H5120": {"bytes": 20503040, "src_sha256": "713aeb9c0d1731ee9ac0e7fb9408a229094e56f2d181d344b35e6e5a800d577f"},
     # profiles/add_rmsnorm_q8_static_T2048_H16384.md
-    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 174932736, "src_sha256": "cddc06d8288450006b0f762dceb2d669b7afc52b278271335d0de623849aceb7"},
+    "add_rmsnorm_q8_static_T2048_H16384": {"bytes": 174872576, "src_sha256": "713aeb9c0d1731ee9ac0e7fb9408a229094e56f2d181d344b35e6e5a800d577f"},
     # profiles/add_rmsnorm_T8192_H4096.md
-    "add_rmsnorm_T8192_H4096": {"bytes": 208786688, "src_sha256": "cddc06d8288450006b0f762dceb2d669b7afc52b278271335d0de623849aceb7"},
+    "add_rmsnorm_T8192_H4096": {"bytes": 208775424, "src_sha256": "713aeb9c0d1731ee9ac0e7fb9408a229094e56f2d181d344b35e6e5a800d577f"},
     # profiles/swiglu_T8192_I14336.md
     "swiglu_T8192_I14336": {"bytes": 657848064, "src_sha256": "74cab478785cc9571472d05ce066d28edc4885cf97aa580d142a4528fab2d0f8"},
     # profiles/swiglu_q8_dynamic_T4096_I28672.md
@@ -60,9 +60,9 @@ TRAFFIC: Dict[str, Dict] = {
     # profiles/swiglu_nvfp4_T2048_I53248.md
     "swiglu_nvfp4_T2048_I53248": {"bytes": 467830272, "src_sha256": "74cab478785cc9571472d05ce066d28edc4885cf97aa580d142a4528fab2d0f8"},
     # profiles/add_rmsnorm_nvfp4_T2048_H16384.md
-    "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 161534976, "src_sha256": "cddc06d8288450006b0f762dceb2d669b7afc52b278271335d0de623849aceb7"},
+    "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 161357312, "src_sha256": "713aeb9c0d1731ee9ac0e7fb9408a229094e56f2d181d344b35e6e5a800d577f"},
     # profiles/allreduce_rmsnorm_q8_static_k8_T2048_H16384.md
-    "allreduce_rmsnorm_q8_static_k8_T2048_H16384": {"bytes": 691182848, "src_sha256": "cddc06d8288450006b0f762dceb2d669b7afc52b278271335d0de623849aceb7"},
+    "allreduce_rmsnorm_q8_static_k8_T2048_H16384": {"bytes": 690852864, "src_sha256": "713aeb9c0d1731ee9ac0e7fb9408a229094e56f2d181d344b35e6e5a800d577f"},
 }
 
 
