@@ -63,6 +63,8 @@ TRAFFIC: Dict[str, Dict] = {
     "add_rmsnorm_nvfp4_T2048_H16384": {"bytes": 161357312, "src_sha256": "713aeb9c0d1731ee9ac0e7fb9408a229094e56f2d181d344b35e6e5a800d577f"},
     # profiles/allreduce_rmsnorm_q8_static_k8_T2048_H16384.md
     "allreduce_rmsnorm_q8_static_k8_T2048_H16384": {"bytes": 690852864, "src_sha256": "713aeb9c0d1731ee9ac0e7fb9408a229094e56f2d181d344b35e6e5a800d577f"},
+    # profiles/allreduce_rmsnorm_k8_T2048_H16384.md
+    "allreduce_rmsnorm_k8_T2048_H16384": {"bytes": 716697600, "src_sha256": "713aeb9c0d1731ee9ac0e7fb9408a229094e56f2d181d344b35e6e5a800d577f"},
 }
 
 
