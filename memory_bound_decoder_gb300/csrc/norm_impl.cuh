@@ -76,7 +76,8 @@ __device__ __forceinline__ float2 exact_side(float2 p, float c_hi, float c_lo) {
 // activation x of the all-reduce half. The CTA's slices of the n partials sit in shared memory (brought in by
 // bulk copies, `slice` vectors each, this thread's vector at index c of every slice).
 //
-// Fast path: the plain fp32 sum s (from +0, packed fp32x2) is exact when the addends' exponents span little.
+// Fast path: the plain fp32 sum s (from +0, each partial's bf16 halves added by the mixed-precision add) is exact
+// when the addends' exponents span little.
 // Every addend is a multiple of 2^(emin - 134) (emin, emax: the smallest and largest bf16 exponent field
 // among the element's addends, read off the smallest and largest magnitude; a field of 0, a zero or a
 // subnormal, is the conservative case) and every partial sum is below k 2^(emax - 126) <= 2^(emax - 126 + L),
